@@ -1,0 +1,267 @@
+"""CPU oracle for the routed MoE FFN layer forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library and the library never calls it: a missing CUDA extension
+is an error, never a fallback to this file.
+
+Everything here is a plain, slow, literal restatement of the pages' formulas in
+float64 with numpy (``@`` is numpy's float64 matrix product, used as a library
+primitive).  Sources, cited by page title and section:
+
+* [MM] "mega_moe" (Ascend CANN operator page), section "计算公式" (computation
+  formula) with its sub-steps "EP Dispatch", "Expert Compute" (Linear1,
+  SwiGLU, Linear2) and "Token Combine".
+* [MG] "Megatron-LM 的 MoE 并行：以 DeepSeek-V4 为例": section "模型与入口"
+  (the MoE output equation y_t = F_s(x_t) + sum_{e in I_t} g_{t,e} F_e(x_t)),
+  section "路由与负载 / 路由张量" (affinity a = sqrt(softplus(l)), selection
+  I_t = TopK(a + beta), mixing weight g = alpha * a / sum_{I_t} a),
+  "路由与负载 / Hash 路由" (ids looked up from tid2eid; gating and weights
+  kept), "AlltoAll 的前向 / 计数与重排" (per-expert counts, permutation with
+  duplication, the four-token split example).
+* [PD] "Megatron 分布式训练全维度并行技术文档", section "4.2 数学推导"
+  (softmax gate G(x) = TopK(softmax(x W_gate))).
+
+Readings taken where the pages are silent:
+the score function is a parameter (sigmoid, sqrt-softplus, softmax); the k ids
+of a token are listed by descending selection score, equal scores to the lower
+expert id; rows inside an expert block follow ascending flat index t*k+j; the
+gate half of Linear1's output is its first I columns; the shared expert has the
+same width I and weight 1; an assignment whose id is outside [0, E) is dropped.
+
+Parity status: routing ids, counts, permutation and the FFN/combine are pinned
+by tests/test_oracle_pins.py (closed forms, brute force, the worked split
+example, reductions to a dense FFN).  The absolute gate and output values for
+the sigmoid and sqrt-softplus rules at the workload sizes rest on these same
+formulas; the pages print no worked numbers for them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SCORE_SIGMOID = 0
+SCORE_SQRT_SOFTPLUS = 1
+SCORE_SOFTMAX = 2
+
+__all__ = [
+    "bf16_to_f64", "round_to_bf16", "f64_to_bf16_bits",
+    "router_logits", "affinity", "select_topk", "gates",
+    "route", "route_from_logits", "route_hash",
+    "dispatch", "swiglu_expert", "forward", "forward_tokens",
+    "SCORE_SIGMOID", "SCORE_SQRT_SOFTPLUS", "SCORE_SOFTMAX",
+]
+
+
+# ----------------------------------------------------------------------------- numbers
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values (exact widening)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (ties to even), returned
+    as float64.  Direct rounding of the 52-bit fraction to 7 bits: no
+    intermediate float32 step, so there is no double rounding."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    u = x.view(np.uint64)
+    drop = np.uint64(45)  # 52 - 7 fraction bits are discarded
+    half = np.uint64(1) << np.uint64(44)
+    lsb = (u >> drop) & np.uint64(1)
+    r = (u + (half - np.uint64(1)) + lsb) & ~((np.uint64(1) << drop) - np.uint64(1))
+    return r.view(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """float64 -> bf16 bit patterns, rounding to nearest even."""
+    r = round_to_bf16(x).astype(np.float32)  # exact: r has 8 significant bits
+    return (r.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def _silu(z):
+    # [MM] conventions: SiLU(z) = z * sigma(z) = z / (1 + e^{-z})
+    return z * _sigmoid(z)
+
+
+# ----------------------------------------------------------------------------- routing
+def router_logits(X_bits, Wg_bits) -> np.ndarray:
+    """[MG] 路由张量: the gating linear maps [n, h] to [n, E] logits, l = X Wg."""
+    return bf16_to_f64(X_bits) @ bf16_to_f64(Wg_bits)
+
+
+def affinity(logits, score_fn: int) -> np.ndarray:
+    """Affinity a[t, e] from the logits.
+
+    sigmoid: a = 1 / (1 + exp(-l)).
+    sqrt-softplus ([MG] 路由张量, V4 rule): a = sqrt(softplus(l)), with
+      softplus(l) = log(1 + e^l) evaluated as max(l, 0) + log1p(e^{-|l|}).
+    softmax ([PD] 4.2): a = softmax over the experts of the token's logits.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    if score_fn == SCORE_SIGMOID:
+        return _sigmoid(l)
+    if score_fn == SCORE_SQRT_SOFTPLUS:
+        return np.sqrt(np.maximum(l, 0.0) + np.log1p(np.exp(-np.abs(l))))
+    if score_fn == SCORE_SOFTMAX:
+        m = l.max(axis=-1, keepdims=True)
+        p = np.exp(l - m)
+        return p / p.sum(axis=-1, keepdims=True)
+    raise ValueError(f"unknown score function {score_fn}")
+
+
+def select_topk(scores, k: int) -> np.ndarray:
+    """Per row, the k largest scores' column ids, listed by descending score;
+    equal scores are listed (and kept) lower id first.  A stable sort of the
+    negated scores gives exactly that order."""
+    s = np.asarray(scores, dtype=np.float64)
+    order = np.argsort(-s, axis=-1, kind="stable")
+    return order[..., :k].astype(np.int32)
+
+
+def gates(a, E_ids, alpha: float, renorm: bool) -> np.ndarray:
+    """[MG] 路由张量: g_{t,e} = alpha * a_{t,e} / sum_{j in I_t} a_{t,j} taken at
+    the selected ids with the raw (un-biased) affinity.  Without
+    renormalisation (the softmax gate of [PD] 4.2) g = alpha * a at the ids.
+    A zero denominator gives zero gates."""
+    a_sel = np.take_along_axis(np.asarray(a, dtype=np.float64), E_ids.astype(np.int64), axis=-1)
+    if not renorm:
+        return alpha * a_sel
+    den = a_sel.sum(axis=-1, keepdims=True)
+    safe = np.where(den > 0, den, 1.0)
+    return np.where(den > 0, alpha * a_sel / safe, 0.0)
+
+
+def route_from_logits(logits, bias, score_fn: int, k: int, alpha: float, renorm: bool):
+    """Selection and gates from given logits: a = score(l); I_t = TopK(a + beta)
+    ([MG] 路由张量; beta is used for selection only); softmax selects on a alone
+    ([PD] 4.2).  Returns (E_ids int32 [T,k], G float64 [T,k], a float64 [T,E])."""
+    a = affinity(logits, score_fn)
+    s = a
+    if bias is not None:
+        if score_fn == SCORE_SOFTMAX:
+            raise ValueError("the softmax gate takes no selection bias")
+        s = a + np.asarray(bias, dtype=np.float64)[None, :]
+    E_ids = select_topk(s, k)
+    return E_ids, gates(a, E_ids, alpha, renorm), a
+
+
+def route(X_bits, Wg_bits, bias, score_fn: int, k: int, alpha: float, renorm: bool):
+    """Router: logits, affinity, biased top-k selection, alpha-scaled gates.
+    Returns (E_ids, G, logits)."""
+    l = router_logits(X_bits, Wg_bits)
+    E_ids, G, _ = route_from_logits(l, bias, score_fn, k, alpha, renorm)
+    return E_ids, G, l
+
+
+def route_hash(X_bits, Wg_bits, token_ids, tid2eid, score_fn: int, alpha: float, renorm: bool):
+    """[MG] Hash 路由: the expert ids are the table row of the token id; the
+    gating linear and the gate formula are unchanged.  Returns (E_ids, G, logits)."""
+    tid2eid = np.asarray(tid2eid, dtype=np.int32)
+    E_ids = tid2eid[np.asarray(token_ids, dtype=np.int64)]
+    l = router_logits(X_bits, Wg_bits)
+    a = affinity(l, score_fn)
+    return E_ids.astype(np.int32), gates(a, E_ids, alpha, renorm), l
+
+
+# ----------------------------------------------------------------------------- dispatch
+def dispatch(E_ids, E: int):
+    """[MM] EP Dispatch: expert e receives the rows of I_e stacked in a fixed
+    order; row(i, k) is the unique position of token i in expert e_{i,k}'s block.
+    [MG] 计数与重排: count[e] assignments per expert; the permutation groups the
+    flat assignment list by expert, copying a token once per selection.
+
+    Fixed order taken here: ascending flat index f = t*k + j inside each block.
+    Returns counts [E], offsets [E+1] (exclusive prefix sum), perm [sum counts]
+    (perm[p] = flat index at block row p) and inv [T*k] (inv[f] = p, or -1 for
+    an id outside [0, E), which is dropped)."""
+    flat = np.asarray(E_ids, dtype=np.int64).reshape(-1)
+    valid = (flat >= 0) & (flat < E)
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat[valid]:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    perm = np.empty(int(offsets[-1]), dtype=np.int64)
+    fill = offsets[:-1].copy()
+    inv = np.full(flat.shape[0], -1, dtype=np.int64)
+    for f in range(flat.shape[0]):  # ascending f: the order inside each block
+        if valid[f]:
+            e = flat[f]
+            perm[fill[e]] = f
+            inv[f] = fill[e]
+            fill[e] += 1
+    return (counts.astype(np.int32), offsets.astype(np.int32),
+            perm.astype(np.int32), inv.astype(np.int32))
+
+
+# ----------------------------------------------------------------------------- experts
+def swiglu_expert(X_rows64, W1e, W2e, act_round_bf16: bool = False) -> np.ndarray:
+    """[MM] Expert Compute: H = X_e W1[e] ([N_e, 2I]); gate = H[:, :I],
+    up = H[:, I:]; A = SiLU(gate) * up; Y_e = A W2[e].  W1e/W2e are bf16 bits.
+    ``act_round_bf16`` rounds A to bf16 before Linear2 (off by default)."""
+    W1 = bf16_to_f64(W1e)
+    W2 = bf16_to_f64(W2e)
+    I = W2.shape[0]
+    Hm = X_rows64 @ W1
+    A = _silu(Hm[:, :I]) * Hm[:, I:]
+    if act_round_bf16:
+        A = round_to_bf16(A)
+    return A @ W2
+
+
+def _get(w, e):
+    return w(e) if callable(w) else w[e]
+
+
+def forward_tokens(tokens, X_rows_bits, E_rows, G_rows, W1, W2, Ws1=None, Ws2=None,
+                   act_round_bf16: bool = False, E: int | None = None) -> np.ndarray:
+    """The layer output for a set of tokens, in float64 (no final rounding).
+
+    [MG] 模型与入口: y_t = F_s(x_t) + sum_{e in I_t} g_{t,e} F_e(x_t).
+    [MM] Token Combine: y_i = sum_k G[i,k] * Y_{e_{i,k}}[row(i,k), :].
+
+    ``tokens`` only labels the rows (X_rows_bits[r] is token tokens[r]); each
+    output row depends on its own token alone.  W1/W2 may be arrays indexed by
+    expert or callables e -> bf16 bits, so that a caller can hand over experts
+    one at a time (then ``E``, the expert count, must be given).  Ws1/Ws2
+    (the shared expert, weight 1) may be None.
+    """
+    R = len(tokens)
+    E_rows = np.asarray(E_rows, dtype=np.int64).reshape(R, -1)
+    G_rows = np.asarray(G_rows, dtype=np.float64).reshape(R, -1)
+    k = E_rows.shape[1]
+    X64 = bf16_to_f64(X_rows_bits).reshape(R, -1)
+    Hdim = X64.shape[1]
+    if E is None:
+        E = np.asarray(W1).shape[0]
+    # dispatch the selected rows: the expert blocks of these tokens
+    counts, offsets, perm, inv = dispatch(E_rows, E)
+    Yp = np.zeros((perm.shape[0], Hdim), dtype=np.float64)
+    for e in range(len(counts)):
+        if counts[e] == 0:
+            continue
+        rows = perm[offsets[e]:offsets[e + 1]]
+        Xe = X64[rows // k]
+        Yp[offsets[e]:offsets[e + 1]] = swiglu_expert(Xe, _get(W1, e), _get(W2, e), act_round_bf16)
+    # combine in j order
+    Y = np.zeros((R, Hdim), dtype=np.float64)
+    for j in range(k):
+        f = np.arange(R) * k + j
+        p = inv[f]
+        ok = p >= 0
+        Y[ok] += G_rows[ok, j:j + 1] * Yp[p[ok]]
+    if Ws1 is not None:
+        Y += swiglu_expert(X64, Ws1, Ws2, act_round_bf16)
+    return Y
+
+
+def forward(X_bits, E_ids, G, W1, W2, Ws1=None, Ws2=None, act_round_bf16: bool = False):
+    """Whole-layer output: float64 Y [T, H] and its bf16 rounding (bits)."""
+    T = np.asarray(X_bits).shape[0]
+    Y = forward_tokens(np.arange(T), X_bits, E_ids, G, W1, W2, Ws1, Ws2, act_round_bf16,
+                       E=np.asarray(W1).shape[0])
+    return Y, f64_to_bf16_bits(Y)

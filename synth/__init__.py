@@ -1,0 +1,263 @@
+"""Seeded synthetic inputs for the routed MoE FFN layer.
+
+This module only draws numbers.  It holds none of the layer's arithmetic (no
+routing, no FFN, no combine); the oracle under ``oracle/`` and the CUDA library
+both consume what it returns, and neither is imported here.
+
+Workloads (shapes follow the pages' own worked layers):
+
+* ``c1`` tiny layer: T=128, H=256, E=8, top-2, I=128, sigmoid routing, bias 0.
+* ``c2`` given-routing layer: T=4096, H=4096, E=32, top-8, I=1536; expert ids
+  are k distinct uniform experts per token, gates are a softmax of k N(0,1)
+  draws per token.
+* ``c3`` V4-Pro-shaped layer: T=4096, H=7168, E=384, top-6, I=2048, one shared
+  expert, sigmoid affinity, selection bias ~N(0, 0.1), alpha = 2.5, and a
+  Zipf(1.1)-skewed expert load (see ``zipf_offsets``).
+* ``c4`` hash-routed layer: the ``c3`` tensors, expert ids looked up in a
+  seeded random ``tid2eid[128000, 6]`` table by uniform token ids.
+* ``c5`` large-FFN layer: T=16384, H=8192, E=64, top-2, I=22016, softmax top-2.
+* ``*s`` variants: the same recipes at sizes a CPU oracle finishes in seconds,
+  still spanning several GEMM tiles with ragged tails.
+
+Value distributions: X ~ N(0,1); Wg and W1 (and the shared Ws1) ~ N(0, 1/H);
+W2 (and Ws2) ~ N(0, 1/I).  Every floating-point tensor that the layer reads in
+bf16 is rounded to bf16 with round-to-nearest-even before use.
+
+Two back ends draw the same recipe: ``numpy`` (host arrays; bf16 carried as
+uint16 bit patterns) for sizes the oracle can take whole, and ``torch`` (device
+tensors) for the full-size workloads, whose weights (up to 69 GB) are too large
+to draw on the host.  The two back ends use different generators and do not
+produce the same numbers; a test always hands one drawing to both sides.
+"""
+from __future__ import annotations
+
+import copy
+import json
+import math
+import os
+
+import numpy as np
+
+__all__ = ["CONFIGS", "get_config", "make_inputs", "make_inputs_torch",
+           "bf16_bits_from_f32", "f32_from_bf16_bits", "zipf_targets",
+           "zipf_offsets"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+# score function codes shared by every layer of this repository's interface
+SCORE_SIGMOID = 0
+SCORE_SQRT_SOFTPLUS = 1
+SCORE_SOFTMAX = 2
+_SCORE_NAMES = {"sigmoid": SCORE_SIGMOID, "sqrt_softplus": SCORE_SQRT_SOFTPLUS,
+                "softmax": SCORE_SOFTMAX}
+
+_BASE = dict(shared=0, score="sigmoid", alpha=1.0, renorm=1, routing="topk",
+             bias=False, skew=None, V=0)
+
+CONFIGS = {
+    # --- the five workloads --------------------------------------------------
+    "c1": dict(_BASE, T=128, H=256, E=8, k=2, I=128),
+    "c2": dict(_BASE, T=4096, H=4096, E=32, k=8, I=1536, routing="given",
+               score="softmax", renorm=0),
+    "c3": dict(_BASE, T=4096, H=7168, E=384, k=6, I=2048, shared=1, alpha=2.5,
+               bias=True, skew="zipf1.1"),
+    "c4": dict(_BASE, T=4096, H=7168, E=384, k=6, I=2048, shared=1, alpha=2.5,
+               bias=True, skew="zipf1.1", routing="hash", V=128000),
+    "c5": dict(_BASE, T=16384, H=8192, E=64, k=2, I=22016, score="softmax",
+               renorm=0),
+    # --- oracle-sized variants of the same recipes ----------------------------
+    "c1s": dict(_BASE, T=128, H=256, E=8, k=2, I=128),
+    "c2s": dict(_BASE, T=333, H=512, E=12, k=4, I=320, routing="given",
+                score="softmax", renorm=0),
+    "c3s": dict(_BASE, T=257, H=448, E=40, k=6, I=192, shared=1, alpha=2.5,
+                bias=True, skew="zipf1.1"),
+    "c3s_sp": dict(_BASE, T=257, H=448, E=40, k=6, I=192, shared=1, alpha=2.5,
+                   bias=True, score="sqrt_softplus"),
+    "c4s": dict(_BASE, T=257, H=448, E=40, k=6, I=192, shared=1, alpha=2.5,
+                bias=True, skew="zipf1.1", routing="hash", V=1000),
+    "c5s": dict(_BASE, T=515, H=384, E=8, k=2, I=704, score="softmax",
+                renorm=0),
+}
+# the pages' own V4-Pro routing rule (sqrt-softplus affinity) at the c3 shapes
+CONFIGS["c3_sp"] = dict(CONFIGS["c3"], score="sqrt_softplus", skew=None)
+
+
+def get_config(name_or_cfg, **overrides) -> dict:
+    """Return a full config dict (a copy) for a workload name or a dict."""
+    if isinstance(name_or_cfg, str):
+        cfg = copy.deepcopy(CONFIGS[name_or_cfg])
+        cfg["name"] = name_or_cfg
+    else:
+        cfg = dict(_BASE)
+        cfg.update(name_or_cfg)
+        cfg.setdefault("name", "custom")
+    cfg.update(overrides)
+    cfg["score_fn"] = _SCORE_NAMES[cfg["score"]]
+    return cfg
+
+
+# --------------------------------------------------------------------------- bf16
+def bf16_bits_from_f32(x) -> np.ndarray:
+    """float32 array -> bf16 bit patterns (uint16), round to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def f32_from_bf16_bits(b) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# --------------------------------------------------------------------------- skew
+def zipf_targets(E: int, A: int, T: int, s: float = 1.1, seed: int = 77) -> np.ndarray:
+    """Target assignment counts per expert: Zipf(s) over a seeded random rank
+    order, clipped at T (a token picks an expert at most once), the clipped
+    excess spread over the unclipped experts in proportion to their share."""
+    rng = np.random.default_rng(seed)
+    rank = rng.permutation(E)  # rank[e] = Zipf rank (0 = hottest) of expert e
+    w = (rank + 1.0) ** (-s)
+    tgt = w / w.sum() * A
+    for _ in range(100):
+        over = tgt > T
+        if not over.any():
+            break
+        excess = (tgt[over] - T).sum()
+        tgt[over] = T
+        free = ~over & (tgt < T)
+        tgt[free] += excess * tgt[free] / tgt[free].sum()
+    return tgt
+
+
+def zipf_offsets(cfg) -> np.ndarray | None:
+    """Per-expert router logit offsets c_e that realise the Zipf load.
+
+    The offsets enter the inputs only: X[:, 0] = 1 and Wg[0, e] = c_e, so the
+    router's logit of expert e carries the extra term c_e.  They come from a
+    table that ``synth/calibrate_skew.py`` writes once (it iterates the
+    oracle's routing on seeded logits); ``None`` if the table lacks this shape.
+    """
+    path = os.path.join(_HERE, "skew_offsets.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    key = f"E{cfg['E']}_k{cfg['k']}_{cfg['score']}_{cfg['skew']}"
+    if key not in tab:
+        return None
+    return np.asarray(tab[key]["c"], dtype=np.float32)
+
+
+# --------------------------------------------------------------------------- numpy
+def _rng(seed: int, tensor_id: int) -> np.random.Generator:
+    return np.random.default_rng([int(seed), int(tensor_id)])
+
+
+def _normal_bf16(seed, tid, shape, std) -> np.ndarray:
+    x = _rng(seed, tid).standard_normal(size=shape, dtype=np.float32) * np.float32(std)
+    return bf16_bits_from_f32(x)
+
+
+def _distinct_rows(rng: np.random.Generator, n: int, E: int, k: int) -> np.ndarray:
+    """n rows of k distinct experts each, a uniform random k-subset per row in
+    random order: the first k of a random permutation (random sort keys)."""
+    out = np.empty((n, k), dtype=np.int32)
+    for r0 in range(0, n, 4096):
+        keys = rng.random((min(4096, n - r0), E))
+        out[r0:r0 + keys.shape[0]] = np.argsort(keys, axis=1, kind="stable")[:, :k]
+    return out
+
+
+def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
+    """Host (numpy) drawing of one workload.  bf16 tensors are uint16 bits."""
+    cfg = get_config(name_or_cfg, **overrides)
+    T, H, E, k, I = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["I"]
+    d = {"cfg": cfg}
+    X = _rng(seed, 1).standard_normal(size=(T, H), dtype=np.float32)
+    Wg = _rng(seed, 2).standard_normal(size=(H, E), dtype=np.float32) * np.float32(1.0 / math.sqrt(H))
+    c = zipf_offsets(cfg) if cfg.get("skew") else None
+    if c is not None and T > 0:
+        X[:, 0] = 1.0
+        Wg[0, :] = c
+    d["X"] = bf16_bits_from_f32(X)
+    d["Wg"] = bf16_bits_from_f32(Wg)
+    d["bias"] = (_rng(seed, 3).standard_normal(size=E, dtype=np.float32) * np.float32(0.1)
+                 if cfg["bias"] else None)
+    d["W1"] = _normal_bf16(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
+    d["W2"] = _normal_bf16(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
+    if cfg["shared"]:
+        d["Ws1"] = _normal_bf16(seed, 6, (H, 2 * I), 1.0 / math.sqrt(H))
+        d["Ws2"] = _normal_bf16(seed, 7, (I, H), 1.0 / math.sqrt(I))
+    else:
+        d["Ws1"] = d["Ws2"] = None
+    if cfg["routing"] == "given":
+        rng = _rng(seed, 8)
+        d["E_ids"] = _distinct_rows(rng, T, E, k)
+        z = _rng(seed, 9).standard_normal(size=(T, k))
+        z = np.exp(z - z.max(axis=1, keepdims=True))
+        d["G"] = (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+    if cfg["routing"] == "hash":
+        V = cfg["V"]
+        d["tid2eid"] = _distinct_rows(_rng(seed, 10), V, E, k)
+        d["token_ids"] = _rng(seed, 11).integers(0, V, size=T, dtype=np.int32)
+    return d
+
+
+# --------------------------------------------------------------------------- torch
+def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", **overrides) -> dict:
+    """Device (torch) drawing of one workload, for sizes too large for the host.
+
+    bf16 tensors are ``torch.bfloat16``; the conversion from the fp32 draw is
+    torch's round-to-nearest-even.  Large weights are drawn one expert at a
+    time so the fp32 temporary stays small.
+    """
+    import torch
+
+    cfg = get_config(name_or_cfg, **overrides)
+    T, H, E, k, I = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["I"]
+    dev = torch.device(device)
+
+    def gen(tid):
+        g = torch.Generator(device=dev)
+        g.manual_seed(int(seed) * 1000 + tid)
+        return g
+
+    def normal(tid, shape, std, per_slice=False):
+        g = gen(tid)
+        if per_slice:
+            out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+            for i in range(shape[0]):
+                out[i] = (torch.randn(shape[1:], generator=g, device=dev) * std).to(torch.bfloat16)
+            return out
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    d = {"cfg": cfg}
+    X = torch.randn((T, H), generator=gen(1), device=dev)
+    Wg = torch.randn((H, E), generator=gen(2), device=dev) * (1.0 / math.sqrt(H))
+    c = zipf_offsets(cfg) if cfg.get("skew") else None
+    if c is not None and T > 0:
+        X[:, 0] = 1.0
+        Wg[0, :] = torch.from_numpy(c).to(dev)
+    d["X"] = X.to(torch.bfloat16)
+    d["Wg"] = Wg.to(torch.bfloat16)
+    del X, Wg
+    d["bias"] = (torch.randn(E, generator=gen(3), device=dev) * 0.1).float() if cfg["bias"] else None
+    d["W1"] = normal(4, (E, H, 2 * I), 1.0 / math.sqrt(H), per_slice=True)
+    d["W2"] = normal(5, (E, I, H), 1.0 / math.sqrt(I), per_slice=True)
+    if cfg["shared"]:
+        d["Ws1"] = normal(6, (H, 2 * I), 1.0 / math.sqrt(H))
+        d["Ws2"] = normal(7, (I, H), 1.0 / math.sqrt(I))
+    else:
+        d["Ws1"] = d["Ws2"] = None
+    if cfg["routing"] == "given":
+        g = gen(8)
+        keys = torch.rand((T, E), generator=g, device=dev)
+        d["E_ids"] = keys.topk(k, dim=1).indices.to(torch.int32).contiguous()
+        z = torch.randn((T, k), generator=gen(9), device=dev)
+        d["G"] = torch.softmax(z, dim=1).float().contiguous()
+    if cfg["routing"] == "hash":
+        V = cfg["V"]
+        keys = torch.rand((V, E), generator=gen(10), device=dev)
+        d["tid2eid"] = keys.topk(k, dim=1).indices.to(torch.int32).contiguous()
+        d["token_ids"] = torch.randint(0, V, (T,), generator=gen(11), device=dev, dtype=torch.int32)
+    return d

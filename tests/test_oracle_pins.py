@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+closed forms, the pages' worked split example, brute-force loops on tiny
+inputs, reductions to a dense SwiGLU FFN and to library routines, and the
+invariants the pages state (k ids per token, sum of counts = T*k, the shared
+expert alone when every gate is zero)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _bits(x):
+    return synth.bf16_bits_from_f32(np.asarray(x, dtype=np.float32))
+
+
+# ------------------------------------------------------------------ bf16 numbers
+def test_round_to_bf16_ties_even():
+    one = 1.0
+    ulp = 2.0 ** -7  # bf16 keeps 7 fraction bits
+    cases = {one + ulp / 2: one,                    # tie, 1.0 is even
+             one + 1.5 * ulp: one + 2 * ulp,        # tie, rounds up to even
+             one + 0.49 * ulp: one,
+             one + 0.51 * ulp: one + ulp,
+             -(one + 1.5 * ulp): -(one + 2 * ulp)}
+    for x, want in cases.items():
+        assert oracle.round_to_bf16(np.array([x]))[0] == want
+
+
+def test_bf16_bits_match_torch_rounding():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(20000) * rng.choice([1e-3, 1, 1e3], 20000)).astype(np.float32)
+    ours = oracle.f64_to_bf16_bits(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    back = oracle.bf16_to_f64(ref)
+    assert np.array_equal(back, torch.from_numpy(x).to(torch.bfloat16).double().numpy())
+
+
+# ------------------------------------------------------------------ affinities and gates
+def test_affinity_closed_forms():
+    l = np.array([[math.log(3.0), -math.log(3.0), 0.0]])
+    np.testing.assert_allclose(oracle.affinity(l, oracle.SCORE_SIGMOID), [[0.75, 0.25, 0.5]], rtol=0, atol=1e-15)
+    # softplus(log(e^c - 1)) = c, so sqrt gives sqrt(c)
+    l = np.array([[math.log(math.e - 1.0), math.log(math.e ** 4 - 1.0), 0.0, -800.0, 800.0]])
+    np.testing.assert_allclose(oracle.affinity(l, oracle.SCORE_SQRT_SOFTPLUS),
+                               [[1.0, 2.0, math.sqrt(math.log(2.0)), 0.0, math.sqrt(800.0)]],
+                               rtol=1e-14, atol=1e-300)
+    l = np.array([[math.log(4.0), math.log(2.0), 0.0, 0.0]])
+    np.testing.assert_allclose(oracle.affinity(l, oracle.SCORE_SOFTMAX), [[0.5, 0.25, 0.125, 0.125]],
+                               rtol=1e-15)
+
+
+@pytest.mark.parametrize("score,logits,want_ids,want_g", [
+    (oracle.SCORE_SIGMOID, [-30.0, math.log(3.0), -30.0, -math.log(3.0)], [1, 3], [0.75, 0.25]),
+    (oracle.SCORE_SQRT_SOFTPLUS, [math.log(math.e - 1.0), -30.0, math.log(math.e ** 4 - 1.0), -30.0],
+     [2, 0], [2.0 / 3.0, 1.0 / 3.0]),
+])
+def test_renormalised_gates_closed_form(score, logits, want_ids, want_g):
+    alpha = 2.5
+    ids, G, _ = oracle.route_from_logits(np.array([logits]), None, score, 2, alpha, True)
+    assert ids.tolist() == [want_ids]
+    np.testing.assert_allclose(G[0], alpha * np.array(want_g), rtol=1e-12)
+    assert abs(G.sum() - alpha) < 1e-12
+
+
+def test_softmax_gate_closed_form():
+    logits = np.array([[0.0, math.log(2.0), 0.0, math.log(4.0)]])
+    ids, G, _ = oracle.route_from_logits(logits, None, oracle.SCORE_SOFTMAX, 2, 1.0, False)
+    assert ids.tolist() == [[3, 1]]
+    np.testing.assert_allclose(G[0], [0.5, 0.25], rtol=1e-15)
+
+
+def test_bias_changes_selection_not_weights():
+    # equal logits: every affinity is sigma(0) = 1/2, so the bias alone orders
+    # the experts and the renormalised gates are alpha / k each.
+    E, k, alpha = 7, 3, 2.5
+    bias = np.array([0.1, -0.2, 0.5, 0.0, 0.3, -0.1, 0.2])
+    ids, G, _ = oracle.route_from_logits(np.zeros((4, E)), bias, oracle.SCORE_SIGMOID, k, alpha, True)
+    assert ids.tolist() == [[2, 4, 6]] * 4
+    np.testing.assert_allclose(G, alpha / k, rtol=1e-15)
+
+
+def test_gate_sums_and_k_equals_E():
+    rng = np.random.default_rng(1)
+    l = rng.standard_normal((50, 9))
+    b = rng.standard_normal(9) * 0.1
+    for sf in (oracle.SCORE_SIGMOID, oracle.SCORE_SQRT_SOFTPLUS):
+        _, G, _ = oracle.route_from_logits(l, b, sf, 4, 2.5, True)
+        np.testing.assert_allclose(G.sum(1), 2.5, rtol=1e-13)
+        ids, G, a = oracle.route_from_logits(l, None, sf, 9, 1.0, True)
+        # k = E, alpha = 1: the gates are the affinities normalised over all experts
+        full = np.take_along_axis(a / a.sum(1, keepdims=True), ids.astype(np.int64), 1)
+        np.testing.assert_allclose(G, full, rtol=1e-13)
+        assert all(sorted(r) == list(range(9)) for r in ids.tolist())
+    _, G, _ = oracle.route_from_logits(l, None, oracle.SCORE_SOFTMAX, 4, 1.0, False)
+    assert (G.sum(1) <= 1.0 + 1e-15).all() and (G > 0).all()
+
+
+def test_topk_matches_python_sort_with_ties():
+    rng = np.random.default_rng(2)
+    s = rng.integers(0, 5, size=(200, 11)).astype(np.float64)  # many exact ties
+    ids = oracle.select_topk(s, 4)
+    for row, got in zip(s, ids):
+        want = sorted(range(11), key=lambda e: (-row[e], e))[:4]
+        assert got.tolist() == want
+
+
+def test_tie_goes_to_lower_id_through_the_router():
+    rng = np.random.default_rng(3)
+    H, E = 64, 6
+    X = _bits(rng.standard_normal((20, H)))
+    Wg = rng.standard_normal((H, E)) / 8
+    Wg[:, 4] = Wg[:, 1]  # experts 1 and 4 always have the same logit
+    bias = np.zeros(E)
+    bias[[1, 4]] = 1.0   # ... and the same, winning, selection score
+    ids, _, l = oracle.route(X, _bits(Wg), bias, oracle.SCORE_SIGMOID, 3, 1.0, True)
+    assert np.array_equal(l[:, 1], l[:, 4])
+    assert (ids[:, 0] == 1).all() and (ids[:, 1] == 4).all()
+    ids, G, _ = oracle.route(X, _bits(Wg), bias, oracle.SCORE_SIGMOID, 1, 1.0, True)
+    assert (ids[:, 0] == 1).all() and np.allclose(G, 1.0)
+
+
+def test_route_bruteforce_tiny():
+    rng = np.random.default_rng(4)
+    T, H, E, k, alpha = 5, 8, 6, 3, 2.5
+    X = _bits(rng.standard_normal((T, H)))
+    Wg = _bits(rng.standard_normal((H, E)) / 3)
+    bias = rng.standard_normal(E) * 0.1
+    xf = synth.f32_from_bf16_bits(X).astype(float).tolist()
+    wf = synth.f32_from_bf16_bits(Wg).astype(float).tolist()
+    for sf in (oracle.SCORE_SIGMOID, oracle.SCORE_SQRT_SOFTPLUS):
+        ids, G, _ = oracle.route(X, Wg, bias, sf, k, alpha, True)
+        for t in range(T):
+            logit = [sum(xf[t][h] * wf[h][e] for h in range(H)) for e in range(E)]
+            if sf == oracle.SCORE_SIGMOID:
+                a = [1.0 / (1.0 + math.exp(-v)) for v in logit]
+            else:
+                a = [math.sqrt(math.log(1.0 + math.exp(v))) for v in logit]
+            order = sorted(range(E), key=lambda e: (-(a[e] + bias[e]), e))[:k]
+            assert ids[t].tolist() == order
+            tot = sum(a[e] for e in order)
+            np.testing.assert_allclose(G[t], [alpha * a[e] / tot for e in order], rtol=1e-12)
+
+
+def test_hash_route_uses_table_rows():
+    d = synth.make_inputs("c4s")
+    c = d["cfg"]
+    ids, G, l = oracle.route_hash(d["X"], d["Wg"], d["token_ids"], d["tid2eid"],
+                                  c["score_fn"], c["alpha"], c["renorm"])
+    assert np.array_equal(ids, d["tid2eid"][d["token_ids"]])
+    np.testing.assert_allclose(G.sum(1), c["alpha"], rtol=1e-13)
+    # same gate formula as the top-k router at those ids
+    a = oracle.affinity(l, c["score_fn"])
+    np.testing.assert_allclose(G, oracle.gates(a, ids, c["alpha"], True), rtol=0)
+
+
+# ------------------------------------------------------------------ dispatch
+def test_split_worked_example(golden_dir):
+    ex = json.load(open(os.path.join(golden_dir, "megatron_split_example.json")))
+    L = ex["experts_per_rank"]
+    toks = ex["tokens"]
+    E = 2 * L
+    send = {}
+    for r in ("0", "1"):
+        E_ids = np.array([v["experts"] for v in toks.values() if str(v["rank"]) == r], dtype=np.int32)
+        counts, offsets, perm, inv = oracle.dispatch(E_ids, E)
+        assert counts.sum() == ex["assignments_per_rank"]
+        # input_splits[j] = sum of count[e] over the experts that rank j holds
+        send[r] = [int(counts[j * L:(j + 1) * L].sum()) for j in range(2)]
+        assert send[r] == ex["send_rows"][r]
+    for dst in ("0", "1"):
+        out = [send[src][int(dst)] for src in ("0", "1")]
+        assert out == ex["output_splits"][dst]
+        assert sum(out) == ex["received_rows"][dst]
+    # all four tokens on one device: counts and the expert blocks
+    E_ids = np.array([v["experts"] for v in toks.values()], dtype=np.int32)
+    counts, offsets, perm, inv = oracle.dispatch(E_ids, E)
+    assert counts.tolist() == [2, 1, 3, 2] and offsets.tolist() == [0, 2, 3, 6, 8]
+    # a = token 0, b = 1, c = 2, d = 3; flat index = token * 2 + slot
+    assert perm.tolist() == [0, 4, 2, 1, 3, 6, 5, 7]
+
+
+def test_dispatch_invariants():
+    d = synth.make_inputs("c3s")
+    c = d["cfg"]
+    ids, _, _ = oracle.route(d["X"], d["Wg"], d["bias"], c["score_fn"], c["k"], c["alpha"], True)
+    T, k, E = c["T"], c["k"], c["E"]
+    assert all(len(set(r)) == k for r in ids.tolist())  # |I_t| = k
+    counts, offsets, perm, inv = oracle.dispatch(ids, E)
+    assert counts.sum() == T * k
+    assert sorted(perm.tolist()) == list(range(T * k))
+    flat = ids.reshape(-1)
+    for e in range(E):
+        blk = perm[offsets[e]:offsets[e + 1]]
+        assert (flat[blk] == e).all() and (np.diff(blk) > 0).all()
+    assert (perm[inv] == np.arange(T * k)).all()
+
+
+def test_dispatch_drops_out_of_range_ids():
+    E_ids = np.array([[0, 5], [-1, 2], [2, 1]], dtype=np.int32)
+    counts, offsets, perm, inv = oracle.dispatch(E_ids, 3)
+    assert counts.tolist() == [1, 1, 2]
+    assert perm.tolist() == [0, 5, 3, 4]
+    assert inv.tolist() == [0, -1, -1, 2, 3, 1]
+
+
+# ------------------------------------------------------------------ FFN and combine
+def _tiny_layer(rng, T=4, H=8, E=3, k=2, I=4, shared=True):
+    X = _bits(rng.standard_normal((T, H)))
+    W1 = _bits(rng.standard_normal((E, H, 2 * I)) / 3)
+    W2 = _bits(rng.standard_normal((E, I, H)) / 2)
+    Ws1 = _bits(rng.standard_normal((H, 2 * I)) / 3) if shared else None
+    Ws2 = _bits(rng.standard_normal((I, H)) / 2) if shared else None
+    E_ids = np.array([rng.choice(E, size=k, replace=False) for _ in range(T)], dtype=np.int32)
+    G = rng.random((T, k))
+    return X, E_ids, G, W1, W2, Ws1, Ws2
+
+
+def _ffn_loops(x, w1, w2):
+    """F(x) = (SiLU(x W_gate) * x W_up) W_down with explicit loops."""
+    H, twoI = len(w1), len(w1[0])
+    I = twoI // 2
+    h = [sum(x[r] * w1[r][c] for r in range(H)) for c in range(twoI)]
+    act = [h[c] / (1.0 + math.exp(-h[c])) * h[I + c] for c in range(I)]
+    return [sum(act[c] * w2[c][o] for c in range(I)) for o in range(len(w2[0]))]
+
+
+def test_forward_bruteforce_tiny():
+    rng = np.random.default_rng(6)
+    X, E_ids, G, W1, W2, Ws1, Ws2 = _tiny_layer(rng)
+    Y, _ = oracle.forward(X, E_ids, G, W1, W2, Ws1, Ws2)
+    f = lambda b: synth.f32_from_bf16_bits(b).astype(float).tolist()  # noqa: E731
+    x, w1, w2, s1, s2 = f(X), f(W1), f(W2), f(Ws1), f(Ws2)
+    for t in range(X.shape[0]):
+        want = _ffn_loops(x[t], s1, s2)
+        for j in range(E_ids.shape[1]):
+            ye = _ffn_loops(x[t], w1[E_ids[t, j]], w2[E_ids[t, j]])
+            want = [a + G[t, j] * b for a, b in zip(want, ye)]
+        np.testing.assert_allclose(Y[t], want, rtol=1e-12, atol=1e-12)
+
+
+def _dense_ffn(X64, W1_64, W2_64):
+    """Dense SwiGLU FFN with SiLU written through tanh: z*sigma(z) = z*(1+tanh(z/2))/2."""
+    I = W2_64.shape[0]
+    g = np.einsum("th,hi->ti", X64, W1_64[:, :I])
+    u = np.einsum("th,hi->ti", X64, W1_64[:, I:])
+    return np.einsum("ti,ih->th", g * (1.0 + np.tanh(g / 2.0)) / 2.0 * u, W2_64)
+
+
+def test_single_expert_reduces_to_dense_ffn():
+    rng = np.random.default_rng(7)
+    X, _, _, W1, W2, _, _ = _tiny_layer(rng, T=9, H=16, E=1, k=1, I=8, shared=False)
+    Y, _ = oracle.forward(X, np.zeros((9, 1), np.int32), np.ones((9, 1)), W1, W2)
+    ref = _dense_ffn(oracle.bf16_to_f64(X), oracle.bf16_to_f64(W1[0]), oracle.bf16_to_f64(W2[0]))
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_zero_gates_leave_the_shared_expert():
+    rng = np.random.default_rng(8)
+    X, E_ids, G, W1, W2, Ws1, Ws2 = _tiny_layer(rng, T=6, H=16, E=4, k=2, I=8)
+    Y, _ = oracle.forward(X, E_ids, np.zeros_like(G), W1, W2, Ws1, Ws2)
+    ref = _dense_ffn(oracle.bf16_to_f64(X), oracle.bf16_to_f64(Ws1), oracle.bf16_to_f64(Ws2))
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-13)
+    Y0, _ = oracle.forward(X, E_ids, np.zeros_like(G), W1, W2)
+    assert (Y0 == 0).all()
+
+
+def test_gates_act_linearly_and_identical_experts():
+    rng = np.random.default_rng(9)
+    X, E_ids, G, W1, W2, Ws1, Ws2 = _tiny_layer(rng, T=6, H=16, E=4, k=3, I=8)
+    S = _dense_ffn(oracle.bf16_to_f64(X), oracle.bf16_to_f64(Ws1), oracle.bf16_to_f64(Ws2))
+    Y1, _ = oracle.forward(X, E_ids, G, W1, W2, Ws1, Ws2)
+    Y3, _ = oracle.forward(X, E_ids, 3.0 * G, W1, W2, Ws1, Ws2)
+    np.testing.assert_allclose(Y3 - S, 3.0 * (Y1 - S), rtol=1e-11, atol=1e-12)
+    # identical experts and gates summing to one give F(x) + F_s(x)
+    W1s = np.repeat(W1[:1], 4, axis=0)
+    W2s = np.repeat(W2[:1], 4, axis=0)
+    Gn = G / G.sum(1, keepdims=True)
+    Y, _ = oracle.forward(X, E_ids, Gn, W1s, W2s, Ws1, Ws2)
+    F = _dense_ffn(oracle.bf16_to_f64(X), oracle.bf16_to_f64(W1[0]), oracle.bf16_to_f64(W2[0]))
+    np.testing.assert_allclose(Y, F + S, rtol=1e-11, atol=1e-12)
+
+
+def test_probability_before_linear2_equals_weighting_in_combine():
+    # the page's fused placement of the gate: g * SwiGLU(.) then Linear2
+    rng = np.random.default_rng(10)
+    X, E_ids, G, W1, W2, _, _ = _tiny_layer(rng, T=5, H=16, E=3, k=2, I=8, shared=False)
+    Y, _ = oracle.forward(X, E_ids, G, W1, W2)
+    x = oracle.bf16_to_f64(X)
+    want = np.zeros_like(Y)
+    for t in range(5):
+        for j in range(2):
+            e = E_ids[t, j]
+            w1 = oracle.bf16_to_f64(W1[e])
+            h = x[t] @ w1
+            act = G[t, j] * (h[:8] / (1 + np.exp(-h[:8])) * h[8:])
+            want[t] += act @ oracle.bf16_to_f64(W2[e])
+    np.testing.assert_allclose(Y, want, rtol=1e-12, atol=1e-13)
+
+
+def test_forward_tokens_subset_matches_whole_layer():
+    d = synth.make_inputs("c2s")
+    Y, _ = oracle.forward(d["X"], d["E_ids"], d["G"], d["W1"], d["W2"])
+    rows = np.array([0, 17, 100, 332])
+    Ys = oracle.forward_tokens(rows, d["X"][rows], d["E_ids"][rows], d["G"][rows],
+                               lambda e: d["W1"][e], lambda e: d["W2"][e], E=d["cfg"]["E"])
+    np.testing.assert_allclose(Ys, Y[rows], rtol=1e-12, atol=1e-13)
