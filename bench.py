@@ -1,0 +1,446 @@
+"""Throughput of the routed MoE FFN layer forward on GB300.
+
+One step = one pass of the whole layer over one batch of synthetic tokens:
+router (gating GEMM, scores, biased top-k, gates), dispatch (counts, scan,
+permutation, row gather), Linear1 + SwiGLU, Linear2 (routed experts and the
+shared expert), gate-weighted combine.  Default workload: the V4-Pro-shaped
+layer (T=4096, H=7168, E=384, top-6, I=2048, one shared expert, sigmoid
+affinity with selection bias, alpha = 2.5, Zipf(1.1) expert load), the only
+one of the pages' workloads that runs every step of the path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3]
+    python bench.py --impl reference ...   # the CPU oracle on this host's cores
+
+Under torchrun each rank runs its own batch (weak scaling, no collective in
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s @1 GB300; grouped-GEMM TFLOP/s and % of bf16 peak"
+UNIT = "tokens/s"
+
+WORKLOAD_TEXT = {
+    "c1": "tiny layer T=128 H=256 E=8 top-2 I=128, sigmoid routing",
+    "c2": "given-routing layer T=4096 H=4096 E=32 top-8 I=1536 (E, G inputs)",
+    "c3": "V4-Pro-shaped layer T=4096 H=7168 E=384 top-6 I=2048 +1 shared, sigmoid+bias, alpha 2.5, Zipf(1.1) load",
+    "c4": "hash-routed layer, V4-Pro shapes, tid2eid[128000, 6]",
+    "c5": "large-FFN layer T=16384 H=8192 E=64 top-2 I=22016, softmax gates",
+    "c3_sp": "V4-Pro-shaped layer with the pages' sqrt-softplus affinity",
+    "c3p": "V4-Pro expert shapes, T=512 E=48 (profiling size)",
+}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 50 ms while running; summary of the samples
+    taken between mark_start() and mark_end()."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows, self.t0, self.t1 = [], None, None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def summary(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not found"}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [r for t, r in self.rows if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        rows = inside if inside else [r for _, r in self.rows]
+        if not rows:
+            return {"unavailable": "no samples"}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ our arm
+def build_step(moe, dd, p, ws, stage_events=None):
+    c = dd["cfg"]
+    routed = c["routing"] != "given"
+    E_ids = dd["E_ids"] if not routed else dd["_E_ids"]
+    G = dd["G"] if not routed else dd["_G"]
+
+    def step(X=None, Y=None, route_events=None):
+        X = dd["X"] if X is None else X
+        Y = dd["_Y"] if Y is None else Y
+        if routed:
+            if route_events:
+                route_events[0].record()
+            if c["routing"] == "hash":
+                moe.moe_route(p, X, dd["Wg"], None, dd["token_ids"], dd["tid2eid"], c["V"], E_ids, G, ws)
+            else:
+                moe.moe_route(p, X, dd["Wg"], dd["bias"], None, None, 0, E_ids, G, ws)
+            if route_events:
+                route_events[1].record()
+        if stage_events is not None:
+            moe.moe_forward_timed(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws,
+                                  stage_events)
+        else:
+            moe.moe_forward(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws)
+    return step
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mixture_experts_ffn_route_gb300 as moe
+    from mixture_experts_ffn_route_gb300 import accounting
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    moe.lib()
+    # one model (weights, seed 1234) on every rank; each rank its own token batch
+    dd = synth.make_inputs_torch(args.workload, seed=1234, token_seed=1234 + rank, device=dev)
+    c = dd["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    has_shared = c["shared"]
+    p = moe.params_from_config(c)
+    ws = moe.alloc_workspace(p, dev)
+    dd["_E_ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+    dd["_G"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+    dd["_Y"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    routed = c["routing"] != "given"
+
+    # events must exist before their handles go to the library
+    K = args.steps
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    rt_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for evs in st_ev + rt_ev:
+        for ev in evs:
+            ev.record()
+    plain_step = build_step(moe, dd, p, ws)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+
+    for _ in range(args.warmup):
+        plain_step()
+    moe.moe_sync_status(ws)
+
+    E_now = dd["_E_ids"] if routed else dd["E_ids"]
+    counts = torch.bincount(E_now.reshape(-1).long(), minlength=E).cpu().numpy()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        build_step(moe, dd, p, ws, stage_events=st_ev[i])(route_events=rt_ev[i] if routed else None)
+    t_end.record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    moe.moe_sync_status(ws)
+    ms = t_start.elapsed_time(t_end) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+
+    def avg(evs, a, b):
+        return sum(e[a].elapsed_time(e[b]) for e in evs) / len(evs)
+    stages = {"dispatch": avg(st_ev, 0, 1), "gemm1_swiglu": avg(st_ev, 1, 2),
+              "gemm2": avg(st_ev, 2, 3), "combine": avg(st_ev, 3, 4)}
+    if routed:
+        stages = {"route": avg(rt_ev, 0, 1), **stages}
+
+    # ---- end to end through the C ABI with host buffers (pinned) each step
+    X_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    X_host.copy_(dd["X"])
+    Y_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    X_dev = torch.empty_like(dd["X"])
+    extra = []
+    if c["routing"] == "given":
+        extra = [(dd["E_ids"], dd["E_ids"].cpu().pin_memory()), (dd["G"], dd["G"].cpu().pin_memory())]
+    elif c["routing"] == "hash":
+        extra = [(dd["token_ids"], dd["token_ids"].cpu().pin_memory())]
+    h2d = X_host.numel() * 2 + sum(h.numel() * h.element_size() for _, h in extra)
+    d2h = Y_host.numel() * 2
+    step = build_step(moe, dd, p, ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        X_dev.copy_(X_host, non_blocking=True)
+        for d_t, h_t in extra:
+            d_t.copy_(h_t, non_blocking=True)
+        step(X=X_dev)
+        Y_host.copy_(dd["_Y"], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    moe.moe_sync_status(ws)
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+    pk = peaks()
+    g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
+    g1_flops = accounting.gemm1_flops(counts, H, I, has_shared, T)
+    g2_flops = accounting.gemm2_flops(counts, H, I, has_shared, T)
+    g1_s = stages["gemm1_swiglu"] / 1e3
+    g2_s = stages["gemm2"] / 1e3
+    gemm_tflops = (g1_flops + g2_flops) / (g1_s + g2_s) / 1e12
+    # the dominant kernel: Linear1 + SwiGLU.  Weight streaming bounds it when the
+    # arithmetic intensity is below the ridge point.
+    ai = g1_flops / g1_bytes
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if ai < ridge:
+        achieved = g1_bytes / g1_s / 1e9
+        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<256,1>)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                "algorithmic_bytes_per_launch": int(g1_bytes),
+                "peak_source": pk["source"] + " hbm_gbs"}
+    else:
+        achieved = g1_flops / g1_s / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<256,1>)", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "algorithmic_flops_per_launch": int(g1_flops),
+                "peak_source": pk["source"] + " bf16_tflops_sustained"}
+    traffic = load_traffic(args.workload)
+    if traffic is not None:
+        roof["traffic"] = traffic
+    launches_per_step = (2 if routed else 0) + 7
+    out = {
+        "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the workload's shapes)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
+                   "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": has_shared,
+                   "routing": c["routing"], "score": c["score"],
+                   "l2": "inputs larger than L2: %.1f GB of expert weights per step"
+                         % ((E + has_shared) * 3 * H * I * 2 / 1e9),
+                   "parallelism": f"replicas x{world} (token batches, no collective)"},
+        "stages_ms": {k_: round(v, 4) for k_, v in stages.items()},
+        "grouped_gemm": {"tflops": round(gemm_tflops, 1),
+                         "pct_bf16_peak": round(100 * gemm_tflops / pk["bf16_tflops_sustained"], 2),
+                         "peak_tflops": pk["bf16_tflops_sustained"],
+                         "gemm1_GBps": round(g1_bytes / g1_s / 1e9, 1),
+                         "gemm2_GBps": round(accounting.gemm2_bytes(counts, H, I, has_shared, T) / g2_s / 1e9, 1)},
+        "roofline": roof,
+        "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": sampler.summary() if sampler else None,
+        "load": {"max_expert_rows": int(counts.max()), "min_expert_rows": int(counts.min()),
+                 "active_experts": int((counts > 0).sum())},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(dd, budget_s=args.cpu_budget)
+    return out
+
+
+def load_traffic(workload):
+    """dram bytes per GEMM1 launch from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", f"gemm1_swiglu_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f).get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+class OracleRunner:
+    """The CPU oracle, as it stands, over successive token slices of the
+    workload.  Inputs come from the same seeded device drawing; expert weights
+    are fetched to the host one expert at a time when a slice needs them."""
+
+    def __init__(self, dd):
+        import torch
+        self.torch = torch
+        self.dd = dd
+        c = dd["cfg"]
+        self.c = c
+        bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+        self.bits = bits
+        self.X = bits(dd["X"])
+        self.Wg = bits(dd["Wg"])
+        self.bias = dd["bias"].cpu().numpy() if dd["bias"] is not None else None
+        self.Ws1 = bits(dd["Ws1"]) if dd["Ws1"] is not None else None
+        self.Ws2 = bits(dd["Ws2"]) if dd["Ws2"] is not None else None
+        if c["routing"] == "given":
+            self.E_ids = dd["E_ids"].cpu().numpy()
+            self.G = dd["G"].cpu().numpy().astype(np.float64)
+        if c["routing"] == "hash":
+            self.tok = dd["token_ids"].cpu().numpy()
+            self.tab = dd["tid2eid"].cpu().numpy()
+        self.pos = 0
+
+    def run(self, n):
+        import oracle
+        c = self.c
+        T = c["T"]
+        rows = (np.arange(n) + self.pos) % T
+        self.pos = (self.pos + n) % T
+        X = self.X[rows]
+        if c["routing"] == "given":
+            ids, G = self.E_ids[rows], self.G[rows]
+        elif c["routing"] == "hash":
+            ids, G, _ = oracle.route_hash(X, self.Wg, self.tok[rows], self.tab, c["score_fn"],
+                                          c["alpha"], c["renorm"])
+        else:
+            ids, G, _ = oracle.route(X, self.Wg, self.bias, c["score_fn"], c["k"], c["alpha"], c["renorm"])
+        W1 = lambda e: self.bits(self.dd["W1"][e])  # noqa: E731
+        W2 = lambda e: self.bits(self.dd["W2"][e])  # noqa: E731
+        Y = oracle.forward_tokens(rows, X, ids, G, W1, W2, self.Ws1, self.Ws2, E=c["E"])
+        oracle.f64_to_bf16_bits(Y)
+        return n
+
+
+def _threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [i.get("num_threads") for i in info if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(dd, budget_s=15.0, tokens_per_slice=2):
+    r = OracleRunner(dd)
+    r.run(1)  # first-call costs (BLAS thread start-up) stay outside the timing
+    t0 = time.time()
+    done = 0
+    while time.time() - t0 < budget_s:
+        done += r.run(tokens_per_slice)
+    dt = time.time() - t0
+    return {"value": round(done / dt, 4), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+            "sample": f"{done} tokens of the workload in slices of {tokens_per_slice} "
+                      f"(route, dispatch, fp64 SwiGLU FFN of every expert a slice touches, "
+                      f"combine), {dt:.1f} s of host time"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    import torch
+    import synth
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    dd = synth.make_inputs_torch(args.workload, seed=1234, device=dev)
+    r = OracleRunner(dd)
+    n = args.ref_tokens
+    for _ in range(args.warmup):
+        r.run(n)
+    t0 = time.time()
+    for _ in range(args.steps):
+        r.run(n)
+    dt = (time.time() - t0) / args.steps
+    v = n / dt
+    sample = (f"each step: {n} tokens of the {args.workload} workload (route, dispatch, fp64 "
+              f"SwiGLU FFN of every expert they touch, combine)")
+    return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}"},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": _threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * moe_ffn.h - C ABI of a single-GPU (sm_103a) forward pass of a routed
+ * Mixture-of-Experts FFN layer.
+ *
+ * The layer computes, for every token t with hidden row x_t,
+ *
+ *     y_t = F_s(x_t) + sum_{e in I_t} g_{t,e} F_e(x_t),   |I_t| = k,
+ *     F(x) = (SiLU(x W1[:, :I]) * x W1[:, I:]) W2,
+ *
+ * the MoE output equation of "Megatron-LM 的 MoE 并行：以 DeepSeek-V4 为例"
+ * (section 模型与入口) with the expert FFN, dispatch and combine of the
+ * "mega_moe" operator page (section 计算公式: EP Dispatch, Expert Compute,
+ * Token Combine).  I_t and g come from the router of the same Megatron page
+ * (section 路由与负载 / 路由张量) or from a token-id hash table (section
+ * 路由与负载 / Hash 路由).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates: scratch space is the caller's workspace, sized
+ *     by moe_workspace_size() and prepared once by moe_workspace_init().
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major, dense.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Host-checkable errors are returned before anything is
+ *     launched.  Data errors found on the device (an expert id outside
+ *     [0, E), a token id outside [0, V), a pipeline wait that timed out) are
+ *     recorded in the workspace's status word; the offending assignment is
+ *     skipped and moe_sync_status() reports the error.
+ *   - Device pointers must be 16-byte aligned.  H and I must be multiples of
+ *     64; for the router, E must be a multiple of 8.
+ *   - One workspace serves one stream at a time: calls that overlap on the
+ *     GPU and share a workspace race.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer    */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement      */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required    */
+  MOE_ERR_BAD_EXPERT_ID = 4, /* device: an expert id outside [0, E)           */
+  MOE_ERR_BAD_TOKEN_ID = 5,  /* device: a hash token id outside [0, V)        */
+  MOE_ERR_TIMEOUT = 6,       /* device: a pipeline wait ran out of time       */
+  MOE_ERR_CUDA = 7           /* a CUDA runtime call failed                    */
+} moe_status;
+
+/* Affinity a = score(l) of a router logit l. */
+typedef enum moe_score_fn {
+  MOE_SCORE_SIGMOID = 0,       /* a = 1 / (1 + exp(-l))                            */
+  MOE_SCORE_SQRT_SOFTPLUS = 1, /* a = sqrt(log(1 + exp(l))): the DeepSeek-V4 rule
+                                  of the Megatron page, section 路由张量          */
+  MOE_SCORE_SOFTMAX = 2        /* a = softmax over experts: the gate of
+                                  "Megatron 分布式训练全维度并行技术文档", 4.2    */
+} moe_score_fn;
+
+typedef struct moe_params {
+  int32_t T;          /* tokens (rows of X); 0 is allowed and does nothing     */
+  int32_t H;          /* hidden size, multiple of 64                          */
+  int32_t E;          /* routed experts, 1..4096                               */
+  int32_t k;          /* experts per token, 1..min(E, 16)                      */
+  int32_t I;          /* expert intermediate size, multiple of 64             */
+  int32_t has_shared; /* 1: add one shared expert (Ws1, Ws2) with weight 1    */
+  int32_t score_fn;   /* moe_score_fn                                          */
+  float alpha;        /* gate scale                                            */
+  int32_t renorm;     /* 1: g = alpha * a / sum_{selected} a;  0: g = alpha * a */
+} moe_params;
+
+/* Bytes of workspace the calls below need for these parameters. */
+size_t moe_workspace_size(const moe_params* p);
+
+/* Zero the workspace's status header.  Call once before the first use of a
+ * workspace (and it may be called again at any time between calls). */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Router (Megatron page, section 路由与负载 / 路由张量; softmax gate of the
+ * parallelism page, section 4.2):
+ *   l = X Wg;  a = score_fn(l);  I_t = TopK_k(a + bias), listed by descending
+ *   selection score, equal scores to the lower expert id;  G[t, j] = alpha *
+ *   a[t, E_ids[t, j]] / sum_j a[t, E_ids[t, j]] (renorm = 1) or alpha * a.
+ * The softmax rule selects on a alone and takes no bias.
+ * Hash routing (section 路由与负载 / Hash 路由): when token_ids != NULL the ids
+ * are E_ids[t, :] = tid2eid[token_ids[t], :] (table order) and the gates use
+ * the same formula at those ids; bias must then be NULL.
+ *   X        [T, H]  bf16      token rows
+ *   Wg       [H, E]  bf16      gating linear (row-major: E contiguous)
+ *   bias     [E]     fp32      selection-only expert bias, or NULL
+ *   token_ids[T]     int32     hash mode only, else NULL
+ *   tid2eid  [V, k]  int32     hash mode only, else NULL
+ *   E_ids    [T, k]  int32     out
+ *   G        [T, k]  fp32      out
+ * A token whose top-k selection is too close to call in float32 is re-decided
+ * with float64 logits, so the ids equal those of an exact evaluation except at
+ * exact ties. */
+moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                     const float* bias, const int32_t* token_ids, const int32_t* tid2eid,
+                     int32_t V, int32_t* E_ids, float* G, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* The router's float32 logits alone, l = X Wg, into logits [T, E] fp32. */
+moe_status moe_route_logits(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                            float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch ("mega_moe" page, section EP Dispatch; Megatron page, section
+ * AlltoAll 的前向 / 计数与重排):
+ *   counts [E]      int32 out   assignments per expert (ids outside [0,E) dropped)
+ *   offsets[E + 1]  int32 out   exclusive prefix sum of counts
+ *   perm   [T * k]  int32 out   perm[p] = flat assignment index t*k + j at expert
+ *                               block row p, ascending inside each block; entries
+ *                               past offsets[E] are left untouched. */
+moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Layer forward ("mega_moe" page, section 计算公式, plus the shared expert of
+ * the Megatron page's MoE output equation):
+ *   X    [T, H]      bf16   token rows
+ *   E_ids[T, k]      int32  expert ids (from moe_route or the caller)
+ *   G    [T, k]      fp32   gates
+ *   W1   [E, H, 2I]  bf16   Linear1; columns [0, I) gate, [I, 2I) up
+ *   W2   [E, I, H]   bf16   Linear2
+ *   Ws1  [H, 2I], Ws2 [I, H]  bf16 shared expert (has_shared = 1), else NULL
+ *   Y    [T, H]      bf16   out; float32 accumulation, one rounding
+ * Every step (dispatch, Linear1 with SwiGLU, Linear2, combine) runs in this
+ * library's kernels, with no host synchronisation. */
+moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                       const float* G, const uint16_t* W1, const uint16_t* W2,
+                       const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* moe_forward, recording caller-created CUDA events (cudaEvent_t, NULL entries
+ * skipped) on `stream` at the stage boundaries, for measurement:
+ *   stage_events[0] before dispatch      [1] after dispatch and row gather
+ *   stage_events[2] after Linear1+SwiGLU [3] after Linear2   [4] after combine
+ * stage_events itself may be NULL (then this is moe_forward). */
+moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                             const float* G, const uint16_t* W1, const uint16_t* W2,
+                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                             size_t ws_bytes, void* stream, void* const* stage_events);
+
+/* Synchronise `stream`, read the workspace's device status word, clear it and
+ * return the most serious error recorded since the last call, in the order
+ * TIMEOUT, BAD_TOKEN_ID, BAD_EXPERT_ID (MOE_OK if none).  A bad hash token
+ * gives its token ids -1 and gates 0; moe_forward then drops those
+ * assignments and records BAD_EXPERT_ID as well. */
+moe_status moe_sync_status(void* ws, size_t ws_bytes, void* stream);
+
+/* Self-test of the device-side wait limit: launches one kernel that waits on
+ * an mbarrier nothing arrives on.  The wait gives up after limit_us
+ * microseconds (1..1000000) and records MOE_ERR_TIMEOUT in the workspace
+ * status word, which moe_sync_status() then returns.  The GPU context stays
+ * usable.  The same bounded wait guards every pipeline wait of the GEMMs. */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

@@ -1,0 +1,84 @@
+"""Algorithmic work of one layer forward: flops and HBM bytes per kernel.
+
+These are the roofline numerators (no padding rows, no re-reads): a weight
+matrix of an expert that receives at least one row is read once, activations
+are read and written once.  Sizes: T tokens, H hidden, E experts, k top-k,
+I intermediate, A = T*k assignments, n_e rows of expert e.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16 = 2
+F32 = 4
+I32 = 4
+
+
+def _counts(counts, has_shared, T):
+    c = np.asarray(counts, dtype=np.int64)
+    n_active = int((c > 0).sum()) + (1 if has_shared and T > 0 else 0)
+    rows = int(c.sum()) + (T if has_shared else 0)
+    return rows, n_active
+
+
+def gemm1_flops(counts, H, I, has_shared=0, T=0):
+    rows, _ = _counts(counts, has_shared, T)
+    return 2 * rows * H * (2 * I)
+
+
+def gemm2_flops(counts, H, I, has_shared=0, T=0):
+    rows, _ = _counts(counts, has_shared, T)
+    return 2 * rows * I * H
+
+
+def router_flops(T, H, E):
+    return 2 * T * H * E
+
+
+def gemm1_bytes(counts, H, I, has_shared=0, T=0):
+    """W1 of every active expert (H x 2I), its input rows (H) and Act rows (I)."""
+    rows, n_active = _counts(counts, has_shared, T)
+    return n_active * H * 2 * I * BF16 + rows * H * BF16 + rows * I * BF16
+
+
+def gemm2_bytes(counts, H, I, has_shared=0, T=0):
+    """W2 of every active expert (I x H), Act rows in, expert output rows out."""
+    rows, n_active = _counts(counts, has_shared, T)
+    return n_active * I * H * BF16 + rows * I * BF16 + rows * H * BF16
+
+
+def dispatch_bytes(T, H, k):
+    """Expert ids in; token rows read once; T*k permuted rows written; perm/inv."""
+    A = T * k
+    return A * I32 + T * H * BF16 + A * H * BF16 + 2 * A * I32
+
+
+def dispatch_payload_bytes(T, H, k):
+    """The permuted activation block alone, T*k rows of H bf16 values."""
+    return T * k * H * BF16
+
+
+def combine_bytes(T, H, k, has_shared=0):
+    """k expert rows (+ the shared row) in, gates and row ids in, one row out."""
+    return (T * k + (T if has_shared else 0)) * H * BF16 + T * k * (F32 + I32) + T * H * BF16
+
+
+def route_bytes(T, H, E, k):
+    """X and Wg in, fp32 logits out and back in, ids and gates out."""
+    return T * H * BF16 + H * E * BF16 + 2 * T * E * F32 + T * k * (I32 + F32)
+
+
+def expert_params(h, f):
+    """Parameters of one SwiGLU expert: gate, up and down projections, 3*h*f."""
+    return 3 * h * f
+
+
+def layer_flops(counts, T, H, E, I, has_shared=0, with_router=True):
+    f = gemm1_flops(counts, H, I, has_shared, T) + gemm2_flops(counts, H, I, has_shared, T)
+    return f + (router_flops(T, H, E) if with_router else 0)
+
+
+def layer_bytes(counts, T, H, E, k, I, has_shared=0, with_router=True):
+    b = (dispatch_bytes(T, H, k) + gemm1_bytes(counts, H, I, has_shared, T)
+         + gemm2_bytes(counts, H, I, has_shared, T) + combine_bytes(T, H, k, has_shared))
+    return b + (route_bytes(T, H, E, k) if with_router else 0)

@@ -1,0 +1,356 @@
+// C ABI of the routed MoE FFN forward pass (declared in include/moe_ffn.h):
+// argument validation, workspace layout and the launch sequence.
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "moe_common.cuh"
+#include "moe_ffn.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+int num_sms() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout (byte offsets, each 256-aligned).
+struct WsLayout {
+  size_t status, logits, chunk_cnt, counts, row_off, tile_off, perm, inv, xp, act, yp, total;
+};
+
+static WsLayout layout(const moe_params& p) {
+  WsLayout L;
+  const size_t T = static_cast<size_t>(p.T), E = static_cast<size_t>(p.E);
+  const size_t A = T * static_cast<size_t>(p.k);
+  const size_t Tsh = p.has_shared ? T : 0;
+  const size_t nchunk = static_cast<size_t>(dispatch_chunks(static_cast<int>(A)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(256);
+  L.logits = take(T * E * sizeof(float));
+  L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
+  L.counts = take((E + 2) * sizeof(int));
+  L.row_off = take((E + 2) * sizeof(int));
+  L.tile_off = take((E + 2) * sizeof(int));
+  L.perm = take(A * sizeof(int));
+  L.inv = take(A * sizeof(int));
+  L.xp = take(A * static_cast<size_t>(p.H) * 2);
+  L.act = take((A + Tsh) * static_cast<size_t>(p.I) * 2);
+  L.yp = take((A + Tsh) * static_cast<size_t>(p.H) * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+static moe_status check_params(const moe_params* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->H <= 0 || p->E <= 0 || p->I <= 0 || p->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->k > p->E || p->score_fn < 0 || p->score_fn > 2) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared != 0 && p->has_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (p->k > 16 || p->E > 4096) return MOE_ERR_UNSUPPORTED;
+  if (p->H % 64 != 0 || p->I % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  // 32-bit row and element counts inside the kernels
+  const long long A = static_cast<long long>(p->T) * p->k;
+  if (A + p->T > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static moe_status check_ws(const moe_params* p, void* ws, size_t ws_bytes) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < layout(*p).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static moe_status run_router_gemm(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                                  float* logits, int* status, cudaStream_t s) {
+  GemmMaps maps;
+  if (!make_map_rows(&maps.a, X, p->T, p->H)) return MOE_ERR_CUDA;
+  if (!make_map_weights(&maps.b, Wg, 1, p->H, p->E)) return MOE_ERR_CUDA;
+  maps.a2 = maps.a;
+  maps.b2 = maps.b;
+  GemmParams g;
+  memset(&g, 0, sizeof(g));
+  g.row_off = nullptr;
+  g.tile_off = nullptr;
+  g.num_groups = 1;
+  g.dense_rows = p->T;
+  g.shared_group = -1;
+  g.a2_shared = 0;
+  g.n_tiles = (p->E + gemm_block_n(kGemmRouter) - 1) / gemm_block_n(kGemmRouter);
+  g.num_kb = p->H / kBK;
+  g.n_out = p->E;
+  g.up_off = 0;
+  g.out = logits;
+  g.ldo = p->E;
+  g.status = status;
+  const int tiles = ((p->T + kBM - 1) / kBM) * g.n_tiles;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  return cuda_status(launch_gemm(kGemmRouter, maps, g, grid, s));
+}
+
+// Waits on an mbarrier that nothing ever arrives on: the bounded wait must
+// give up after limit_ns and record kFlagTimeout in the status word.
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, &abort_flag, limit_ns);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [0, E)";
+    case MOE_ERR_BAD_TOKEN_ID: return "hash token id outside [0, V)";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_size(const moe_params* p) {
+  if (check_params(p) != MOE_OK) return 0;
+  return layout(*p).total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_sync_status(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int flags = 0;
+  if (cudaMemcpyAsync(&flags, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
+  if (flags & kFlagBadToken) return MOE_ERR_BAD_TOKEN_ID;
+  if (flags & kFlagBadExpert) return MOE_ERR_BAD_EXPERT_ID;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                      void* stream) {
+  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  if (limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      at<int>(ws, 0), static_cast<unsigned long long>(limit_us) * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_route_logits(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                            float* logits, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  if (p->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !Wg || !logits || !aligned16(X) || !aligned16(Wg) || !aligned16(logits))
+    return MOE_ERR_INVALID_ARG;
+  return run_router_gemm(p, X, Wg, logits, at<int>(ws, 0), static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                     const float* bias, const int32_t* token_ids, const int32_t* tid2eid,
+                     int32_t V, int32_t* E_ids, float* G, void* ws, size_t ws_bytes,
+                     void* stream) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  if (p->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const bool hash = token_ids != nullptr;
+  if (hash && (tid2eid == nullptr || V <= 0 || bias != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!hash && tid2eid != nullptr) return MOE_ERR_INVALID_ARG;
+  if (bias != nullptr && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !Wg || !E_ids || !G || !aligned16(X) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  float* logits = at<float>(ws, L.logits);
+  if ((st = run_router_gemm(p, X, Wg, logits, status, s)) != MOE_OK) return st;
+  return cuda_status(launch_route_select(logits, X, Wg, bias, token_ids, tid2eid, V, p->T, p->H,
+                                         p->E, p->k, p->score_fn, p->alpha, p->renorm, E_ids, G,
+                                         status, s));
+}
+
+static DispatchBufs dispatch_bufs(const moe_params* p, void* ws, const WsLayout& L) {
+  DispatchBufs b;
+  b.chunk_cnt = at<int>(ws, L.chunk_cnt);
+  b.counts = at<int>(ws, L.counts);
+  b.row_off = at<int>(ws, L.row_off);
+  b.tile_off = at<int>(ws, L.tile_off);
+  b.perm = at<int>(ws, L.perm);
+  b.inv = at<int>(ws, L.inv);
+  b.nchunk = dispatch_chunks(p->T * p->k);
+  return b;
+}
+
+moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                        void* stream) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  if (!counts || !offsets || (p->T > 0 && (!E_ids || !perm))) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const DispatchBufs b = dispatch_bufs(p, ws, L);
+  cudaError_t e = launch_dispatch(E_ids, p->T, p->k, p->E, 0, b, at<int>(ws, L.status), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t A = static_cast<size_t>(p->T) * p->k;
+  e = cudaMemcpyAsync(counts, b.counts, p->E * sizeof(int), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(offsets, b.row_off, (p->E + 1) * sizeof(int), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && A > 0)
+    e = cudaMemcpyAsync(perm, b.perm, A * sizeof(int), cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                             const float* G, const uint16_t* W1, const uint16_t* W2,
+                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                             size_t ws_bytes, void* stream, void* const* stage_events) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !E_ids || !G || !W1 || !W2 || !Y) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared && (!Ws1 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared && (!aligned16(Ws1) || !aligned16(Ws2))) return MOE_ERR_INVALID_ARG;
+
+  const WsLayout L = layout(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  const DispatchBufs b = dispatch_bufs(p, ws, L);
+  const int T = p->T, H = p->H, E = p->E, k = p->k, I = p->I;
+  const int A = T * k;
+  const int Tsh = p->has_shared ? T : 0;
+  uint16_t* Xp = at<uint16_t>(ws, L.xp);
+  uint16_t* Act = at<uint16_t>(ws, L.act);
+  float* Yp = at<float>(ws, L.yp);
+
+  auto mark = [&](int i) -> cudaError_t {
+    if (stage_events == nullptr || stage_events[i] == nullptr) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_dispatch(E_ids, T, k, E, p->has_shared, b, status, s);
+  if (e == cudaSuccess) e = launch_gather_rows(X, b.perm, b.row_off, E, A, k, H, Xp, s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  const int groups = E + (p->has_shared ? 1 : 0);
+  const int mt_bound = (A + kBM - 1) / kBM + E + (Tsh + kBM - 1) / kBM;
+
+  // Linear1 + SwiGLU:  Act = SwiGLU(Xp W1[e]);  shared group reads X directly
+  {
+    GemmMaps maps;
+    bool ok = make_map_rows(&maps.a, Xp, A, H) && make_map_rows(&maps.a2, X, T, H) &&
+              make_map_weights(&maps.b, W1, E, H, 2 * I);
+    if (ok) ok = p->has_shared ? make_map_weights(&maps.b2, Ws1, 1, H, 2 * I) : (maps.b2 = maps.b, true);
+    if (!ok) return MOE_ERR_CUDA;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = groups;
+    g.shared_group = p->has_shared ? E : -1;
+    g.a2_shared = 1;
+    g.n_tiles = (I + 127) / 128;
+    g.num_kb = H / kBK;
+    g.n_out = I;
+    g.up_off = I;
+    g.out = Act;
+    g.ldo = I;
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if ((e = launch_gemm(kGemmSwiGLU, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // Linear2:  Yp = Act W2[e] in fp32 (shared group uses Ws2)
+  {
+    GemmMaps maps;
+    bool ok = make_map_rows(&maps.a, Act, A + Tsh, I) && make_map_weights(&maps.b, W2, E, I, H);
+    if (ok) ok = p->has_shared ? make_map_weights(&maps.b2, Ws2, 1, I, H) : (maps.b2 = maps.b, true);
+    if (!ok) return MOE_ERR_CUDA;
+    maps.a2 = maps.a;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = groups;
+    g.shared_group = p->has_shared ? E : -1;
+    g.a2_shared = 0;
+    g.n_tiles = (H + 255) / 256;
+    g.num_kb = I / kBK;
+    g.n_out = H;
+    g.up_off = 0;
+    g.out = Yp;
+    g.ldo = H;
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if ((e = launch_gemm(kGemmPlain, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
+}
+
+moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                       const float* G, const uint16_t* W1, const uint16_t* W2,
+                       const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return moe_forward_timed(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, ws_bytes, stream, nullptr);
+}
+
+}  // extern "C"

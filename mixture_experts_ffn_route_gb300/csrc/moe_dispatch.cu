@@ -1,0 +1,271 @@
+// Dispatch and combine: the on-device permute and un-permute around the
+// expert GEMMs.
+//
+// "mega_moe" page, section 计算公式 / EP Dispatch: expert e receives the rows
+// of the tokens that selected it, stacked in a fixed order, and row(i, k) is
+// the unique row of token i in the block of its k-th expert.  "Megatron-LM 的
+// MoE 并行：以 DeepSeek-V4 为例", section AlltoAll 的前向 / 计数与重排: count the
+// assignments of each expert, then permute with duplication so each expert's
+// rows are contiguous.  Here the fixed order inside a block is ascending flat
+// assignment index f = t*k + j, which makes the result deterministic.
+//
+//   count   : per chunk of kChunk assignments, per-expert counts (smem atomics)
+//   scan    : per-expert exclusive prefix over chunks, then over experts
+//             (row offsets) and over 128-row tiles (tile offsets for the GEMMs)
+//   place   : one block per (expert, chunk): ballot-prefix ranks give each
+//             assignment its row; writes perm[row] = f and inv[f] = row
+//   gather  : Xp[row] = X[perm[row] / k], 16-byte vectors, one warp per row
+//   combine : "mega_moe" page, section Token Combine: y_t = sum_j G[t, j] *
+//             Yp[inv[t*k + j]] (+ the shared expert's row); Yp is fp32, the sum
+//             is fp32 and y_t is rounded to bf16 once
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 4096;
+constexpr int kThreads = 1024;
+
+int dispatch_chunks(int A) { return A <= 0 ? 0 : (A + kChunk - 1) / kChunk; }
+
+__global__ void __launch_bounds__(kThreads)
+    dispatch_count_kernel(const int32_t* __restrict__ E_ids, int A, int E, int* __restrict__ chunk_cnt,
+                          int* __restrict__ inv, int* status) {
+  extern __shared__ int hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int f0 = blockIdx.x * kChunk;
+  const int f1 = min(A, f0 + kChunk);
+  bool bad = false;
+  for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const int e = E_ids[f];
+    if (e >= 0 && e < E) {
+      atomicAdd(&hist[e], 1);
+    } else {
+      inv[f] = -1;
+      bad = true;
+    }
+  }
+  if (bad) set_flag(status, kFlagBadExpert);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_cnt[static_cast<long long>(blockIdx.x) * E + i] = hist[i];
+}
+
+// Block-wide exclusive scan of one int per thread; returns the block total.
+__device__ int block_exclusive_scan(int v, int* out, int* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+  const int total = warp_tot[(blockDim.x >> 5) - 1];
+  *out = before;
+  __syncthreads();
+  return total;
+}
+
+// Single block.  After it: chunk_cnt[c][e] = rows of expert e in chunks < c;
+// counts[e]; row_off[e] (exclusive, row_off[E] = valid assignments); tile_off.
+// With a shared expert, group E is the T shared rows placed after all
+// routed rows: counts[E] = T, row_off[E + 1] = row_off[E] + T.
+__global__ void __launch_bounds__(kThreads)
+    dispatch_scan_kernel(int* __restrict__ chunk_cnt, int nchunk, int E, int T, int has_shared,
+                         int* __restrict__ counts, int* __restrict__ row_off, int* __restrict__ tile_off) {
+  __shared__ int warp_tot[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < nchunk; ++c) {
+      const long long i = static_cast<long long>(c) * E + e;
+      const int v = chunk_cnt[i];
+      chunk_cnt[i] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  __syncthreads();
+  // exclusive scans over experts, kThreads experts per pass
+  int row_carry = 0, tile_carry = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int n = (e < E) ? counts[e] : 0;
+    int rb, tb;
+    const int rt = block_exclusive_scan(n, &rb, warp_tot);
+    const int tt = block_exclusive_scan((n + kBM - 1) / kBM, &tb, warp_tot);
+    if (e < E) {
+      row_off[e] = row_carry + rb;
+      tile_off[e] = tile_carry + tb;
+    }
+    row_carry += rt;
+    tile_carry += tt;
+  }
+  if (threadIdx.x == 0) {
+    row_off[E] = row_carry;
+    tile_off[E] = tile_carry;
+    if (has_shared) {
+      counts[E] = T;
+      row_off[E + 1] = row_carry + T;
+      tile_off[E + 1] = tile_carry + (T + kBM - 1) / kBM;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    dispatch_place_kernel(const int32_t* __restrict__ E_ids, int A, int E, int nchunk,
+                          const int* __restrict__ chunk_base, const int* __restrict__ counts,
+                          const int* __restrict__ row_off, int* __restrict__ perm, int* __restrict__ inv) {
+  __shared__ int wcount[32];
+  const int e = blockIdx.x, c = blockIdx.y;
+  const int b0 = chunk_base[static_cast<long long>(c) * E + e];
+  const int b1 = (c + 1 < nchunk) ? chunk_base[static_cast<long long>(c + 1) * E + e] : counts[e];
+  if (b1 == b0) return;  // no assignment of e in this chunk (block-uniform)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int pos = row_off[e] + b0;
+  const int f1 = min(A, (c + 1) * kChunk);
+  for (int f0 = c * kChunk; f0 < f1; f0 += blockDim.x) {
+    const int f = f0 + threadIdx.x;
+    const bool mine = (f < f1) && (E_ids[f] == e);
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) wcount[warp] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+      const int cw = wcount[w];
+      before += (w < warp) ? cw : 0;
+      total += cw;
+    }
+    if (mine) {
+      const int row = pos + before + __popc(m & ((1u << lane) - 1u));
+      perm[row] = f;
+      inv[f] = row;
+    }
+    pos += total;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,
+                            const DispatchBufs& b, int* status, cudaStream_t s) {
+  const int A = T * k;
+  if (A > 0) {
+    const size_t sh = static_cast<size_t>(E) * sizeof(int);
+    if (sh > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(sh));
+      if (e != cudaSuccess) return e;
+    }
+    dispatch_count_kernel<<<b.nchunk, kThreads, sh, s>>>(E_ids, A, E, b.chunk_cnt, b.inv, status);
+  }
+  dispatch_scan_kernel<<<1, kThreads, 0, s>>>(b.chunk_cnt, b.nchunk, E, T, has_shared, b.counts,
+                                              b.row_off, b.tile_off);
+  if (A > 0) {
+    dispatch_place_kernel<<<dim3(E, b.nchunk), kThreads, 0, s>>>(E_ids, A, E, b.nchunk,
+                                                                 b.chunk_cnt, b.counts, b.row_off,
+                                                                 b.perm, b.inv);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------- gather
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint16_t* __restrict__ X, const int* __restrict__ perm,
+                       const int* __restrict__ row_off, int E, int k, int H, uint16_t* __restrict__ Xp) {
+  const int rows = row_off[E];
+  const int vecs = H / 8;  // 16-byte vectors per row
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int p = gw; p < rows; p += nw) {
+    const int t = perm[p] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<long long>(p) * H);
+    int i = lane;
+    for (; i + 96 < vecs; i += 128) {
+      const uint4 a = __ldg(src + i), b2 = __ldg(src + i + 32), c2 = __ldg(src + i + 64),
+                  d2 = __ldg(src + i + 96);
+      dst[i] = a;
+      dst[i + 32] = b2;
+      dst[i + 64] = c2;
+      dst[i + 96] = d2;
+    }
+    for (; i < vecs; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+cudaError_t launch_gather_rows(const uint16_t* X, const int* perm, const int* row_off, int E,
+                               int A, int k, int H, uint16_t* Xp, cudaStream_t s) {
+  if (A <= 0) return cudaSuccess;
+  const int warps_needed = A;
+  int blocks = (warps_needed + 7) / 8;
+  const int cap = num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(X, perm, row_off, E, k, H, Xp);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------- combine
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float* __restrict__ Yp, const int* __restrict__ inv,
+                   const float* __restrict__ G, const int* __restrict__ row_off, int k, int H,
+                   int E, int has_shared, uint16_t* __restrict__ Y) {
+  __shared__ int rows[17];
+  __shared__ float w[17];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = inv[static_cast<long long>(t) * k + threadIdx.x];
+    w[threadIdx.x] = G[static_cast<long long>(t) * k + threadIdx.x];
+  }
+  if (threadIdx.x == 0 && has_shared) {
+    rows[k] = row_off[E] + t;
+    w[k] = 1.0f;
+  }
+  __syncthreads();
+  const int n = k + (has_shared ? 1 : 0);
+  const int vecs = H / 8;
+  for (int c = threadIdx.x; c < vecs; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < n; ++j) {
+      const int p = rows[j];
+      if (p < 0) continue;
+      const float4* src = reinterpret_cast<const float4*>(Yp + static_cast<long long>(p) * H) + 2 * c;
+      const float4 u = __ldg(src), v = __ldg(src + 1);
+      const float g = w[j];
+      acc[0] += g * u.x; acc[1] += g * u.y; acc[2] += g * u.z; acc[3] += g * u.w;
+      acc[4] += g * v.x; acc[5] += g * v.y; acc[6] += g * v.z; acc[7] += g * v.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(Y + static_cast<long long>(t) * H)[c] = o;
+  }
+}
+
+cudaError_t launch_combine(const float* Yp, const int* inv, const float* G, const int* row_off,
+                           int T, int k, int H, int E, int has_shared, uint16_t* Y, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_kernel<<<T, kCombineThreads, 0, s>>>(Yp, inv, G, row_off, k, H, E, has_shared, Y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

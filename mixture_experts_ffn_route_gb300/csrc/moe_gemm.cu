@@ -1,0 +1,335 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// Serves the three contractions of the layer:
+//   router  : logits[T, E] = X[T, H] Wg[H, E]                      (fp32 out)
+//   Linear1 : Act[rows, I] = SiLU(Xp W1[e][:, :I]) * (Xp W1[e][:, I:])  (bf16 out)
+//   Linear2 : Yp[rows, H]  = Act W2[e]                              (fp32 out)
+// The expert FFN is the "Expert Compute" step of the "mega_moe" page
+// (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
+// projection); the router product is the gating linear of "Megatron-LM 的 MoE
+// 并行：以 DeepSeek-V4 为例" (section 路由张量).
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: A tile [128 rows x 64 k] K-major and B tile
+//               [64 k x BN cols] MN-major (the weights keep their [K][N] row-major
+//               layout), both with 128-byte swizzle, into a STAGES-deep ring.
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16)
+//               into one of two TMEM accumulators and commits to mbarriers.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one token row per thread),
+//               fuse SwiGLU (bf16 out) or store fp32, free the
+//               accumulator so the next tile's MMAs overlap this epilogue.
+// Tiles are walked in (group, column tile, 128-row tile) order, striding by
+// gridDim.x.  Group row ranges come from device memory.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;  // 16 KB
+  static constexpr int B_BYTES = BN * kBK * 2;   // 8 KB per 64 columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+};
+
+struct TileInfo {
+  int group, m, n;
+  int row0, row_end;  // output rows [row0, row_end) of this tile's group
+  int a_row0;         // first A row fetched for this tile
+  bool second;        // uses the second (shared-expert) tensor maps
+};
+
+// Tile order: group by group; inside a group, column tile by column tile, and
+// the 128-row tiles of one column tile consecutively.  CTAs running at the
+// same time then share one weight column block through L2 while the group's
+// rows (the smaller operand) stay resident, so each weight byte is read from
+// HBM about once even when a group spans many row tiles.
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
+  TileInfo t;
+  if (p.row_off == nullptr) {
+    const int mt = (p.dense_rows + kBM - 1) / kBM;
+    t.group = 0;
+    t.n = tile / mt;
+    t.m = tile - t.n * mt;
+    t.row0 = t.m * kBM;
+    t.row_end = p.dense_rows;
+  } else {
+    // largest g with tile_off[g] * n_tiles <= tile (groups without tiles share
+    // their start with the next group)
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.tile_off + mid) * p.n_tiles <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int t0 = __ldg(p.tile_off + lo);
+    const int mt = __ldg(p.tile_off + lo + 1) - t0;
+    const int local = tile - t0 * p.n_tiles;
+    t.group = lo;
+    t.n = local / mt;
+    t.m = local - t.n * mt;
+    t.row0 = __ldg(p.row_off + lo) + t.m * kBM;
+    t.row_end = __ldg(p.row_off + lo + 1);
+  }
+  t.second = (t.group == p.shared_group);
+  t.a_row0 = (t.second && p.a2_shared) ? t.m * kBM : t.row0;
+  return t;
+}
+
+template <int BN, int KIND>
+__device__ __forceinline__ int b_box_col(const GemmParams& p, int n, int j) {
+  if (KIND == kGemmSwiGLU) {
+    // columns [0, 128) of the tile: gate n*128.. ; columns [128, 256): up
+    return (j < 2) ? n * 128 + j * 64 : p.up_off + n * 128 + (j - 2) * 64;
+  }
+  return n * BN + j * 64;
+}
+
+template <int BN, int KIND>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t tiles0 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bar_area);
+  const uint32_t empty0 = full0 + 8 * C::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * C::STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (p.shared_group >= 0) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_mt = (p.row_off == nullptr) ? (p.dense_rows + kBM - 1) / kBM
+                                              : __ldg(p.tile_off + p.num_groups);
+  const int total = total_mt * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo t = decode_tile(p, tile);
+        const CUtensorMap* mA = (t.second && p.a2_shared) ? &tmA2 : &tmA;
+        const CUtensorMap* mB = t.second ? &tmB2 : &tmB;
+        const int bz = t.second ? 0 : t.group;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(sa, mA, fb, kb * kBK, t.a_row0);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_3d(sb + j * (64 * kBK * 2), mB, fb, b_box_col<BN, KIND>(p, t.n, j),
+                        kb * kBK, bz);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, true);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: K-major rows of 128 B; a 16-wide k step is 32 B along the row.
+            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            // B: MN-major; rows of 128 B hold 64 n-values of one k; 8-row groups
+            // are 1024 B apart (SBO) and 64-column blocks 8 KB apart (LBO).
+            const uint64_t bd = smem_desc_sw128(sb + kk * 16 * 128, 64 * kBK * 2, 1024);
+            mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(tfull0 + 8 * acc);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const TileInfo t = decode_tile(p, tile);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, p.status, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row = t.row0 + r;
+      const bool row_ok = row < t.row_end;
+      if (KIND == kGemmSwiGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + static_cast<long long>(row) * p.ldo;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          float g[32], u[32];
+          tmem_ld_32x32(tb + c, g);
+          tmem_ld_32x32(tb + 128 + c, u);
+          const int col = t.n * 128 + c;
+          if (row_ok && col < p.n_out) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
+              const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+              w[i] = pack_bf16x2(a0, a1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      } else {  // router logits and Linear2 expert outputs: fp32
+        float* out = static_cast<float*>(p.out) + static_cast<long long>(row) * p.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld_32x32(tb + c, v);
+          const int col = t.n * BN + c;
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (col + 4 * i < p.n_out)
+                *reinterpret_cast<float4*>(out + col + 4 * i) =
+                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [rows, cols] bf16 row-major, box = 64 columns x 128 rows, 128-byte swizzle.
+bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBM)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [groups, K, N] bf16 row-major (N contiguous), box = 64 n x 64 k x 1.
+bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
+                        static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N * K) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_block_n(GemmKind kind) { return kind == kGemmRouter ? 128 : 256; }
+
+template <int BN, int KIND>
+static cudaError_t launch_one(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  auto kern = gemm_tc_kernel<BN, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       GemmCfg<BN>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 192, GemmCfg<BN>::SMEM_BYTES, s>>>(m.a, m.a2, m.b, m.b2, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p, int grid,
+                        cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  switch (kind) {
+    case kGemmRouter: return launch_one<128, kGemmRouter>(maps, p, grid, s);
+    case kGemmSwiGLU: return launch_one<256, kGemmSwiGLU>(maps, p, grid, s);
+    default: return launch_one<256, kGemmPlain>(maps, p, grid, s);
+  }
+}
+
+}  // namespace moe

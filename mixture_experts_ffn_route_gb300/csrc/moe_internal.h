@@ -1,0 +1,78 @@
+// Internal interface between the C ABI (moe_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBM = 128;  // GEMM tile rows (tokens)
+constexpr int kBK = 64;   // GEMM k-block (one 128-byte swizzle row of bf16)
+
+enum GemmKind { kGemmRouter = 0, kGemmSwiGLU = 1, kGemmPlain = 2 };
+
+// One grouped GEMM launch.  Groups are row ranges [row_off[g], row_off[g+1])
+// of the A operand and of the output; tile_off[g] is the running count of
+// 128-row tiles before group g.  Both arrays live on the device (written by
+// the dispatch scan) so no host synchronisation is needed.  With
+// row_off == nullptr there is one group of `dense_rows` rows.
+struct GemmParams {
+  const int* row_off;
+  const int* tile_off;
+  int num_groups;
+  int dense_rows;
+  int shared_group;  // group served by the second tensor maps, or -1
+  int a2_shared;     // 1: that group's A rows come from map a2, starting at row 0
+  int n_tiles;       // output column tiles per 128-row tile
+  int num_kb;        // K / 64
+  int n_out;         // valid output columns
+  int up_off;        // SwiGLU: column of the first "up" column of W1 (= I)
+  void* out;
+  long long ldo;     // output row stride, elements
+  int* status;
+};
+
+struct GemmMaps {
+  CUtensorMap a, a2, b, b2;
+};
+
+// Tensor-map helpers (host).  Return false if the driver rejects the map.
+bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
+bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N);
+
+// Launch the tcgen05 GEMM of the given kind on `grid` persistent CTAs.
+cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p, int grid,
+                        cudaStream_t s);
+int gemm_block_n(GemmKind kind);
+
+// Router top-k / hash epilogue over fp32 logits [T, E].
+cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* Wg,
+                                const float* bias, const int32_t* token_ids,
+                                const int32_t* tid2eid, int V, int T, int H, int E, int k,
+                                int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
+                                int* status, cudaStream_t s);
+
+// Dispatch: counts, offsets, permutation, inverse, tile offsets, gathered rows.
+struct DispatchBufs {
+  int* chunk_cnt;    // [nchunk * E]
+  int* counts;       // [E + 1]
+  int* row_off;      // [E + 2]
+  int* tile_off;     // [E + 2]
+  int* perm;         // [T * k]
+  int* inv;          // [T * k]
+  int nchunk;
+};
+int dispatch_chunks(int A);
+cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,
+                            const DispatchBufs& b, int* status, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* X, const int* perm, const int* row_off, int E,
+                               int A, int k, int H, uint16_t* Xp, cudaStream_t s);
+cudaError_t launch_combine(const float* Yp, const int* inv, const float* G,
+                           const int* row_off, int T, int k, int H, int E, int has_shared,
+                           uint16_t* Y, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -78,6 +78,9 @@ CONFIGS = {
     "c5s": dict(_BASE, T=515, H=384, E=8, k=2, I=704, score="softmax",
                 renorm=0),
 }
+# V4-Pro expert shapes at a size one ncu capture can take (4.2 GB of weights,
+# ~64 rows per expert as in c3, uniform load)
+CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
 # the pages' own V4-Pro routing rule (sqrt-softplus affinity) at the c3 shapes
 CONFIGS["c3_sp"] = dict(CONFIGS["c3"], score="sqrt_softplus", skew=None)
 
@@ -204,12 +207,16 @@ def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
 
 
 # --------------------------------------------------------------------------- torch
-def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", **overrides) -> dict:
+def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=None,
+                      weights: bool = True, **overrides) -> dict:
     """Device (torch) drawing of one workload, for sizes too large for the host.
 
     bf16 tensors are ``torch.bfloat16``; the conversion from the fp32 draw is
     torch's round-to-nearest-even.  Large weights are drawn one expert at a
-    time so the fp32 temporary stays small.
+    time so the fp32 temporary stays small.  ``token_seed`` (default: seed)
+    draws the token-side tensors (X, given ids and gates, token ids) so that
+    several batches can share one set of weights; ``weights=False`` skips the
+    expert weights (router-only use).
     """
     import torch
 
@@ -217,9 +224,11 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", **overrides)
     T, H, E, k, I = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["I"]
     dev = torch.device(device)
 
-    def gen(tid):
+    tseed = seed if token_seed is None else token_seed
+
+    def gen(tid, token_side=False):
         g = torch.Generator(device=dev)
-        g.manual_seed(int(seed) * 1000 + tid)
+        g.manual_seed(int(tseed if token_side else seed) * 1000 + tid)
         return g
 
     def normal(tid, shape, std, per_slice=False):
@@ -232,7 +241,7 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", **overrides)
         return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
 
     d = {"cfg": cfg}
-    X = torch.randn((T, H), generator=gen(1), device=dev)
+    X = torch.randn((T, H), generator=gen(1, True), device=dev)
     Wg = torch.randn((H, E), generator=gen(2), device=dev) * (1.0 / math.sqrt(H))
     c = zipf_offsets(cfg) if cfg.get("skew") else None
     if c is not None and T > 0:
@@ -241,23 +250,29 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", **overrides)
     d["X"] = X.to(torch.bfloat16)
     d["Wg"] = Wg.to(torch.bfloat16)
     del X, Wg
-    d["bias"] = (torch.randn(E, generator=gen(3), device=dev) * 0.1).float() if cfg["bias"] else None
-    d["W1"] = normal(4, (E, H, 2 * I), 1.0 / math.sqrt(H), per_slice=True)
-    d["W2"] = normal(5, (E, I, H), 1.0 / math.sqrt(I), per_slice=True)
-    if cfg["shared"]:
+    # the selection bias is small and drawn on the host, identically in both
+    # back ends: the skew offsets were calibrated against these values
+    d["bias"] = (torch.from_numpy(_rng(seed, 3).standard_normal(size=E, dtype=np.float32)
+                                  * np.float32(0.1)).to(dev) if cfg["bias"] else None)
+    if weights:
+        d["W1"] = normal(4, (E, H, 2 * I), 1.0 / math.sqrt(H), per_slice=True)
+        d["W2"] = normal(5, (E, I, H), 1.0 / math.sqrt(I), per_slice=True)
+    else:
+        d["W1"] = d["W2"] = None
+    if cfg["shared"] and weights:
         d["Ws1"] = normal(6, (H, 2 * I), 1.0 / math.sqrt(H))
         d["Ws2"] = normal(7, (I, H), 1.0 / math.sqrt(I))
     else:
         d["Ws1"] = d["Ws2"] = None
     if cfg["routing"] == "given":
-        g = gen(8)
+        g = gen(8, True)
         keys = torch.rand((T, E), generator=g, device=dev)
         d["E_ids"] = keys.topk(k, dim=1).indices.to(torch.int32).contiguous()
-        z = torch.randn((T, k), generator=gen(9), device=dev)
+        z = torch.randn((T, k), generator=gen(9, True), device=dev)
         d["G"] = torch.softmax(z, dim=1).float().contiguous()
     if cfg["routing"] == "hash":
         V = cfg["V"]
         keys = torch.rand((V, E), generator=gen(10), device=dev)
         d["tid2eid"] = keys.topk(k, dim=1).indices.to(torch.int32).contiguous()
-        d["token_ids"] = torch.randint(0, V, (T,), generator=gen(11), device=dev, dtype=torch.int32)
+        d["token_ids"] = torch.randint(0, V, (T,), generator=gen(11, True), device=dev, dtype=torch.int32)
     return d

@@ -15,3 +15,22 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def _lib_is_stale():
+    from mixture_experts_ffn_route_gb300 import build as b
+    if not os.path.exists(b.LIB):
+        return True
+    t = os.path.getmtime(b.LIB)
+    deps = b.sources() + [os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC) if f.endswith((".cuh", ".h"))]
+    deps.append(os.path.join(ROOT, "include", "moe_ffn.h"))
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+@pytest.fixture(scope="session")
+def built_lib():
+    """The in-tree CUDA library, (re)built with nvcc when missing or stale."""
+    from mixture_experts_ffn_route_gb300 import build as b
+    if _lib_is_stale():
+        b.build()
+    return b.LIB

@@ -1,0 +1,342 @@
+"""Parity of the CUDA library (through its C ABI) with the CPU oracle.
+
+Expert ids, counts, offsets and the permutation must match bit for bit; gates
+within 2e-4 relative; Y within 2e-2 * RMS(Y_ref) beyond the bf16 output's own
+rounding (tests/_gpu.py).  Small workloads are compared element by element;
+the full-size workloads compare routing and dispatch on every token and Y on
+sampled tokens."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_route_gb300 as moe
+import oracle
+import synth
+from _gpu import (DEV, bf, check_gates, check_y, host_bits, params, run_forward, run_route,
+                  to_device, to_host)
+
+pytestmark = pytest.mark.gpu
+
+SMALL_ROUTED = ["c1", "c3s", "c3s_sp", "c4s", "c5s"]
+SMALL_ALL = ["c1", "c2s", "c3s", "c3s_sp", "c4s", "c5s"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_lib):
+    moe.lib()
+    torch.cuda.set_device(DEV)
+
+
+def oracle_route(h):
+    c = h["cfg"]
+    if c["routing"] == "hash":
+        return oracle.route_hash(h["X"], h["Wg"], h["token_ids"], h["tid2eid"], c["score_fn"],
+                                 c["alpha"], c["renorm"])
+    return oracle.route(h["X"], h["Wg"], h["bias"], c["score_fn"], c["k"], c["alpha"], c["renorm"])
+
+
+def host_inputs(name, **kw):
+    h = synth.make_inputs(name, **kw)
+    return h, to_device(h)
+
+
+# ---------------------------------------------------------------------- router
+@pytest.mark.parametrize("name", ["c1", "c3s", "c3s_sp", "c5s"])
+def test_router_scores_within_decision_band(name):
+    h, dd = host_inputs(name)
+    c = h["cfg"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    L = torch.empty((c["T"], c["E"]), dtype=torch.float32, device=DEV)
+    moe.moe_route_logits(p, dd["X"], dd["Wg"], L, ws)
+    moe.moe_sync_status(ws)
+    l32 = L.cpu().numpy().astype(np.float64)
+    l64 = oracle.router_logits(h["X"], h["Wg"])
+    if c["score_fn"] == oracle.SCORE_SOFTMAX:
+        # selection on the logit, band 1e-3 * max(1, |l|): keep the error below a quarter
+        assert (np.abs(l32 - l64) / np.maximum(1.0, np.abs(l64))).max() < 2.5e-4
+    else:
+        s32 = oracle.affinity(l32, c["score_fn"])
+        s64 = oracle.affinity(l64, c["score_fn"])
+        assert np.abs(s32 - s64).max() < 5e-5  # a quarter of the 2e-4 score band
+
+
+@pytest.mark.parametrize("name", ["c3", "c3_sp", "c5"])
+def test_router_scores_within_decision_band_full_size(name):
+    dd = synth.make_inputs_torch(name, device=DEV, weights=False)
+    c = dd["cfg"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    L = torch.empty((c["T"], c["E"]), dtype=torch.float32, device=DEV)
+    moe.moe_route_logits(p, dd["X"], dd["Wg"], L, ws)
+    moe.moe_sync_status(ws)
+    l32 = L.cpu().numpy().astype(np.float64)
+    l64 = oracle.router_logits(host_bits(dd["X"]), host_bits(dd["Wg"]))
+    if c["score_fn"] == oracle.SCORE_SOFTMAX:
+        assert (np.abs(l32 - l64) / np.maximum(1.0, np.abs(l64))).max() < 2.5e-4
+    else:
+        s32 = oracle.affinity(l32, c["score_fn"])
+        s64 = oracle.affinity(l64, c["score_fn"])
+        assert np.abs(s32 - s64).max() < 5e-5
+
+
+@pytest.mark.parametrize("name", SMALL_ROUTED)
+def test_route_matches_oracle(name):
+    h, dd = host_inputs(name)
+    p = params(h["cfg"])
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref, _ = oracle_route(h)
+    assert np.array_equal(E_ids.cpu().numpy(), ids_ref)
+    check_gates(G, G_ref, name)
+
+
+def test_route_equal_scores_go_to_the_lower_id():
+    rng = np.random.default_rng(11)
+    T, H, E, k = 64, 128, 16, 4
+    X = synth.bf16_bits_from_f32(rng.standard_normal((T, H)))
+    Wg = rng.standard_normal((H, E)).astype(np.float32) / 11
+    Wg[:, 9] = Wg[:, 2]
+    Wg[:, 13] = Wg[:, 2]
+    bias = np.zeros(E, np.float32)
+    bias[[2, 9, 13]] = 0.75  # always selected, always tied
+    Wg = synth.bf16_bits_from_f32(Wg)
+    p = moe.make_params(T, H, E, k, 64)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    G = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    moe.moe_route(p, bf(X), bf(Wg), torch.from_numpy(bias).to(DEV), None, None, 0, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids = E_ids.cpu().numpy()
+    assert (ids[:, :3] == [2, 9, 13]).all()
+    ids_ref, G_ref, _ = oracle.route(X, Wg, bias, 0, k, 1.0, 1)
+    assert np.array_equal(ids, ids_ref)
+    check_gates(G, G_ref)
+
+
+# ---------------------------------------------------------------------- dispatch
+def _dispatch_gpu(p, E_ids):
+    ws = moe.alloc_workspace(p, DEV)
+    counts = torch.full((p.E,), -5, dtype=torch.int32, device=DEV)
+    offsets = torch.full((p.E + 1,), -5, dtype=torch.int32, device=DEV)
+    perm = torch.full((p.T * p.k,), -5, dtype=torch.int32, device=DEV)
+    moe.moe_dispatch(p, E_ids, counts, offsets, perm, ws)
+    code = moe.moe_sync_status(ws, raise_on_error=False)
+    return code, counts.cpu().numpy(), offsets.cpu().numpy(), perm.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["c2s", "c3s", "c4s", "c5s"])
+def test_dispatch_matches_oracle(name):
+    h, dd = host_inputs(name)
+    c = h["cfg"]
+    ids = h["E_ids"] if c["routing"] == "given" else oracle_route(h)[0]
+    code, counts, offsets, perm = _dispatch_gpu(params(c), torch.from_numpy(ids).to(DEV))
+    assert code == moe.MOE_OK
+    rc, ro, rp, _ = oracle.dispatch(ids, c["E"])
+    assert np.array_equal(counts, rc) and np.array_equal(offsets, ro)
+    assert np.array_equal(perm, rp)
+
+
+def test_dispatch_drops_bad_ids_and_reports_them():
+    rng = np.random.default_rng(12)
+    T, E, k = 5000, 24, 3  # two chunks of assignments
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[7, 1] = -1
+    ids[4100, 0] = E
+    ids[4999, 2] = 10 ** 6
+    p = moe.make_params(T, 64, E, k, 64)
+    code, counts, offsets, perm = _dispatch_gpu(p, torch.from_numpy(ids).to(DEV))
+    assert code == moe.MOE_ERR_BAD_EXPERT_ID
+    rc, ro, rp, _ = oracle.dispatch(ids, E)
+    assert np.array_equal(counts, rc) and np.array_equal(offsets, ro)
+    assert np.array_equal(perm[:len(rp)], rp)
+
+
+# ---------------------------------------------------------------------- forward
+def _reference_ids(h):
+    c = h["cfg"]
+    if c["routing"] == "given":
+        return h["E_ids"], h["G"].astype(np.float64)
+    ids, G, _ = oracle_route(h)
+    return ids, G
+
+
+@pytest.mark.parametrize("name", SMALL_ALL)
+def test_forward_matches_oracle(name):
+    h, dd = host_inputs(name)
+    c = h["cfg"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    ids_ref, G_ref = _reference_ids(h)
+    if c["routing"] == "given":
+        E_ids, G = dd["E_ids"], dd["G"]
+    else:
+        E_ids, G = run_route(p, dd, ws)
+    Y = run_forward(p, dd, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    assert np.array_equal(E_ids.cpu().numpy(), ids_ref)
+    Y_ref, _ = oracle.forward(h["X"], ids_ref, G_ref, h["W1"], h["W2"], h["Ws1"], h["Ws2"])
+    check_y(Y, Y_ref, name)
+
+
+EDGE = [
+    dict(T=1, H=64, E=1, k=1, I=64),
+    dict(T=3, H=128, E=2, k=2, I=64),
+    dict(T=17, H=64, E=5, k=5, I=128, shared=1),
+    dict(T=129, H=192, E=3, k=1, I=64),
+    dict(T=40, H=256, E=40, k=2, I=64),
+    dict(T=600, H=128, E=6, k=1, I=192, hot=True),
+    dict(T=260, H=320, E=9, k=3, I=448, shared=1),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "T{T}_H{H}_E{E}_k{k}_I{I}".format(**s))
+def test_forward_edge_shapes(shape):
+    shape = dict(shape)
+    hot = shape.pop("hot", False)
+    h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0), seed=99)
+    if hot:
+        h["E_ids"][:] = 0  # every token to expert 0: several 128-row tiles, other experts empty
+    c = h["cfg"]
+    dd = to_device(h)
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    Y = run_forward(p, dd, dd["E_ids"], dd["G"], ws)
+    moe.moe_sync_status(ws)
+    Y_ref, _ = oracle.forward(h["X"], h["E_ids"], h["G"].astype(np.float64), h["W1"], h["W2"],
+                              h["Ws1"], h["Ws2"])
+    check_y(Y, Y_ref, str(shape))
+
+
+def test_forward_with_no_tokens_writes_nothing():
+    h, dd = host_inputs("c3s")
+    p = params(h["cfg"], T=0)
+    ws = moe.alloc_workspace(p, DEV)
+    Y = torch.full((4, h["cfg"]["H"]), 3.0, dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward(p, dd["X"], dd["X"], dd["X"], dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws)
+    moe.moe_sync_status(ws)
+    assert (Y == 3.0).all()
+
+
+def test_bad_expert_ids_are_skipped_and_reported():
+    h, dd = host_inputs("c2s")
+    c = h["cfg"]
+    ids = h["E_ids"].copy()
+    ids[3, 0] = -1
+    ids[100, 2] = c["E"] + 5
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    Y = run_forward(p, dd, torch.from_numpy(ids).to(DEV), dd["G"], ws)
+    assert moe.moe_sync_status(ws, raise_on_error=False) == moe.MOE_ERR_BAD_EXPERT_ID
+    assert moe.moe_sync_status(ws, raise_on_error=False) == moe.MOE_OK  # cleared
+    Y_ref, _ = oracle.forward(h["X"], ids, h["G"].astype(np.float64), h["W1"], h["W2"])
+    check_y(Y, Y_ref, "dropped assignments")
+
+
+def test_bad_hash_token_ids_are_reported():
+    h, dd = host_inputs("c4s")
+    c = h["cfg"]
+    tok = h["token_ids"].copy()
+    tok[5] = c["V"]
+    tok[6] = -3
+    dd["token_ids"] = torch.from_numpy(tok).to(DEV)
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    assert moe.moe_sync_status(ws, raise_on_error=False) == moe.MOE_ERR_BAD_TOKEN_ID
+    ids = E_ids.cpu().numpy()
+    assert (ids[5] == -1).all() and (ids[6] == -1).all() and (G.cpu().numpy()[5:7] == 0).all()
+    good = np.ones(c["T"], bool)
+    good[5:7] = False
+    ids_ref = h["tid2eid"][h["token_ids"]]
+    assert np.array_equal(ids[good], ids_ref[good])
+
+
+def test_poisoned_workspace_does_not_leak_into_the_output():
+    h, dd = host_inputs("c3s")
+    c = h["cfg"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    ws.fill_(0xFF)  # NaN patterns in every bf16 and fp32 scratch buffer
+    moe.moe_workspace_init(ws)
+    E_ids, G = run_route(p, dd, ws)
+    Y = run_forward(p, dd, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref = _reference_ids(h)
+    Y_ref, _ = oracle.forward(h["X"], ids_ref, G_ref, h["W1"], h["W2"], h["Ws1"], h["Ws2"])
+    check_y(Y, Y_ref, "poisoned workspace")
+
+
+def test_forward_is_deterministic():
+    h, dd = host_inputs("c5s")
+    p = params(h["cfg"])
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    Y1 = run_forward(p, dd, E_ids, G, ws).clone()
+    Y2 = run_forward(p, dd, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+
+
+def test_device_wait_limit_reports_timeout():
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    moe.moe_workspace_init(ws)
+    moe.moe_selftest_wait_timeout(ws, 20000)  # 20 ms
+    assert moe.moe_sync_status(ws, raise_on_error=False) == moe.MOE_ERR_TIMEOUT
+    # the context is still usable
+    h, dd = host_inputs("c1")
+    p = params(h["cfg"])
+    ws2 = moe.alloc_workspace(p, DEV)
+    E_ids, _ = run_route(p, dd, ws2)
+    moe.moe_sync_status(ws2)
+    assert np.array_equal(E_ids.cpu().numpy(), oracle_route(h)[0])
+
+
+# ---------------------------------------------------------------------- full size
+FULL = {"c2": 6, "c3": 6, "c4": 6, "c5": 3, "c3_sp": 4}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workload(name):
+    dd = synth.make_inputs_torch(name, device=DEV)
+    c = dd["cfg"]
+    T, k, E = c["T"], c["k"], c["E"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    hX = host_bits(dd["X"])
+    # routing on every token
+    if c["routing"] == "given":
+        E_ids, G = dd["E_ids"], dd["G"]
+        ids_ref, G_ref = E_ids.cpu().numpy(), G.cpu().numpy().astype(np.float64)
+    else:
+        E_ids, G = run_route(p, dd, ws)
+        moe.moe_sync_status(ws)
+        hWg = host_bits(dd["Wg"])
+        if c["routing"] == "hash":
+            ids_ref, G_ref, l64 = oracle.route_hash(hX, hWg, dd["token_ids"].cpu().numpy(),
+                                                    dd["tid2eid"].cpu().numpy(), c["score_fn"],
+                                                    c["alpha"], c["renorm"])
+        else:
+            bias = dd["bias"].cpu().numpy() if dd["bias"] is not None else None
+            ids_ref, G_ref, l64 = oracle.route(hX, hWg, bias, c["score_fn"], k, c["alpha"], c["renorm"])
+        assert np.array_equal(E_ids.cpu().numpy(), ids_ref), "expert ids differ"
+        check_gates(G, G_ref, name)
+    # dispatch on every assignment
+    code, counts, offsets, perm = _dispatch_gpu(p, E_ids)
+    assert code == moe.MOE_OK
+    rc, ro, rp, _ = oracle.dispatch(ids_ref, E)
+    assert np.array_equal(counts, rc) and np.array_equal(offsets, ro) and np.array_equal(perm, rp)
+    # Y on sampled tokens
+    Y = run_forward(p, dd, E_ids, G, ws)
+    Y2 = run_forward(p, dd, E_ids, G, ws, Y=torch.empty_like(Y))
+    moe.moe_sync_status(ws)
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16)), "not deterministic"
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, FULL[name], replace=False)]))
+    W1 = lambda e: host_bits(dd["W1"][e])  # noqa: E731
+    W2 = lambda e: host_bits(dd["W2"][e])  # noqa: E731
+    Ws1 = host_bits(dd["Ws1"]) if dd["Ws1"] is not None else None
+    Ws2 = host_bits(dd["Ws2"]) if dd["Ws2"] is not None else None
+    Y_ref = oracle.forward_tokens(rows, hX[rows], ids_ref[rows], G_ref[rows], W1, W2, Ws1, Ws2, E=E)
+    check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
