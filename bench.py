@@ -109,6 +109,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
+# ------------------------------------------------------------------ ranks
+def rank_seeds(rank: int, base: int = 1234):
+    """(weight seed, token seed) of a rank: one model everywhere, one token
+    batch per rank."""
+    return base, base + rank
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of each rank's value (the job is as slow as its slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ our arm
 def build_step(moe, dd, p, ws, stage_events=None):
     c = dd["cfg"]
@@ -145,8 +163,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.lib()
-    # one model (weights, seed 1234) on every rank; each rank its own token batch
-    dd = synth.make_inputs_torch(args.workload, seed=1234, token_seed=1234 + rank, device=dev)
+    wseed, tseed = rank_seeds(rank)
+    dd = synth.make_inputs_torch(args.workload, seed=wseed, token_seed=tseed, device=dev)
     c = dd["cfg"]
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     has_shared = c["shared"]
@@ -189,12 +207,7 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.mark_end()
     moe.moe_sync_status(ws)
-    ms = t_start.elapsed_time(t_end) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world, dev)
 
     def avg(evs, a, b):
         return sum(e[a].elapsed_time(e[b]) for e in evs) / len(evs)
@@ -229,11 +242,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record()
     torch.cuda.synchronize()
     moe.moe_sync_status(ws)
-    e2e_ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
 
     if rank != 0:
         return None
@@ -263,10 +272,11 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "algorithmic_flops_per_launch": int(g1_flops),
                 "peak_source": pk["source"] + " bf16_tflops_sustained"}
-    traffic = load_traffic(args.workload)
-    if traffic is not None:
-        roof["traffic"] = traffic
-    launches_per_step = (2 if routed else 0) + 7
+    if roof["bound"] == "hbm":
+        roof["traffic"] = load_traffic(args.workload, g1_bytes)
+    # route: transpose Wg, gating GEMM, select, recheck, reselect (hash: GEMM, select);
+    # forward: count, scan, place, gather, Linear1, Linear2, combine
+    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + 7
     out = {
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -297,13 +307,19 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
-def load_traffic(workload):
-    """dram bytes per GEMM1 launch from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", f"gemm1_swiglu_{workload}.json")
+def load_traffic(workload, algorithmic_bytes):
+    """DRAM bytes of one Linear1 launch from the committed ncu summary: the
+    traffic / algorithmic-bytes ratio captured on the c3p shapes, applied to
+    this launch (the c3 and c4 layers share those expert shapes)."""
+    if workload not in ("c3", "c4", "c3p"):
+        return None
+    path = os.path.join(ROOT, "profiles", "gemm1_swiglu_c3p.md")
     if not os.path.exists(path):
         return None
+    import re
     with open(path) as f:
-        return json.load(f).get("dram_bytes_per_launch")
+        m = re.search(r"dram_bytes_per_launch_c3_scaled_ratio:\s*([0-9.]+)", f.read())
+    return int(float(m.group(1)) * algorithmic_bytes) if m else None
 
 
 # ------------------------------------------------------------------ oracle (CPU)

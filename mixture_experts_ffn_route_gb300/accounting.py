@@ -42,9 +42,10 @@ def gemm1_bytes(counts, H, I, has_shared=0, T=0):
 
 
 def gemm2_bytes(counts, H, I, has_shared=0, T=0):
-    """W2 of every active expert (I x H), Act rows in, expert output rows out."""
+    """W2 of every active expert (I x H), Act rows in (bf16), expert output
+    rows out (fp32)."""
     rows, n_active = _counts(counts, has_shared, T)
-    return n_active * I * H * BF16 + rows * I * BF16 + rows * H * BF16
+    return n_active * I * H * BF16 + rows * I * BF16 + rows * H * F32
 
 
 def dispatch_bytes(T, H, k):
@@ -59,8 +60,9 @@ def dispatch_payload_bytes(T, H, k):
 
 
 def combine_bytes(T, H, k, has_shared=0):
-    """k expert rows (+ the shared row) in, gates and row ids in, one row out."""
-    return (T * k + (T if has_shared else 0)) * H * BF16 + T * k * (F32 + I32) + T * H * BF16
+    """k fp32 expert rows (+ the shared row) in, gates and row ids in, one bf16
+    row out."""
+    return (T * k + (T if has_shared else 0)) * H * F32 + T * k * (F32 + I32) + T * H * BF16
 
 
 def route_bytes(T, H, E, k):

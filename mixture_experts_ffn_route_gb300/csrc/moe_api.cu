@@ -30,7 +30,8 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct WsLayout {
-  size_t status, logits, chunk_cnt, counts, row_off, tile_off, perm, inv, xp, act, yp, total;
+  size_t status, logits, wgt, rcount, flagged, pairs, s64, chunk_cnt, counts, row_off, tile_off,
+      perm, inv, xp, act, yp, total;
 };
 
 static WsLayout layout(const moe_params& p) {
@@ -43,6 +44,11 @@ static WsLayout layout(const moe_params& p) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(256);
   L.logits = take(T * E * sizeof(float));
+  L.wgt = take(static_cast<size_t>(p.H) * E * 2);
+  L.rcount = take(4 * sizeof(int));
+  L.flagged = take(T * 4 * sizeof(int));
+  L.pairs = take(T * E * 2 * sizeof(int));
+  L.s64 = take(T * E * sizeof(double));
   L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
   L.counts = take((E + 2) * sizeof(int));
   L.row_off = take((E + 2) * sizeof(int));
@@ -213,10 +219,20 @@ moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(ws, L.status);
   float* logits = at<float>(ws, L.logits);
+  uint16_t* WgT = at<uint16_t>(ws, L.wgt);
+  RouteScratch rs;
+  rs.counters = at<int>(ws, L.rcount);
+  rs.flagged = at<int4>(ws, L.flagged);
+  rs.pairs = at<int2>(ws, L.pairs);
+  rs.s64 = at<double>(ws, L.s64);
+  if (!hash) {
+    if (cudaMemsetAsync(rs.counters, 0, 4 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_transpose_wg(Wg, p->H, p->E, WgT, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if ((st = run_router_gemm(p, X, Wg, logits, status, s)) != MOE_OK) return st;
-  return cuda_status(launch_route_select(logits, X, Wg, bias, token_ids, tid2eid, V, p->T, p->H,
+  return cuda_status(launch_route_select(logits, X, WgT, bias, token_ids, tid2eid, V, p->T, p->H,
                                          p->E, p->k, p->score_fn, p->alpha, p->renorm, E_ids, G,
-                                         status, s));
+                                         rs, status, s));
 }
 
 static DispatchBufs dispatch_bufs(const moe_params* p, void* ws, const WsLayout& L) {

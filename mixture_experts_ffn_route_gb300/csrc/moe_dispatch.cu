@@ -12,7 +12,7 @@
 //   count   : per chunk of kChunk assignments, per-expert counts (smem atomics)
 //   scan    : per-expert exclusive prefix over chunks, then over experts
 //             (row offsets) and over 128-row tiles (tile offsets for the GEMMs)
-//   place   : one block per (expert, chunk): ballot-prefix ranks give each
+//   place   : one warp per (expert, chunk): ballot-prefix ranks give each
 //             assignment its row; writes perm[row] = f and inv[f] = row
 //   gather  : Xp[row] = X[perm[row] / k], 16-byte vectors, one warp per row
 //   combine : "mega_moe" page, section Token Combine: y_t = sum_j G[t, j] *
@@ -124,37 +124,36 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// One block per (32 experts, chunk): the chunk's ids are staged in shared
+// memory once; warp w ranks expert 32 * blockIdx.x + w with ballots, in
+// ascending flat index order.
 __global__ void __launch_bounds__(kThreads)
     dispatch_place_kernel(const int32_t* __restrict__ E_ids, int A, int E, int nchunk,
                           const int* __restrict__ chunk_base, const int* __restrict__ counts,
                           const int* __restrict__ row_off, int* __restrict__ perm, int* __restrict__ inv) {
-  __shared__ int wcount[32];
-  const int e = blockIdx.x, c = blockIdx.y;
+  __shared__ int ids[kChunk];
+  const int c = blockIdx.y;
+  const int f0 = c * kChunk;
+  const int n = min(A - f0, kChunk);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ids[i] = E_ids[f0 + i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + warp;
+  if (e >= E) return;
   const int b0 = chunk_base[static_cast<long long>(c) * E + e];
   const int b1 = (c + 1 < nchunk) ? chunk_base[static_cast<long long>(c + 1) * E + e] : counts[e];
-  if (b1 == b0) return;  // no assignment of e in this chunk (block-uniform)
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (b1 == b0) return;  // no assignment of e in this chunk
   int pos = row_off[e] + b0;
-  const int f1 = min(A, (c + 1) * kChunk);
-  for (int f0 = c * kChunk; f0 < f1; f0 += blockDim.x) {
-    const int f = f0 + threadIdx.x;
-    const bool mine = (f < f1) && (E_ids[f] == e);
+  for (int i0 = 0; i0 < n && pos < row_off[e] + b1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool mine = (i < n) && (ids[i] == e);
     const unsigned m = __ballot_sync(0xffffffffu, mine);
-    if (lane == 0) wcount[warp] = __popc(m);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
-      const int cw = wcount[w];
-      before += (w < warp) ? cw : 0;
-      total += cw;
-    }
     if (mine) {
-      const int row = pos + before + __popc(m & ((1u << lane) - 1u));
-      perm[row] = f;
-      inv[f] = row;
+      const int row = pos + __popc(m & ((1u << lane) - 1u));
+      perm[row] = f0 + i;
+      inv[f0 + i] = row;
     }
-    pos += total;
-    __syncthreads();
+    pos += __popc(m);
   }
 }
 
@@ -174,7 +173,7 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
   dispatch_scan_kernel<<<1, kThreads, 0, s>>>(b.chunk_cnt, b.nchunk, E, T, has_shared, b.counts,
                                               b.row_off, b.tile_off);
   if (A > 0) {
-    dispatch_place_kernel<<<dim3(E, b.nchunk), kThreads, 0, s>>>(E_ids, A, E, b.nchunk,
+    dispatch_place_kernel<<<dim3((E + 31) / 32, b.nchunk), kThreads, 0, s>>>(E_ids, A, E, b.nchunk,
                                                                  b.chunk_cnt, b.counts, b.row_off,
                                                                  b.perm, b.inv);
   }
@@ -198,12 +197,12 @@ __global__ void __launch_bounds__(256)
     for (; i + 96 < vecs; i += 128) {
       const uint4 a = __ldg(src + i), b2 = __ldg(src + i + 32), c2 = __ldg(src + i + 64),
                   d2 = __ldg(src + i + 96);
-      dst[i] = a;
-      dst[i + 32] = b2;
-      dst[i + 64] = c2;
-      dst[i + 96] = d2;
+      __stcs(dst + i, a);
+      __stcs(dst + i + 32, b2);
+      __stcs(dst + i + 64, c2);
+      __stcs(dst + i + 96, d2);
     }
-    for (; i < vecs; i += 32) dst[i] = __ldg(src + i);
+    for (; i < vecs; i += 32) __stcs(dst + i, __ldg(src + i));
   }
 }
 
@@ -247,7 +246,7 @@ __global__ void __launch_bounds__(kCombineThreads)
       const int p = rows[j];
       if (p < 0) continue;
       const float4* src = reinterpret_cast<const float4*>(Yp + static_cast<long long>(p) * H) + 2 * c;
-      const float4 u = __ldg(src), v = __ldg(src + 1);
+      const float4 u = __ldcs(src), v = __ldcs(src + 1);  // read once
       const float g = w[j];
       acc[0] += g * u.x; acc[1] += g * u.y; acc[2] += g * u.z; acc[3] += g * u.w;
       acc[4] += g * v.x; acc[5] += g * v.y; acc[6] += g * v.z; acc[7] += g * v.w;

@@ -47,12 +47,20 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
                         cudaStream_t s);
 int gemm_block_n(GemmKind kind);
 
-// Router top-k / hash epilogue over fp32 logits [T, E].
-cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* Wg,
+// Router selection over fp32 logits [T, E] (top-k with a float64 re-decision
+// of close tokens, or the hash lookup).  Scratch for the re-decision:
+struct RouteScratch {
+  int* counters;  // [0] close tokens, [1] candidate pairs; zeroed before select
+  int4* flagged;  // [T]      {token, first pair, pair count, 0}
+  int2* pairs;    // [T * E]  {token, expert}
+  double* s64;    // [T * E]  float64 selection score of each pair
+};
+cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT, cudaStream_t s);
+cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
                                 const float* bias, const int32_t* token_ids,
                                 const int32_t* tid2eid, int V, int T, int H, int E, int k,
                                 int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
-                                int* status, cudaStream_t s);
+                                const RouteScratch& rs, int* status, cudaStream_t s);
 
 // Dispatch: counts, offsets, permutation, inverse, tile offsets, gathered rows.
 struct DispatchBufs {

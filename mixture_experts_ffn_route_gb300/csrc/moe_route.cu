@@ -7,12 +7,20 @@
 // softmax(l), which is the top-k of l itself.  Section 路由与负载 / Hash 路由:
 // the ids are a table row of the token id, the gate formula is unchanged.
 //
-// One warp per token.  The k winners are found by k+1 rounds of a warp
-// arg-max (larger score first, equal scores to the lower id).  The fp32
-// selection is final unless two neighbouring scores among the first k+1 are
-// closer than a decision band; such a token is re-decided with float64 logits
-// recomputed from X and Wg for every expert within the band of the k-th score,
-// so that the ids equal those of an exact evaluation except at exact ties.
+// Exact ids from inexact logits.  The fp32 tensor-core logit is within a few
+// 1e-5 of the exact value, so the fp32 selection is final unless two
+// neighbouring scores among the first k+1 lie within a decision band.  Such a
+// token is re-decided in three steps:
+//   select    one warp per token: fp32 top-(k+1) by k+1 warp arg-max rounds;
+//             a close token appends every expert scoring within twice the band
+//             of its k-th score to a list of (token, expert) pairs;
+//   recheck   one warp per pair: the logit sum_h X[t,h] Wg[h,e] to ~48 bits
+//             over a transposed copy of Wg (contiguous rows; each bf16 product
+//             is exact in fp32 and the sum is carried as a float pair), then
+//             its float64 selection score;
+//   reselect  one warp per close token: top-k of the float64 scores of its
+//             candidates, larger score first, equal scores to the lower id.
+// The ids then equal those of an exact evaluation except at exact ties.
 #include <float.h>
 
 #include "moe_common.cuh"
@@ -20,13 +28,12 @@
 
 namespace moe {
 
-constexpr int kWarps = 8;          // tokens per block
+constexpr int kWarps = 8;  // tokens (or pairs) per 256-thread block
 constexpr int kMaxK = 16;
-// Decision bands.  The fp32 tensor-core logit differs from the exact one by
-// at most a few 1e-5 at the workload sizes.  Sigmoid and sqrt-softplus have
-// slope <= 1/2, so their scores are within ~2e-5 of exact and a band of 2e-4
-// on the score leaves a margin of about 10x.  Softmax selects on the logit
-// itself; its band is 1e-3 * max(1, |l|).
+// Decision bands.  Sigmoid and sqrt-softplus have slope <= 1/3, so their fp32
+// scores are within ~2e-5 of exact; a band of 2e-4 on the score leaves a
+// margin of about 10x.  Softmax selects on the logit itself; its band is
+// 1e-3 * max(1, |l|).
 constexpr float kBand = 2e-4f;
 constexpr float kBandSoftmax = 1e-3f;
 
@@ -46,32 +53,24 @@ __device__ __forceinline__ double score_f64(double l, int fn) {
   return l;
 }
 
-// (value, id) arg-max across the warp: larger value, then lower id.
-__device__ __forceinline__ void warp_argmax(float& v, int& id) {
+// (value, id) order: larger value first, equal values lower id first.
+template <typename V>
+__device__ __forceinline__ bool before(V v, int id, V ov, int oid) {
+  return v > ov || (v == ov && id < oid);
+}
+
+template <typename V>
+__device__ __forceinline__ void warp_argmax(V& v, int& id) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const V ov = __shfl_xor_sync(0xffffffffu, v, o);
     const int oid = __shfl_xor_sync(0xffffffffu, id, o);
-    if (ov > v || (ov == v && oid < id)) { v = ov; id = oid; }
+    if (before(ov, oid, v, id)) { v = ov; id = oid; }
   }
 }
 
-__device__ __forceinline__ void warp_argmax_d(double& v, int& id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oid = __shfl_xor_sync(0xffffffffu, id, o);
-    if (ov > v || (ov == v && oid < id)) { v = ov; id = oid; }
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
+template <typename V>
+__device__ __forceinline__ V warp_sum(V v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
@@ -83,24 +82,51 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// float64 logit l[t, e] = sum_h X[t, h] Wg[h, e] (bf16 products are exact).
-__device__ double logit_f64(const uint16_t* __restrict__ xrow, const uint16_t* __restrict__ Wg,
-                            int H, int E, int e, int lane) {
-  double acc = 0.0;
-  for (int h = lane; h < H; h += 32) {
-    const float x = __uint_as_float(static_cast<uint32_t>(__ldg(xrow + h)) << 16);
-    const float w = __uint_as_float(static_cast<uint32_t>(__ldg(Wg + static_cast<long long>(h) * E + e)) << 16);
-    acc += static_cast<double>(x) * static_cast<double>(w);
+// Softmax normaliser of one token's logits: max and sum of exp(l - max).
+__device__ __forceinline__ void softmax_norm(const float* lrow, int E, int lane, float& lmax,
+                                             float& zsum) {
+  lmax = -FLT_MAX;
+  for (int e = lane; e < E; e += 32) lmax = fmaxf(lmax, lrow[e]);
+  lmax = warp_max(lmax);
+  zsum = 0.0f;
+  for (int e = lane; e < E; e += 32) zsum += expf(lrow[e] - lmax);
+  zsum = warp_sum(zsum);
+}
+
+// Lane 0 writes ids and gates of one token from the fp32 logits.
+__device__ void write_gates(const float* lrow, int E, int k, int fn, float alpha, int renorm,
+                            const int* sel, bool tok_ok, float lmax, float zsum, int32_t* ids,
+                            float* G, int* status) {
+  float a[kMaxK];
+  float den = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const int e = sel[j];
+    float v = 0.0f;
+    if (e >= 0 && e < E) {
+      const float l = lrow[e];
+      v = (fn == 2) ? expf(l - lmax) / zsum : score_f32(l, fn);
+    } else if (tok_ok) {
+      set_flag(status, kFlagBadExpert);  // a table entry outside [0, E)
+    }
+    a[j] = v;
+    den += v;
   }
-  return warp_sum_d(acc);
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float g = alpha * a[j];
+    if (renorm) g = den > 0.0f ? alpha * a[j] / den : 0.0f;
+    ids[j] = sel[j];
+    G[j] = g;
+  }
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
-    route_select_kernel(const float* __restrict__ logits, const uint16_t* __restrict__ X,
-                        const uint16_t* __restrict__ Wg, const float* __restrict__ bias,
+    route_select_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                         const int32_t* __restrict__ token_ids, const int32_t* __restrict__ tid2eid,
-                        int V, int T, int H, int E, int k, int fn, float alpha, int renorm,
-                        int32_t* __restrict__ E_ids, float* __restrict__ G, int* status) {
+                        int V, int T, int E, int k, int fn, float alpha, int renorm,
+                        int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs,
+                        int* status) {
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + warp;
@@ -108,14 +134,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   float* s = sh + warp * E;  // selection scores of this token
   const float* lrow = logits + static_cast<long long>(t) * E;
 
-  // softmax normaliser (max and sum over all experts)
-  float lmax = -FLT_MAX, zsum = 0.0f;
-  if (fn == 2) {
-    for (int e = lane; e < E; e += 32) lmax = fmaxf(lmax, lrow[e]);
-    lmax = warp_max(lmax);
-    for (int e = lane; e < E; e += 32) zsum += expf(lrow[e] - lmax);
-    zsum = warp_sum(zsum);
-  }
+  float lmax = 0.0f, zsum = 1.0f;
+  if (fn == 2) softmax_norm(lrow, E, lane, lmax, zsum);
 
   int sel[kMaxK];
   bool tok_ok = true;
@@ -142,7 +162,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       int bid = 0x7fffffff;
       for (int e = lane; e < E; e += 32) {
         const float v = s[e];
-        if (v > best || (v == best && e < bid)) { best = v; bid = e; }
+        if (before(v, e, best, bid)) { best = v; bid = e; }
       }
       warp_argmax(best, bid);
       top[r] = best;
@@ -150,15 +170,12 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (lane == 0) s[bid] = -FLT_MAX;  // taken
       __syncwarp();
     }
-    // ambiguity: two neighbouring scores among the first k+1 within the band
     bool close = false;
 #pragma unroll 1
-    for (int r = 0; r + 1 < rounds; ++r) {
-      close |= (top[r] - top[r + 1]) < band_at(top[r], fn);
-    }
+    for (int r = 0; r + 1 < rounds; ++r) close |= (top[r] - top[r + 1]) < band_at(top[r], fn);
     if (close) {
-      // candidates: the k winners plus every expert within the band below the
-      // k-th score; restore the scores, then decide in float64.
+      // candidates: every expert within twice the band below the k-th score
+      // (the k winners among them); restore the scores and list the pairs.
       for (int e = lane; e < E; e += 32) {
         float v = score_f32(lrow[e], fn);
         if (bias != nullptr) v += bias[e];
@@ -167,75 +184,154 @@ __global__ void __launch_bounds__(kWarps * 32)
       __syncwarp();
       const float kth = top[k - 1];
       const float lim = kth - 2.0f * band_at(kth, fn);
-      const uint16_t* xrow = X + static_cast<long long>(t) * H;
-      // candidates are taken one at a time by the whole warp; every lane keeps
-      // the same sorted list of the k best float64 scores.
-      double best_v[kMaxK];
-      int best_id[kMaxK];
-#pragma unroll 1
-      for (int j = 0; j < k; ++j) { best_v[j] = -DBL_MAX; best_id[j] = 0x7fffffff; }
-#pragma unroll 1
+      int count = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool cand = (e < E) && (s[e] >= lim);
-        unsigned m = __ballot_sync(0xffffffffu, cand);
-        while (m) {
-          const int c = e0 + __ffs(m) - 1;
-          m &= m - 1;
-          const double l64 = logit_f64(xrow, Wg, H, E, c, lane);
-          double v = score_f64(l64, fn);
-          if (bias != nullptr) v += static_cast<double>(bias[c]);
-          // insert (v, c) into the sorted top-k list (all lanes hold copies)
-          int pos = k;
-#pragma unroll 1
-          for (int j = k - 1; j >= 0; --j) {
-            if (v > best_v[j] || (v == best_v[j] && c < best_id[j])) pos = j; else break;
-          }
-          if (pos < k) {
-#pragma unroll 1
-            for (int j = k - 1; j > pos; --j) { best_v[j] = best_v[j - 1]; best_id[j] = best_id[j - 1]; }
-            best_v[pos] = v;
-            best_id[pos] = c;
-          }
-        }
+        count += __popc(__ballot_sync(0xffffffffu, e < E && s[e] >= lim));
       }
-#pragma unroll 1
-      for (int j = 0; j < k; ++j) sel[j] = best_id[j];
+      int base = 0;
+      if (lane == 0) {
+        base = atomicAdd(rs.counters + 1, count);
+        const int fi = atomicAdd(rs.counters + 0, 1);
+        rs.flagged[fi] = make_int4(t, base, count, 0);
+      }
+      base = __shfl_sync(0xffffffffu, base, 0);
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool cand = e < E && s[e] >= lim;
+        const unsigned m = __ballot_sync(0xffffffffu, cand);
+        if (cand) rs.pairs[base + __popc(m & ((1u << lane) - 1u))] = make_int2(t, e);
+        base += __popc(m);
+      }
     }
   }
+  // fp32 decision (a close token's ids and gates are rewritten by reselect)
+  if (lane == 0)
+    write_gates(lrow, E, k, fn, alpha, renorm, sel, tok_ok, lmax, zsum,
+                E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
+}
 
-  // ------------------------------------------------------------------ gates
-  if (lane == 0) {
-    float a[kMaxK];
-    float den = 0.0f;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      const int e = sel[j];
-      float v = 0.0f;
-      if (e >= 0 && e < E) {
-        const float l = lrow[e];
-        v = (fn == 2) ? expf(l - lmax) / zsum : score_f32(l, fn);
-      } else if (tok_ok) {
-        set_flag(status, kFlagBadExpert);  // a table entry outside [0, E)
+// Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// Float64 selection score of the listed (token, expert) pairs.  Each bf16 x
+// bf16 product is exact in fp32; the products are summed as unevaluated float
+// pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's fp64 rate is low),
+// and the pairs are folded into float64 for the warp sum.  The result is
+// within ~1e-12 of the exact logit at the workload sizes.
+__global__ void __launch_bounds__(kWarps * 32)
+    route_recheck_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
+                         const float* __restrict__ bias, int H, int fn, RouteScratch rs) {
+  const int n = rs.counters[1];
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int vecs = H / 8;
+  for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+    const int2 pr = rs.pairs[i];
+    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(pr.x) * H);
+    const uint4* wr = reinterpret_cast<const uint4*>(WgT + static_cast<long long>(pr.y) * H);
+    // eight independent (hi, lo) accumulators, one per element of a 16-byte
+    // vector: each sees H / 256 terms, which keeps the rounding of lo tiny
+    float hi[8], lo[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.0f;
+#pragma unroll 2
+    for (int v = lane; v < vecs; v += 32) {
+      const uint4 a = __ldg(xr + v), b = __ldg(wr + v);
+      const float p[8] = {bf16_lo(a.x) * bf16_lo(b.x), bf16_hi(a.x) * bf16_hi(b.x),
+                          bf16_lo(a.y) * bf16_lo(b.y), bf16_hi(a.y) * bf16_hi(b.y),
+                          bf16_lo(a.z) * bf16_lo(b.z), bf16_hi(a.z) * bf16_hi(b.z),
+                          bf16_lo(a.w) * bf16_lo(b.w), bf16_hi(a.w) * bf16_hi(b.w)};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float sum, err;
+        two_sum(hi[q], p[q], sum, err);
+        hi[q] = sum;
+        lo[q] += err;
       }
-      a[j] = v;
-      den += v;
     }
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      float g = alpha * a[j];
-      if (renorm) g = den > 0.0f ? alpha * a[j] / den : 0.0f;
-      E_ids[static_cast<long long>(t) * k + j] = sel[j];
-      G[static_cast<long long>(t) * k + j] = g;
+    double part = 0.0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) part += static_cast<double>(hi[q]) + static_cast<double>(lo[q]);
+    const double l = warp_sum(part);
+    if (lane == 0) {
+      double v = score_f64(l, fn);
+      if (bias != nullptr) v += static_cast<double>(bias[pr.y]);
+      rs.s64[i] = v;
     }
   }
 }
 
-cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* Wg,
+// Re-decide each close token from the float64 scores of its candidates.
+__global__ void __launch_bounds__(kWarps * 32)
+    route_reselect_kernel(const float* __restrict__ logits, int E,
+                          int k, int fn, float alpha, int renorm, int32_t* __restrict__ E_ids,
+                          float* __restrict__ G, RouteScratch rs, int* status) {
+  const int n = rs.counters[0];
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < n; j += nw) {
+    const int4 f = rs.flagged[j];
+    const int t = f.x, base = f.y, count = f.z;
+    int sel[kMaxK];
+    double last_v = DBL_MAX;
+    int last_id = -1;
+    // round r: the best candidate strictly after the previous winner in the
+    // (larger score, lower id) order, so no candidate is taken twice
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      double best = -DBL_MAX;
+      int bid = 0x7fffffff;
+      for (int i = lane; i < count; i += 32) {
+        const int e = rs.pairs[base + i].y;
+        const double v = rs.s64[base + i];
+        if (before(last_v, last_id, v, e) && before(v, e, best, bid)) { best = v; bid = e; }
+      }
+      warp_argmax(best, bid);
+      sel[r] = bid;
+      last_v = best;
+      last_id = bid;
+    }
+    const float* lrow = logits + static_cast<long long>(t) * E;
+    float lmax = 0.0f, zsum = 1.0f;
+    if (fn == 2) softmax_norm(lrow, E, lane, lmax, zsum);
+    if (lane == 0)
+      write_gates(lrow, E, k, fn, alpha, renorm, sel, true, lmax, zsum,
+                  E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
+  }
+}
+
+// WgT[e][h] = Wg[h][e], 32 x 32 tiles through shared memory.
+__global__ void transpose_wg_kernel(const uint16_t* __restrict__ Wg, int H, int E,
+                                    uint16_t* __restrict__ WgT) {
+  __shared__ uint16_t tile[32][33];
+  const int e0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int h = h0 + i, e = e0 + threadIdx.x;
+    if (h < H && e < E) tile[i][threadIdx.x] = Wg[static_cast<long long>(h) * E + e];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int e = e0 + i, h = h0 + threadIdx.x;
+    if (h < H && e < E) WgT[static_cast<long long>(e) * H + h] = tile[threadIdx.x][i];
+  }
+}
+
+cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT, cudaStream_t s) {
+  dim3 grid((E + 31) / 32, (H + 31) / 32);
+  transpose_wg_kernel<<<grid, dim3(32, 8), 0, s>>>(Wg, H, E, WgT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
                                 const float* bias, const int32_t* token_ids,
                                 const int32_t* tid2eid, int V, int T, int H, int E, int k,
                                 int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
-                                int* status, cudaStream_t s) {
+                                const RouteScratch& rs, int* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int blocks = (T + kWarps - 1) / kWarps;
   const size_t sh = static_cast<size_t>(kWarps) * E * sizeof(float);
@@ -245,9 +341,14 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                          static_cast<int>(sh));
     if (e != cudaSuccess) return e;
   }
-  route_select_kernel<<<blocks, kWarps * 32, sh, s>>>(logits, X, Wg, bias, token_ids, tid2eid, V,
-                                                      T, H, E, k, score_fn, alpha, renorm, E_ids,
-                                                      G, status);
+  route_select_kernel<<<blocks, kWarps * 32, sh, s>>>(logits, bias, token_ids, tid2eid, V, T, E,
+                                                      k, score_fn, alpha, renorm, E_ids, G, rs,
+                                                      status);
+  if (token_ids != nullptr) return cudaGetLastError();
+  const int grid = 2 * num_sms();
+  route_recheck_kernel<<<grid, kWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
+  route_reselect_kernel<<<grid, kWarps * 32, 0, s>>>(logits, E, k, score_fn, alpha, renorm, E_ids,
+                                                     G, rs, status);
   return cudaGetLastError();
 }
 

@@ -123,4 +123,4 @@ def test_accounting_counts_active_experts_once():
     assert accounting.gemm1_flops(counts, H, I) == 2 * 133 * H * 2 * I
     assert accounting.gemm1_bytes(counts, H, I) == 2 * H * 2 * I * 2 + 133 * H * 2 + 133 * I * 2
     with_shared = accounting.gemm2_bytes(counts, H, I, has_shared=1, T=10)
-    assert with_shared == 3 * I * H * 2 + 143 * I * 2 + 143 * H * 2
+    assert with_shared == 3 * I * H * 2 + 143 * I * 2 + 143 * H * 4

@@ -115,6 +115,45 @@ def test_route_equal_scores_go_to_the_lower_id():
     check_gates(G, G_ref)
 
 
+@pytest.mark.parametrize("score", [0, 1, 2])
+def test_route_near_ties_are_decided_exactly(score):
+    # experts 3 and 5 differ only in Wg[0, :], by one bf16 step of 2^-11, and
+    # X[:, 0] = +-2^-20: their logits differ by exactly 2^-31, far below what an
+    # fp32 accumulation resolves, so the order comes from the re-decision.
+    rng = np.random.default_rng(13)
+    T, H, E, k = 64, 256, 16, 4
+    X = rng.standard_normal((T, H)).astype(np.float32)
+    X[:, 0] = np.where(np.arange(T) % 2 == 0, 2.0 ** -20, -(2.0 ** -20))
+    Wg = (rng.standard_normal((H, E)) / 16).astype(np.float32)
+    Wg[:, 5] = Wg[:, 3]
+    Wg[0, 3] = 2.0 ** -4
+    Wg[0, 5] = 2.0 ** -4 + 2.0 ** -11
+    Xb, Wgb = synth.bf16_bits_from_f32(X), synth.bf16_bits_from_f32(Wg)
+    bias = None
+    if score != oracle.SCORE_SOFTMAX:
+        bias = np.zeros(E, np.float32)
+        bias[[3, 5]] = 5.0  # always the first two
+    else:
+        # softmax selects on the logit: make columns 3 and 5 large (and equal
+        # apart from row 0) against positive token rows
+        Xb = synth.bf16_bits_from_f32(np.concatenate([X[:, :1], np.abs(X[:, 1:])], 1))
+        Wgb[1:, 3] = synth.bf16_bits_from_f32(np.full(H - 1, 0.25, np.float32))
+        Wgb[1:, 5] = Wgb[1:, 3]
+    p = moe.make_params(T, H, E, k, 64, score_fn=score, renorm=0 if score == 2 else 1)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    G = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    b = torch.from_numpy(bias).to(DEV) if bias is not None else None
+    moe.moe_route(p, bf(Xb), bf(Wgb), b, None, None, 0, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref, l64 = oracle.route(Xb, Wgb, bias, score, k, 1.0, p.renorm)
+    assert (np.abs(l64[:, 5] - l64[:, 3]) == 2.0 ** -31).all()
+    ids = E_ids.cpu().numpy()
+    want = np.where((np.arange(T) % 2 == 0)[:, None], [5, 3], [3, 5])
+    assert (ids[:, :2] == want).all()
+    assert np.array_equal(ids, ids_ref)
+
+
 # ---------------------------------------------------------------------- dispatch
 def _dispatch_gpu(p, E_ids):
     ws = moe.alloc_workspace(p, DEV)
