@@ -134,6 +134,23 @@ moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_
                        const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* Dispatch for callers that cannot provide a workspace.  There is no
+ * counterpart of this call in the pages: it exists because some callers may not
+ * allocate device memory where they route tokens (their device memory is held
+ * by another allocator, or a cudaMalloc/cudaFree, which can synchronise the
+ * device, is not acceptable on their path).  Same results as moe_dispatch
+ * (counts [E], offsets [E + 1], perm [T * k], all caller-owned device memory),
+ * but the scratch is a fixed array inside the library (about 1.2 MB, held on
+ * every GPU that loads the library until the process exits).
+ * Limits: T * k <= 262144 and E <= 512, else MOE_ERR_UNSUPPORTED before any
+ * device work.  The call allocates nothing.  Its first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU race, so serialise them.  Ids outside [0, E) are dropped
+ * without a status report. */
+moe_status moe_dispatch_noalloc(const moe_params* p, const int32_t* E_ids, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, void* stream);
+
 /* moe_forward, recording caller-created CUDA events (cudaEvent_t, NULL entries
  * skipped) on `stream` at the stage boundaries, for measurement:
  *   stage_events[0] before dispatch      [1] after dispatch and row gather

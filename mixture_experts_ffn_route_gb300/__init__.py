@@ -57,6 +57,7 @@ SIGNATURES = {
     "moe_forward": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_timed": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                          ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P]),
     "moe_sync_status": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -160,6 +161,14 @@ def moe_route_logits(p, X, Wg, logits, ws, stream=None):
 def moe_dispatch(p, E_ids, counts, offsets, perm, ws, stream=None):
     return _check(lib().moe_dispatch(ctypes.byref(p), _ptr(E_ids), _ptr(counts), _ptr(offsets),
                                      _ptr(perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(p, E_ids, counts, offsets, perm, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate device
+    memory where they route tokens; scratch is a fixed array in the library
+    (limits T*k <= 262144, E <= 512).  Calls that overlap on the GPU race."""
+    return _check(lib().moe_dispatch_noalloc(ctypes.byref(p), _ptr(E_ids), _ptr(counts), _ptr(offsets),
+                                             _ptr(perm), _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_forward(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, stream=None):
