@@ -16,14 +16,20 @@
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16)
 //               into one of two TMEM accumulators and commits to mbarriers.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one token row per thread),
-//               fuse SwiGLU (bf16 out) or store fp32, free the
-//               accumulator so the next tile's MMAs overlap this epilogue.
+//               fuse SwiGLU (bf16 out) or keep fp32, stage through shared memory
+//               for full-line stores, free the accumulator so the next tile's
+//               MMAs overlap this epilogue.
 // Tiles are walked in (group, column tile, 128-row tile) order, striding by
 // gridDim.x.  Group row ranges come from device memory.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
+
+// Row pitch (32-bit words) of the epilogue staging buffer: 32 data words plus
+// 4 of padding, so 16-byte accesses by the 8 lanes of one phase touch 8
+// distinct bank quads.
+constexpr int kStgWords = 36;
 
 template <int BN>
 struct GemmCfg {
@@ -33,7 +39,9 @@ struct GemmCfg {
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  // epilogue staging: per epilogue warp 32 rows x kStgWords 32-bit words
+  static constexpr int STG_BYTES = 4 * 32 * kStgWords * 4;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES + STG_BYTES;
 };
 
 struct TileInfo {
@@ -99,6 +107,7 @@ __global__ void __launch_bounds__(192, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 4));
+  uint32_t* stg_area = reinterpret_cast<uint32_t*>(bar_area + C::BAR_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -199,8 +208,12 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Each warp owns 32 accumulator rows (its TMEM lane quarter).  A chunk of
+    // 32 columns goes TMEM -> registers (one row per lane) -> a padded shared
+    // staging block -> global memory with every store instruction writing
+    // whole 128-byte lines (4 rows of fp32 or 8 rows of bf16 per instruction).
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;
+    uint32_t* stg = stg_area + q * 32 * kStgWords;
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const TileInfo t = decode_tile(p, tile);
@@ -210,44 +223,66 @@ __global__ void __launch_bounds__(192, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int row = t.row0 + r;
-      const bool row_ok = row < t.row_end;
+      const int wrow0 = t.row0 + q * 32;  // first output row of this warp
       if (KIND == kGemmSwiGLU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + static_cast<long long>(row) * p.ldo;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           float g[32], u[32];
           tmem_ld_32x32(tb + c, g);
           tmem_ld_32x32(tb + 128 + c, u);
           const int col = t.n * 128 + c;
-          if (row_ok && col < p.n_out) {
-            uint32_t w[16];
+          uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
-              const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
-              w[i] = pack_bf16x2(a0, a1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
+            const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+            w[i] = pack_bf16x2(a0, a1);
           }
+          uint4* srow = reinterpret_cast<uint4*>(stg + lane * kStgWords);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            srow[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          __syncwarp();
+          if (col < p.n_out) {
+            // 8 rows x 64 bytes per instruction: lane -> row rr + lane/4, quad lane%4
+            const int qd = lane & 3;
+#pragma unroll
+            for (int rr = 0; rr < 32; rr += 8) {
+              const int r = rr + (lane >> 2);
+              const uint4 v = reinterpret_cast<const uint4*>(stg + r * kStgWords)[qd];
+              const int grow = wrow0 + r;
+              if (grow < t.row_end)
+                *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 8 * qd) = v;
+            }
+          }
+          __syncwarp();
         }
       } else {  // router logits and Linear2 expert outputs: fp32
-        float* out = static_cast<float*>(p.out) + static_cast<long long>(row) * p.ldo;
+        float* out = static_cast<float*>(p.out);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld_32x32(tb + c, v);
           const int col = t.n * BN + c;
-          if (row_ok) {
+          float4* srow = reinterpret_cast<float4*>(stg + lane * kStgWords);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (col + 4 * i < p.n_out)
-                *reinterpret_cast<float4*>(out + col + 4 * i) =
-                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            srow[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          __syncwarp();
+          // 4 rows x 128 bytes per instruction: lane -> row rr + lane/8, quad lane%8
+          const int qd = lane & 7;
+          if (col + 4 * qd < p.n_out) {
+#pragma unroll
+            for (int rr = 0; rr < 32; rr += 4) {
+              const int r = rr + (lane >> 3);
+              const float4 x = reinterpret_cast<const float4*>(stg + r * kStgWords)[qd];
+              const int grow = wrow0 + r;
+              if (grow < t.row_end)
+                *reinterpret_cast<float4*>(out + static_cast<long long>(grow) * p.ldo + col + 4 * qd) = x;
+            }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
