@@ -153,7 +153,7 @@ moe_status moe_dispatch_noalloc(const moe_params* p, const int32_t* E_ids, int32
 
 /* moe_forward, recording caller-created CUDA events (cudaEvent_t, NULL entries
  * skipped) on `stream` at the stage boundaries, for measurement:
- *   stage_events[0] before dispatch      [1] after dispatch and row gather
+ *   stage_events[0] before dispatch      [1] after dispatch
  *   stage_events[2] after Linear1+SwiGLU [3] after Linear2   [4] after combine
  * stage_events itself may be NULL (then this is moe_forward). */
 moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32_t* E_ids,

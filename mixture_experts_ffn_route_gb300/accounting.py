@@ -36,7 +36,8 @@ def router_flops(T, H, E):
 
 
 def gemm1_bytes(counts, H, I, has_shared=0, T=0):
-    """W1 of every active expert (H x 2I), its input rows (H) and Act rows (I)."""
+    """W1 of every active expert (H x 2I), its input rows (H; gathered from the
+    token rows by the permutation) and Act rows (I)."""
     rows, n_active = _counts(counts, has_shared, T)
     return n_active * H * 2 * I * BF16 + rows * H * BF16 + rows * I * BF16
 
@@ -49,9 +50,10 @@ def gemm2_bytes(counts, H, I, has_shared=0, T=0):
 
 
 def dispatch_bytes(T, H, k):
-    """Expert ids in; token rows read once; T*k permuted rows written; perm/inv."""
+    """Expert ids in (twice: count and place); perm and inv out.  The permuted
+    token rows are not materialised (Linear1 gathers them)."""
     A = T * k
-    return A * I32 + T * H * BF16 + A * H * BF16 + 2 * A * I32
+    return 2 * A * I32 + 2 * A * I32
 
 
 def dispatch_payload_bytes(T, H, k):

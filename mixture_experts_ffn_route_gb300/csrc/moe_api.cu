@@ -31,7 +31,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace layout (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, wgt, rcount, flagged, pairs, s64, chunk_cnt, counts, row_off, tile_off,
-      perm, inv, xp, act, yp, total;
+      perm, inv, act, yp, total;
 };
 
 static WsLayout layout(const moe_params& p) {
@@ -55,7 +55,6 @@ static WsLayout layout(const moe_params& p) {
   L.tile_off = take((E + 2) * sizeof(int));
   L.perm = take(A * sizeof(int));
   L.inv = take(A * sizeof(int));
-  L.xp = take(A * static_cast<size_t>(p.H) * 2);
   L.act = take((A + Tsh) * static_cast<size_t>(p.I) * 2);
   L.yp = take((A + Tsh) * static_cast<size_t>(p.H) * sizeof(float));
   L.total = o;
@@ -288,7 +287,6 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
   const int T = p->T, H = p->H, E = p->E, k = p->k, I = p->I;
   const int A = T * k;
   const int Tsh = p->has_shared ? T : 0;
-  uint16_t* Xp = at<uint16_t>(ws, L.xp);
   uint16_t* Act = at<uint16_t>(ws, L.act);
   float* Yp = at<float>(ws, L.yp);
 
@@ -298,18 +296,18 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
   };
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = launch_dispatch(E_ids, T, k, E, p->has_shared, b, status, s);
-  if (e == cudaSuccess) e = launch_gather_rows(X, b.perm, b.row_off, E, A, k, H, Xp, s);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   const int groups = E + (p->has_shared ? 1 : 0);
   const int mt_bound = (A + kBM - 1) / kBM + E + (Tsh + kBM - 1) / kBM;
 
-  // Linear1 + SwiGLU:  Act = SwiGLU(Xp W1[e]);  shared group reads X directly
+  // Linear1 + SwiGLU:  Act = SwiGLU(X[rows of e] W1[e]), the rows gathered from
+  // X by the permutation inside the GEMM; the shared group takes X as it is
   {
     GemmMaps maps;
-    bool ok = make_map_rows(&maps.a, Xp, A, H) && make_map_rows(&maps.a2, X, T, H) &&
-              make_map_weights(&maps.b, W1, E, H, 2 * I);
+    bool ok = make_map_rows(&maps.a, X, T, H) && make_map_weights(&maps.b, W1, E, H, 2 * I);
+    maps.a2 = maps.a;
     if (ok) ok = p->has_shared ? make_map_weights(&maps.b2, Ws1, 1, H, 2 * I) : (maps.b2 = maps.b, true);
     if (!ok) return MOE_ERR_CUDA;
     GemmParams g;
@@ -318,7 +316,11 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
     g.tile_off = b.tile_off;
     g.num_groups = groups;
     g.shared_group = p->has_shared ? E : -1;
-    g.a2_shared = 1;
+    g.a2_shared = 0;
+    g.gather_src = X;
+    g.gather_perm = b.perm;
+    g.gather_k = k;
+    g.gather_rows = T;
     g.n_tiles = (I + 127) / 128;
     g.num_kb = H / kBK;
     g.n_out = I;

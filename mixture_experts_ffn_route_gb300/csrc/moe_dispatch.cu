@@ -14,7 +14,8 @@
 //             (row offsets) and over 128-row tiles (tile offsets for the GEMMs)
 //   place   : one warp per (expert, chunk): ballot-prefix ranks give each
 //             assignment its row; writes perm[row] = f and inv[f] = row
-//   gather  : Xp[row] = X[perm[row] / k], 16-byte vectors, one warp per row
+// The permuted token rows themselves are never written: Linear1 copies them
+// from X by perm while it loads its A tiles.
 //   combine : "mega_moe" page, section Token Combine: y_t = sum_j G[t, j] *
 //             Yp[inv[t*k + j]] (+ the shared expert's row); Yp is fp32, the sum
 //             is fp32 and y_t is rounded to bf16 once
@@ -177,43 +178,6 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
                                                                  b.chunk_cnt, b.counts, b.row_off,
                                                                  b.perm, b.inv);
   }
-  return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------- gather
-__global__ void __launch_bounds__(256)
-    gather_rows_kernel(const uint16_t* __restrict__ X, const int* __restrict__ perm,
-                       const int* __restrict__ row_off, int E, int k, int H, uint16_t* __restrict__ Xp) {
-  const int rows = row_off[E];
-  const int vecs = H / 8;  // 16-byte vectors per row
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int p = gw; p < rows; p += nw) {
-    const int t = perm[p] / k;
-    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<long long>(p) * H);
-    int i = lane;
-    for (; i + 96 < vecs; i += 128) {
-      const uint4 a = __ldg(src + i), b2 = __ldg(src + i + 32), c2 = __ldg(src + i + 64),
-                  d2 = __ldg(src + i + 96);
-      __stcs(dst + i, a);
-      __stcs(dst + i + 32, b2);
-      __stcs(dst + i + 64, c2);
-      __stcs(dst + i + 96, d2);
-    }
-    for (; i < vecs; i += 32) __stcs(dst + i, __ldg(src + i));
-  }
-}
-
-cudaError_t launch_gather_rows(const uint16_t* X, const int* perm, const int* row_off, int E,
-                               int A, int k, int H, uint16_t* Xp, cudaStream_t s) {
-  if (A <= 0) return cudaSuccess;
-  const int warps_needed = A;
-  int blocks = (warps_needed + 7) / 8;
-  const int cap = num_sms() * 8;
-  if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(X, perm, row_off, E, k, H, Xp);
   return cudaGetLastError();
 }
 

@@ -2,17 +2,20 @@
 //
 // Serves the three contractions of the layer:
 //   router  : logits[T, E] = X[T, H] Wg[H, E]                      (fp32 out)
-//   Linear1 : Act[rows, I] = SiLU(Xp W1[e][:, :I]) * (Xp W1[e][:, I:])  (bf16 out)
+//   Linear1 : Act[rows, I] = SiLU(X_e W1[e][:, :I]) * (X_e W1[e][:, I:])  (bf16 out)
 //   Linear2 : Yp[rows, H]  = Act W2[e]                              (fp32 out)
 // The expert FFN is the "Expert Compute" step of the "mega_moe" page
 // (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
 // projection); the router product is the gating linear of "Megatron-LM 的 MoE
 // 并行：以 DeepSeek-V4 为例" (section 路由张量).
 //
-// Structure (one CTA per SM, 192 threads):
+// Structure (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: A tile [128 rows x 64 k] K-major and B tile
 //               [64 k x BN cols] MN-major (the weights keep their [K][N] row-major
 //               layout), both with 128-byte swizzle, into a STAGES-deep ring.
+//   warps 6..9  Linear1 only: copy the A rows straight from the token rows X
+//               by the dispatch permutation (cp.async), so the permuted rows
+//               are never written to memory.
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16)
 //               into one of two TMEM accumulators and commits to mbarriers.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one token row per thread),
@@ -97,7 +100,7 @@ __device__ __forceinline__ int b_box_col(const GemmParams& p, int n, int j) {
 }
 
 template <int BN, int KIND>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                    const GemmParams p) {
@@ -118,9 +121,11 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
 
+  const bool gather = (KIND == kGemmSwiGLU) && (p.gather_src != nullptr);
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      // the TMA producer's arrival, plus one per gather thread when gathering
+      mbar_init(full0 + 8 * s, gather ? 1 + 128 : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -150,6 +155,8 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for a free stage, posts the byte count and loads B, and A
+    // too unless the gather warps copy the A rows.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -163,14 +170,70 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(sa, mA, fb, kb * kBK, t.a_row0);
+          if (gather) {
+            mbar_arrive_expect_tx(fb, C::B_BYTES);
+          } else {
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            tma_load_2d(sa, mA, fb, kb * kBK, t.a_row0);
+          }
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_3d(sb + j * (64 * kBK * 2), mB, fb, b_box_col<BN, KIND>(p, t.n, j),
                         kb * kBK, bz);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ row gather
+    // Linear1 only: the four gather warps copy each A tile's 128 token rows
+    // (assignment row r -> token perm[r] / k) into the 128-byte-swizzled
+    // K-major layout the MMA reads: 16-byte chunk c of tile row r lands at
+    // chunk c ^ (r % 8).  Eight lanes cover one 128-byte row segment, so one
+    // instruction moves four whole rows.  Every thread then arrives on the
+    // stage's barrier when its copies have landed (cp.async.mbarrier.arrive),
+    // which lets the warps run the full ring ahead of the MMA.  Rows past the
+    // group's end are not copied: their stale products only reach accumulator
+    // rows the epilogue never stores.
+    if (gather) {
+      const int gw = warp - 6;       // 0..3: rows 32*gw .. 32*gw + 31
+      const int c = lane & 7;        // 16-byte chunk of the row segment
+      const int rq = lane >> 3;      // row within a group of four
+      const long long ld = static_cast<long long>(p.num_kb) * kBK;  // X row stride
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+        const TileInfo t = decode_tile(p, tile);
+        int tok[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 32 * gw + 4 * i + rq;
+          if (t.second) {
+            const int x = t.m * kBM + r;
+            tok[i] = x < p.gather_rows ? x : -1;
+          } else {
+            const int row = t.row0 + r;
+            tok[i] = row < t.row_end ? __ldg(p.gather_perm + row) / p.gather_k : -1;
+          }
+        }
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+          const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 32 * gw + 4 * i + rq;
+            if (tok[i] >= 0)
+              cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4),
+                         p.gather_src + tok[i] * ld + kb * kBK + c * 8);
+          }
+          cp_async_arrive(full0 + 8 * stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
@@ -188,6 +251,9 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
+          // rows copied by the gather warps were written through the generic
+          // proxy; order them before the tensor cores read the stage
+          if (gather) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
@@ -353,7 +419,7 @@ static cudaError_t launch_one(const GemmMaps& m, const GemmParams& p, int grid, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        GemmCfg<BN>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, GemmCfg<BN>::SMEM_BYTES, s>>>(m.a, m.a2, m.b, m.b2, p);
+  kern<<<grid, 320, GemmCfg<BN>::SMEM_BYTES, s>>>(m.a, m.a2, m.b, m.b2, p);
   return cudaGetLastError();
 }
 

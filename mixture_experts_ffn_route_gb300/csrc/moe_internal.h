@@ -29,6 +29,14 @@ struct GemmParams {
   int num_kb;        // K / 64
   int n_out;         // valid output columns
   int up_off;        // SwiGLU: column of the first "up" column of W1 (= I)
+  // Linear1 row gather: when gather_src is set, the A rows of a routed group
+  // are the token rows gather_src[gather_perm[row] / gather_k] and those of the
+  // shared group are gather_src[row - its first row]; they are copied by four
+  // gather warps instead of TMA (map a is unused).
+  const uint16_t* gather_src;  // X [gather_rows, K]
+  const int* gather_perm;
+  int gather_k;
+  int gather_rows;
   void* out;
   long long ldo;     // output row stride, elements
   int* status;
@@ -75,8 +83,6 @@ struct DispatchBufs {
 int dispatch_chunks(int A);
 cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,
                             const DispatchBufs& b, int* status, cudaStream_t s);
-cudaError_t launch_gather_rows(const uint16_t* X, const int* perm, const int* row_off, int E,
-                               int A, int k, int H, uint16_t* Xp, cudaStream_t s);
 cudaError_t launch_combine(const float* Yp, const int* inv, const float* G,
                            const int* row_off, int T, int k, int H, int E, int has_shared,
                            uint16_t* Y, cudaStream_t s);
