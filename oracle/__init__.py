@@ -21,6 +21,9 @@ primitive).  Sources, cited by page title and section:
   duplication, the four-token split example).
 * [PD] "Megatron 分布式训练全维度并行技术文档", section "4.2 数学推导"
   (softmax gate G(x) = TopK(softmax(x W_gate))).
+* [MM] again, section "计算过程", A8W8 scenario: per-token int8 activations,
+  per-channel int8 weights, int32 products, dequantisation, per-row
+  re-quantisation of the SwiGLU output.
 
 Readings taken where the pages are silent:
 the score function is a parameter (sigmoid, sqrt-softplus, softmax); the k ids
@@ -48,6 +51,7 @@ __all__ = [
     "router_logits", "affinity", "select_topk", "gates",
     "route", "route_from_logits", "route_hash",
     "dispatch", "swiglu_expert", "forward", "forward_tokens",
+    "round_half_away", "quantize_rows_int8", "swiglu_expert_a8w8", "forward_a8w8_tokens",
     "SCORE_SIGMOID", "SCORE_SQRT_SOFTPLUS", "SCORE_SOFTMAX",
 ]
 
@@ -265,3 +269,68 @@ def forward(X_bits, E_ids, G, W1, W2, Ws1=None, Ws2=None, act_round_bf16: bool =
     Y = forward_tokens(np.arange(T), X_bits, E_ids, G, W1, W2, Ws1, Ws2, act_round_bf16,
                        E=np.asarray(W1).shape[0])
     return Y, f64_to_bf16_bits(Y)
+
+
+# ----------------------------------------------------------------------------- A8W8-INT
+# [MM] 计算过程, A8W8 scenario: per-token int8 activations, per-channel int8
+# weights, int8 x int8 -> int32 products, dequantisation by both scales, and
+# the SwiGLU output re-quantised per row before Linear2.
+def round_half_away(z) -> np.ndarray:
+    """[MM] conventions: the nearest integer, halves away from zero (四舍五入).
+    Evaluated in float64, where |z| + 0.5 is exact for any float32 z."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.sign(z) * np.floor(np.abs(z) + 0.5)
+
+
+def quantize_rows_int8(x, dtype=np.float64):
+    """[MM] A8W8 EP Dispatch / Linear2: s_i = max|x_i| / 127 and
+    q_i = round(x_i / s_i) in [-127, 127], evaluated in ``dtype``.  A row of
+    zeros has s = 0 and codes 0.  Returns (q int32 [R, C], s dtype [R])."""
+    x = np.asarray(x, dtype=dtype)
+    amax = np.abs(x).max(axis=-1)
+    s = (amax / dtype(127.0)).astype(dtype)
+    safe = np.where(s > 0, s, dtype(1.0)).astype(dtype)
+    q = round_half_away((x / safe[..., None]).astype(dtype))
+    q = np.where(s[..., None] > 0, q, 0.0)
+    return q.astype(np.int32), s
+
+
+def swiglu_expert_a8w8(q_rows, sx_rows, W1q, S1, W2q, S2) -> np.ndarray:
+    """[MM] A8W8 Expert Compute for one expert: C = Q W1q (int32, exact);
+    H = (C * s^W1) * s^X; A = SiLU(H[:, :I]) * H[:, I:]; s^A, A8 =
+    quantize(A) per row; D = A8 W2q (int32, exact); Y = (D * s^W2) * s^A."""
+    C = np.asarray(q_rows, np.int64) @ np.asarray(W1q, np.int64)
+    Hm = (C.astype(np.float64) * np.asarray(S1, np.float64)[None, :]) * np.asarray(sx_rows, np.float64)[:, None]
+    I = np.asarray(W2q).shape[0]
+    A = _silu(Hm[:, :I]) * Hm[:, I:]
+    A8, sA = quantize_rows_int8(A, np.float64)
+    D = A8.astype(np.int64) @ np.asarray(W2q, np.int64)
+    return (D.astype(np.float64) * np.asarray(S2, np.float64)[None, :]) * sA[:, None]
+
+
+def forward_a8w8_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: int) -> np.ndarray:
+    """A8W8 layer output for a set of tokens, float64.  The token codes are
+    decided in float32, as the kernel decides them; every later step is
+    float64 with exact integer products.  W1q/W2q/S1/S2 may be arrays indexed
+    by expert or callables e -> array."""
+    R = len(tokens)
+    E_rows = np.asarray(E_rows, dtype=np.int64).reshape(R, -1)
+    G_rows = np.asarray(G_rows, dtype=np.float64).reshape(R, -1)
+    k = E_rows.shape[1]
+    x32 = bf16_to_f64(X_rows_bits).reshape(R, -1).astype(np.float32)
+    q, sx = quantize_rows_int8(x32, np.float32)
+    counts, offsets, perm, inv = dispatch(E_rows, E)
+    Hdim = x32.shape[1]
+    Yp = np.zeros((perm.shape[0], Hdim), dtype=np.float64)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        rows = perm[offsets[e]:offsets[e + 1]] // k
+        Yp[offsets[e]:offsets[e + 1]] = swiglu_expert_a8w8(
+            q[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e))
+    Y = np.zeros((R, Hdim), dtype=np.float64)
+    for j in range(k):
+        p = inv[np.arange(R) * k + j]
+        ok = p >= 0
+        Y[ok] += G_rows[ok, j:j + 1] * Yp[p[ok]]
+    return Y

@@ -18,6 +18,9 @@ Workloads (shapes follow the pages' own worked layers):
 * ``c5`` large-FFN layer: T=16384, H=8192, E=64, top-2, I=22016, softmax top-2.
 * ``*s`` variants: the same recipes at sizes a CPU oracle finishes in seconds,
   still spanning several GEMM tiles with ragged tails.
+* ``*_q`` variants: the A8W8-INT form of a workload -- int8 expert weights
+  (codes ~ round(N(0, 40^2)) clipped to +-127) with per-output-channel fp32
+  scales, no shared expert.
 
 Value distributions: X ~ N(0,1); Wg and W1 (and the shared Ws1) ~ N(0, 1/H);
 W2 (and Ws2) ~ N(0, 1/I).  Every floating-point tensor that the layer reads in
@@ -52,7 +55,7 @@ _SCORE_NAMES = {"sigmoid": SCORE_SIGMOID, "sqrt_softplus": SCORE_SQRT_SOFTPLUS,
                 "softmax": SCORE_SOFTMAX}
 
 _BASE = dict(shared=0, score="sigmoid", alpha=1.0, renorm=1, routing="topk",
-             bias=False, skew=None, V=0)
+             bias=False, skew=None, V=0, quant=None)
 
 CONFIGS = {
     # --- the five workloads --------------------------------------------------
@@ -78,6 +81,13 @@ CONFIGS = {
     "c5s": dict(_BASE, T=515, H=384, E=8, k=2, I=704, score="softmax",
                 renorm=0),
 }
+# A8W8-INT variants ("mega_moe" page, A8W8 scenario): int8 expert weights with
+# per-output-channel fp32 scales; no shared expert (the operator has none).
+CONFIGS["c2s_q"] = dict(CONFIGS["c2s"], quant="a8w8")
+CONFIGS["c3s_q"] = dict(CONFIGS["c3s"], shared=0, quant="a8w8")
+CONFIGS["c5s_q"] = dict(CONFIGS["c5s"], quant="a8w8")
+CONFIGS["c2_q"] = dict(CONFIGS["c2"], quant="a8w8")
+CONFIGS["c3_q"] = dict(CONFIGS["c3"], shared=0, quant="a8w8")
 # V4-Pro expert shapes at a size one ncu capture can take (4.2 GB of weights,
 # ~64 rows per expert as in c3, uniform load)
 CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
@@ -161,6 +171,19 @@ def _normal_bf16(seed, tid, shape, std) -> np.ndarray:
     return bf16_bits_from_f32(x)
 
 
+# int8 weights: codes drawn as round(N(0, 40^2)) clipped to [-127, 127] and a
+# per-output-channel scale near std / 40 (times U(0.75, 1.25)), so that
+# code * scale has the spread of the bf16 weights of the same layer.
+_CODE_STD = 40.0
+
+
+def _int8_weights(seed, tid, shape, std):
+    rng = _rng(seed, 100 + tid)
+    codes = np.clip(np.rint(rng.standard_normal(size=shape, dtype=np.float32) * _CODE_STD), -127, 127)
+    scales = (std / _CODE_STD) * rng.uniform(0.75, 1.25, size=(shape[0], shape[2]))
+    return codes.astype(np.int8), scales.astype(np.float32)
+
+
 def _distinct_rows(rng: np.random.Generator, n: int, E: int, k: int) -> np.ndarray:
     """n rows of k distinct experts each, a uniform random k-subset per row in
     random order: the first k of a random permutation (random sort keys)."""
@@ -186,8 +209,12 @@ def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
     d["Wg"] = bf16_bits_from_f32(Wg)
     d["bias"] = (_rng(seed, 3).standard_normal(size=E, dtype=np.float32) * np.float32(0.1)
                  if cfg["bias"] else None)
-    d["W1"] = _normal_bf16(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
-    d["W2"] = _normal_bf16(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
+    if cfg.get("quant") == "a8w8":
+        d["W1"], d["S1"] = _int8_weights(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
+        d["W2"], d["S2"] = _int8_weights(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
+    else:
+        d["W1"] = _normal_bf16(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
+        d["W2"] = _normal_bf16(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
     if cfg["shared"]:
         d["Ws1"] = _normal_bf16(seed, 6, (H, 2 * I), 1.0 / math.sqrt(H))
         d["Ws2"] = _normal_bf16(seed, 7, (I, H), 1.0 / math.sqrt(I))
@@ -254,7 +281,18 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
     # back ends: the skew offsets were calibrated against these values
     d["bias"] = (torch.from_numpy(_rng(seed, 3).standard_normal(size=E, dtype=np.float32)
                                   * np.float32(0.1)).to(dev) if cfg["bias"] else None)
-    if weights:
+    def int8_weights(tid, shape, std):
+        g = gen(100 + tid)
+        codes = torch.empty(shape, dtype=torch.int8, device=dev)
+        for i in range(shape[0]):
+            codes[i] = (torch.randn(shape[1:], generator=g, device=dev) * _CODE_STD).round_().clamp_(-127, 127).to(torch.int8)
+        u = torch.rand((shape[0], shape[2]), generator=g, device=dev) * 0.5 + 0.75
+        return codes, (u * (std / _CODE_STD)).float().contiguous()
+
+    if weights and cfg.get("quant") == "a8w8":
+        d["W1"], d["S1"] = int8_weights(4, (E, H, 2 * I), 1.0 / math.sqrt(H))
+        d["W2"], d["S2"] = int8_weights(5, (E, I, H), 1.0 / math.sqrt(I))
+    elif weights:
         d["W1"] = normal(4, (E, H, 2 * I), 1.0 / math.sqrt(H), per_slice=True)
         d["W2"] = normal(5, (E, I, H), 1.0 / math.sqrt(I), per_slice=True)
     else:

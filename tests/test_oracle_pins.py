@@ -311,3 +311,71 @@ def test_forward_tokens_subset_matches_whole_layer():
     Ys = oracle.forward_tokens(rows, d["X"][rows], d["E_ids"][rows], d["G"][rows],
                                lambda e: d["W1"][e], lambda e: d["W2"][e], E=d["cfg"]["E"])
     np.testing.assert_allclose(Ys, Y[rows], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ A8W8-INT
+def test_round_half_away_from_zero():
+    z = np.array([0.5, -0.5, 1.5, 2.5, -2.5, 0.49999997, -1.4999999], dtype=np.float32)
+    assert oracle.round_half_away(z).tolist() == [1, -1, 2, 3, -3, 0, -1]
+
+
+def test_int8_row_quantisation_closed_forms():
+    q, s = oracle.quantize_rows_int8(np.array([[127.0, 63.5, -63.5, 0.49], [0.0, 0.0, 0.0, 0.0]]))
+    assert q.tolist() == [[127, 64, -64, 0], [0, 0, 0, 0]] and s.tolist() == [1.0, 0.0]
+    rng = np.random.default_rng(20)
+    x = rng.standard_normal((64, 300)) * rng.uniform(0.01, 100, size=(64, 1))
+    for dt in (np.float32, np.float64):
+        q, s = oracle.quantize_rows_int8(x.astype(dt), dt)
+        assert (np.abs(q) <= 127).all()
+        # the largest magnitude of each row becomes exactly +-127
+        amax_idx = np.abs(x).argmax(1)
+        assert (np.abs(q[np.arange(64), amax_idx]) == 127).all()
+        # reconstruction within half a step
+        assert (np.abs(x - q * s[:, None].astype(np.float64)) <= 0.5 * s[:, None] * (1 + 1e-6)).all()
+
+
+def test_a8w8_expert_matches_integer_brute_force():
+    rng = np.random.default_rng(21)
+    N, H, I = 3, 8, 4
+    q = rng.integers(-127, 128, size=(N, H))
+    sx = rng.uniform(0.01, 0.1, size=N)
+    W1q = rng.integers(-127, 128, size=(H, 2 * I))
+    S1 = rng.uniform(0.001, 0.01, size=2 * I)
+    W2q = rng.integers(-127, 128, size=(I, H))
+    S2 = rng.uniform(0.001, 0.01, size=H)
+    Y = oracle.swiglu_expert_a8w8(q, sx, W1q, S1, W2q, S2)
+    for n in range(N):
+        C = [sum(int(q[n, h]) * int(W1q[h, c]) for h in range(H)) for c in range(2 * I)]
+        Hv = [C[c] * S1[c] * sx[n] for c in range(2 * I)]
+        A = [Hv[c] / (1 + math.exp(-Hv[c])) * Hv[I + c] for c in range(I)]
+        sA = max(abs(a) for a in A) / 127
+        A8 = [int(math.copysign(math.floor(abs(a / sA) + 0.5), a)) for a in A]
+        D = [sum(A8[i] * int(W2q[i, o]) for i in range(I)) for o in range(H)]
+        np.testing.assert_allclose(Y[n], [D[o] * S2[o] * sA for o in range(H)], rtol=1e-12)
+
+
+def test_a8w8_layer_within_the_activation_quantisation_bound():
+    # Quantised token rows and weights that are exactly code * scale: then the
+    # A8W8 layer differs from the plain float layer on the dequantised operands
+    # only through the re-quantisation of the SwiGLU output, bounded per
+    # element by sum_i |dA_i| |W2[i, o]| <= (s_A / 2) sum_i |W2[i, o]|.
+    d = synth.make_inputs("c3s_q")
+    c = d["cfg"]
+    T, k, E, I = c["T"], c["k"], c["E"], c["I"]
+    ids, G, _ = oracle.route(d["X"], d["Wg"], d["bias"], c["score_fn"], k, c["alpha"], True)
+    Y = oracle.forward_a8w8_tokens(np.arange(T), d["X"], ids, G, d["W1"], d["S1"], d["W2"], d["S2"], E=E)
+    x32 = oracle.bf16_to_f64(d["X"]).astype(np.float32)
+    q, sx = oracle.quantize_rows_int8(x32, np.float32)
+    Xd = q * sx[:, None].astype(np.float64)
+    for t in (0, 5, T - 1):
+        want = np.zeros(c["H"])
+        bound = np.zeros(c["H"])
+        for j in range(k):
+            e = ids[t, j]
+            W1 = d["W1"][e].astype(np.float64) * d["S1"][e][None, :].astype(np.float64)
+            W2 = d["W2"][e].astype(np.float64) * d["S2"][e][None, :].astype(np.float64)
+            h = Xd[t] @ W1
+            a = h[:I] / (1 + np.exp(-h[:I])) * h[I:]
+            want += G[t, j] * (a @ W2)
+            bound += abs(G[t, j]) * (np.abs(a).max() / 127 / 2) * np.abs(W2).sum(0)
+        assert (np.abs(Y[t] - want) <= bound * (1 + 1e-9) + 1e-12).all()
