@@ -41,6 +41,8 @@ WORKLOAD_TEXT = {
     "c5": "large-FFN layer T=16384 H=8192 E=64 top-2 I=22016, softmax gates",
     "c3_sp": "V4-Pro-shaped layer with the pages' sqrt-softplus affinity",
     "c3p": "V4-Pro expert shapes, T=512 E=48 (profiling size)",
+    "c3_q": "V4-Pro-shaped layer, A8W8-INT form (int8 weights, per-token int8 activations), no shared expert",
+    "c2_q": "given-routing layer, A8W8-INT form",
 }
 
 
@@ -146,7 +148,10 @@ def build_step(moe, dd, p, ws, stage_events=None):
                 moe.moe_route(p, X, dd["Wg"], dd["bias"], None, None, 0, E_ids, G, ws)
             if route_events:
                 route_events[1].record()
-        if stage_events is not None:
+        if c.get("quant") == "a8w8":
+            moe.moe_forward_a8w8(p, X, E_ids, G, dd["W1"], dd["S1"], dd["W2"], dd["S2"], Y,
+                                 dd["_ws_q"], stage_events)
+        elif stage_events is not None:
             moe.moe_forward_timed(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws,
                                   stage_events)
         else:
@@ -170,6 +175,9 @@ def run_ours(args, rank, world, local_rank):
     has_shared = c["shared"]
     p = moe.params_from_config(c)
     ws = moe.alloc_workspace(p, dev)
+    quant = c.get("quant") == "a8w8"
+    if quant:
+        dd["_ws_q"] = moe.alloc_workspace_a8w8(p, dev)
     dd["_E_ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
     dd["_G"] = torch.empty((T, k), dtype=torch.float32, device=dev)
     dd["_Y"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -207,12 +215,17 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.mark_end()
     moe.moe_sync_status(ws)
+    if quant:
+        moe.moe_sync_status(dd["_ws_q"])
     ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world, dev)
 
     def avg(evs, a, b):
         return sum(e[a].elapsed_time(e[b]) for e in evs) / len(evs)
     stages = {"dispatch": avg(st_ev, 0, 1), "gemm1_swiglu": avg(st_ev, 1, 2),
               "gemm2": avg(st_ev, 2, 3), "combine": avg(st_ev, 3, 4)}
+    if quant:
+        stages = {"dispatch_quant": stages["dispatch"], "gemm1_swiglu": stages["gemm1_swiglu"],
+                  "quant_gemm2": stages["gemm2"], "combine": stages["combine"]}
     if routed:
         stages = {"route": avg(rt_ev, 0, 1), **stages}
 
@@ -247,11 +260,16 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     pk = peaks()
-    g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
+    if quant:
+        g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=1, x_bytes=2, act_bytes=4)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=1, act_bytes=2)
+    else:
+        g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T)
     g1_flops = accounting.gemm1_flops(counts, H, I, has_shared, T)
     g2_flops = accounting.gemm2_flops(counts, H, I, has_shared, T)
     g1_s = stages["gemm1_swiglu"] / 1e3
-    g2_s = stages["gemm2"] / 1e3
+    g2_s = stages["quant_gemm2" if quant else "gemm2"] / 1e3
     gemm_tflops = (g1_flops + g2_flops) / (g1_s + g2_s) / 1e12
     # the dominant kernel: Linear1 + SwiGLU.  Weight streaming bounds it when the
     # arithmetic intensity is below the ridge point.
@@ -259,7 +277,7 @@ def run_ours(args, rank, world, local_rank):
     ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if ai < ridge:
         achieved = g1_bytes / g1_s / 1e9
-        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<256,1>)", "bound": "hbm",
+        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<1>)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
                 "algorithmic_bytes_per_launch": int(g1_bytes),
@@ -267,33 +285,37 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved = g1_flops / g1_s / 1e12
         peak = pk["bf16_tflops_sustained"]
-        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<256,1>)", "bound": "tensor",
+        roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<1>)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "algorithmic_flops_per_launch": int(g1_flops),
                 "peak_source": pk["source"] + " bf16_tflops_sustained"}
-    if roof["bound"] == "hbm":
+    if roof["bound"] == "hbm" and not quant:
         roof["traffic"] = load_traffic(args.workload, g1_bytes)
+    if quant:
+        roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_tc_kernel<3>)"
     # route: transpose Wg, gating GEMM, select, recheck, reselect (hash: GEMM, select);
     # forward: count, scan, place, gather, Linear1, Linear2, combine
-    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + 7
+    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + (9 if quant else 7)
     out = {
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if quant else "bf16",
         "data": "synthetic (seeded; random-init weights of the workload's shapes)",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
                    "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": has_shared,
                    "routing": c["routing"], "score": c["score"],
                    "l2": "inputs larger than L2: %.1f GB of expert weights per step"
-                         % ((E + has_shared) * 3 * H * I * 2 / 1e9),
+                         % ((E + has_shared) * 3 * H * I * (1 if quant else 2) / 1e9),
+                   "weights": "int8 + per-channel fp32 scales (A8W8-INT)" if quant else "bf16",
                    "parallelism": f"replicas x{world} (token batches, no collective)"},
         "stages_ms": {k_: round(v, 4) for k_, v in stages.items()},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1),
                          "pct_bf16_peak": round(100 * gemm_tflops / pk["bf16_tflops_sustained"], 2),
                          "peak_tflops": pk["bf16_tflops_sustained"],
                          "gemm1_GBps": round(g1_bytes / g1_s / 1e9, 1),
-                         "gemm2_GBps": round(accounting.gemm2_bytes(counts, H, I, has_shared, T) / g2_s / 1e9, 1)},
+                         "gemm2_GBps": round(g2_bytes / g2_s / 1e9, 1)},
         "roofline": roof,
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

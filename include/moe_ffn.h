@@ -161,6 +161,32 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
                              const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
                              size_t ws_bytes, void* stream, void* const* stage_events);
 
+/* Bytes of workspace moe_forward_a8w8 needs for these parameters. */
+size_t moe_workspace_size_a8w8(const moe_params* p);
+
+/* Layer forward in the A8W8-INT form of the "mega_moe" page (section 计算过程,
+ * A8W8 scenario), no shared expert (has_shared must be 0):
+ *   each token row is quantised, s^X_t = max|x_t| / 127, q_t = round(x_t / s^X_t)
+ *   (nearest integer, halves away from zero; float32);
+ *   per expert: C = Q_e W1q[e] (int32), H = (C * S1[e]) * s^X, A = SiLU(H[:, :I])
+ *   * H[:, I:], each row of A re-quantised the same way (s^A, A8), D = A8 W2q[e]
+ *   (int32), Y_e = (D * S2[e]) * s^A;  y_t = sum_j G[t, j] Y[row(t, j)].
+ *   W1q [E, H, 2I] int8, S1 [E, 2I] fp32 (per output channel)
+ *   W2q [E, I, H]  int8, S2 [E, H]  fp32
+ *   X [T, H] bf16, E_ids [T, k], G [T, k] fp32, Y [T, H] bf16 out.
+ * The int8 products run on the fp16 tensor-core path (GB300's int8 tensor rate
+ * is far lower): codes are exact in fp16 and the fp32 accumulator holds each
+ * int32 sum exactly while every partial sum stays below 2^24 in magnitude
+ * (always true for K * 127 * 127 < 2^24, i.e. K <= 1040; beyond that, true
+ * unless the codes of a row and a column agree in sign at full scale).
+ * stage_events: NULL, or 5 caller-created cudaEvent_t recorded at: start,
+ * after dispatch and token quantisation, after Linear1, after the
+ * re-quantisation and Linear2, after combine. */
+moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                            const float* G, const int8_t* W1q, const float* S1,
+                            const int8_t* W2q, const float* S2, uint16_t* Y, void* ws,
+                            size_t ws_bytes, void* stream, void* const* stage_events);
+
 /* Synchronise `stream`, read the workspace's device status word, clear it and
  * return the most serious error recorded since the last call, in the order
  * TIMEOUT, BAD_TOKEN_ID, BAD_EXPERT_ID (MOE_OK if none).  A bad hash token

@@ -58,6 +58,9 @@ SIGNATURES = {
     "moe_forward_timed": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                          ctypes.POINTER(ctypes.c_void_p)]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P]),
+    "moe_workspace_size_a8w8": (_SZ, [_PP]),
+    "moe_forward_a8w8": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                        ctypes.POINTER(ctypes.c_void_p)]),
     "moe_sync_status": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -185,6 +188,31 @@ def moe_forward_timed(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, stage_events, str
     return _check(lib().moe_forward_timed(ctypes.byref(p), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1),
                                           _ptr(W2), _ptr(Ws1), _ptr(Ws2), _ptr(Y), _ptr(ws), ws.numel(),
                                           _stream(stream), arr), "moe_forward_timed")
+
+
+def moe_workspace_size_a8w8(p: MoeParams) -> int:
+    return int(lib().moe_workspace_size_a8w8(ctypes.byref(p)))
+
+
+def alloc_workspace_a8w8(p: MoeParams, device="cuda", stream=None):
+    """A zero-headed uint8 device tensor of moe_workspace_size_a8w8(p) bytes."""
+    import torch
+    n = moe_workspace_size_a8w8(p)
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_workspace_size_a8w8")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_forward_a8w8(p, X, E_ids, G, W1q, S1, W2q, S2, Y, ws, stage_events=None, stream=None):
+    """A8W8-INT layer forward (int8 weights with per-channel scales)."""
+    arr = None
+    if stage_events is not None:
+        arr = (ctypes.c_void_p * 5)(*[(ev.cuda_event if ev is not None else None) for ev in stage_events])
+    return _check(lib().moe_forward_a8w8(ctypes.byref(p), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1q), _ptr(S1),
+                                         _ptr(W2q), _ptr(S2), _ptr(Y), _ptr(ws), ws.numel(), _stream(stream),
+                                         arr), "moe_forward_a8w8")
 
 
 def moe_selftest_wait_timeout(ws, limit_us: int, stream=None):

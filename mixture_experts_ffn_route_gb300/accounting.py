@@ -35,18 +35,19 @@ def router_flops(T, H, E):
     return 2 * T * H * E
 
 
-def gemm1_bytes(counts, H, I, has_shared=0, T=0):
+def gemm1_bytes(counts, H, I, has_shared=0, T=0, w_bytes=BF16, x_bytes=BF16, act_bytes=BF16):
     """W1 of every active expert (H x 2I), its input rows (H; gathered from the
-    token rows by the permutation) and Act rows (I)."""
+    token rows by the permutation) and Act rows (I).  The A8W8 form reads int8
+    weights (w_bytes 1), fp16 token codes and writes fp32 Act (act_bytes 4)."""
     rows, n_active = _counts(counts, has_shared, T)
-    return n_active * H * 2 * I * BF16 + rows * H * BF16 + rows * I * BF16
+    return n_active * H * 2 * I * w_bytes + rows * H * x_bytes + rows * I * act_bytes
 
 
-def gemm2_bytes(counts, H, I, has_shared=0, T=0):
-    """W2 of every active expert (I x H), Act rows in (bf16), expert output
-    rows out (fp32)."""
+def gemm2_bytes(counts, H, I, has_shared=0, T=0, w_bytes=BF16, act_bytes=BF16):
+    """W2 of every active expert (I x H), Act rows in (bf16, or fp16 codes),
+    expert output rows out (fp32)."""
     rows, n_active = _counts(counts, has_shared, T)
-    return n_active * I * H * BF16 + rows * I * BF16 + rows * H * F32
+    return n_active * I * H * w_bytes + rows * I * act_bytes + rows * H * F32
 
 
 def dispatch_bytes(T, H, k):

@@ -61,6 +61,36 @@ static WsLayout layout(const moe_params& p) {
   return L;
 }
 
+// Workspace layout of the A8W8 forward.
+struct WsLayoutQ {
+  size_t status, chunk_cnt, counts, row_off, tile_off, perm, inv, xq, sx, act, aq, sa, yp, total;
+};
+
+static WsLayoutQ layout_a8w8(const moe_params& p) {
+  WsLayoutQ L;
+  const size_t T = static_cast<size_t>(p.T), E = static_cast<size_t>(p.E);
+  const size_t A = T * static_cast<size_t>(p.k);
+  const size_t H = static_cast<size_t>(p.H), I = static_cast<size_t>(p.I);
+  const size_t nchunk = static_cast<size_t>(dispatch_chunks(static_cast<int>(A)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(256);
+  L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
+  L.counts = take((E + 2) * sizeof(int));
+  L.row_off = take((E + 2) * sizeof(int));
+  L.tile_off = take((E + 2) * sizeof(int));
+  L.perm = take(A * sizeof(int));
+  L.inv = take(A * sizeof(int));
+  L.xq = take(T * H * 2);
+  L.sx = take(T * sizeof(float));
+  L.act = take(A * I * sizeof(float));
+  L.aq = take(A * I * 2);
+  L.sa = take(A * sizeof(float));
+  L.yp = take(A * H * sizeof(float));
+  L.total = o;
+  return L;
+}
+
 static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 static moe_status check_params(const moe_params* p) {
@@ -369,6 +399,121 @@ moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_
                        const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
                        size_t ws_bytes, void* stream) {
   return moe_forward_timed(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, ws_bytes, stream, nullptr);
+}
+
+size_t moe_workspace_size_a8w8(const moe_params* p) {
+  if (check_params(p) != MOE_OK) return 0;
+  return layout_a8w8(*p).total;
+}
+
+moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                            const float* G, const int8_t* W1q, const float* S1,
+                            const int8_t* W2q, const float* S2, uint16_t* Y, void* ws,
+                            size_t ws_bytes, void* stream, void* const* stage_events) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if (p->has_shared) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+      ws_bytes < layout_a8w8(*p).total)
+    return MOE_ERR_WORKSPACE;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !E_ids || !G || !W1q || !S1 || !W2q || !S2 || !Y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W1q) || !aligned16(W2q) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+
+  const WsLayoutQ L = layout_a8w8(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  DispatchBufs b;
+  b.chunk_cnt = at<int>(ws, L.chunk_cnt);
+  b.counts = at<int>(ws, L.counts);
+  b.row_off = at<int>(ws, L.row_off);
+  b.tile_off = at<int>(ws, L.tile_off);
+  b.perm = at<int>(ws, L.perm);
+  b.inv = at<int>(ws, L.inv);
+  b.nchunk = dispatch_chunks(p->T * p->k);
+  const int T = p->T, H = p->H, E = p->E, k = p->k, I = p->I;
+  const int A = T * k;
+  uint16_t* Xq = at<uint16_t>(ws, L.xq);
+  float* sX = at<float>(ws, L.sx);
+  float* Act = at<float>(ws, L.act);
+  uint16_t* Aq = at<uint16_t>(ws, L.aq);
+  float* sA = at<float>(ws, L.sa);
+  float* Yp = at<float>(ws, L.yp);
+  auto mark = [&](int i) -> cudaError_t {
+    if (stage_events == nullptr || stage_events[i] == nullptr) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
+  };
+  const int mt_bound = (A + kBM - 1) / kBM + E;
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_dispatch(E_ids, T, k, E, 0, b, status, s);
+  if (e == cudaSuccess) e = launch_quant_rows_bf16(X, T, H, Xq, sX, s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // Linear1: C = Q_e W1q[e] (token codes gathered by the permutation),
+  // dequantised, SwiGLU, fp32 out
+  {
+    GemmMaps maps;
+    if (!make_map_rows(&maps.a, Xq, T, H) || !make_map_weights_i8(&maps.b, W1q, E, H, 2 * I))
+      return MOE_ERR_CUDA;
+    maps.a2 = maps.a;
+    maps.b2 = maps.b;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = E;
+    g.shared_group = -1;
+    g.gather_src = Xq;
+    g.gather_perm = b.perm;
+    g.gather_k = k;
+    g.gather_rows = T;
+    g.n_tiles = (I + 127) / 128;
+    g.num_kb = H / kBK;
+    g.n_out = I;
+    g.up_off = I;
+    g.out = Act;
+    g.ldo = I;
+    g.scale_col = S1;
+    g.scale_ld = 2LL * I;
+    g.scale_row = sX;
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if (launch_gemm(kGemmSwiGLU_Q8, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // per-row re-quantisation of the SwiGLU output, then Linear2
+  if (launch_quant_rows_f32(Act, b.row_off + E, A, I, Aq, sA, s) != cudaSuccess) return MOE_ERR_CUDA;
+  {
+    GemmMaps maps;
+    if (!make_map_rows(&maps.a, Aq, A, I) || !make_map_weights_i8(&maps.b, W2q, E, I, H))
+      return MOE_ERR_CUDA;
+    maps.a2 = maps.a;
+    maps.b2 = maps.b;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = E;
+    g.shared_group = -1;
+    g.n_tiles = (H + 255) / 256;
+    g.num_kb = I / kBK;
+    g.n_out = H;
+    g.out = Yp;
+    g.ldo = H;
+    g.scale_col = S2;
+    g.scale_ld = H;
+    g.scale_row = sA;
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if (launch_gemm(kGemmPlain_Q8, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -150,9 +151,10 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulator.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem], 16-bit inputs (fp16 or bf16 by the
+// instruction descriptor), fp32 accumulator.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -204,13 +206,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format;
-//   bit 15 A major (0 = K-major); bit 16 B major (1 = MN-major);
+// Instruction descriptor, kind::f16 with fp32 D.
+//   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16,
+//   1 = bf16); bit 15 A major (0 = K-major); bit 16 B major (1 = MN-major);
 //   bits 17-22 N >> 3; bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+constexpr uint32_t kFmtF16 = 0;
+constexpr uint32_t kFmtBF16 = 1;
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, uint32_t fmt, bool a_mn_major,
+                                                    bool b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }

@@ -11,7 +11,13 @@ namespace moe {
 constexpr int kBM = 128;  // GEMM tile rows (tokens)
 constexpr int kBK = 64;   // GEMM k-block (one 128-byte swizzle row of bf16)
 
-enum GemmKind { kGemmRouter = 0, kGemmSwiGLU = 1, kGemmPlain = 2 };
+enum GemmKind {
+  kGemmRouter = 0,     // fp32 logits
+  kGemmSwiGLU = 1,     // Linear1 + SwiGLU, bf16 out
+  kGemmPlain = 2,      // Linear2, fp32 out
+  kGemmSwiGLU_Q8 = 3,  // A8W8 Linear1 + dequantisation + SwiGLU, fp32 out
+  kGemmPlain_Q8 = 4    // A8W8 Linear2 + dequantisation, fp32 out
+};
 
 // One grouped GEMM launch.  Groups are row ranges [row_off[g], row_off[g+1])
 // of the A operand and of the output; tile_off[g] is the running count of
@@ -37,6 +43,12 @@ struct GemmParams {
   const int* gather_perm;
   int gather_k;
   int gather_rows;
+  // int8 forms: per-column weight scales of group g at scale_col + g *
+  // scale_ld, and the per-row activation scales (Linear1: indexed by token,
+  // Linear2: by assignment row)
+  const float* scale_col;
+  long long scale_ld;
+  const float* scale_row;
   void* out;
   long long ldo;     // output row stride, elements
   int* status;
@@ -49,6 +61,15 @@ struct GemmMaps {
 // Tensor-map helpers (host).  Return false if the driver rejects the map.
 bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
 bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N);
+bool make_map_weights_i8(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N);
+
+// Per-row int8 quantisation ("mega_moe" A8W8): s = max|x| / 127 and codes
+// round(x / s) (halves away from zero), written as fp16 values.  rows_dev,
+// when set, gives the row count on the device (rows is then an upper bound).
+cudaError_t launch_quant_rows_bf16(const uint16_t* x, int rows, int cols, uint16_t* codes,
+                                   float* scales, cudaStream_t s);
+cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_max, int cols,
+                                  uint16_t* codes, float* scales, cudaStream_t s);
 
 // Launch the tcgen05 GEMM of the given kind on `grid` persistent CTAs.
 cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p, int grid,

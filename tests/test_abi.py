@@ -98,6 +98,14 @@ def test_argument_errors_return_before_any_launch(lib):
     assert route(_p(E=12, k=2)) == moe.MOE_ERR_UNSUPPORTED               # E % 8 != 0
     assert route(_p(T=0)) == moe.MOE_OK
 
+    def fwd_q(p, ws_bytes=None):
+        n = moe.moe_workspace_size_a8w8(p) if ws_bytes is None else ws_bytes
+        return lib.moe_forward_a8w8(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, fake_ws, n,
+                                    None, None)
+    assert fwd_q(_p(has_shared=1)) == moe.MOE_ERR_UNSUPPORTED  # the A8W8 form has no shared expert
+    assert fwd_q(_p(), ws_bytes=1024) == moe.MOE_ERR_WORKSPACE
+    assert fwd_q(_p(T=0)) == moe.MOE_OK
+
 
 def test_accounting_pins_from_the_pages():
     MiB = 1 << 20
