@@ -41,6 +41,7 @@ WORKLOAD_TEXT = {
     "c5": "large-FFN layer T=16384 H=8192 E=64 top-2 I=22016, softmax gates",
     "c3_sp": "V4-Pro-shaped layer with the pages' sqrt-softplus affinity",
     "c3p": "V4-Pro expert shapes, T=512 E=48 (profiling size)",
+    "c3r": "V4-Pro router at full size with I=64 (profiling size for the routing kernels)",
     "c3_q": "V4-Pro-shaped layer, A8W8-INT form (int8 weights, per-token int8 activations), no shared expert",
     "c2_q": "given-routing layer, A8W8-INT form",
 }
@@ -229,30 +230,63 @@ def run_ours(args, rank, world, local_rank):
     if routed:
         stages = {"route": avg(rt_ev, 0, 1), **stages}
 
-    # ---- end to end through the C ABI with host buffers (pinned) each step
+    # ---- end to end through the C ABI with host buffers (pinned) each step.
+    # A serving loop: step i's token rows (and given ids / gates, or hash token
+    # ids) are copied host->device, the layer runs, and Y is copied back to
+    # pinned host memory.  Copies run on a second stream into two device
+    # slots, so the next step's input copy and the previous step's output copy
+    # overlap this step's compute; every copy of every step is inside the
+    # timed region.
     X_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
     X_host.copy_(dd["X"])
     Y_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
-    X_dev = torch.empty_like(dd["X"])
-    extra = []
-    if c["routing"] == "given":
-        extra = [(dd["E_ids"], dd["E_ids"].cpu().pin_memory()), (dd["G"], dd["G"].cpu().pin_memory())]
-    elif c["routing"] == "hash":
-        extra = [(dd["token_ids"], dd["token_ids"].cpu().pin_memory())]
-    h2d = X_host.numel() * 2 + sum(h.numel() * h.element_size() for _, h in extra)
+    in_keys = ["X"] + {"given": ["E_ids", "G"], "hash": ["token_ids"]}.get(c["routing"], [])
+    host_in = {key: (X_host if key == "X" else dd[key].cpu().pin_memory()) for key in in_keys}
+    slots = []
+    for _ in range(2):
+        dslot = dict(dd)
+        for key in in_keys:
+            dslot[key] = torch.empty_like(dd[key])
+        dslot["_Y"] = torch.empty_like(dd["_Y"])
+        slots.append((dslot, build_step(moe, dslot, p, ws)))
+    h2d = sum(host_in[key].numel() * host_in[key].element_size() for key in in_keys)
     d2h = Y_host.numel() * 2
-    step = build_step(moe, dd, p, ws)
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+    in_ready, in_free, y_ready, y_free = ev(), ev(), ev(), ev()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K):
-        X_dev.copy_(X_host, non_blocking=True)
-        for d_t, h_t in extra:
-            d_t.copy_(h_t, non_blocking=True)
-        step(X=X_dev)
-        Y_host.copy_(dd["_Y"], non_blocking=True)
-    e1.record()
+    e0.record(comp)
+
+    def h2d_copy(i):
+        sl = i % 2
+        copy.wait_stream(comp) if i == 0 else None
+        with torch.cuda.stream(copy):
+            if i >= 2:
+                copy.wait_event(in_free[sl])  # step i - 2 has read this slot
+            for key in in_keys:
+                slots[sl][0][key].copy_(host_in[key], non_blocking=True)
+            in_ready[sl].record(copy)
+
+    h2d_copy(0)
+    for i in range(K):
+        sl = i % 2
+        if i + 1 < K:
+            h2d_copy(i + 1)
+        comp.wait_event(in_ready[sl])
+        if i >= 2:
+            comp.wait_event(y_free[sl])  # Y of step i - 2 is on the host
+        slots[sl][1]()
+        in_free[sl].record(comp)
+        y_ready[sl].record(comp)
+        with torch.cuda.stream(copy):
+            copy.wait_event(y_ready[sl])
+            Y_host.copy_(slots[sl][0]["_Y"], non_blocking=True)
+            y_free[sl].record(copy)
+    comp.wait_stream(copy)
+    e1.record(comp)
     torch.cuda.synchronize()
     moe.moe_sync_status(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)

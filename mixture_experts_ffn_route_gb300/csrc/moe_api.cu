@@ -253,7 +253,7 @@ moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
   rs.counters = at<int>(ws, L.rcount);
   rs.flagged = at<int4>(ws, L.flagged);
   rs.pairs = at<int2>(ws, L.pairs);
-  rs.s64 = at<double>(ws, L.s64);
+  rs.key = at<unsigned long long>(ws, L.s64);
   if (!hash) {
     if (cudaMemsetAsync(rs.counters, 0, 4 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_transpose_wg(Wg, p->H, p->E, WgT, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -82,7 +82,7 @@ struct RouteScratch {
   int* counters;  // [0] close tokens, [1] candidate pairs; zeroed before select
   int4* flagged;  // [T]      {token, first pair, pair count, 0}
   int2* pairs;    // [T * E]  {token, expert}
-  double* s64;    // [T * E]  float64 selection score of each pair
+  unsigned long long* key;  // [T * E]  order-preserving key of each pair's float64 score
 };
 cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT, cudaStream_t s);
 cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,

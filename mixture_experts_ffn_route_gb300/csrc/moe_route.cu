@@ -14,7 +14,7 @@
 //   select    one warp per token: fp32 top-(k+1) by k+1 warp arg-max rounds;
 //             a close token appends every expert scoring within twice the band
 //             of its k-th score to a list of (token, expert) pairs;
-//   recheck   one warp per pair: the logit sum_h X[t,h] Wg[h,e] to ~48 bits
+//   recheck   four warps per pair: the logit sum_h X[t,h] Wg[h,e] to ~48 bits
 //             over a transposed copy of Wg (contiguous rows; each bf16 product
 //             is exact in fp32 and the sum is carried as a float pair), then
 //             its float64 selection score;
@@ -93,32 +93,39 @@ __device__ __forceinline__ void softmax_norm(const float* lrow, int E, int lane,
   zsum = warp_sum(zsum);
 }
 
-// Lane 0 writes ids and gates of one token from the fp32 logits.
-__device__ void write_gates(const float* lrow, int E, int k, int fn, float alpha, int renorm,
-                            const int* sel, bool tok_ok, float lmax, float zsum, int32_t* ids,
-                            float* G, int* status) {
-  float a[kMaxK];
-  float den = 0.0f;
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const int e = sel[j];
-    float v = 0.0f;
-    if (e >= 0 && e < E) {
-      const float l = lrow[e];
-      v = (fn == 2) ? expf(l - lmax) / zsum : score_f32(l, fn);
+// The whole warp writes ids and gates of one token from the fp32 logits:
+// lane j < k loads its own logit, the warp sums the affinities.
+__device__ __forceinline__ void write_gates(const float* lrow, int E, int k, int fn, float alpha,
+                                            int renorm, int my_sel, bool tok_ok, float lmax,
+                                            float zsum, int lane, int32_t* ids, float* G,
+                                            int* status) {
+  float a = 0.0f;
+  const bool mine = lane < k;
+  if (mine) {
+    if (my_sel >= 0 && my_sel < E) {
+      const float l = lrow[my_sel];
+      a = (fn == 2) ? expf(l - lmax) / zsum : score_f32(l, fn);
     } else if (tok_ok) {
       set_flag(status, kFlagBadExpert);  // a table entry outside [0, E)
     }
-    a[j] = v;
-    den += v;
   }
+  // sum over j < k in j order (lanes beyond k hold 0)
+  float den = 0.0f;
+  for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, a, j);
+  if (mine) {
+    float g = alpha * a;
+    if (renorm) g = den > 0.0f ? alpha * a / den : 0.0f;
+    ids[lane] = my_sel;
+    G[lane] = g;
+  }
+}
+
+// Lane j of the warp receives sel[j] (k <= 16 <= 32).
+__device__ __forceinline__ int lane_sel(const int* sel, int k, int lane) {
+  int v = -1;
 #pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    float g = alpha * a[j];
-    if (renorm) g = den > 0.0f ? alpha * a[j] / den : 0.0f;
-    ids[j] = sel[j];
-    G[j] = g;
-  }
+  for (int j = 0; j < k; ++j) v = (lane == j) ? sel[j] : v;
+  return v;
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -148,9 +155,10 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int j = 0; j < k; ++j) sel[j] = tok_ok ? tid2eid[static_cast<long long>(tok) * k + j] : -1;
   } else {
     // ---------------------------------------------------------------- top-k
+#pragma unroll 8
     for (int e = lane; e < E; e += 32) {
-      float v = score_f32(lrow[e], fn);
-      if (bias != nullptr) v += bias[e];
+      float v = score_f32(__ldg(lrow + e), fn);
+      if (bias != nullptr) v += __ldg(bias + e);
       s[e] = v;
     }
     __syncwarp();
@@ -206,9 +214,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
   // fp32 decision (a close token's ids and gates are rewritten by reselect)
-  if (lane == 0)
-    write_gates(lrow, E, k, fn, alpha, renorm, sel, tok_ok, lmax, zsum,
-                E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
+  write_gates(lrow, E, k, fn, alpha, renorm, lane_sel(sel, k, lane), tok_ok, lmax, zsum, lane,
+              E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
 }
 
 // Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
@@ -218,51 +225,88 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = (a - (s - bb)) + (b - bb);
 }
 
-// Float64 selection score of the listed (token, expert) pairs.  Each bf16 x
-// bf16 product is exact in fp32; the products are summed as unevaluated float
-// pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's fp64 rate is low),
-// and the pairs are folded into float64 for the warp sum.  The result is
-// within ~1e-12 of the exact logit at the workload sizes.
-__global__ void __launch_bounds__(kWarps * 32)
+// (H, L) += (h, l) for unevaluated float pairs: TwoSum of the high parts,
+// the low parts added to the error, renormalised (Fast2Sum).
+__device__ __forceinline__ void ff_add(float& H, float& L, float h, float l) {
+  float s, e;
+  two_sum(H, h, s, e);
+  e += L + l;
+  H = s + e;
+  L = e - (H - s);
+}
+
+// Order-preserving 64-bit key of a double: larger double, larger key.
+__device__ __forceinline__ unsigned long long order_key(double v) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+
+constexpr int kRecheckWarps = 4;  // warps that share one (token, expert) pair
+
+// Float64 selection score of the listed (token, expert) pairs, four warps to a
+// pair.  Each bf16 x bf16 product is exact in fp32; the products are summed as
+// unevaluated float pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's
+// fp64 rate is low), folded as float pairs across the lanes of each warp, and
+// the four warps' sums added in float64 in a fixed order.  The logit is within ~1e-12 of
+// the exact value at the workload sizes.  The score is stored as an
+// order-preserving integer key so the reselection compares integers.
+__global__ void __launch_bounds__(kRecheckWarps * 32)
     route_recheck_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
                          const float* __restrict__ bias, int H, int fn, RouteScratch rs) {
+  __shared__ double part[kRecheckWarps];
   const int n = rs.counters[1];
-  const int lane = threadIdx.x & 31;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int vecs = H / 8;
-  for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int vecs = H / 8;  // 16-byte vectors per row
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
     const int2 pr = rs.pairs[i];
     const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(pr.x) * H);
     const uint4* wr = reinterpret_cast<const uint4*>(WgT + static_cast<long long>(pr.y) * H);
-    // eight independent (hi, lo) accumulators, one per element of a 16-byte
-    // vector: each sees H / 256 terms, which keeps the rounding of lo tiny
+    // eight independent (hi, lo) accumulators, one per element of a vector
     float hi[8], lo[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.0f;
-#pragma unroll 2
-    for (int v = lane; v < vecs; v += 32) {
-      const uint4 a = __ldg(xr + v), b = __ldg(wr + v);
-      const float p[8] = {bf16_lo(a.x) * bf16_lo(b.x), bf16_hi(a.x) * bf16_hi(b.x),
-                          bf16_lo(a.y) * bf16_lo(b.y), bf16_hi(a.y) * bf16_hi(b.y),
-                          bf16_lo(a.z) * bf16_lo(b.z), bf16_hi(a.z) * bf16_hi(b.z),
-                          bf16_lo(a.w) * bf16_lo(b.w), bf16_hi(a.w) * bf16_hi(b.w)};
+    for (int v0 = threadIdx.x; v0 < vecs; v0 += 8 * kRecheckWarps * 32) {
+      uint4 a[8], b[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float sum, err;
-        two_sum(hi[q], p[q], sum, err);
-        hi[q] = sum;
-        lo[q] += err;
+      for (int u = 0; u < 8; ++u) {  // all loads of this round first
+        const int v = v0 + u * kRecheckWarps * 32;
+        a[u] = v < vecs ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+        b[u] = v < vecs ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float p[8] = {bf16_lo(a[u].x) * bf16_lo(b[u].x), bf16_hi(a[u].x) * bf16_hi(b[u].x),
+                            bf16_lo(a[u].y) * bf16_lo(b[u].y), bf16_hi(a[u].y) * bf16_hi(b[u].y),
+                            bf16_lo(a[u].z) * bf16_lo(b[u].z), bf16_hi(a[u].z) * bf16_hi(b[u].z),
+                            bf16_lo(a[u].w) * bf16_lo(b[u].w), bf16_hi(a[u].w) * bf16_hi(b[u].w)};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float sum, err;
+          two_sum(hi[q], p[q], sum, err);
+          hi[q] = sum;
+          lo[q] += err;
+        }
       }
     }
-    double part = 0.0;
+    // fold the eight pairs and then the warp's lanes as float pairs (fp32
+    // pipes); one conversion to float64 per warp
+    float H0 = hi[0], L0 = lo[0];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) part += static_cast<double>(hi[q]) + static_cast<double>(lo[q]);
-    const double l = warp_sum(part);
-    if (lane == 0) {
+    for (int q = 1; q < 8; ++q) ff_add(H0, L0, hi[q], lo[q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      ff_add(H0, L0, __shfl_xor_sync(0xffffffffu, H0, o), __shfl_xor_sync(0xffffffffu, L0, o));
+    if (lane == 0) part[warp] = static_cast<double>(H0) + static_cast<double>(L0);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double l = 0.0;
+#pragma unroll
+      for (int w = 0; w < kRecheckWarps; ++w) l += part[w];
       double v = score_f64(l, fn);
       if (bias != nullptr) v += static_cast<double>(bias[pr.y]);
-      rs.s64[i] = v;
+      rs.key[i] = order_key(v);
     }
+    __syncthreads();
   }
 }
 
@@ -277,31 +321,48 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < n; j += nw) {
     const int4 f = rs.flagged[j];
     const int t = f.x, base = f.y, count = f.z;
-    int sel[kMaxK];
-    double last_v = DBL_MAX;
+    // candidates held in registers, up to 4 per lane (count <= 128); more
+    // candidates than that are read from memory each round.  Scores are
+    // order-preserving integer keys: larger key = larger score.
+    constexpr int kHold = 4;
+    unsigned long long cv[kHold];
+    int ce[kHold];
+#pragma unroll
+    for (int h = 0; h < kHold; ++h) {
+      const int i = lane + 32 * h;
+      cv[h] = i < count ? rs.key[base + i] : 0ull;
+      ce[h] = i < count ? rs.pairs[base + i].y : 0x7fffffff;
+    }
+    int my_sel = -1;
+    unsigned long long last_v = ~0ull;
     int last_id = -1;
     // round r: the best candidate strictly after the previous winner in the
     // (larger score, lower id) order, so no candidate is taken twice
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
-      double best = -DBL_MAX;
+      unsigned long long best = 0ull;
       int bid = 0x7fffffff;
-      for (int i = lane; i < count; i += 32) {
+#pragma unroll
+      for (int h = 0; h < kHold; ++h)
+        if (before(last_v, last_id, cv[h], ce[h]) && before(cv[h], ce[h], best, bid)) {
+          best = cv[h];
+          bid = ce[h];
+        }
+      for (int i = lane + 32 * kHold; i < count; i += 32) {
         const int e = rs.pairs[base + i].y;
-        const double v = rs.s64[base + i];
+        const unsigned long long v = rs.key[base + i];
         if (before(last_v, last_id, v, e) && before(v, e, best, bid)) { best = v; bid = e; }
       }
       warp_argmax(best, bid);
-      sel[r] = bid;
+      if (lane == r) my_sel = bid;
       last_v = best;
       last_id = bid;
     }
     const float* lrow = logits + static_cast<long long>(t) * E;
     float lmax = 0.0f, zsum = 1.0f;
     if (fn == 2) softmax_norm(lrow, E, lane, lmax, zsum);
-    if (lane == 0)
-      write_gates(lrow, E, k, fn, alpha, renorm, sel, true, lmax, zsum,
-                  E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
+    write_gates(lrow, E, k, fn, alpha, renorm, my_sel, true, lmax, zsum, lane,
+                E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
   }
 }
 
@@ -346,7 +407,7 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                                       status);
   if (token_ids != nullptr) return cudaGetLastError();
   const int grid = 2 * num_sms();
-  route_recheck_kernel<<<grid, kWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
+  route_recheck_kernel<<<4 * grid, kRecheckWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
   route_reselect_kernel<<<grid, kWarps * 32, 0, s>>>(logits, E, k, score_fn, alpha, renorm, E_ids,
                                                      G, rs, status);
   return cudaGetLastError();

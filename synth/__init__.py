@@ -91,6 +91,9 @@ CONFIGS["c3_q"] = dict(CONFIGS["c3"], shared=0, quant="a8w8")
 # V4-Pro expert shapes at a size one ncu capture can take (4.2 GB of weights,
 # ~64 rows per expert as in c3, uniform load)
 CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
+# the V4-Pro router at full size with a token-sized FFN (I = 64): a workload
+# whose routing kernels one ncu capture can take (1.1 GB of weights)
+CONFIGS["c3r"] = dict(CONFIGS["c3"], I=64)
 # the pages' own V4-Pro routing rule (sqrt-softplus affinity) at the c3 shapes
 CONFIGS["c3_sp"] = dict(CONFIGS["c3"], score="sqrt_softplus", skew=None)
 
