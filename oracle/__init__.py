@@ -24,6 +24,11 @@ primitive).  Sources, cited by page title and section:
 * [MM] again, section "计算过程", A8W8 scenario: per-token int8 activations,
   per-channel int8 weights, int32 products, dequantisation, per-row
   re-quantisation of the SwiGLU output.
+* [MM] again, section "计算过程", MXFP scenario (the four stages: MX
+  quantisation of the dispatched rows, GMM1 + SwiGLU + MX quantisation, GMM2,
+  weighted combine) and section "约束说明" (group size 32, FLOAT8_E8M0
+  scales, element types FLOAT8_E4M3FN / FLOAT8_E5M2, weight1 [E, 2I, H] with
+  scales [E, 2I, ceil(H/64), 2], weight2 [E, H, I] with scales over I).
 
 Readings taken where the pages are silent:
 the score function is a parameter (sigmoid, sqrt-softplus, softmax); the k ids
@@ -34,7 +39,10 @@ same width I and weight 1; an assignment whose id is outside [0, E) is dropped.
 
 Parity status: routing ids, counts, permutation and the FFN/combine are pinned
 by tests/test_oracle_pins.py (closed forms, brute force, the worked split
-example, reductions to a dense FFN).  The absolute gate and output values for
+example, reductions to a dense FFN).  The MX functions are pinned against the
+FP8 code tables and round-to-nearest-even conversion of torch's float8 types,
+a hand-worked group, closed forms of the shared exponent and of the rounding
+error, and a scalar brute-force layer.  The absolute gate and output values for
 the sigmoid and sqrt-softplus rules at the workload sizes rest on these same
 formulas; the pages print no worked numbers for them.
 """
@@ -328,6 +336,155 @@ def forward_a8w8_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E
         rows = perm[offsets[e]:offsets[e + 1]] // k
         Yp[offsets[e]:offsets[e + 1]] = swiglu_expert_a8w8(
             q[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e))
+    Y = np.zeros((R, Hdim), dtype=np.float64)
+    for j in range(k):
+        p = inv[np.arange(R) * k + j]
+        ok = p >= 0
+        Y[ok] += G_rows[ok, j:j + 1] * Yp[p[ok]]
+    return Y
+
+
+# ----------------------------------------------------------------------------- MXFP8 (A8W8-FP)
+# [MM] 计算过程, MXFP scenario (dispatch_quant_mode 4): the token rows are
+# quantised per group of 32 consecutive elements along the contraction with a
+# shared power-of-two scale (FLOAT8_E8M0) and FP8 elements (FLOAT8_E4M3FN or
+# FLOAT8_E5M2); the weights arrive quantised the same way (W1 [E, 2I, H] with
+# scales over H, W2 [E, H, I] with scales over I, both stored K-contiguous);
+# Linear1 and Linear2 multiply the dequantised operands; the SwiGLU output is
+# re-quantised the same way before Linear2; the combine is unquantised.
+#
+# Readings (the pages name the operation Q_MX without spelling it out): the
+# shared exponent follows the OCP Microscaling formats definition,
+# X = floor(log2(max|v|)) - emax_elem, clamped to the E8M0 range [-127, 127]
+# (a group of zeros gets X = -127); each element is v / 2^X rounded to the
+# nearest FP8 value, ties to even mantissa, magnitudes beyond the largest
+# finite value saturating to it; the sign of zero is kept.
+
+# name -> (exponent bits, mantissa bits, exponent bias, largest finite value)
+FP8_FORMATS = {
+    "e4m3": (4, 3, 7, 448.0),      # FLOAT8_E4M3FN: no infinities, S.1111.111 is NaN
+    "e5m2": (5, 2, 15, 57344.0),   # FLOAT8_E5M2: IEEE-style, exponent 11111 is Inf/NaN
+}
+MX_GROUP = 32
+
+
+def fp8_decode(codes, fmt: str) -> np.ndarray:
+    """Value of each FP8 code from the format's definition (sign, biased
+    exponent, mantissa; exponent field 0 is subnormal), float64."""
+    eb, mb, bias, _ = FP8_FORMATS[fmt]
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c >> 7, -1.0, 1.0)
+    ef = (c >> mb) & ((1 << eb) - 1)
+    mf = c & ((1 << mb) - 1)
+    mag = np.where(ef == 0, mf / 2.0 ** mb * 2.0 ** (1 - bias),
+                   (1.0 + mf / 2.0 ** mb) * 2.0 ** (ef.astype(np.float64) - bias))
+    v = sign * mag
+    if fmt == "e4m3":
+        v = np.where((ef == 15) & (mf == 7), np.nan, v)
+    else:
+        v = np.where(ef == 31, np.where(mf == 0, sign * np.inf, np.nan), v)
+    return v
+
+
+def fp8_round(v, fmt: str) -> np.ndarray:
+    """Nearest FP8 value to v (float64), ties to the even mantissa, magnitude
+    saturated at the largest finite value.  The grid spacing at |v| is
+    2^(e - mantissa_bits) with e = floor(log2|v|), never below the subnormal
+    spacing 2^(1 - bias - mantissa_bits)."""
+    eb, mb, bias, vmax = FP8_FORMATS[fmt]
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), vmax)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, 1 - bias)
+    q = 2.0 ** (e - mb)
+    r = np.minimum(np.round(a / q) * q, vmax)   # np.round: halves to even
+    return np.copysign(r, v)
+
+
+def fp8_encode(v, fmt: str) -> np.ndarray:
+    """FP8 code (uint8) of fp8_round(v): the sign bit of v, then the code of
+    the rounded magnitude found in the table of finite non-negative codes."""
+    r = fp8_round(v, fmt)
+    pos = np.arange(128)
+    vals = fp8_decode(pos, fmt)
+    finite = np.isfinite(vals)
+    pos, vals = pos[finite], vals[finite]          # ascending with the code
+    mag = np.searchsorted(vals, np.abs(r))
+    assert np.array_equal(vals[mag], np.abs(r)), "rounded value off the FP8 grid"
+    return (pos[mag] | np.where(np.signbit(r), 0x80, 0)).astype(np.uint8)
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """FLOAT8_E8M0 scale: 2^(code - 127); code 255 is NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    return np.where(c == 255, np.nan, 2.0 ** (c.astype(np.float64) - 127))
+
+
+def mx_quantize(x, fmt: str, dtype=np.float64):
+    """Q_MX over the last axis (its length a multiple of 32): per group of 32,
+    X = floor(log2 max|v|) - emax_elem clamped to [-127, 127], elements
+    fp8(v / 2^X).  The group maximum and its exponent are taken in ``dtype``
+    (exact in either precision); v / 2^X is exact.  Returns (codes uint8
+    [..., K], scale codes uint8 [..., K/32])."""
+    eb, mb, bias, vmax = FP8_FORMATS[fmt]
+    emax = int(np.floor(np.log2(vmax)))
+    x = np.asarray(x, dtype=dtype)
+    K = x.shape[-1]
+    assert K % MX_GROUP == 0
+    g = x.reshape(x.shape[:-1] + (K // MX_GROUP, MX_GROUP)).astype(np.float64)
+    amax = np.abs(g).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))), -np.inf)
+    X = np.clip(ex - emax, -127, 127)
+    codes = fp8_encode(g / 2.0 ** X[..., None], fmt).reshape(x.shape)
+    return codes, (X + 127).astype(np.uint8)
+
+
+def mx_dequantize(codes, scales, fmt: str) -> np.ndarray:
+    """DQ_MX: element value times the scale of its group of 32 along the last
+    axis, float64."""
+    v = fp8_decode(codes, fmt)
+    s = np.repeat(e8m0_decode(scales), MX_GROUP, axis=-1)
+    return v * s
+
+
+def swiglu_expert_mx(xq, sx, W1q, S1, W2q, S2, fmt: str) -> np.ndarray:
+    """[MM] MXFP Expert Compute for one expert.  xq/sx: the expert's token
+    rows quantised [m, H] / [m, H/32]; W1q [2I, H], S1 [2I, H/32]; W2q [H, I],
+    S2 [H, I/32].  Z = DQ(xq) DQ(W1)^T; U = Z^(x) * sigma(Z^(x)) * Z^(y) with
+    Z^(x) the first I columns; (Uq, SU) = Q_MX(U); O = DQ(Uq) DQ(W2)^T."""
+    Xd = mx_dequantize(xq, sx, fmt)
+    W1d = mx_dequantize(W1q, S1, fmt)
+    Z = Xd @ W1d.T
+    I = np.asarray(W2q).shape[1]
+    U = _silu(Z[:, :I]) * Z[:, I:]
+    Uq, SU = mx_quantize(U, fmt)
+    return mx_dequantize(Uq, SU, fmt) @ mx_dequantize(W2q, S2, fmt).T
+
+
+def forward_mx_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: int,
+                      fmt: str) -> np.ndarray:
+    """MXFP layer output for a set of tokens, float64 (the caller rounds to
+    bf16).  The token rows are quantised once per token (a row's groups do
+    not depend on which expert receives it, so quantising after the gather,
+    as the pages order it, gives the same codes).  W1q/S1/W2q/S2 may be
+    arrays indexed by expert or callables e -> array."""
+    R = len(tokens)
+    E_rows = np.asarray(E_rows, dtype=np.int64).reshape(R, -1)
+    G_rows = np.asarray(G_rows, dtype=np.float64).reshape(R, -1)
+    k = E_rows.shape[1]
+    x = bf16_to_f64(X_rows_bits).reshape(R, -1)
+    xq, sx = mx_quantize(x, fmt)
+    counts, offsets, perm, inv = dispatch(E_rows, E)
+    Hdim = x.shape[1]
+    Yp = np.zeros((perm.shape[0], Hdim), dtype=np.float64)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        rows = perm[offsets[e]:offsets[e + 1]] // k
+        Yp[offsets[e]:offsets[e + 1]] = swiglu_expert_mx(
+            xq[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e), fmt)
     Y = np.zeros((R, Hdim), dtype=np.float64)
     for j in range(k):
         p = inv[np.arange(R) * k + j]

@@ -88,6 +88,14 @@ CONFIGS["c3s_q"] = dict(CONFIGS["c3s"], shared=0, quant="a8w8")
 CONFIGS["c5s_q"] = dict(CONFIGS["c5s"], quant="a8w8")
 CONFIGS["c2_q"] = dict(CONFIGS["c2"], quant="a8w8")
 CONFIGS["c3_q"] = dict(CONFIGS["c3"], shared=0, quant="a8w8")
+# MXFP forms: FP8 weight codes with E8M0 group scales (no shared expert).
+# H and I are multiples of 128 (one block of 128 FP8 elements = 4 groups).
+CONFIGS["c2s_mx"] = dict(CONFIGS["c2s"], I=384, quant="mx_e4m3")
+CONFIGS["c3s_mx"] = dict(CONFIGS["c3s"], H=512, I=256, shared=0, quant="mx_e4m3")
+CONFIGS["c3s_mx5"] = dict(CONFIGS["c3s"], H=512, I=256, shared=0, quant="mx_e5m2")
+CONFIGS["c5s_mx"] = dict(CONFIGS["c5s"], I=640, quant="mx_e4m3")
+CONFIGS["c2_mx"] = dict(CONFIGS["c2"], quant="mx_e4m3")
+CONFIGS["c3_mx"] = dict(CONFIGS["c3"], shared=0, quant="mx_e4m3")
 # V4-Pro expert shapes at a size one ncu capture can take (4.2 GB of weights,
 # ~64 rows per expert as in c3, uniform load)
 CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
@@ -187,6 +195,33 @@ def _int8_weights(seed, tid, shape, std):
     return codes.astype(np.int8), scales.astype(np.float32)
 
 
+# MX weights (FP8 element codes, E8M0 group scales), drawn as bytes: a random
+# sign bit and a magnitude code from a rounded normal in code space centred on
+# the code of 1.0 (E4M3: 0x38, eight codes per octave; E5M2: 0x3C, four per
+# octave), clipped to the finite codes; group scale codes 2^floor(log2 std)
+# or half of it.  Layout [E, N, K] with scales [E, N, K/32] (K contiguous).
+_MX_CODES = {"mx_e4m3": (56.0, 8.0, 126), "mx_e5m2": (60.0, 4.0, 123)}
+
+
+def mx_format(quant) -> str | None:
+    """'e4m3' / 'e5m2' for an MX workload, else None."""
+    return quant[3:] if quant in _MX_CODES else None
+
+
+def _mx_scale_code(std) -> int:
+    return 127 + int(math.floor(math.log2(std)))
+
+
+def _mx_weights(seed, tid, shape, std, quant):
+    rng = _rng(seed, 200 + tid)
+    c0, w, top = _MX_CODES[quant]
+    mag = np.clip(np.rint(rng.standard_normal(size=shape, dtype=np.float32) * w + c0), 0, top)
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << 7
+    s0 = _mx_scale_code(std)
+    scales = rng.integers(s0 - 1, s0 + 1, size=shape[:-1] + (shape[-1] // 32,), dtype=np.int32)
+    return (mag.astype(np.uint8) | sign), scales.astype(np.uint8)
+
+
 def _distinct_rows(rng: np.random.Generator, n: int, E: int, k: int) -> np.ndarray:
     """n rows of k distinct experts each, a uniform random k-subset per row in
     random order: the first k of a random permutation (random sort keys)."""
@@ -215,6 +250,9 @@ def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
     if cfg.get("quant") == "a8w8":
         d["W1"], d["S1"] = _int8_weights(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
         d["W2"], d["S2"] = _int8_weights(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
+    elif mx_format(cfg.get("quant")):
+        d["W1"], d["S1"] = _mx_weights(seed, 4, (E, 2 * I, H), 1.0 / math.sqrt(H), cfg["quant"])
+        d["W2"], d["S2"] = _mx_weights(seed, 5, (E, H, I), 1.0 / math.sqrt(I), cfg["quant"])
     else:
         d["W1"] = _normal_bf16(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
         d["W2"] = _normal_bf16(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
@@ -292,9 +330,25 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
         u = torch.rand((shape[0], shape[2]), generator=g, device=dev) * 0.5 + 0.75
         return codes, (u * (std / _CODE_STD)).float().contiguous()
 
+    def mx_weights(tid, shape, std):
+        g = gen(200 + tid)
+        c0, w, top = _MX_CODES[cfg["quant"]]
+        codes = torch.empty(shape, dtype=torch.uint8, device=dev)
+        for i in range(shape[0]):
+            mag = (torch.randn(shape[1:], generator=g, device=dev) * w + c0).round_().clamp_(0, top)
+            sign = torch.randint(0, 2, shape[1:], generator=g, device=dev, dtype=torch.int32) * 128
+            codes[i] = (mag.to(torch.int32) + sign).to(torch.uint8)
+        s0 = _mx_scale_code(std)
+        scales = torch.randint(s0 - 1, s0 + 1, shape[:-1] + (shape[-1] // 32,), generator=g,
+                               device=dev, dtype=torch.int32).to(torch.uint8)
+        return codes, scales
+
     if weights and cfg.get("quant") == "a8w8":
         d["W1"], d["S1"] = int8_weights(4, (E, H, 2 * I), 1.0 / math.sqrt(H))
         d["W2"], d["S2"] = int8_weights(5, (E, I, H), 1.0 / math.sqrt(I))
+    elif weights and mx_format(cfg.get("quant")):
+        d["W1"], d["S1"] = mx_weights(4, (E, 2 * I, H), 1.0 / math.sqrt(H))
+        d["W2"], d["S2"] = mx_weights(5, (E, H, I), 1.0 / math.sqrt(I))
     elif weights:
         d["W1"] = normal(4, (E, H, 2 * I), 1.0 / math.sqrt(H), per_slice=True)
         d["W2"] = normal(5, (E, I, H), 1.0 / math.sqrt(I), per_slice=True)

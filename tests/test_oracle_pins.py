@@ -379,3 +379,167 @@ def test_a8w8_layer_within_the_activation_quantisation_bound():
             want += G[t, j] * (a @ W2)
             bound += abs(G[t, j]) * (np.abs(a).max() / 127 / 2) * np.abs(W2).sum(0)
         assert (np.abs(Y[t] - want) <= bound * (1 + 1e-9) + 1e-12).all()
+
+
+# ------------------------------------------------------------------ MXFP8
+_TORCH_FP8 = {"e4m3": "float8_e4m3fn", "e5m2": "float8_e5m2"}
+
+
+def _torch_fp8(fmt):
+    torch = pytest.importorskip("torch")
+    dt = getattr(torch, _TORCH_FP8[fmt], None)
+    if dt is None:
+        pytest.skip("this torch has no %s" % _TORCH_FP8[fmt])
+    return torch, dt
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_decode_matches_torch_table(fmt):
+    torch, dt = _torch_fp8(fmt)
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(dt).to(torch.float64).numpy()
+    ours = oracle.fp8_decode(np.arange(256), fmt)
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_rounding_matches_torch_in_range(fmt):
+    """Inside the finite range the rounding is the library's round-to-nearest-
+    even conversion; the exact midpoints between neighbouring codes decide the
+    tie rule."""
+    torch, dt = _torch_fp8(fmt)
+    vmax = oracle.FP8_FORMATS[fmt][3]
+    grid = oracle.fp8_decode(np.arange(128), fmt)
+    grid = grid[np.isfinite(grid)]
+    mids = (grid[:-1] + grid[1:]) / 2
+    rng = np.random.default_rng(11)
+    rand = np.exp(rng.uniform(np.log(1e-7), np.log(vmax), 20000)) * rng.choice([-1, 1], 20000)
+    v = np.concatenate([mids, -mids, grid, -grid, rand, [0.0, -0.0]]).astype(np.float32)
+    assert np.all(np.abs(v) <= vmax)
+    ref = torch.from_numpy(v).to(dt).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.fp8_encode(v.astype(np.float64), fmt), ref)
+
+
+def test_fp8_saturates_to_the_largest_finite_value():
+    # E4M3FN: S.1111.110 = 1.75 * 2^8 = 448; E5M2: S.11110.11 = 1.75 * 2^15
+    for fmt, code in (("e4m3", 0x7E), ("e5m2", 0x7B)):
+        vmax = oracle.FP8_FORMATS[fmt][3]
+        v = np.array([vmax, vmax * 1.01, vmax * 1.2, 1e30, -vmax * 1.2, -1e30])
+        got = oracle.fp8_encode(v, fmt)
+        assert list(got) == [code, code, code, code, code | 0x80, code | 0x80]
+
+
+def test_mx_quantize_worked_group():
+    """Worked by hand: x = 1..32.  max 32 = 2^5, E4M3 emax = 8, so the shared
+    exponent is 5 - 8 = -3 (scale code 124) and the elements are 8x.  In
+    [128, 256) the E4M3 spacing is 2^(7-3) = 16: 136 = 8.5 steps rounds to
+    the even 8 (128 -> 16), 152 = 9.5 steps to 10 (160 -> 20), 168 = 10.5
+    to 10 (160 -> 20), 184 = 11.5 to 12 (192 -> 24), 200 = 12.5 to 12,
+    216 = 13.5 to 14 (224 -> 28), 232 = 14.5 to 14, 248 = 15.5 to 16
+    (256 -> 32); below 128 every 8x is on the grid."""
+    x = np.arange(1, 33, dtype=np.float64)
+    q, s = oracle.mx_quantize(x, "e4m3")
+    assert list(s) == [124]
+    want = list(range(1, 17)) + [16, 18, 20, 20, 20, 22, 24, 24, 24, 26, 28, 28, 28, 30, 32, 32]
+    assert list(oracle.mx_dequantize(q, s, "e4m3")) == want
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_mx_quantize_closed_forms(fmt):
+    """The shared exponent from frexp (an independent route to floor(log2)),
+    the rounding error bound of each element, exact round trips of values
+    already on the MX grid, and a group of zeros."""
+    eb, mb, bias, vmax = oracle.FP8_FORMATS[fmt]
+    emax = {"e4m3": 8, "e5m2": 15}[fmt]
+    rng = np.random.default_rng(3)
+    G = 400
+    x = rng.standard_normal((G, 32)) * np.exp(rng.uniform(-20, 20, (G, 1)))
+    q, s = oracle.mx_quantize(x, fmt)
+    d = oracle.mx_dequantize(q, s, fmt)
+    for g in range(G):
+        amax = float(np.abs(x[g]).max())
+        X = math.frexp(amax)[1] - 1 - emax
+        assert int(s[g, 0]) == X + 127
+        for v, dv in zip(x[g], d[g]):
+            a = abs(v) / 2.0 ** X
+            if a >= vmax:
+                assert dv == math.copysign(vmax, v) * 2.0 ** X
+                continue
+            e = max(math.frexp(a)[1] - 1, 1 - bias) if a > 0 else 1 - bias
+            assert abs(dv - v) <= 2.0 ** (e - mb - 1) * 2.0 ** X
+    # values on the grid come back unchanged
+    grid = oracle.mx_dequantize(q, s, fmt)
+    q2, s2 = oracle.mx_quantize(grid, fmt)
+    assert np.array_equal(oracle.mx_dequantize(q2, s2, fmt), grid)
+    qz, sz = oracle.mx_quantize(np.zeros((1, 64)), fmt)
+    assert list(sz[0]) == [0, 0] and not qz.any()
+
+
+def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt):
+    """Per token, per expert, scalar loops: FP8 codes decoded by torch's float8
+    type, scales 2^(code-127) by ldexp, shared exponents by frexp, element
+    rounding by torch's conversion after clamping to the finite range."""
+    torch, dt = _torch_fp8(fmt)
+    vmax = oracle.FP8_FORMATS[fmt][3]
+    emax = {"e4m3": 8, "e5m2": 15}[fmt]
+
+    def dec(code):
+        return torch.tensor([int(code)], dtype=torch.uint8).view(dt).to(torch.float64).item()
+
+    def quant_row(v):
+        out = []
+        for g0 in range(0, len(v), 32):
+            grp = v[g0:g0 + 32]
+            amax = max(abs(t) for t in grp)
+            X = max(-127, math.frexp(amax)[1] - 1 - emax) if amax > 0 else -127
+            for t in grp:
+                c = min(max(t / 2.0 ** X, -vmax), vmax)
+                code = torch.tensor([c], dtype=torch.float32).to(dt).view(torch.uint8).item()
+                out.append(math.ldexp(dec(code), X))
+        return out
+
+    T, k = E_ids.shape
+    H = X.shape[1]
+    I = W2q.shape[2]
+    Y = np.zeros((T, H))
+    for t in range(T):
+        xd = quant_row([float(v) for v in X[t]])
+        for j in range(k):
+            e = int(E_ids[t, j])
+            z = []
+            for n in range(2 * I):
+                acc = 0.0
+                for h in range(H):
+                    w = math.ldexp(dec(W1q[e, n, h]), int(S1[e, n, h // 32]) - 127)
+                    acc += xd[h] * w
+                z.append(acc)
+            u = [z[i] / (1.0 + math.exp(-z[i])) * z[I + i] for i in range(I)]
+            ud = quant_row(u)
+            for hh in range(H):
+                acc = 0.0
+                for i in range(I):
+                    acc += ud[i] * math.ldexp(dec(W2q[e, hh, i]), int(S2[e, hh, i // 32]) - 127)
+                Y[t, hh] += float(G[t, j]) * acc
+    return Y
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_mx_layer_matches_scalar_bruteforce(fmt):
+    rng = np.random.default_rng(21)
+    T, H, I, E, k = 4, 64, 32, 3, 2
+    X = oracle.round_to_bf16(rng.standard_normal((T, H)))
+    codes = np.arange(256)
+    vals = oracle.fp8_decode(codes, fmt)
+    finite = codes[np.isfinite(vals) & (np.abs(vals) <= 4.0)]
+    W1q = rng.choice(finite, (E, 2 * I, H)).astype(np.uint8)
+    W2q = rng.choice(finite, (E, H, I)).astype(np.uint8)
+    S1 = rng.integers(118, 124, (E, 2 * I, H // 32)).astype(np.uint8)
+    S2 = rng.integers(118, 124, (E, H, I // 32)).astype(np.uint8)
+    E_ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1]])
+    G = rng.uniform(0.1, 1.0, (T, k))
+    got = oracle.forward_mx_tokens(np.arange(T), oracle.f64_to_bf16_bits(X), E_ids, G,
+                                   W1q, S1, W2q, S2, E, fmt)
+    want = _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt)
+    scale = np.abs(want).max()
+    assert np.allclose(got, want, rtol=1e-9, atol=1e-12 * scale)
