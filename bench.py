@@ -44,7 +44,16 @@ WORKLOAD_TEXT = {
     "c3r": "V4-Pro router at full size with I=64 (profiling size for the routing kernels)",
     "c3_q": "V4-Pro-shaped layer, A8W8-INT form (int8 weights, per-token int8 activations), no shared expert",
     "c2_q": "given-routing layer, A8W8-INT form",
+    "c3_mx": "V4-Pro-shaped layer, MXFP8 form (E4M3 codes, E8M0 scales per 32), no shared expert",
+    "c2_mx": "given-routing layer, MXFP8 form (E4M3)",
+    "c3p_mx": "V4-Pro expert shapes, T=512 E=48, MXFP8 form (profiling size)",
 }
+
+
+def synth_mx_format(cfg):
+    """'e4m3' / 'e5m2' for an MX workload, else None."""
+    q = cfg.get("quant") or ""
+    return q[3:] if q.startswith("mx_") else None
 
 
 def peaks():
@@ -152,6 +161,9 @@ def build_step(moe, dd, p, ws, stage_events=None):
         if c.get("quant") == "a8w8":
             moe.moe_forward_a8w8(p, X, E_ids, G, dd["W1"], dd["S1"], dd["W2"], dd["S2"], Y,
                                  dd["_ws_q"], stage_events)
+        elif synth_mx_format(c):
+            moe.moe_forward_mx(p, moe.MX_FORMATS[synth_mx_format(c)], X, E_ids, G, dd["W1"], dd["S1"],
+                               dd["W2"], dd["S2"], Y, dd["_ws_q"], stage_events)
         elif stage_events is not None:
             moe.moe_forward_timed(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws,
                                   stage_events)
@@ -177,8 +189,11 @@ def run_ours(args, rank, world, local_rank):
     p = moe.params_from_config(c)
     ws = moe.alloc_workspace(p, dev)
     quant = c.get("quant") == "a8w8"
+    mx = synth_mx_format(c)
     if quant:
         dd["_ws_q"] = moe.alloc_workspace_a8w8(p, dev)
+    if mx:
+        dd["_ws_q"] = moe.alloc_workspace_mx(p, dev)
     dd["_E_ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
     dd["_G"] = torch.empty((T, k), dtype=torch.float32, device=dev)
     dd["_Y"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -216,7 +231,7 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.mark_end()
     moe.moe_sync_status(ws)
-    if quant:
+    if quant or mx:
         moe.moe_sync_status(dd["_ws_q"])
     ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world, dev)
 
@@ -227,6 +242,9 @@ def run_ours(args, rank, world, local_rank):
     if quant:
         stages = {"dispatch_quant": stages["dispatch"], "gemm1_swiglu": stages["gemm1_swiglu"],
                   "quant_gemm2": stages["gemm2"], "combine": stages["combine"]}
+    if mx:
+        stages = {"dispatch_quant": stages["dispatch"], "gemm1_swiglu_quant": stages["gemm1_swiglu"],
+                  "gemm2": stages["gemm2"], "combine": stages["combine"]}
     if routed:
         stages = {"route": avg(rt_ev, 0, 1), **stages}
 
@@ -297,18 +315,26 @@ def run_ours(args, rank, world, local_rank):
     if quant:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=1, x_bytes=2, act_bytes=4)
         g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=1, act_bytes=2)
+    elif mx:
+        g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=accounting.MX8,
+                                          x_bytes=accounting.MX8, act_bytes=accounting.MX8)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=accounting.MX8,
+                                          act_bytes=accounting.MX8)
     else:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
         g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T)
     g1_flops = accounting.gemm1_flops(counts, H, I, has_shared, T)
     g2_flops = accounting.gemm2_flops(counts, H, I, has_shared, T)
-    g1_s = stages["gemm1_swiglu"] / 1e3
+    g1_s = stages["gemm1_swiglu_quant" if mx else "gemm1_swiglu"] / 1e3
     g2_s = stages["quant_gemm2" if quant else "gemm2"] / 1e3
     gemm_tflops = (g1_flops + g2_flops) / (g1_s + g2_s) / 1e12
     # the dominant kernel: Linear1 + SwiGLU.  Weight streaming bounds it when the
     # arithmetic intensity is below the ridge point.
     ai = g1_flops / g1_bytes
-    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    # the FP8 block-scaled tensor rate is twice the bf16 rate (nominal 4.5 vs
+    # 2.25 PFLOP/s dense): its peak is the measured bf16 figure times 2
+    tc_peak = pk["bf16_tflops_sustained"] * (2 if mx else 1)
+    ridge = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
     if ai < ridge:
         achieved = g1_bytes / g1_s / 1e9
         roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<1>)", "bound": "hbm",
@@ -318,35 +344,40 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": pk["source"] + " hbm_gbs"}
     else:
         achieved = g1_flops / g1_s / 1e12
-        peak = pk["bf16_tflops_sustained"]
+        peak = tc_peak
         roof = {"kernel": "grouped Linear1 + SwiGLU (gemm_tc_kernel<1>)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "algorithmic_flops_per_launch": int(g1_flops),
-                "peak_source": pk["source"] + " bf16_tflops_sustained"}
-    if roof["bound"] == "hbm" and not quant:
+                "peak_source": pk["source"] + " bf16_tflops_sustained" + (" x 2 (fp8)" if mx else "")}
+    if roof["bound"] == "hbm" and not quant and not mx:
         roof["traffic"] = load_traffic(args.workload, g1_bytes)
     if quant:
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_tc_kernel<3>)"
+    if mx:
+        roof["kernel"] = "grouped MX Linear1 + SwiGLU + Q_MX (gemm_mx_kernel<true, %d>)" % moe.MX_FORMATS[mx]
     # route: transpose Wg, gating GEMM, select, recheck, reselect (hash: GEMM, select);
-    # forward: count, scan, place, gather, Linear1, Linear2, combine
-    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + (9 if quant else 7)
+    # forward: count, scan, place, Linear1 (row gather fused), Linear2, combine;
+    # A8W8 adds the token and the activation quantisation, MX the token one
+    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + (8 if quant else (7 if mx else 6))
     out = {
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8" if quant else "bf16",
+        "dtype": "int8" if quant else (mx if mx else "bf16"),
         "data": "synthetic (seeded; random-init weights of the workload's shapes)",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
                    "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": has_shared,
                    "routing": c["routing"], "score": c["score"],
                    "l2": "inputs larger than L2: %.1f GB of expert weights per step"
-                         % ((E + has_shared) * 3 * H * I * (1 if quant else 2) / 1e9),
-                   "weights": "int8 + per-channel fp32 scales (A8W8-INT)" if quant else "bf16",
+                         % ((E + has_shared) * 3 * H * I * (1 if quant else (accounting.MX8 if mx else 2)) / 1e9),
+                   "weights": ("int8 + per-channel fp32 scales (A8W8-INT)" if quant else
+                               (f"{mx} codes + E8M0 scales per 32 (MX)" if mx else "bf16")),
                    "parallelism": f"replicas x{world} (token batches, no collective)"},
         "stages_ms": {k_: round(v, 4) for k_, v in stages.items()},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1),
                          "pct_bf16_peak": round(100 * gemm_tflops / pk["bf16_tflops_sustained"], 2),
+                         "pct_own_dtype_peak": round(100 * gemm_tflops / tc_peak, 2),
                          "peak_tflops": pk["bf16_tflops_sustained"],
                          "gemm1_GBps": round(g1_bytes / g1_s / 1e9, 1),
                          "gemm2_GBps": round(g2_bytes / g2_s / 1e9, 1)},
@@ -419,9 +450,18 @@ class OracleRunner:
                                           c["alpha"], c["renorm"])
         else:
             ids, G, _ = oracle.route(X, self.Wg, self.bias, c["score_fn"], c["k"], c["alpha"], c["renorm"])
-        W1 = lambda e: self.bits(self.dd["W1"][e])  # noqa: E731
-        W2 = lambda e: self.bits(self.dd["W2"][e])  # noqa: E731
-        Y = oracle.forward_tokens(rows, X, ids, G, W1, W2, self.Ws1, self.Ws2, E=c["E"])
+        dd = self.dd
+        raw = lambda key: (lambda e: dd[key][e].cpu().numpy())  # noqa: E731
+        if c.get("quant") == "a8w8":
+            Y = oracle.forward_a8w8_tokens(rows, X, ids, G, raw("W1"), raw("S1"), raw("W2"), raw("S2"),
+                                           E=c["E"])
+        elif synth_mx_format(c):
+            Y = oracle.forward_mx_tokens(rows, X, ids, G, raw("W1"), raw("S1"), raw("W2"), raw("S2"),
+                                         E=c["E"], fmt=synth_mx_format(c))
+        else:
+            W1 = lambda e: self.bits(dd["W1"][e])  # noqa: E731
+            W2 = lambda e: self.bits(dd["W2"][e])  # noqa: E731
+            Y = oracle.forward_tokens(rows, X, ids, G, W1, W2, self.Ws1, self.Ws2, E=c["E"])
         oracle.f64_to_bf16_bits(Y)
         return n
 

@@ -23,6 +23,10 @@ SCORE_SIGMOID = 0
 SCORE_SQRT_SOFTPLUS = 1
 SCORE_SOFTMAX = 2
 
+MOE_MX_E4M3 = 0
+MOE_MX_E5M2 = 1
+MX_FORMATS = {"e4m3": MOE_MX_E4M3, "e5m2": MOE_MX_E5M2}
+
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
 MOE_ERR_UNSUPPORTED = 2
@@ -61,6 +65,10 @@ SIGNATURES = {
     "moe_workspace_size_a8w8": (_SZ, [_PP]),
     "moe_forward_a8w8": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                         ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_quantize_mx": (ctypes.c_int, [_I32, _P, _I32, _I32, _P, _P, _P]),
+    "moe_workspace_size_mx": (_SZ, [_PP]),
+    "moe_forward_mx": (ctypes.c_int, [_PP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                      ctypes.POINTER(ctypes.c_void_p)]),
     "moe_sync_status": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -213,6 +221,38 @@ def moe_forward_a8w8(p, X, E_ids, G, W1q, S1, W2q, S2, Y, ws, stage_events=None,
     return _check(lib().moe_forward_a8w8(ctypes.byref(p), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1q), _ptr(S1),
                                          _ptr(W2q), _ptr(S2), _ptr(Y), _ptr(ws), ws.numel(), _stream(stream),
                                          arr), "moe_forward_a8w8")
+
+
+def moe_quantize_mx(fmt: int, X, Q, S, stream=None):
+    """Q_MX of the bf16 rows of X [rows, cols] into codes Q and E8M0 scales S."""
+    rows, cols = X.shape
+    return _check(lib().moe_quantize_mx(int(fmt), _ptr(X), int(rows), int(cols), _ptr(Q), _ptr(S),
+                                        _stream(stream)), "moe_quantize_mx")
+
+
+def moe_workspace_size_mx(p: MoeParams) -> int:
+    return int(lib().moe_workspace_size_mx(ctypes.byref(p)))
+
+
+def alloc_workspace_mx(p: MoeParams, device="cuda", stream=None):
+    """A zero-headed uint8 device tensor of moe_workspace_size_mx(p) bytes."""
+    import torch
+    n = moe_workspace_size_mx(p)
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_workspace_size_mx")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_forward_mx(p, fmt: int, X, E_ids, G, W1, S1, W2, S2, Y, ws, stage_events=None, stream=None):
+    """MX (FP8 codes + E8M0 group scales) layer forward."""
+    arr = None
+    if stage_events is not None:
+        arr = (ctypes.c_void_p * 5)(*[(ev.cuda_event if ev is not None else None) for ev in stage_events])
+    return _check(lib().moe_forward_mx(ctypes.byref(p), int(fmt), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1),
+                                       _ptr(S1), _ptr(W2), _ptr(S2), _ptr(Y), _ptr(ws), ws.numel(),
+                                       _stream(stream), arr), "moe_forward_mx")
 
 
 def moe_selftest_wait_timeout(ws, limit_us: int, stream=None):

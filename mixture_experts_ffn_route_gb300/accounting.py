@@ -12,6 +12,7 @@ import numpy as np
 BF16 = 2
 F32 = 4
 I32 = 4
+MX8 = 1 + 1 / 32  # an FP8 code plus its share of the E8M0 scale of its group of 32
 
 
 def _counts(counts, has_shared, T):

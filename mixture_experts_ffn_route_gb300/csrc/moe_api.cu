@@ -91,6 +91,35 @@ static WsLayoutQ layout_a8w8(const moe_params& p) {
   return L;
 }
 
+// Workspace layout of the MX forward.
+struct WsLayoutMX {
+  size_t status, chunk_cnt, counts, row_off, tile_off, perm, inv, xq, sx, uq, su, yp, total;
+};
+
+static WsLayoutMX layout_mx(const moe_params& p) {
+  WsLayoutMX L;
+  const size_t T = static_cast<size_t>(p.T), E = static_cast<size_t>(p.E);
+  const size_t A = T * static_cast<size_t>(p.k);
+  const size_t H = static_cast<size_t>(p.H), I = static_cast<size_t>(p.I);
+  const size_t nchunk = static_cast<size_t>(dispatch_chunks(static_cast<int>(A)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(256);
+  L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
+  L.counts = take((E + 2) * sizeof(int));
+  L.row_off = take((E + 2) * sizeof(int));
+  L.tile_off = take((E + 2) * sizeof(int));
+  L.perm = take(A * sizeof(int));
+  L.inv = take(A * sizeof(int));
+  L.xq = take(A * H);
+  L.sx = take(A * H / 32);
+  L.uq = take(A * I);
+  L.su = take(A * I / 32);
+  L.yp = take(A * H * sizeof(float));
+  L.total = o;
+  return L;
+}
+
 static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 static moe_status check_params(const moe_params* p) {
@@ -509,6 +538,133 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
     if (launch_gemm(kGemmPlain_Q8, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
+}
+
+moe_status moe_quantize_mx(int32_t fmt, const uint16_t* X, int32_t rows, int32_t cols,
+                           uint8_t* Q, uint8_t* S, void* stream) {
+  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E5M2) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!X || !Q || !S || !aligned16(X) || !aligned16(Q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_mx_quant_rows(fmt, X, rows, cols, Q, S, nullptr, 0,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_size_mx(const moe_params* p) {
+  if (check_params(p) != MOE_OK) return 0;
+  return layout_mx(*p).total;
+}
+
+moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
+                          const int32_t* E_ids, const float* G, const uint8_t* W1,
+                          const uint8_t* S1, const uint8_t* W2, const uint8_t* S2, uint16_t* Y,
+                          void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E5M2) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared) return MOE_ERR_UNSUPPORTED;
+  if (p->H % kMxBK != 0 || p->I % kMxBK != 0) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+      ws_bytes < layout_mx(*p).total)
+    return MOE_ERR_WORKSPACE;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !E_ids || !G || !W1 || !S1 || !W2 || !S2 || !Y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(S1) & 3u) != 0 || (reinterpret_cast<uintptr_t>(S2) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
+
+  const WsLayoutMX L = layout_mx(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  DispatchBufs b;
+  b.chunk_cnt = at<int>(ws, L.chunk_cnt);
+  b.counts = at<int>(ws, L.counts);
+  b.row_off = at<int>(ws, L.row_off);
+  b.tile_off = at<int>(ws, L.tile_off);
+  b.perm = at<int>(ws, L.perm);
+  b.inv = at<int>(ws, L.inv);
+  b.nchunk = dispatch_chunks(p->T * p->k);
+  const int T = p->T, H = p->H, E = p->E, k = p->k, I = p->I;
+  const int A = T * k;
+  uint8_t* Xq = at<uint8_t>(ws, L.xq);
+  uint8_t* SX = at<uint8_t>(ws, L.sx);
+  uint8_t* Uq = at<uint8_t>(ws, L.uq);
+  uint8_t* SU = at<uint8_t>(ws, L.su);
+  float* Yp = at<float>(ws, L.yp);
+  auto mark = [&](int i) -> cudaError_t {
+    if (stage_events == nullptr || stage_events[i] == nullptr) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
+  };
+  const int mt_bound = (A + kBM - 1) / kBM + E;
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_dispatch(E_ids, T, k, E, 0, b, status, s);
+  // each token row quantised once and written to its k rows in expert order
+  if (e == cudaSuccess) e = launch_mx_quant_rows(fmt, X, T, H, Xq, SX, b.inv, k, s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // Linear1 + SwiGLU + Q_MX on the token codes in expert order
+  {
+    GemmMaps maps;
+    if (!make_map_mx_rows(&maps.a, Xq, A, H) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 64))
+      return MOE_ERR_CUDA;
+    maps.a2 = maps.a;
+    maps.b2 = maps.b;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = E;
+    g.shared_group = -1;
+    g.n_tiles = I / 64;
+    g.num_kb = H / kMxBK;
+    g.n_out = I;
+    g.up_off = I;
+    g.out = Uq;
+    g.ldo = I;
+    g.out_sf = SU;
+    g.out_sf_ld = I / 32;
+    g.sfa = SX;
+    g.sfb = S1;
+    g.sf_ld = H / 32;
+    g.sfb_ld = 2LL * I * (H / 32);
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if (launch_gemm_mx(true, fmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // Linear2 on the re-quantised SwiGLU rows, fp32 out
+  {
+    GemmMaps maps;
+    if (!make_map_mx_rows(&maps.a, Uq, A, I) || !make_map_mx_weights(&maps.b, W2, E, H, I, 128))
+      return MOE_ERR_CUDA;
+    maps.a2 = maps.a;
+    maps.b2 = maps.b;
+    GemmParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = E;
+    g.shared_group = -1;
+    g.n_tiles = H / 128;
+    g.num_kb = I / kMxBK;
+    g.n_out = H;
+    g.out = Yp;
+    g.ldo = H;
+    g.sfa = SU;
+    g.sfb = S2;
+    g.sf_ld = I / 32;
+    g.sfb_ld = static_cast<long long>(H) * (I / 32);
+    g.status = status;
+    const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
+    const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
+    if (launch_gemm_mx(false, fmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);

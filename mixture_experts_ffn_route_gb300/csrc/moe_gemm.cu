@@ -36,6 +36,7 @@
 // gridDim.x.  Group row ranges come from device memory.
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_tile.cuh"
 
 namespace moe {
 
@@ -71,49 +72,6 @@ struct GemmCfg {
   static_assert(8 * (2 * STAGES + 2 * RAW_STAGES + 4) + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-
-struct TileInfo {
-  int group, m, n;
-  int row0, row_end;  // output rows [row0, row_end) of this tile's group
-  int a_row0;         // first A row fetched for this tile
-  bool second;        // uses the second (shared-expert) tensor maps
-};
-
-// Tile order: group by group; inside a group, column tile by column tile, and
-// the 128-row tiles of one column tile consecutively.  CTAs running at the
-// same time then share one weight column block through L2 while the group's
-// rows (the smaller operand) stay resident, so each weight byte is read from
-// HBM about once even when a group spans many row tiles.
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
-  TileInfo t;
-  if (p.row_off == nullptr) {
-    const int mt = (p.dense_rows + kBM - 1) / kBM;
-    t.group = 0;
-    t.n = tile / mt;
-    t.m = tile - t.n * mt;
-    t.row0 = t.m * kBM;
-    t.row_end = p.dense_rows;
-  } else {
-    // largest g with tile_off[g] * n_tiles <= tile (groups without tiles share
-    // their start with the next group)
-    int lo = 0, hi = p.num_groups - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.tile_off + mid) * p.n_tiles <= tile) lo = mid; else hi = mid - 1;
-    }
-    const int t0 = __ldg(p.tile_off + lo);
-    const int mt = __ldg(p.tile_off + lo + 1) - t0;
-    const int local = tile - t0 * p.n_tiles;
-    t.group = lo;
-    t.n = local / mt;
-    t.m = local - t.n * mt;
-    t.row0 = __ldg(p.row_off + lo) + t.m * kBM;
-    t.row_end = __ldg(p.row_off + lo + 1);
-  }
-  t.second = (t.group == p.shared_group);
-  t.a_row0 = (t.second && p.a2_shared) ? t.m * kBM : t.row0;
-  return t;
-}
 
 // First weight column of 64-wide B box j (bf16 forms) or 128-wide raw box j
 // (int8 forms) of column tile n.  SwiGLU tiles hold 128 gate columns followed
@@ -596,6 +554,36 @@ bool make_map_weights_i8(CUtensorMap* m, const void* base, int64_t groups, int64
                         static_cast<cuuint64_t>(groups)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(N * K)};
   cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kBK), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, cols] FP8 codes (bytes, cols contiguous), box = 128 columns x 128
+// rows, 128-byte swizzle.
+bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(kBM)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [groups, N, K] FP8 codes (K contiguous), box = 128 k x box_rows n x 1,
+// 128-byte swizzle: the K-major B tiles of the MX forms.
+bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K,
+                         int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

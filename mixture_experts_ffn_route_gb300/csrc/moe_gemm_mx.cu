@@ -1,0 +1,460 @@
+// Persistent grouped GEMM for the MX forms on the block-scaled tensor cores
+// (tcgen05.mma kind::mxf8f6f4: FP8 operands, one E8M0 scale per 32 k for
+// every row of A and of B, fp32 accumulator in TMEM).
+//
+//   Linear1: Z = DQ(Xq_e) DQ(W1[e])^T, U = Z_g * sigma(Z_g) * Z_u, and U
+//            re-quantised per 32 columns: FP8 codes + E8M0 scales out
+//   Linear2: O = DQ(Uq) DQ(W2[e])^T, fp32 out
+// These are the stages GMM1 + SwiGLU + MX quantisation and GMM2 of the MXFP
+// scenario on the "mega_moe" page (section 计算过程).  The weights keep the
+// pages' K-contiguous layout ([E, 2I, H] and [E, H, I]) with their scales
+// [E, N, K/32].
+//
+// Structure (one CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile [128 rows x 128 k] and B tile
+//               [128 n x 128 k], both K-major with 128-byte swizzle (Linear1:
+//               64 gate rows of W1 and the matching 64 up rows; Linear2: 128
+//               rows of W2).  Linear1's A rows are the token codes already laid
+//               out in expert order by the quantisation kernel.
+//   warp 1      allocates 512 TMEM columns (two 128-column accumulators and a
+//               pair of scale slots per stage); one lane copies the stage's two
+//               scale atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues
+//               four MMAs (M 128, N 128, K 32) whose scale byte is the k step.
+//   warps 2..5  epilogue (one accumulator row per thread).
+//   warps 6..9  per k-block, the 4 scale bytes of each of the 128 A rows and
+//               128 B rows into the stage's two 512-byte atoms (cp.async).
+// A scale atom holds 128 rows x 4 groups: row r's 4 bytes are the 32-bit word
+// at byte (r % 32) * 16 + (r / 32) * 4.  Copied with warpx4, TMEM lane l then
+// holds rows l % 32 + 32 c in column c, which is where the MMA reads the scale
+// of A row m (lane m, column m / 32) and of B row n (lane n % 32 of each lane
+// quarter, column n / 32); the byte inside the word is the MMA's scale id.
+#include <cuda_fp8.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "moe_tile.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMxBN = 128;
+constexpr int kMxA = kBM * kMxBK;     // 16 KB
+constexpr int kMxB = kMxBN * kMxBK;   // 16 KB
+constexpr int kMxAtom = 512;          // 128 rows x 4 scale bytes
+constexpr int kMxStageBytes = kMxA + kMxB + 2 * kMxAtom;  // 33 KB, a multiple of 1024
+constexpr int kMxStages = 6;
+constexpr int kMxRing = kMxStages * kMxStageBytes;
+constexpr int kMxBarBytes = 256;
+constexpr int kMxStgWords = 36;       // staging row pitch (32 data words + 4 pad)
+constexpr int kMxStg = 4 * 32 * kMxStgWords * 4;
+constexpr int kMxSmem = kMxRing + 1024 + kMxBarBytes + kMxStg;
+constexpr int kMxThreads = 320;
+constexpr int kMxTmemCols = 512;
+constexpr int kMxSfCol = 256;         // stage s: A scales at 256 + 8 s, B scales at 260 + 8 s
+static_assert(kMxStageBytes % 1024 == 0, "stage alignment");
+static_assert(kMxSfCol + 8 * kMxStages <= kMxTmemCols, "TMEM columns");
+static_assert(8 * (2 * kMxStages + 4) + 8 <= kMxBarBytes, "barrier area");
+static_assert(kMxSmem <= 232448, "shared memory");
+
+// 4-byte global -> shared copy.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Copy a 32-row x 16-byte matrix from shared memory to TMEM columns
+// [taddr, taddr + 4), replicated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled matrix (layout type 0): 8-row
+// core matrices of 16-byte rows, `sbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// D[tmem] (+)= (A * sA)(B * sB)^T with FP8 A, B and E8M0 scales in TMEM.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind: bits 4-5 B scale id,
+// 7-9 A format, 10-12 B format (0 = E4M3, 1 = E5M2), 15/16 A/B major
+// (0 = K-major), 17-22 N >> 3, 23 scale type (1 = E8M0), 24-28 M >> 4,
+// 29-30 A scale id.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t fmt) {
+  return (fmt << 7) | (fmt << 10) | ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
+  return (a_id << 29) | (b_id << 4);
+}
+
+// Largest power-of-two exponent of the element format: E4M3 448 = 1.75 * 2^8,
+// E5M2 57344 = 1.75 * 2^15.
+template <int FMT>
+struct Fp8 {
+  static constexpr int EMAX = FMT == 0 ? 8 : 15;
+  static constexpr __nv_fp8_interpretation_t KIND = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+};
+
+// Shared exponent of a group with maximum magnitude `amax` (the OCP MX rule):
+// floor(log2 amax) - emax, clamped below at -127; read off the fp32 exponent
+// field (a zero or subnormal maximum gives -127).
+template <int FMT>
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - Fp8<FMT>::EMAX;
+  return e < -127 ? -127 : e;
+}
+
+// Four values (already divided by the group scale) -> four FP8 codes, round to
+// nearest even with saturation, first value in the lowest byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, Fp8<FMT>::KIND);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, Fp8<FMT>::KIND);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Quantise 32 values of one group: 8 words of codes, returns the scale code.
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_group(const float (&v)[32], uint32_t (&w)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = mx_exponent<FMT>(amax);
+  // 2^-X, exact: X is in [-127, 120] so 127 - X is a normal exponent field
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = fp8x4<FMT>(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  return static_cast<uint32_t>(X + 127);
+}
+
+template <bool SWIGLU, int FMT>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + kMxRing;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * kMxStages + 4));
+  uint32_t* stg_area = reinterpret_cast<uint32_t*>(bar_area + kMxBarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t tiles0 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bar_area);
+  const uint32_t empty0 = full0 + 8 * kMxStages;
+  const uint32_t tfull0 = empty0 + 8 * kMxStages;
+  const uint32_t tempty0 = tfull0 + 16;
+
+  if (threadIdx.x == 0) {
+    // a stage is complete when the TMA bytes have landed (one arrival with the
+    // byte count) and each of the 128 row threads' copies have (one each)
+    for (int s = 0; s < kMxStages; ++s) {
+      mbar_init(full0 + 8 * s, 1 + 128);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kMxTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = __ldg(p.tile_off + p.num_groups) * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo t = decode_tile(p, tile);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t sa = tiles0 + stage * kMxStageBytes;
+          const uint32_t sb = sa + kMxA;
+          const int kx = kb * kMxBK;
+          mbar_arrive_expect_tx(fb, kMxA + kMxB);
+          tma_load_2d(sa, &tmA, fb, kx, t.row0);
+          if (SWIGLU) {
+            tma_load_3d(sb, &tmB, fb, kx, t.n * 64, t.group);
+            tma_load_3d(sb + 64 * kMxBK, &tmB, fb, kx, p.up_off + t.n * 64, t.group);
+          } else {
+            tma_load_3d(sb, &tmB, fb, kx, t.n * kMxBN, t.group);
+          }
+          if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ row threads
+    // Thread (gw, lane) copies the 4 scale bytes of A row and B row
+    // 32 gw + lane for each k-block.  A rows past the group's end are not
+    // copied: whatever their stale scales hold only reaches accumulator rows
+    // that are never stored.
+    const int sr = 32 * (warp - 6) + lane;  // scale row of this thread
+    const uint32_t atom_off = static_cast<uint32_t>((sr & 31) * 16 + (sr >> 5) * 4);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+      const TileInfo t = decode_tile(p, tile);
+      const int row = t.row0 + sr;
+      const uint8_t* sfa_src =
+          row < t.row_end ? p.sfa + static_cast<long long>(row) * p.sf_ld : nullptr;
+      const int nr = SWIGLU ? (sr < 64 ? t.n * 64 + sr : p.up_off + t.n * 64 + (sr - 64))
+                            : t.n * kMxBN + sr;
+      const uint8_t* sfb_src = p.sfb + t.group * p.sfb_ld + static_cast<long long>(nr) * p.sf_ld;
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const uint32_t atoms = tiles0 + stage * kMxStageBytes + kMxA + kMxB;
+        if (sfa_src != nullptr) cp_async4(atoms + atom_off, sfa_src + kb * 4);
+        cp_async4(atoms + kMxAtom + atom_off, sfb_src + kb * 4);
+        cp_async_arrive(full0 + 8 * stage);
+        if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN, FMT);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kMxBN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
+          // the row threads' copies went through the generic proxy
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t sa = tiles0 + stage * kMxStageBytes;
+          const uint32_t sb = sa + kMxA;
+          const uint32_t atoms = sb + kMxB;
+          const uint32_t tsa = tmem_base + kMxSfCol + 8 * stage;
+          const uint32_t tsb = tsa + 4;
+          // scale atoms -> TMEM; executes before the MMAs issued after it
+          tmem_cp_atom(tsa, smem_desc_plain(atoms, 128, 128));
+          tmem_cp_atom(tsb, smem_desc_plain(atoms + kMxAtom, 128, 128));
+#pragma unroll
+          for (int kk = 0; kk < kMxBK / 32; ++kk) {
+            // K-major rows of 128 B; a 32-wide k step is 32 B along the row
+            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
+            mma_mx(d, ad, bd, idesc | idesc_sf_ids(kk, kk), tsa, tsb, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(tfull0 + 8 * acc);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    uint32_t* stg = stg_area + q * 32 * kMxStgWords;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const TileInfo t = decode_tile(p, tile);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, p.status, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kMxBN;
+      const int wrow0 = t.row0 + q * 32;
+      if (SWIGLU) {
+        // 64 SwiGLU columns = two scale groups, each held whole by this thread
+        uint8_t* out = static_cast<uint8_t*>(p.out);
+        uint32_t w[16];
+        uint32_t sc[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float g[32], u[32];
+          tmem_ld_32x32(tb + 32 * h, g);
+          tmem_ld_32x32(tb + 64 + 32 * h, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+          uint32_t wh[8];
+          sc[h] = mx_group<FMT>(g, wh);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[8 * h + i] = wh[i];
+        }
+        uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) srow4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        __syncwarp();
+        // 8 rows x 64 bytes per store instruction
+        const int qd = lane & 3;
+        const int col = t.n * 64;
+#pragma unroll
+        for (int rr = 0; rr < 32; rr += 8) {
+          const int r = rr + (lane >> 2);
+          const uint4 v = reinterpret_cast<const uint4*>(stg + r * kMxStgWords)[qd];
+          const int grow = wrow0 + r;
+          if (grow < t.row_end)
+            *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 16 * qd) = v;
+        }
+        const int row = wrow0 + lane;
+        if (row < t.row_end)
+          *reinterpret_cast<uint16_t*>(p.out_sf + static_cast<long long>(row) * p.out_sf_ld + 2 * t.n) =
+              static_cast<uint16_t>(sc[0] | (sc[1] << 8));
+        __syncwarp();
+      } else {
+        float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < kMxBN; c += 32) {
+          float v[32];
+          tmem_ld_32x32(tb + c, v);
+          const int col = t.n * kMxBN + c;
+          float4* srow4 = reinterpret_cast<float4*>(stg + lane * kMxStgWords);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            srow4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          __syncwarp();
+          // 4 rows x 128 bytes per store instruction
+          const int qd = lane & 7;
+#pragma unroll
+          for (int rr = 0; rr < 32; rr += 4) {
+            const int r = rr + (lane >> 3);
+            const float4 x = reinterpret_cast<const float4*>(stg + r * kMxStgWords)[qd];
+            const int grow = wrow0 + r;
+            if (grow < t.row_end)
+              *reinterpret_cast<float4*>(out + static_cast<long long>(grow) * p.ldo + col + 4 * qd) = x;
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kMxTmemCols);
+  }
+}
+
+// Q_MX of bf16 rows: one warp per row, one lane per group of 32 at a time.
+// With `inv` set, row t's codes and scales go to rows inv[t * k + j] (j < k,
+// skipping dropped assignments, inv = -1) of the outputs: the rows in expert
+// order that the MX Linear1 reads, each token quantised once.
+template <int FMT>
+__global__ void __launch_bounds__(256)
+    mx_quant_rows_kernel(const uint16_t* __restrict__ x, int rows, int cols,
+                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                         const int* __restrict__ inv, int k) {
+  const int lane = threadIdx.x & 31;
+  const int groups = cols / 32;
+  const int wpb = blockDim.x >> 5;
+  for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpb) {
+    const uint16_t* xr = x + static_cast<long long>(row) * cols;
+    int dst[16];
+    int ndst = 1;
+    dst[0] = row;
+    if (inv != nullptr) {
+      ndst = 0;
+      for (int j = 0; j < k; ++j) {
+        const int r = __ldg(inv + static_cast<long long>(row) * k + j);
+        if (r >= 0) dst[ndst++] = r;
+      }
+    }
+    for (int g = lane; g < groups; g += 32) {
+      const uint4* src = reinterpret_cast<const uint4*>(xr + 32 * g);
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 b = __ldcs(src + j);
+        const uint32_t u[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * j + 2 * i] = bf16_lo(u[i]);
+          v[8 * j + 2 * i + 1] = bf16_hi(u[i]);
+        }
+      }
+      uint32_t w[8];
+      const uint32_t sc = mx_group<FMT>(v, w);
+      for (int d = 0; d < ndst; ++d) {
+        uint4* out = reinterpret_cast<uint4*>(codes + static_cast<long long>(dst[d]) * cols + 32 * g);
+        out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        scales[static_cast<long long>(dst[d]) * groups + g] = static_cast<uint8_t>(sc);
+      }
+    }
+  }
+}
+
+template <bool SWIGLU, int FMT>
+cudaError_t launch_mx(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  auto kern = gemm_mx_kernel<SWIGLU, FMT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kMxThreads, kMxSmem, s>>>(m.a, m.b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_mx(bool swiglu, int fmt, const GemmMaps& maps, const GemmParams& p,
+                           int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  if (swiglu) return fmt == 0 ? launch_mx<true, 0>(maps, p, grid, s) : launch_mx<true, 1>(maps, p, grid, s);
+  return fmt == 0 ? launch_mx<false, 0>(maps, p, grid, s) : launch_mx<false, 1>(maps, p, grid, s);
+}
+
+cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                 uint8_t* scales, const int* inv, int k, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (inv != nullptr && (k < 1 || k > 16)) return cudaErrorInvalidValue;
+  const int wpb = 8;
+  long long blocks = (rows + wpb - 1) / wpb;
+  if (blocks > 8LL * num_sms()) blocks = 8LL * num_sms();
+  if (fmt == 0)
+    mx_quant_rows_kernel<0><<<static_cast<int>(blocks), 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+  else
+    mx_quant_rows_kernel<1><<<static_cast<int>(blocks), 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
