@@ -611,7 +611,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
   // Linear1 + SwiGLU + Q_MX on the token codes in expert order
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Xq, A, H) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 64))
+    if (!make_map_mx_rows(&maps.a, Xq, A, H) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 128))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -621,7 +621,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
     g.tile_off = b.tile_off;
     g.num_groups = E;
     g.shared_group = -1;
-    g.n_tiles = I / 64;
+    g.n_tiles = (I + 127) / 128;
     g.num_kb = H / kMxBK;
     g.n_out = I;
     g.up_off = I;
@@ -642,7 +642,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
   // Linear2 on the re-quantised SwiGLU rows, fp32 out
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Uq, A, I) || !make_map_mx_weights(&maps.b, W2, E, H, I, 128))
+    if (!make_map_mx_rows(&maps.a, Uq, A, I) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -652,7 +652,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
     g.tile_off = b.tile_off;
     g.num_groups = E;
     g.shared_group = -1;
-    g.n_tiles = H / 128;
+    g.n_tiles = (H + 255) / 256;
     g.num_kb = I / kMxBK;
     g.n_out = H;
     g.out = Yp;

@@ -12,22 +12,27 @@
 //
 // Structure (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: A tile [128 rows x 128 k] and B tile
-//               [128 n x 128 k], both K-major with 128-byte swizzle (Linear1:
-//               64 gate rows of W1 and the matching 64 up rows; Linear2: 128
+//               [256 n x 128 k], both K-major with 128-byte swizzle (Linear1:
+//               128 gate rows of W1 and the matching 128 up rows; Linear2: 256
 //               rows of W2).  Linear1's A rows are the token codes already laid
 //               out in expert order by the quantisation kernel.
-//   warp 1      allocates 512 TMEM columns (two 128-column accumulators and a
-//               pair of scale slots per stage); one lane copies the stage's two
-//               scale atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues
-//               four MMAs (M 128, N 128, K 32) whose scale byte is the k step.
+//   warp 1      allocates TMEM (one 256-column accumulator and the scale slots
+//               of every stage); one lane copies the stage's scale atoms into
+//               TMEM (tcgen05.cp 32x128b.warpx4) and issues four MMAs
+//               (M 128, N 256, K 32) whose scale byte is the k step.
 //   warps 2..5  epilogue (one accumulator row per thread).
 //   warps 6..9  per k-block, the 4 scale bytes of each of the 128 A rows and
-//               128 B rows into the stage's two 512-byte atoms (cp.async).
+//               256 B rows into the stage's three 512-byte atoms (cp.async).
+// The tile is as wide as for bf16 so that each k-block moves one A byte per
+// two B bytes; two 256-column accumulators would leave no TMEM for the scales,
+// so there is one, and the stages the producer loads ahead carry the MMA over
+// the epilogue.
 // A scale atom holds 128 rows x 4 groups: row r's 4 bytes are the 32-bit word
 // at byte (r % 32) * 16 + (r / 32) * 4.  Copied with warpx4, TMEM lane l then
 // holds rows l % 32 + 32 c in column c, which is where the MMA reads the scale
 // of A row m (lane m, column m / 32) and of B row n (lane n % 32 of each lane
-// quarter, column n / 32); the byte inside the word is the MMA's scale id.
+// quarter, column n / 32; rows 128..255 from the second atom, 4 columns on);
+// the byte inside the word is the MMA's scale id.
 #include <cuda_fp8.h>
 
 #include "moe_common.cuh"
@@ -37,12 +42,13 @@
 namespace moe {
 namespace {
 
-constexpr int kMxBN = 128;
+constexpr int kMxBN = 256;
 constexpr int kMxA = kBM * kMxBK;     // 16 KB
-constexpr int kMxB = kMxBN * kMxBK;   // 16 KB
+constexpr int kMxB = kMxBN * kMxBK;   // 32 KB
 constexpr int kMxAtom = 512;          // 128 rows x 4 scale bytes
-constexpr int kMxStageBytes = kMxA + kMxB + 2 * kMxAtom;  // 33 KB, a multiple of 1024
-constexpr int kMxStages = 6;
+constexpr int kMxAtoms = 1 + kMxBN / 128;
+constexpr int kMxStageBytes = ((kMxA + kMxB + kMxAtoms * kMxAtom + 1023) / 1024) * 1024;
+constexpr int kMxStages = 4;
 constexpr int kMxRing = kMxStages * kMxStageBytes;
 constexpr int kMxBarBytes = 256;
 constexpr int kMxStgWords = 36;       // staging row pitch (32 data words + 4 pad)
@@ -50,10 +56,10 @@ constexpr int kMxStg = 4 * 32 * kMxStgWords * 4;
 constexpr int kMxSmem = kMxRing + 1024 + kMxBarBytes + kMxStg;
 constexpr int kMxThreads = 320;
 constexpr int kMxTmemCols = 512;
-constexpr int kMxSfCol = 256;         // stage s: A scales at 256 + 8 s, B scales at 260 + 8 s
-static_assert(kMxStageBytes % 1024 == 0, "stage alignment");
-static_assert(kMxSfCol + 8 * kMxStages <= kMxTmemCols, "TMEM columns");
-static_assert(8 * (2 * kMxStages + 4) + 8 <= kMxBarBytes, "barrier area");
+constexpr int kMxSfCol = kMxBN;       // stage s: A scales at kMxSfCol + 12 s, B at + 4
+constexpr int kMxSfStride = 4 * kMxAtoms;
+static_assert(kMxSfCol + kMxSfStride * kMxStages <= kMxTmemCols, "TMEM columns");
+static_assert(8 * (2 * kMxStages + 2) + 8 <= kMxBarBytes, "barrier area");
 static_assert(kMxSmem <= 232448, "shared memory");
 
 // 4-byte global -> shared copy.
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + kMxRing;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * kMxStages + 4));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * kMxStages + 2));
   uint32_t* stg_area = reinterpret_cast<uint32_t*>(bar_area + kMxBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -162,8 +168,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t tiles0 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bar_area);
   const uint32_t empty0 = full0 + 8 * kMxStages;
-  const uint32_t tfull0 = empty0 + 8 * kMxStages;
-  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t tfull = empty0 + 8 * kMxStages;  // accumulator ready for the epilogue
+  const uint32_t tempty = tfull + 8;              // accumulator drained
 
   if (threadIdx.x == 0) {
     // a stage is complete when the TMA bytes have landed (one arrival with the
@@ -172,10 +178,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(full0 + 8 * s, 1 + 128);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 128);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -206,8 +210,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           mbar_arrive_expect_tx(fb, kMxA + kMxB);
           tma_load_2d(sa, &tmA, fb, kx, t.row0);
           if (SWIGLU) {
-            tma_load_3d(sb, &tmB, fb, kx, t.n * 64, t.group);
-            tma_load_3d(sb + 64 * kMxBK, &tmB, fb, kx, p.up_off + t.n * 64, t.group);
+            tma_load_3d(sb, &tmB, fb, kx, t.n * 128, t.group);
+            tma_load_3d(sb + 128 * kMxBK, &tmB, fb, kx, p.up_off + t.n * 128, t.group);
           } else {
             tma_load_3d(sb, &tmB, fb, kx, t.n * kMxBN, t.group);
           }
@@ -217,12 +221,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ row threads
-    // Thread (gw, lane) copies the 4 scale bytes of A row and B row
-    // 32 gw + lane for each k-block.  A rows past the group's end are not
-    // copied: whatever their stale scales hold only reaches accumulator rows
-    // that are never stored.
-    const int sr = 32 * (warp - 6) + lane;  // scale row of this thread
-    const uint32_t atom_off = static_cast<uint32_t>((sr & 31) * 16 + (sr >> 5) * 4);
+    // Thread (gw, lane) copies the 4 scale bytes of A row r and of B rows r
+    // and r + 128, r = 8 gw + lane / 4 + 32 (lane % 4), for each k-block: the
+    // 32 lanes of a warp then write 32 consecutive words of an atom.  A rows
+    // past the group's end and B rows past the output's end are not copied:
+    // whatever their stale scales hold only reaches accumulator entries that
+    // are never stored.
+    const int gw = warp - 6;
+    const int sr = 8 * gw + (lane >> 2) + 32 * (lane & 3);
+    const uint32_t atom_off = static_cast<uint32_t>(128 * gw + 4 * lane);
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -231,9 +238,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int row = t.row0 + sr;
       const uint8_t* sfa_src =
           row < t.row_end ? p.sfa + static_cast<long long>(row) * p.sf_ld : nullptr;
-      const int nr = SWIGLU ? (sr < 64 ? t.n * 64 + sr : p.up_off + t.n * 64 + (sr - 64))
-                            : t.n * kMxBN + sr;
-      const uint8_t* sfb_src = p.sfb + t.group * p.sfb_ld + static_cast<long long>(nr) * p.sf_ld;
+      const uint8_t* sfb_src[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // B row sr + 128 h of the tile: Linear1 holds 128 gate rows, then the
+        // matching up rows
+        const int c = SWIGLU ? t.n * 128 + sr : t.n * kMxBN + 128 * h + sr;
+        const int nr = SWIGLU ? (h == 0 ? c : p.up_off + c) : c;
+        sfb_src[h] = c < p.n_out
+                         ? p.sfb + t.group * p.sfb_ld + static_cast<long long>(nr) * p.sf_ld
+                         : nullptr;
+      }
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         bool w = true;
@@ -241,7 +256,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         const uint32_t atoms = tiles0 + stage * kMxStageBytes + kMxA + kMxB;
         if (sfa_src != nullptr) cp_async4(atoms + atom_off, sfa_src + kb * 4);
-        cp_async4(atoms + kMxAtom + atom_off, sfb_src + kb * 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (sfb_src[h] != nullptr) cp_async4(atoms + (1 + h) * kMxAtom + atom_off, sfb_src[h] + kb * 4);
         cp_async_arrive(full0 + 8 * stage);
         if (++stage == kMxStages) { stage = 0; phase ^= 1; }
       }
@@ -255,11 +272,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, p.status, abort_flag)) break;
+        if (!mbar_wait(tempty, (local & 1) ^ 1, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * kMxBN;
+        const uint32_t d = tmem_base;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
           // the row threads' copies went through the generic proxy
@@ -268,11 +283,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sa = tiles0 + stage * kMxStageBytes;
           const uint32_t sb = sa + kMxA;
           const uint32_t atoms = sb + kMxB;
-          const uint32_t tsa = tmem_base + kMxSfCol + 8 * stage;
+          const uint32_t tsa = tmem_base + kMxSfCol + kMxSfStride * stage;
           const uint32_t tsb = tsa + 4;
           // scale atoms -> TMEM; executes before the MMAs issued after it
-          tmem_cp_atom(tsa, smem_desc_plain(atoms, 128, 128));
-          tmem_cp_atom(tsb, smem_desc_plain(atoms + kMxAtom, 128, 128));
+#pragma unroll
+          for (int a = 0; a < kMxAtoms; ++a)
+            tmem_cp_atom(tsa + 4 * a, smem_desc_plain(atoms + a * kMxAtom, 128, 128));
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk) {
             // K-major rows of 128 B; a 32-wide k step is 32 B along the row
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           mma_commit(empty0 + 8 * stage);
           if (++stage == kMxStages) { stage = 0; phase ^= 1; }
         }
-        mma_commit(tfull0 + 8 * acc);
+        mma_commit(tfull);
       }
     }
   } else {
@@ -293,49 +309,64 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const TileInfo t = decode_tile(p, tile);
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, p.status, abort_flag);
+      const bool got = mbar_wait(tfull, local & 1, p.status, abort_flag);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kMxBN;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const int wrow0 = t.row0 + q * 32;
+      const int row = wrow0 + lane;
+      if (wrow0 >= t.row_end) {
+        // all 32 rows of this warp lie past the group's end: nothing to store
+        tc_fence_before();
+        mbar_arrive(tempty);
+        continue;
+      }
       if (SWIGLU) {
-        // 64 SwiGLU columns = two scale groups, each held whole by this thread
+        // 128 SwiGLU columns = four scale groups, each held whole by this
+        // thread: codes staged as 128 bytes per row, scales as one word
         uint8_t* out = static_cast<uint8_t*>(p.out);
-        uint32_t w[16];
-        uint32_t sc[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        const int col = t.n * 128;
+        uint32_t sc = 0;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
           float g[32], u[32];
           tmem_ld_32x32(tb + 32 * h, g);
-          tmem_ld_32x32(tb + 64 + 32 * h, u);
+          tmem_ld_32x32(tb + 128 + 32 * h, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
-          uint32_t wh[8];
-          sc[h] = mx_group<FMT>(g, wh);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w[8 * h + i] = wh[i];
+          // SiLU(g) * u; the fast divide (2 ulp) returns 0 once 1 + e^-g
+          // exceeds 2^126, the limit of g / (1 + e^-g) there
+          for (int i = 0; i < 32; ++i) g[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+          uint32_t w[8];
+          sc |= mx_group<FMT>(g, w) << (8 * h);
+          uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords + 8 * h);
+          srow4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          srow4[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) srow4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        // the accumulator has been read: the next tile's MMAs may start
+        tc_fence_before();
+        mbar_arrive(tempty);
         __syncwarp();
-        // 8 rows x 64 bytes per store instruction
-        const int qd = lane & 3;
-        const int col = t.n * 64;
+        // 4 rows x 128 bytes per store instruction
+        const int qd = lane & 7;
+        if (col + 16 * qd < p.n_out) {
 #pragma unroll
-        for (int rr = 0; rr < 32; rr += 8) {
-          const int r = rr + (lane >> 2);
-          const uint4 v = reinterpret_cast<const uint4*>(stg + r * kMxStgWords)[qd];
-          const int grow = wrow0 + r;
-          if (grow < t.row_end)
-            *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 16 * qd) = v;
+          for (int rr = 0; rr < 32; rr += 4) {
+            const int r = rr + (lane >> 3);
+            const uint4 v = reinterpret_cast<const uint4*>(stg + r * kMxStgWords)[qd];
+            const int grow = wrow0 + r;
+            if (grow < t.row_end)
+              *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 16 * qd) = v;
+          }
         }
-        const int row = wrow0 + lane;
-        if (row < t.row_end)
-          *reinterpret_cast<uint16_t*>(p.out_sf + static_cast<long long>(row) * p.out_sf_ld + 2 * t.n) =
-              static_cast<uint16_t>(sc[0] | (sc[1] << 8));
+        if (row < t.row_end) {
+          // scale bytes of the groups inside the output (a last tile past I
+          // keeps only its first two)
+          uint8_t* sdst = p.out_sf + static_cast<long long>(row) * p.out_sf_ld + 4 * t.n;
+          if (col + 128 <= p.n_out)
+            *reinterpret_cast<uint32_t*>(sdst) = sc;
+          else
+            *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sc);
+        }
         __syncwarp();
       } else {
         float* out = static_cast<float*>(p.out);
@@ -343,6 +374,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         for (int c = 0; c < kMxBN; c += 32) {
           float v[32];
           tmem_ld_32x32(tb + c, v);
+          if (c + 32 == kMxBN) {
+            tc_fence_before();
+            mbar_arrive(tempty);
+          }
           const int col = t.n * kMxBN + c;
           float4* srow4 = reinterpret_cast<float4*>(stg + lane * kMxStgWords);
 #pragma unroll
@@ -351,19 +386,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           __syncwarp();
           // 4 rows x 128 bytes per store instruction
           const int qd = lane & 7;
+          if (col < p.n_out) {
 #pragma unroll
-          for (int rr = 0; rr < 32; rr += 4) {
-            const int r = rr + (lane >> 3);
-            const float4 x = reinterpret_cast<const float4*>(stg + r * kMxStgWords)[qd];
-            const int grow = wrow0 + r;
-            if (grow < t.row_end)
-              *reinterpret_cast<float4*>(out + static_cast<long long>(grow) * p.ldo + col + 4 * qd) = x;
+            for (int rr = 0; rr < 32; rr += 4) {
+              const int r = rr + (lane >> 3);
+              const float4 x = reinterpret_cast<const float4*>(stg + r * kMxStgWords)[qd];
+              const int grow = wrow0 + r;
+              if (grow < t.row_end)
+                *reinterpret_cast<float4*>(out + static_cast<long long>(grow) * p.ldo + col + 4 * qd) = x;
+            }
           }
           __syncwarp();
         }
       }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
     }
   }
 
