@@ -394,6 +394,12 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int wrow0 = t.row0 + q * 32;  // first output row of this warp
+      if (wrow0 >= t.row_end) {
+        // all 32 rows of this warp lie past the group's end: nothing to store
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+        continue;
+      }
       // int8 forms: this row's activation scale (token scale for Linear1, row
       // scale for Linear2) and the group's per-column weight scales
       float srow = 0.0f;
@@ -416,8 +422,10 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
-            const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+            // SiLU(g) * u; the fast divide (2 ulp) returns 0 once 1 + e^-g
+            // exceeds 2^126, the limit of g / (1 + e^-g) there
+            const float a0 = __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
+            const float a1 = __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
             w[i] = pack_bf16x2(a0, a1);
           }
           uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kStgWords);
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
               const bool in = col + i < p.n_out;
               const float hg = (v[i] * (in ? __ldg(scol + col + i) : 0.0f)) * srow;
               const float hu = (u[i] * (in ? __ldg(scol + p.up_off + col + i) : 0.0f)) * srow;
-              v[i] = hg / (1.0f + __expf(-hg)) * hu;
+              v[i] = __fdividef(hg, 1.0f + __expf(-hg)) * hu;
             }
           } else if (KIND == kGemmPlain_Q8) {
 #pragma unroll
