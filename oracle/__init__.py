@@ -24,6 +24,10 @@ primitive).  Sources, cited by page title and section:
 * [MM] again, section "计算过程", A8W8 scenario: per-token int8 activations,
   per-channel int8 weights, int32 products, dequantisation, per-row
   re-quantisation of the SwiGLU output.
+* [MG] section "反向的通信" and [PD] section 4.7 "反向流程": the backward (un-permute
+  backward, expert dgrad and wgrad, the k input gradients of a token summed,
+  router backward; the top-k ids are constants, the selected experts' scores
+  and mixing weights are differentiable).
 * [MM] again, section "计算过程", MXFP scenario (the four stages: MX
   quantisation of the dispatched rows, GMM1 + SwiGLU + MX quantisation, GMM2,
   weighted combine) and section "约束说明" (group size 32, FLOAT8_E8M0
@@ -42,7 +46,10 @@ by tests/test_oracle_pins.py (closed forms, brute force, the worked split
 example, reductions to a dense FFN).  The MX functions are pinned against the
 FP8 code tables and round-to-nearest-even conversion of torch's float8 types,
 a hand-worked group, closed forms of the shared exponent and of the rounding
-error, and a scalar brute-force layer.  The absolute gate and output values for
+error, and a scalar brute-force layer.  The backward is pinned by central
+finite differences of the oracle's forward (every parameter of tiny layers,
+all three score functions, with and without renormalisation) and by torch's
+float64 reverse-mode differentiation of a larger layer.  The absolute gate and output values for
 the sigmoid and sqrt-softplus rules at the workload sizes rest on these same
 formulas; the pages print no worked numbers for them.
 """
@@ -69,6 +76,14 @@ def bf16_to_f64(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float64 values (exact widening)."""
     b = np.asarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def as_f64(w) -> np.ndarray:
+    """bf16 bit patterns (uint16) decoded, any floating array as float64: the
+    oracle's functions take either, so that a test can hand them real-valued
+    parameters (finite differences)."""
+    w = np.asarray(w)
+    return bf16_to_f64(w) if w.dtype == np.uint16 else w.astype(np.float64)
 
 
 def round_to_bf16(x) -> np.ndarray:
@@ -102,7 +117,7 @@ def _silu(z):
 # ----------------------------------------------------------------------------- routing
 def router_logits(X_bits, Wg_bits) -> np.ndarray:
     """[MG] 路由张量: the gating linear maps [n, h] to [n, E] logits, l = X Wg."""
-    return bf16_to_f64(X_bits) @ bf16_to_f64(Wg_bits)
+    return as_f64(X_bits) @ as_f64(Wg_bits)
 
 
 def affinity(logits, score_fn: int) -> np.ndarray:
@@ -215,8 +230,8 @@ def swiglu_expert(X_rows64, W1e, W2e, act_round_bf16: bool = False) -> np.ndarra
     """[MM] Expert Compute: H = X_e W1[e] ([N_e, 2I]); gate = H[:, :I],
     up = H[:, I:]; A = SiLU(gate) * up; Y_e = A W2[e].  W1e/W2e are bf16 bits.
     ``act_round_bf16`` rounds A to bf16 before Linear2 (off by default)."""
-    W1 = bf16_to_f64(W1e)
-    W2 = bf16_to_f64(W2e)
+    W1 = as_f64(W1e)
+    W2 = as_f64(W2e)
     I = W2.shape[0]
     Hm = X_rows64 @ W1
     A = _silu(Hm[:, :I]) * Hm[:, I:]
@@ -246,7 +261,7 @@ def forward_tokens(tokens, X_rows_bits, E_rows, G_rows, W1, W2, Ws1=None, Ws2=No
     E_rows = np.asarray(E_rows, dtype=np.int64).reshape(R, -1)
     G_rows = np.asarray(G_rows, dtype=np.float64).reshape(R, -1)
     k = E_rows.shape[1]
-    X64 = bf16_to_f64(X_rows_bits).reshape(R, -1)
+    X64 = as_f64(X_rows_bits).reshape(R, -1)
     Hdim = X64.shape[1]
     if E is None:
         E = np.asarray(W1).shape[0]
@@ -277,6 +292,117 @@ def forward(X_bits, E_ids, G, W1, W2, Ws1=None, Ws2=None, act_round_bf16: bool =
     Y = forward_tokens(np.arange(T), X_bits, E_ids, G, W1, W2, Ws1, Ws2, act_round_bf16,
                        E=np.asarray(W1).shape[0])
     return Y, f64_to_bf16_bits(Y)
+
+
+# ----------------------------------------------------------------------------- backward
+# [MG] 反向的通信: for an upstream gradient dL/dy_t the gradient flows through
+# the selected experts' branches, the shared expert, and the router: the top-k
+# ids are constants, the selected experts' continuous scores and mixing weights
+# stay differentiable (hash layers included).  The backward runs the forward's
+# dependencies in reverse: un-permute backward (one gradient row per
+# assignment), expert dgrad and wgrad, the k expert input gradients of a token
+# added (the permute duplicated the row), then router and input.  [PD] 4.7
+# 反向流程 lists the same steps: d(w_e Y_e) = w_e dY, expert backward (dW_gate,
+# dW_up, dW_down and the input gradient), router backward (dW_gate of the
+# router).  Below, plain chain rule in float64.
+def _silu_grad(z):
+    """d/dz [z sigma(z)] = sigma(z) (1 + z (1 - sigma(z)))."""
+    s = _sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+def swiglu_expert_backward(X_rows64, W1e, W2e, dOut):
+    """Gradients of Y = (SiLU(X W1[:, :I]) * X W1[:, I:]) W2 for dL/dY = dOut
+    ([n, H]): returns (dX [n, H], dW1 [H, 2I], dW2 [I, H], Y [n, H])."""
+    W1 = as_f64(W1e)
+    W2 = as_f64(W2e)
+    I = W2.shape[0]
+    Hm = X_rows64 @ W1
+    Hg, Hu = Hm[:, :I], Hm[:, I:]
+    A = _silu(Hg) * Hu
+    dA = dOut @ W2.T
+    dH = np.concatenate([dA * Hu * _silu_grad(Hg), dA * _silu(Hg)], axis=1)
+    return dH @ W1.T, X_rows64.T @ dH, A.T @ dOut, A @ W2
+
+
+def affinity_backward(logits, da, score_fn: int) -> np.ndarray:
+    """dL/dl from dL/da for a = score(l), elementwise (sigmoid: a (1 - a);
+    sqrt-softplus: sigma(l) / (2 a)) or through the softmax Jacobian
+    (a (da - sum(a da)))."""
+    l = np.asarray(logits, dtype=np.float64)
+    a = affinity(l, score_fn)
+    if score_fn == SCORE_SIGMOID:
+        return da * a * (1.0 - a)
+    if score_fn == SCORE_SQRT_SOFTPLUS:
+        return da * _sigmoid(l) / (2.0 * a)
+    if score_fn == SCORE_SOFTMAX:
+        return a * (da - (a * da).sum(axis=-1, keepdims=True))
+    raise ValueError(f"unknown score function {score_fn}")
+
+
+def gates_backward(a, E_ids, dG, alpha: float, renorm: bool) -> np.ndarray:
+    """dL/da [T, E] from dL/dg [T, k] for the gates of ``gates``: with
+    renormalisation g_j = alpha a_j / S, S = sum_i a_i over the selected ids,
+    so dL/da_i = (alpha / S)(dG_i - sum_j dG_j a_j / S); without, alpha dG.
+    Zero where S = 0 and at the experts not selected."""
+    a = np.asarray(a, dtype=np.float64)
+    ids = np.asarray(E_ids, dtype=np.int64)
+    dG = np.asarray(dG, dtype=np.float64)
+    a_sel = np.take_along_axis(a, ids, axis=-1)
+    if renorm:
+        S = a_sel.sum(axis=-1, keepdims=True)
+        safe = np.where(S > 0, S, 1.0)
+        da_sel = np.where(S > 0, alpha / safe * (dG - (dG * a_sel).sum(axis=-1, keepdims=True) / safe), 0.0)
+    else:
+        da_sel = alpha * dG
+    da = np.zeros_like(a)
+    for j in range(ids.shape[1]):
+        np.add.at(da, (np.arange(a.shape[0]), ids[:, j]), da_sel[:, j])
+    return da
+
+
+def backward(X_bits, Wg_bits, E_ids, dY, W1, W2, Ws1, Ws2, score_fn: int, alpha: float,
+             renorm: bool, E: int | None = None) -> dict:
+    """Gradients of the layer for upstream dY [T, H] at the routing E_ids (from
+    the top-k or the hash table; held constant).  W1/W2 arrays or callables
+    e -> weights; Ws1/Ws2 may be None.  Returns float64 arrays: dX [T, H],
+    dWg [H, E], dW1 [E, H, 2I], dW2 [E, I, H], dWs1, dWs2 (or None), dG [T, k]
+    (the mixing-weight gradient <dY_t, Y_e(x_t)>) and dlogits [T, E]."""
+    X = as_f64(X_bits)
+    Wg = as_f64(Wg_bits)
+    ids = np.asarray(E_ids, dtype=np.int64)
+    T, k = ids.shape
+    dY = np.asarray(dY, dtype=np.float64)
+    if E is None:
+        E = np.asarray(W1).shape[0]
+    l = X @ Wg
+    a = affinity(l, score_fn)
+    G = gates(a, ids.astype(np.int32), alpha, renorm)
+    counts, offsets, perm, inv = dispatch(ids, E)
+    dX = np.zeros_like(X)
+    dG = np.zeros((T, k))
+    dW1 = dW2 = None
+    for e in range(E):
+        W1e, W2e = _get(W1, e), _get(W2, e)
+        if dW1 is None:
+            dW1 = np.zeros((E,) + np.shape(W1e))
+            dW2 = np.zeros((E,) + np.shape(W2e))
+        if counts[e] == 0:
+            continue
+        f = perm[offsets[e]:offsets[e + 1]]     # flat assignment ids t * k + j
+        t, j = f // k, f % k
+        # un-permute backward: the assignment's gradient row is g_{t,j} dY_t
+        dXe, dW1[e], dW2[e], Ye = swiglu_expert_backward(X[t], W1e, W2e, G[t, j][:, None] * dY[t])
+        dG[t, j] = (dY[t] * Ye).sum(axis=1)
+        np.add.at(dX, t, dXe)                    # the k dgrads of a token add up
+    dWs1 = dWs2 = None
+    if Ws1 is not None:
+        dXs, dWs1, dWs2, _ = swiglu_expert_backward(X, Ws1, Ws2, dY)
+        dX += dXs
+    dl = affinity_backward(l, gates_backward(a, ids, dG, alpha, renorm), score_fn)
+    dX += dl @ Wg.T
+    return {"dX": dX, "dWg": X.T @ dl, "dW1": dW1, "dW2": dW2, "dWs1": dWs1, "dWs2": dWs2,
+            "dG": dG, "dlogits": dl}
 
 
 # ----------------------------------------------------------------------------- A8W8-INT

@@ -543,3 +543,81 @@ def test_mx_layer_matches_scalar_bruteforce(fmt):
     want = _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt)
     scale = np.abs(want).max()
     assert np.allclose(got, want, rtol=1e-9, atol=1e-12 * scale)
+
+
+# ------------------------------------------------------------------ backward
+def _bwd_case(seed, T, H, E, k, I, shared):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((T, H))
+    Wg = rng.standard_normal((H, E)) / math.sqrt(H)
+    W1 = rng.standard_normal((E, H, 2 * I)) / math.sqrt(H)
+    W2 = rng.standard_normal((E, I, H)) / math.sqrt(I)
+    Ws1 = rng.standard_normal((H, 2 * I)) / math.sqrt(H) if shared else None
+    Ws2 = rng.standard_normal((I, H)) / math.sqrt(I) if shared else None
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    dY = rng.standard_normal((T, H))
+    return X, Wg, W1, W2, Ws1, Ws2, ids, dY
+
+
+def _layer_loss(X, Wg, W1, W2, Ws1, Ws2, ids, dY, score_fn, alpha, renorm):
+    """sum(dY * Y) through the oracle's forward functions, routing ids fixed."""
+    a = oracle.affinity(oracle.router_logits(X, Wg), score_fn)
+    G = oracle.gates(a, ids, alpha, renorm)
+    Y = oracle.forward_tokens(np.arange(X.shape[0]), X, ids, G, W1, W2, Ws1, Ws2, E=W1.shape[0])
+    return float((dY * Y).sum())
+
+
+@pytest.mark.parametrize("score_fn,renorm,shared", [(0, True, True), (1, True, False),
+                                                     (2, False, True), (2, True, False),
+                                                     (0, False, False)])
+def test_backward_matches_central_differences(score_fn, renorm, shared):
+    """Every parameter and input entry of a tiny layer: the oracle's gradient
+    against (L(p + h) - L(p - h)) / 2h of the oracle's forward."""
+    X, Wg, W1, W2, Ws1, Ws2, ids, dY = _bwd_case(4 + score_fn, T=3, H=6, E=4, k=2, I=3, shared=shared)
+    alpha = 2.5 if renorm else 1.0
+    g = oracle.backward(X, Wg, ids, dY, W1, W2, Ws1, Ws2, score_fn, alpha, renorm)
+    params = {"dX": X, "dWg": Wg, "dW1": W1, "dW2": W2}
+    if shared:
+        params.update(dWs1=Ws1, dWs2=Ws2)
+    h = 1e-6
+    for name, P in params.items():
+        fd = np.zeros_like(P)
+        for idx in np.ndindex(P.shape):
+            keep = P[idx]
+            P[idx] = keep + h
+            up = _layer_loss(X, Wg, W1, W2, Ws1, Ws2, ids, dY, score_fn, alpha, renorm)
+            P[idx] = keep - h
+            dn = _layer_loss(X, Wg, W1, W2, Ws1, Ws2, ids, dY, score_fn, alpha, renorm)
+            P[idx] = keep
+            fd[idx] = (up - dn) / (2 * h)
+        assert np.allclose(g[name], fd, rtol=1e-6, atol=1e-7), name
+
+
+def test_backward_matches_torch_autograd():
+    """A larger layer against torch's reverse-mode differentiation (float64)
+    of the same forward: sigmoid affinity, renormalised alpha-scaled gates,
+    shared expert."""
+    torch = pytest.importorskip("torch")
+    X, Wg, W1, W2, Ws1, Ws2, ids, dY = _bwd_case(9, T=17, H=32, E=6, k=3, I=16, shared=True)
+    alpha = 2.5
+    g = oracle.backward(X, Wg, ids, dY, W1, W2, Ws1, Ws2, 0, alpha, True)
+    t = {n: torch.tensor(v, dtype=torch.float64, requires_grad=True)
+         for n, v in dict(X=X, Wg=Wg, W1=W1, W2=W2, Ws1=Ws1, Ws2=Ws2).items()}
+    idt = torch.tensor(ids, dtype=torch.int64)
+    a = torch.sigmoid(t["X"] @ t["Wg"])
+    a_sel = torch.gather(a, 1, idt)
+    G = alpha * a_sel / a_sel.sum(dim=1, keepdim=True)
+    I = W2.shape[1]
+
+    def ffn(x, w1, w2):
+        h = x @ w1
+        return (torch.nn.functional.silu(h[:, :I]) * h[:, I:]) @ w2
+
+    Y = ffn(t["X"], t["Ws1"], t["Ws2"])
+    for j in range(ids.shape[1]):
+        rows = [G[r, j] * ffn(t["X"][r:r + 1], t["W1"][int(ids[r, j])], t["W2"][int(ids[r, j])])
+                for r in range(X.shape[0])]
+        Y = Y + torch.cat(rows, dim=0)
+    (torch.tensor(dY) * Y).sum().backward()
+    for n, key in dict(X="dX", Wg="dWg", W1="dW1", W2="dW2", Ws1="dWs1", Ws2="dWs2").items():
+        assert np.allclose(g[key], t[n].grad.numpy(), rtol=1e-9, atol=1e-11), key
