@@ -187,6 +187,46 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
                             const int8_t* W2q, const float* S2, uint16_t* Y, void* ws,
                             size_t ws_bytes, void* stream, void* const* stage_events);
 
+/* Bytes of workspace moe_forward_train and moe_backward need (the forward's
+ * workspace plus the tensors the backward keeps or builds). */
+size_t moe_workspace_size_train(const moe_params* p);
+
+/* moe_forward that also keeps, in the workspace, what moe_backward needs: the
+ * routing permutation, the Linear1 pre-activations (bf16), the SwiGLU output
+ * and the expert output rows.  Same arguments and results as moe_forward;
+ * the workspace must hold moe_workspace_size_train(p) bytes. */
+moe_status moe_forward_train(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                             const float* G, const uint16_t* W1, const uint16_t* W2,
+                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Backward of the layer for the upstream gradient dY [T, H] (bf16), after
+ * moe_forward_train on the same workspace, inputs and routing.  The top-k ids
+ * are constants; the selected experts' gates and affinities carry gradient to
+ * the router ("Megatron-LM 的 MoE 并行：以 DeepSeek-V4 为例", section 反向的通信;
+ * the parallelism page's section 4.7, 反向流程):
+ *   dG[t, j]  = <dY_t, Y_e(x_t)>                       (mixing-weight gradient)
+ *   expert e: dYp = g dY (rows of e), dA = dYp W2[e]^T, dHg = dA * Hu * SiLU'(Hg),
+ *             dHu = dA * SiLU(Hg), dW2[e] = A^T dYp, dW1[e] = X_e^T dH,
+ *             dX_e = dH W1[e]^T;  the shared expert likewise with g = 1;
+ *   router:   dL/da from dG through the gate rule, dL/dl through the affinity,
+ *             dWg = X^T dl, and dX gets dl Wg^T;
+ *   dX_t = sum over the token's assignments of dX_e + shared + router parts.
+ * Outputs: dX [T, H] bf16; dWg [H, E], dW1 [E, H, 2I], dW2 [E, I, H], dWs1
+ * [H, 2I], dWs2 [I, H] fp32 (overwritten, not accumulated); dG [T, k] fp32
+ * or NULL.  E_ids and G as given to the forward (top-k or hash routing).  The
+ * products run on bf16 tensor cores with fp32 accumulation; dY, the gate-
+ * scaled rows, the pre-activations and their gradient and the logit
+ * gradient are bf16.  E must be a multiple of 8.  stage_events: NULL or 5
+ * cudaEvent_t recorded at: start, after the un-permute backward, after the
+ * two input-gradient GEMMs, after the weight gradients, at the end. */
+moe_status moe_backward(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                        const int32_t* E_ids, const float* G, const uint16_t* W1,
+                        const uint16_t* W2, const uint16_t* Ws1, const uint16_t* Ws2,
+                        const uint16_t* dY, uint16_t* dX, float* dWg, float* dW1, float* dW2,
+                        float* dWs1, float* dWs2, float* dG, void* ws, size_t ws_bytes,
+                        void* stream, void* const* stage_events);
+
 /* Element formats of the MX forms ("mega_moe" page, section 约束说明:
  * dispatch_quant_out_dtype FLOAT8_E4M3FN or FLOAT8_E5M2, group size 32,
  * FLOAT8_E8M0 scales).  The values are also the tensor cores' format codes. */

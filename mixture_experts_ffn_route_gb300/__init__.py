@@ -65,6 +65,10 @@ SIGNATURES = {
     "moe_workspace_size_a8w8": (_SZ, [_PP]),
     "moe_forward_a8w8": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                         ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_workspace_size_train": (_SZ, [_PP]),
+    "moe_forward_train": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_backward": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _SZ, _P, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_quantize_mx": (ctypes.c_int, [_I32, _P, _I32, _I32, _P, _P, _P]),
     "moe_workspace_size_mx": (_SZ, [_PP]),
     "moe_forward_mx": (ctypes.c_int, [_PP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
@@ -221,6 +225,39 @@ def moe_forward_a8w8(p, X, E_ids, G, W1q, S1, W2q, S2, Y, ws, stage_events=None,
     return _check(lib().moe_forward_a8w8(ctypes.byref(p), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1q), _ptr(S1),
                                          _ptr(W2q), _ptr(S2), _ptr(Y), _ptr(ws), ws.numel(), _stream(stream),
                                          arr), "moe_forward_a8w8")
+
+
+def moe_workspace_size_train(p: MoeParams) -> int:
+    return int(lib().moe_workspace_size_train(ctypes.byref(p)))
+
+
+def alloc_workspace_train(p: MoeParams, device="cuda", stream=None):
+    """A zero-headed uint8 device tensor of moe_workspace_size_train(p) bytes."""
+    import torch
+    n = moe_workspace_size_train(p)
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_workspace_size_train")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_forward_train(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, stream=None):
+    return _check(lib().moe_forward_train(ctypes.byref(p), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1), _ptr(W2),
+                                          _ptr(Ws1), _ptr(Ws2), _ptr(Y), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "moe_forward_train")
+
+
+def moe_backward(p, X, Wg, E_ids, G, W1, W2, Ws1, Ws2, dY, dX, dWg, dW1, dW2, dWs1, dWs2, dG, ws,
+                 stage_events=None, stream=None):
+    """Layer backward after moe_forward_train on the same workspace."""
+    arr = None
+    if stage_events is not None:
+        arr = (ctypes.c_void_p * 5)(*[(ev.cuda_event if ev is not None else None) for ev in stage_events])
+    return _check(lib().moe_backward(ctypes.byref(p), _ptr(X), _ptr(Wg), _ptr(E_ids), _ptr(G), _ptr(W1),
+                                     _ptr(W2), _ptr(Ws1), _ptr(Ws2), _ptr(dY), _ptr(dX), _ptr(dWg), _ptr(dW1),
+                                     _ptr(dW2), _ptr(dWs1), _ptr(dWs2), _ptr(dG), _ptr(ws), ws.numel(),
+                                     _stream(stream), arr), "moe_backward")
 
 
 def moe_quantize_mx(fmt: int, X, Q, S, stream=None):

@@ -120,6 +120,33 @@ static WsLayoutMX layout_mx(const moe_params& p) {
   return L;
 }
 
+// Training workspace: the forward's layout, then what the backward keeps or
+// builds.  Rows R = T k (+ T with a shared expert) in the forward's order.
+struct WsLayoutTrain {
+  WsLayout f;
+  size_t h, dyp, dh, xp, dxr, dl, dg, koff, total;
+};
+
+static WsLayoutTrain layout_train(const moe_params& p) {
+  WsLayoutTrain L;
+  L.f = layout(p);
+  const size_t T = static_cast<size_t>(p.T), E = static_cast<size_t>(p.E);
+  const size_t R = T * static_cast<size_t>(p.k) + (p.has_shared ? T : 0);
+  const size_t H = static_cast<size_t>(p.H), I = static_cast<size_t>(p.I);
+  size_t o = L.f.total;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.h = take(R * 2 * I * 2);      // Linear1 pre-activations, bf16
+  L.dyp = take(R * H * 2);        // un-permuted output gradient rows, bf16
+  L.dh = take(R * 2 * I * 2);     // gradient of the pre-activations, bf16
+  L.xp = take(R * H * 2);         // token rows in expert order, bf16
+  L.dxr = take(T * H * 4);        // router part of dX, fp32
+  L.dl = take(T * E * 2);         // logit gradient, bf16
+  L.dg = take(T * static_cast<size_t>(p.k) * 4);
+  L.koff = take(2 * sizeof(int));
+  L.total = o;
+  return L;
+}
+
 static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 static moe_status check_params(const moe_params* p) {
@@ -326,10 +353,14 @@ moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* coun
   return cuda_status(e);
 }
 
-moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
-                             const float* G, const uint16_t* W1, const uint16_t* W2,
-                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
-                             size_t ws_bytes, void* stream, void* const* stage_events) {
+}  // extern "C"
+
+// The bf16 forward; with h_out set, Linear1 also keeps its pre-activations.
+static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                               const float* G, const uint16_t* W1, const uint16_t* W2,
+                               const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                               size_t ws_bytes, void* stream, void* const* stage_events,
+                               uint16_t* h_out) {
   moe_status st = check_params(p);
   if (st != MOE_OK) return st;
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
@@ -386,6 +417,7 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
     g.up_off = I;
     g.out = Act;
     g.ldo = I;
+    g.h_out = h_out;
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
@@ -421,6 +453,16 @@ moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32
   e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
+}
+
+extern "C" {
+
+moe_status moe_forward_timed(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                             const float* G, const uint16_t* W1, const uint16_t* W2,
+                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                             size_t ws_bytes, void* stream, void* const* stage_events) {
+  return forward_impl(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, ws_bytes, stream, stage_events,
+                      nullptr);
 }
 
 moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
@@ -541,6 +583,205 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
+}
+
+size_t moe_workspace_size_train(const moe_params* p) {
+  if (check_params(p) != MOE_OK) return 0;
+  return layout_train(*p).total;
+}
+
+moe_status moe_forward_train(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
+                             const float* G, const uint16_t* W1, const uint16_t* W2,
+                             const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
+                             size_t ws_bytes, void* stream) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || ws_bytes < layout_train(*p).total) return MOE_ERR_WORKSPACE;
+  return forward_impl(p, X, E_ids, G, W1, W2, Ws1, Ws2, Y, ws, ws_bytes, stream, nullptr,
+                      at<uint16_t>(ws, layout_train(*p).h));
+}
+
+moe_status moe_backward(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
+                        const int32_t* E_ids, const float* G, const uint16_t* W1,
+                        const uint16_t* W2, const uint16_t* Ws1, const uint16_t* Ws2,
+                        const uint16_t* dY, uint16_t* dX, float* dWg, float* dW1, float* dW2,
+                        float* dWs1, float* dWs2, float* dG, void* ws, size_t ws_bytes,
+                        void* stream, void* const* stage_events) {
+  moe_status st = check_params(p);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+      ws_bytes < layout_train(*p).total)
+    return MOE_ERR_WORKSPACE;
+  if (p->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (p->T == 0) return MOE_OK;
+  if (!X || !Wg || !E_ids || !G || !W1 || !W2 || !dY || !dX || !dWg || !dW1 || !dW2)
+    return MOE_ERR_INVALID_ARG;
+  if (p->has_shared && (!Ws1 || !Ws2 || !dWs1 || !dWs2)) return MOE_ERR_INVALID_ARG;
+  const void* al[] = {X, Wg, W1, W2, dY, dX, dWg, dW1, dW2};
+  for (const void* q : al)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared && (!aligned16(Ws1) || !aligned16(Ws2) || !aligned16(dWs1) || !aligned16(dWs2)))
+    return MOE_ERR_INVALID_ARG;
+
+  const WsLayoutTrain L = layout_train(*p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.f.status);
+  const DispatchBufs b = dispatch_bufs(p, ws, L.f);
+  const int T = p->T, H = p->H, E = p->E, k = p->k, I = p->I;
+  const int A = T * k;
+  const int sh = p->has_shared ? 1 : 0;
+  const int R = A + (sh ? T : 0);
+  const int groups = E + sh;
+  const int mt_bound = (A + kBM - 1) / kBM + E + (sh ? (T + kBM - 1) / kBM : 0);
+  uint16_t* Act = at<uint16_t>(ws, L.f.act);
+  float* Yp = at<float>(ws, L.f.yp);
+  float* dXp = Yp;  // Yp is read by the un-permute backward before Linear1's dgrad writes here
+  uint16_t* Hs = at<uint16_t>(ws, L.h);
+  uint16_t* dYp = at<uint16_t>(ws, L.dyp);
+  uint16_t* dH = at<uint16_t>(ws, L.dh);
+  uint16_t* Xp = at<uint16_t>(ws, L.xp);
+  float* dXr = at<float>(ws, L.dxr);
+  uint16_t* dl = at<uint16_t>(ws, L.dl);
+  float* dGw = dG != nullptr ? dG : at<float>(ws, L.dg);
+  int* koff = at<int>(ws, L.koff);
+  float* logits = at<float>(ws, L.f.logits);
+  auto mark = [&](int i) -> cudaError_t {
+    if (stage_events == nullptr || stage_events[i] == nullptr) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
+  };
+  auto grid_of = [&](long long tiles) { return tiles < num_sms() ? static_cast<int>(tiles) : num_sms(); };
+  cudaError_t e = mark(0);
+  // un-permute backward and the permuted token rows
+  if (e == cudaSuccess) e = cudaMemsetAsync(dGw, 0, static_cast<size_t>(A) * sizeof(float), s);
+  if (e == cudaSuccess)
+    e = launch_unpermute_bwd(dY, G, b.perm, b.row_off, Yp, R, k, H, E, sh, dYp, dGw, s);
+  if (e == cudaSuccess) e = launch_gather_rows(X, b.perm, b.row_off, R, k, H, E, sh, Xp, s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // dgrad of Linear2 with the SwiGLU backward: dH from dYp W2[e]^T and H
+  {
+    CUtensorMap ma, mb, mb2;
+    bool ok = make_map_bf16_2d(&ma, dYp, R, H, 64, kBM) && make_map_bf16_kmajor_b(&mb, W2, E, I, H);
+    if (ok) ok = sh ? make_map_bf16_kmajor_b(&mb2, Ws2, 1, I, H) : (mb2 = mb, true);
+    if (!ok) return MOE_ERR_CUDA;
+    BwdParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = groups;
+    g.shared_group = sh ? E : -1;
+    g.n_tiles = (I + 255) / 256;
+    g.num_kb = H / kBK;
+    g.N = I;
+    g.out = dH;
+    g.ldo = 2LL * I;
+    g.h_in = Hs;
+    g.up_off = I;
+    g.status = status;
+    if (launch_gemm_bwd(false, false, kBwdSwiGLU, false, ma, mb, mb2, g,
+                        grid_of(static_cast<long long>(mt_bound) * g.n_tiles), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  // dgrad of Linear1: dXp = dH W1[e]^T, fp32
+  {
+    CUtensorMap ma, mb, mb2;
+    bool ok = make_map_bf16_2d(&ma, dH, R, 2LL * I, 64, kBM) && make_map_bf16_kmajor_b(&mb, W1, E, H, 2LL * I);
+    if (ok) ok = sh ? make_map_bf16_kmajor_b(&mb2, Ws1, 1, H, 2LL * I) : (mb2 = mb, true);
+    if (!ok) return MOE_ERR_CUDA;
+    BwdParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.tile_off = b.tile_off;
+    g.num_groups = groups;
+    g.shared_group = sh ? E : -1;
+    g.n_tiles = (H + 255) / 256;
+    g.num_kb = 2 * I / kBK;
+    g.N = H;
+    g.out = dXp;
+    g.ldo = H;
+    g.status = status;
+    if (launch_gemm_bwd(false, false, kBwdF32, false, ma, mb, mb2, g,
+                        grid_of(static_cast<long long>(mt_bound) * g.n_tiles), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  // weight gradients: dW2[e] = Act_e^T dYp_e, dW1[e] = Xp_e^T dH_e (shared group -> dWs*)
+  for (int w = 0; w < 2; ++w) {
+    const int M = w == 0 ? I : H, N = w == 0 ? H : 2 * I;
+    CUtensorMap ma, mb;
+    const uint16_t* Aop = w == 0 ? Act : Xp;
+    const uint16_t* Bop = w == 0 ? dYp : dH;
+    if (!make_map_bf16_2d(&ma, Aop, R, M, 64, 64) || !make_map_bf16_2d(&mb, Bop, R, N, 64, 64))
+      return MOE_ERR_CUDA;
+    BwdParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = b.row_off;
+    g.num_groups = groups;
+    g.shared_group = sh ? E : -1;
+    g.m_tiles = (M + kBM - 1) / kBM;
+    g.n_tiles = (N + 255) / 256;
+    g.M = M;
+    g.N = N;
+    g.out = w == 0 ? dW2 : dW1;
+    g.out2 = w == 0 ? dWs2 : dWs1;
+    g.out_group_stride = static_cast<long long>(M) * N;
+    g.ldo = N;
+    g.status = status;
+    if (launch_gemm_bwd(true, true, kBwdF32, true, ma, mb, mb, g,
+                        grid_of(static_cast<long long>(groups) * g.m_tiles * g.n_tiles), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  // router backward: logits again, dL/dlogits, dWg = X^T dl, dXr = dl Wg^T
+  if ((st = run_router_gemm(p, X, Wg, logits, status, s)) != MOE_OK) return st;
+  if (launch_router_bwd(logits, E_ids, dGw, T, E, k, p->score_fn, p->alpha, p->renorm, dl, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  {
+    const int kroff[2] = {0, T};
+    if (cudaMemcpyAsync(koff, kroff, sizeof(kroff), cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    CUtensorMap ma, mb;
+    if (!make_map_bf16_2d(&ma, X, T, H, 64, 64) || !make_map_bf16_2d(&mb, dl, T, E, 64, 64))
+      return MOE_ERR_CUDA;
+    BwdParams g;
+    memset(&g, 0, sizeof(g));
+    g.row_off = koff;
+    g.num_groups = 1;
+    g.shared_group = -1;
+    g.m_tiles = (H + kBM - 1) / kBM;
+    g.n_tiles = (E + 255) / 256;
+    g.M = H;
+    g.N = E;
+    g.out = dWg;
+    g.ldo = E;
+    g.status = status;
+    if (launch_gemm_bwd(true, true, kBwdF32, true, ma, mb, mb, g, grid_of(g.m_tiles * g.n_tiles), s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  {
+    CUtensorMap ma, mb;
+    if (!make_map_bf16_2d(&ma, dl, T, E, 64, kBM) || !make_map_bf16_kmajor_b(&mb, Wg, 1, H, E))
+      return MOE_ERR_CUDA;
+    BwdParams g;
+    memset(&g, 0, sizeof(g));
+    g.dense_rows = T;
+    g.num_groups = 1;
+    g.shared_group = -1;
+    g.n_tiles = (H + 255) / 256;
+    g.num_kb = (E + kBK - 1) / kBK;
+    g.N = H;
+    g.out = dXr;
+    g.ldo = H;
+    g.status = status;
+    if (launch_gemm_bwd(false, false, kBwdF32, false, ma, mb, mb, g,
+                        grid_of(static_cast<long long>((T + kBM - 1) / kBM) * g.n_tiles), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  e = launch_dx_reduce(dXp, b.inv, b.row_off, dXr, T, k, H, E, sh, dX, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }

@@ -419,6 +419,19 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
           tmem_ld_32x32(tb + c, g);
           tmem_ld_32x32(tb + 128 + c, u);
           const int col = t.n * 128 + c;
+          if (p.h_out != nullptr && wrow0 + lane < t.row_end && col < p.n_out) {
+            // keep the pre-activations for the backward (bf16, gate | up)
+            uint16_t* hrow = p.h_out + static_cast<long long>(wrow0 + lane) * (2 * p.up_off);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              reinterpret_cast<uint4*>(hrow + col)[i] =
+                  make_uint4(pack_bf16x2(g[8 * i], g[8 * i + 1]), pack_bf16x2(g[8 * i + 2], g[8 * i + 3]),
+                             pack_bf16x2(g[8 * i + 4], g[8 * i + 5]), pack_bf16x2(g[8 * i + 6], g[8 * i + 7]));
+              reinterpret_cast<uint4*>(hrow + p.up_off + col)[i] =
+                  make_uint4(pack_bf16x2(u[8 * i], u[8 * i + 1]), pack_bf16x2(u[8 * i + 2], u[8 * i + 3]),
+                             pack_bf16x2(u[8 * i + 4], u[8 * i + 5]), pack_bf16x2(u[8 * i + 6], u[8 * i + 7]));
+            }
+          }
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -594,6 +607,36 @@ bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64
   cuuint32_t box[3] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, cols] bf16 row-major, box = box_cols x box_rows, 128-byte swizzle.
+bool make_map_bf16_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols,
+                      int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [groups, N, K] bf16 (K contiguous): the K-major B tiles of the backward's
+// input gradients (W2 [E, I, H] read as N = I, K = H; W1 [E, H, 2I] as N = H,
+// K = 2I; Wg [H, E] as N = H, K = E), box = 64 k x 256 n x 1.
+bool make_map_bf16_kmajor_b(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N * K) * 2};
+  cuuint32_t box[3] = {64, 256, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -62,6 +62,9 @@ struct GemmParams {
   long long sfb_ld;
   uint8_t* out_sf;
   int out_sf_ld;
+  // Linear1 (bf16): when set, the pre-activations (gate and up halves, bf16)
+  // are also written to h_out [rows, 2 up_off], kept for the backward
+  uint16_t* h_out;
 };
 
 struct GemmMaps {
@@ -97,6 +100,52 @@ bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64
 cudaError_t launch_gemm_mx(bool swiglu, int fmt, const GemmMaps& maps, const GemmParams& p,
                            int grid, cudaStream_t s);
 constexpr int kMxBK = 128;  // MX k-block: 128 FP8 codes (one 128-byte swizzle row) = 4 groups
+
+// Backward GEMMs (bf16 operands, fp32 accumulation).  Groups split the rows
+// (M) as in the forward (row_off / tile_off, shared group on map b2), or, for
+// the weight gradients, the contraction (K): group g contracts rows
+// [row_off[g], row_off[g + 1]) of both operands into its own [M, N] output.
+enum BwdEpi { kBwdF32 = 0, kBwdSwiGLU = 1 };
+struct BwdParams {
+  const int* row_off;
+  const int* tile_off;
+  int num_groups;
+  int dense_rows;    // split-M mode without groups: one group of this many rows
+  int shared_group;  // split-M: group served by map b2; split-K: group written to out2
+  int m_tiles;       // split-K: 128-row tiles of each group's output
+  int n_tiles;       // 256-column tiles of the output
+  int num_kb;        // split-M: K / 64 (rounded up)
+  int M, N;          // output rows per group (split-K) and valid output columns
+  void* out;         // fp32 [rows or M, ldo], or bf16 dH for the SwiGLU backward
+  long long ldo;
+  long long out_group_stride;  // split-K: elements between group outputs
+  void* out2;                  // split-K: output of the shared group
+  const uint16_t* h_in;        // SwiGLU backward: pre-activations [rows, 2I]
+  int up_off;                  // column of the up half in h_in and out (= I)
+  int* status;
+};
+// A_MN / B_MN: the operand's contiguous dimension is M / N (else K).
+// Maps: A K-major [rows, K] box 64 x 128; A MN-major [K rows, M] box 64 x 64;
+// B K-major [groups, N, K] box 64 x 256 x 1; B MN-major [K rows, N] box 64 x 64.
+bool make_map_bf16_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols,
+                      int box_rows);
+bool make_map_bf16_kmajor_b(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K);
+cudaError_t launch_gemm_bwd(bool a_mn, bool b_mn, int epi, bool split_k, const CUtensorMap& a,
+                            const CUtensorMap& b, const CUtensorMap& b2, const BwdParams& p,
+                            int grid, cudaStream_t s);
+
+// Elementwise steps of the backward (moe_backward.cu).  Permuted rows are the
+// routed rows [0, row_off[E]) then, with a shared expert, its T rows.
+cudaError_t launch_unpermute_bwd(const uint16_t* dY, const float* G, const int* perm,
+                                 const int* row_off, const float* Yp, int rows_max, int k, int H,
+                                 int E, int has_shared, uint16_t* dYp, float* dG, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* X, const int* perm, const int* row_off, int rows_max,
+                               int k, int H, int E, int has_shared, uint16_t* Xp, cudaStream_t s);
+cudaError_t launch_dx_reduce(const float* dXp, const int* inv, const int* row_off, const float* dXr,
+                             int T, int k, int H, int E, int has_shared, uint16_t* dX, cudaStream_t s);
+cudaError_t launch_router_bwd(const float* logits, const int32_t* E_ids, const float* dG, int T,
+                              int E, int k, int score_fn, float alpha, int renorm, uint16_t* dl,
+                              cudaStream_t s);
 
 // Launch the tcgen05 GEMM of the given kind on `grid` persistent CTAs.
 cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p, int grid,

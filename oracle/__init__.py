@@ -311,18 +311,33 @@ def _silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def swiglu_expert_backward(X_rows64, W1e, W2e, dOut):
+def swiglu_expert_backward(X_rows64, W1e, W2e, dOut, round_bf16: bool = False, mass: bool = False):
     """Gradients of Y = (SiLU(X W1[:, :I]) * X W1[:, I:]) W2 for dL/dY = dOut
-    ([n, H]): returns (dX [n, H], dW1 [H, 2I], dW2 [I, H], Y [n, H])."""
+    ([n, H]): returns (dX [n, H], dW1 [H, 2I], dW2 [I, H], Y [n, H]).
+
+    ``round_bf16`` rounds to bf16 where a path that keeps its tensors in bf16
+    would: the pre-activations H (as used by the backward), the SwiGLU output
+    A (used for Y and dW2), the incoming row gradient dOut and dH; every
+    product and sum stays float64.  ``mass`` appends, for each of the four
+    results, the sum of the magnitudes of the products of its last
+    contraction (|dH| |W1|^T, |X|^T |dH|, |A|^T |dOut|, |A| |W2|): one
+    rounding step of a bf16 operand moves a result by at most 2^-8 of it."""
+    r = round_to_bf16 if round_bf16 else (lambda v: v)
     W1 = as_f64(W1e)
     W2 = as_f64(W2e)
     I = W2.shape[0]
     Hm = X_rows64 @ W1
-    Hg, Hu = Hm[:, :I], Hm[:, I:]
-    A = _silu(Hg) * Hu
+    A = r(_silu(Hm[:, :I]) * Hm[:, I:])
+    Hk = r(Hm)
+    Hg, Hu = Hk[:, :I], Hk[:, I:]
+    dOut = r(dOut)
     dA = dOut @ W2.T
-    dH = np.concatenate([dA * Hu * _silu_grad(Hg), dA * _silu(Hg)], axis=1)
-    return dH @ W1.T, X_rows64.T @ dH, A.T @ dOut, A @ W2
+    dH = r(np.concatenate([dA * Hu * _silu_grad(Hg), dA * _silu(Hg)], axis=1))
+    out = (dH @ W1.T, X_rows64.T @ dH, A.T @ dOut, A @ W2)
+    if mass:
+        aH, aA, aO = np.abs(dH), np.abs(A), np.abs(dOut)
+        out += (aH @ np.abs(W1).T, np.abs(X_rows64).T @ aH, aA.T @ aO, aA @ np.abs(W2))
+    return out
 
 
 def affinity_backward(logits, da, score_fn: int) -> np.ndarray:
@@ -362,12 +377,19 @@ def gates_backward(a, E_ids, dG, alpha: float, renorm: bool) -> np.ndarray:
 
 
 def backward(X_bits, Wg_bits, E_ids, dY, W1, W2, Ws1, Ws2, score_fn: int, alpha: float,
-             renorm: bool, E: int | None = None) -> dict:
+             renorm: bool, E: int | None = None, round_bf16: bool = False,
+             mass: bool = False, weight_experts=None) -> dict:
     """Gradients of the layer for upstream dY [T, H] at the routing E_ids (from
     the top-k or the hash table; held constant).  W1/W2 arrays or callables
     e -> weights; Ws1/Ws2 may be None.  Returns float64 arrays: dX [T, H],
     dWg [H, E], dW1 [E, H, 2I], dW2 [E, I, H], dWs1, dWs2 (or None), dG [T, k]
-    (the mixing-weight gradient <dY_t, Y_e(x_t)>) and dlogits [T, E]."""
+    (the mixing-weight gradient <dY_t, Y_e(x_t)>) and dlogits [T, E].
+    ``round_bf16``: as in swiglu_expert_backward, and the logit gradient is
+    rounded to bf16 before its two products (dWg, the router part of dX).
+    ``mass``: also "mass_<name>" for dX, dWg, dW1, dW2, dWs1, dWs2 and dG, the
+    sums of product magnitudes of each result's last contractions.
+    ``weight_experts``: if given, dW1 and dW2 (and their masses) are dicts
+    holding only these experts (full-size checks of a few experts)."""
     X = as_f64(X_bits)
     Wg = as_f64(Wg_bits)
     ids = np.asarray(E_ids, dtype=np.int64)
@@ -382,27 +404,59 @@ def backward(X_bits, Wg_bits, E_ids, dY, W1, W2, Ws1, Ws2, score_fn: int, alpha:
     dX = np.zeros_like(X)
     dG = np.zeros((T, k))
     dW1 = dW2 = None
+    m = {"dX": np.zeros_like(X), "dG": np.zeros((T, k))} if mass else None
+    keep = None if weight_experts is None else set(int(e) for e in weight_experts)
+    if keep is not None:
+        dW1, dW2 = {}, {}
+        if mass:
+            m["dW1"], m["dW2"] = {}, {}
     for e in range(E):
+        if counts[e] == 0 and keep is None and dW1 is not None:
+            continue
         W1e, W2e = _get(W1, e), _get(W2, e)
         if dW1 is None:
             dW1 = np.zeros((E,) + np.shape(W1e))
             dW2 = np.zeros((E,) + np.shape(W2e))
+            if mass:
+                m["dW1"], m["dW2"] = np.zeros_like(dW1), np.zeros_like(dW2)
+        if keep is not None and e in keep:
+            dW1[e], dW2[e] = np.zeros(np.shape(W1e)), np.zeros(np.shape(W2e))
+            if mass:
+                m["dW1"][e], m["dW2"][e] = np.zeros_like(dW1[e]), np.zeros_like(dW2[e])
         if counts[e] == 0:
             continue
         f = perm[offsets[e]:offsets[e + 1]]     # flat assignment ids t * k + j
         t, j = f // k, f % k
         # un-permute backward: the assignment's gradient row is g_{t,j} dY_t
-        dXe, dW1[e], dW2[e], Ye = swiglu_expert_backward(X[t], W1e, W2e, G[t, j][:, None] * dY[t])
+        res = swiglu_expert_backward(X[t], W1e, W2e, G[t, j][:, None] * dY[t], round_bf16, mass)
+        dXe, Ye = res[0], res[3]
+        if keep is None or e in keep:
+            dW1[e], dW2[e] = res[1], res[2]
         dG[t, j] = (dY[t] * Ye).sum(axis=1)
         np.add.at(dX, t, dXe)                    # the k dgrads of a token add up
+        if mass:
+            np.add.at(m["dX"], t, res[4])
+            if keep is None or e in keep:
+                m["dW1"][e], m["dW2"][e] = res[5], res[6]
+            m["dG"][t, j] = (np.abs(dY[t]) * res[7]).sum(axis=1)
     dWs1 = dWs2 = None
     if Ws1 is not None:
-        dXs, dWs1, dWs2, _ = swiglu_expert_backward(X, Ws1, Ws2, dY)
+        res = swiglu_expert_backward(X, Ws1, Ws2, dY, round_bf16, mass)
+        dXs, dWs1, dWs2 = res[:3]
         dX += dXs
+        if mass:
+            m["dX"] += res[4]
+            m["dWs1"], m["dWs2"] = res[5], res[6]
     dl = affinity_backward(l, gates_backward(a, ids, dG, alpha, renorm), score_fn)
-    dX += dl @ Wg.T
-    return {"dX": dX, "dWg": X.T @ dl, "dW1": dW1, "dW2": dW2, "dWs1": dWs1, "dWs2": dWs2,
-            "dG": dG, "dlogits": dl}
+    dlr = round_to_bf16(dl) if round_bf16 else dl
+    dX += dlr @ Wg.T
+    out = {"dX": dX, "dWg": X.T @ dlr, "dW1": dW1, "dW2": dW2, "dWs1": dWs1, "dWs2": dWs2,
+           "dG": dG, "dlogits": dl}
+    if mass:
+        m["dX"] += np.abs(dlr) @ np.abs(Wg).T
+        m["dWg"] = np.abs(X).T @ np.abs(dlr)
+        out.update({"mass_" + key: v for key, v in m.items()})
+    return out
 
 
 # ----------------------------------------------------------------------------- A8W8-INT

@@ -275,6 +275,12 @@ def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
     return d
 
 
+def upstream_grad(T: int, H: int, seed: int = 1234) -> np.ndarray:
+    """The upstream gradient dL/dY [T, H] of a backward step: N(0, 1) in bf16
+    (uint16 bits)."""
+    return _normal_bf16(seed, 12, (T, H), 1.0)
+
+
 # --------------------------------------------------------------------------- torch
 def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=None,
                       weights: bool = True, **overrides) -> dict:
