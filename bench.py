@@ -394,6 +394,136 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+def run_train(args, rank, world, local_rank):
+    """One training step of the layer: route, moe_forward_train, moe_backward
+    (all gradients) on one batch; the upstream gradient is a seeded bf16
+    N(0, 1) tensor.  Reports tokens/s of the whole step."""
+    import torch
+    import mixture_experts_ffn_route_gb300 as moe
+    from mixture_experts_ffn_route_gb300 import accounting
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    moe.lib()
+    wseed, tseed = rank_seeds(rank)
+    dd = synth.make_inputs_torch(args.workload, seed=wseed, token_seed=tseed, device=dev)
+    c = dd["cfg"]
+    if c["routing"] == "given" or c.get("quant"):
+        raise SystemExit("--train needs a routed bf16 workload")
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    sh = c["shared"]
+    p = moe.params_from_config(c)
+    ws = moe.alloc_workspace_train(p, dev)
+    dY = torch.from_numpy(synth.upstream_grad(T, H, seed=tseed).view(np.int16)).to(dev).view(torch.bfloat16)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    G = torch.empty((T, k), dtype=torch.float32, device=dev)
+    Y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device=dev)  # noqa: E731
+    grads = {"dX": torch.empty((T, H), dtype=torch.bfloat16, device=dev), "dWg": f32(H, E),
+             "dW1": f32(E, H, 2 * I), "dW2": f32(E, I, H), "dG": f32(T, k),
+             "dWs1": f32(H, 2 * I) if sh else None, "dWs2": f32(I, H) if sh else None}
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record()
+
+    def step(X=None, dYs=None, evs=None):
+        X = dd["X"] if X is None else X
+        dYs = dY if dYs is None else dYs
+        if evs:
+            evs[0].record()
+        if c["routing"] == "hash":
+            moe.moe_route(p, X, dd["Wg"], None, dd["token_ids"], dd["tid2eid"], c["V"], E_ids, G, ws)
+        else:
+            moe.moe_route(p, X, dd["Wg"], dd["bias"], None, None, 0, E_ids, G, ws)
+        if evs:
+            evs[1].record()
+        moe.moe_forward_train(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws)
+        moe.moe_backward(p, X, dd["Wg"], E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], dYs,
+                         grads["dX"], grads["dWg"], grads["dW1"], grads["dW2"], grads["dWs1"],
+                         grads["dWs2"], grads["dG"], ws, stage_events=evs[2:] if evs else None)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    moe.moe_sync_status(ws)
+    counts = torch.bincount(E_ids.reshape(-1).long(), minlength=E).cpu().numpy()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        step(evs=ev[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    moe.moe_sync_status(ws)
+    ms = max_over_ranks(t0.elapsed_time(t1) / K, world, dev)
+
+    def avg(a, b):
+        return sum(e[a].elapsed_time(e[b]) for e in ev) / K
+    stages = {"route": avg(0, 1), "forward": avg(1, 2), "unpermute_bwd": avg(2, 3),
+              "dgrad": avg(3, 4), "wgrad": avg(4, 5), "router_bwd_dx": avg(5, 6)}
+
+    # end to end: X and dY from pinned host memory, Y and dX back, every step
+    Xh = dd["X"].cpu().pin_memory()
+    dYh = dY.cpu().pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    dXh = torch.empty_like(Xh).pin_memory()
+    Xd, dYd = torch.empty_like(dd["X"]), torch.empty_like(dY)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        Xd.copy_(Xh, non_blocking=True)
+        dYd.copy_(dYh, non_blocking=True)
+        step(Xd, dYd)
+        Yh.copy_(Y, non_blocking=True)
+        dXh.copy_(grads["dX"], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    if rank != 0:
+        return None
+    pk = peaks()
+    # dominant kernel: the weight gradients, bound by writing fp32 dW1 and dW2
+    rows, n_act = accounting._counts(counts, sh, T)
+    wg_bytes = (n_act * 3 * H * I * 4                 # dW1, dW2 (and the shared) fp32 written
+                + 2 * rows * (I + H) * 2 + 2 * rows * (H + 2 * I) * 2)  # bf16 operands read
+    achieved = wg_bytes / (stages["wgrad"] / 1e3) / 1e9
+    out = {
+        "metric": "MoE-layer training-step tokens/s (route + forward + backward) @1 GB300",
+        "value": round(T * world / (ms / 1e3), 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the workload's shapes, N(0,1) upstream gradient)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}, training step",
+                   "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": sh,
+                   "gradients": "dX bf16; dWg, dW1, dW2, dWs fp32",
+                   "l2": "inputs larger than L2",
+                   "parallelism": f"replicas x{world} (token batches, no collective)"},
+        "stages_ms": {k_: round(v, 4) for k_, v in stages.items()},
+        "roofline": {"kernel": "weight gradients (gemm_bwd_kernel<1,1,0,1>, split K)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": int(wg_bytes / 2),
+                     "peak_source": pk["source"] + " hbm_gbs"},
+        "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(2 * T * H * 2), "d2h_bytes_per_step": int(2 * T * H * 2)},
+        # route 5 (hash 2) + forward 6 + backward: unpermute, gather, 2 dgrad,
+        # 2 wgrad, router GEMM, router backward, dWg, dXr, dX sum = 11
+        "gpu_launches": ({"hash": 2}.get(c["routing"], 5) + 6 + 11) * K,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    return out
+
+
 def load_traffic(workload, algorithmic_bytes):
     """DRAM bytes of one Linear1 launch from the committed ncu summary: the
     traffic / algorithmic-bytes ratio captured on the c3p shapes, applied to
@@ -532,6 +662,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (route + forward + backward) instead of the forward")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -545,6 +677,8 @@ def main(argv=None):
         torch.distributed.init_process_group("nccl")
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.train:
+        out = run_train(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None:
