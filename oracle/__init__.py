@@ -31,8 +31,9 @@ primitive).  Sources, cited by page title and section:
 * [MM] again, section "计算过程", MXFP scenario (the four stages: MX
   quantisation of the dispatched rows, GMM1 + SwiGLU + MX quantisation, GMM2,
   weighted combine) and section "约束说明" (group size 32, FLOAT8_E8M0
-  scales, element types FLOAT8_E4M3FN / FLOAT8_E5M2, weight1 [E, 2I, H] with
-  scales [E, 2I, ceil(H/64), 2], weight2 [E, H, I] with scales over I).
+  scales, element types FLOAT8_E4M3FN / FLOAT8_E5M2 / FLOAT4_E2M1, the
+  A8W8-FP, A8W4-FP and A4W4-FP scenarios, weight1 [E, 2I, H] with scales
+  [E, 2I, ceil(H/64), 2], weight2 [E, H, I] with scales over I).
 
 Readings taken where the pages are silent:
 the score function is a parameter (sigmoid, sqrt-softplus, softmax); the k ids
@@ -544,16 +545,23 @@ def forward_a8w8_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E
 FP8_FORMATS = {
     "e4m3": (4, 3, 7, 448.0),      # FLOAT8_E4M3FN: no infinities, S.1111.111 is NaN
     "e5m2": (5, 2, 15, 57344.0),   # FLOAT8_E5M2: IEEE-style, exponent 11111 is Inf/NaN
+    "e2m1": (2, 1, 1, 6.0),        # FLOAT4_E2M1: 4-bit, no infinities or NaN
 }
 MX_GROUP = 32
 
 
+def _code_bits(fmt: str) -> int:
+    eb, mb, _, _ = FP8_FORMATS[fmt]
+    return 1 + eb + mb
+
+
 def fp8_decode(codes, fmt: str) -> np.ndarray:
-    """Value of each FP8 code from the format's definition (sign, biased
-    exponent, mantissa; exponent field 0 is subnormal), float64."""
+    """Value of each FP8 (or FP4) code from the format's definition (sign,
+    biased exponent, mantissa; exponent field 0 is subnormal), float64."""
     eb, mb, bias, _ = FP8_FORMATS[fmt]
-    c = np.asarray(codes, dtype=np.int64) & 0xFF
-    sign = np.where(c >> 7, -1.0, 1.0)
+    nb = _code_bits(fmt)
+    c = np.asarray(codes, dtype=np.int64) & ((1 << nb) - 1)
+    sign = np.where(c >> (nb - 1), -1.0, 1.0)
     ef = (c >> mb) & ((1 << eb) - 1)
     mf = c & ((1 << mb) - 1)
     mag = np.where(ef == 0, mf / 2.0 ** mb * 2.0 ** (1 - bias),
@@ -561,7 +569,7 @@ def fp8_decode(codes, fmt: str) -> np.ndarray:
     v = sign * mag
     if fmt == "e4m3":
         v = np.where((ef == 15) & (mf == 7), np.nan, v)
-    else:
+    elif fmt == "e5m2":
         v = np.where(ef == 31, np.where(mf == 0, sign * np.inf, np.nan), v)
     return v
 
@@ -586,13 +594,24 @@ def fp8_encode(v, fmt: str) -> np.ndarray:
     """FP8 code (uint8) of fp8_round(v): the sign bit of v, then the code of
     the rounded magnitude found in the table of finite non-negative codes."""
     r = fp8_round(v, fmt)
-    pos = np.arange(128)
+    nb = _code_bits(fmt)
+    pos = np.arange(1 << (nb - 1))
     vals = fp8_decode(pos, fmt)
     finite = np.isfinite(vals)
     pos, vals = pos[finite], vals[finite]          # ascending with the code
     mag = np.searchsorted(vals, np.abs(r))
     assert np.array_equal(vals[mag], np.abs(r)), "rounded value off the FP8 grid"
-    return (pos[mag] | np.where(np.signbit(r), 0x80, 0)).astype(np.uint8)
+    return (pos[mag] | np.where(np.signbit(r), 1 << (nb - 1), 0)).astype(np.uint8)
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    """FLOAT4_E2M1 codes stored two per byte (element 2i in the low nibble,
+    2i + 1 in the high nibble) -> one code per element along the last axis."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0x0F
+    out[..., 1::2] = b >> 4
+    return out
 
 
 def e8m0_decode(codes) -> np.ndarray:
@@ -629,22 +648,26 @@ def mx_dequantize(codes, scales, fmt: str) -> np.ndarray:
     return v * s
 
 
-def swiglu_expert_mx(xq, sx, W1q, S1, W2q, S2, fmt: str) -> np.ndarray:
+def swiglu_expert_mx(xq, sx, W1q, S1, W2q, S2, fmt: str, wfmt: str | None = None) -> np.ndarray:
     """[MM] MXFP Expert Compute for one expert.  xq/sx: the expert's token
     rows quantised [m, H] / [m, H/32]; W1q [2I, H], S1 [2I, H/32]; W2q [H, I],
-    S2 [H, I/32].  Z = DQ(xq) DQ(W1)^T; U = Z^(x) * sigma(Z^(x)) * Z^(y) with
-    Z^(x) the first I columns; (Uq, SU) = Q_MX(U); O = DQ(Uq) DQ(W2)^T."""
+    S2 [H, I/32] (one code per element).  Z = DQ(xq) DQ(W1)^T; U = Z^(x) *
+    sigma(Z^(x)) * Z^(y) with Z^(x) the first I columns; (Uq, SU) = Q_MX(U);
+    O = DQ(Uq) DQ(W2)^T.  ``fmt`` is the activations' element type, ``wfmt``
+    the weights' (default: the same; "e2m1" with "e4m3" activations is the
+    pages' A8W4-FP scenario, "e2m1" for both A4W4-FP)."""
+    wfmt = fmt if wfmt is None else wfmt
     Xd = mx_dequantize(xq, sx, fmt)
-    W1d = mx_dequantize(W1q, S1, fmt)
+    W1d = mx_dequantize(W1q, S1, wfmt)
     Z = Xd @ W1d.T
     I = np.asarray(W2q).shape[1]
     U = _silu(Z[:, :I]) * Z[:, I:]
     Uq, SU = mx_quantize(U, fmt)
-    return mx_dequantize(Uq, SU, fmt) @ mx_dequantize(W2q, S2, fmt).T
+    return mx_dequantize(Uq, SU, fmt) @ mx_dequantize(W2q, S2, wfmt).T
 
 
 def forward_mx_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: int,
-                      fmt: str) -> np.ndarray:
+                      fmt: str, wfmt: str | None = None) -> np.ndarray:
     """MXFP layer output for a set of tokens, float64 (the caller rounds to
     bf16).  The token rows are quantised once per token (a row's groups do
     not depend on which expert receives it, so quantising after the gather,
@@ -664,7 +687,7 @@ def forward_mx_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: 
             continue
         rows = perm[offsets[e]:offsets[e + 1]] // k
         Yp[offsets[e]:offsets[e + 1]] = swiglu_expert_mx(
-            xq[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e), fmt)
+            xq[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e), fmt, wfmt)
     Y = np.zeros((R, Hdim), dtype=np.float64)
     for j in range(k):
         p = inv[np.arange(R) * k + j]

@@ -96,6 +96,13 @@ CONFIGS["c3s_mx5"] = dict(CONFIGS["c3s"], H=512, I=256, shared=0, quant="mx_e5m2
 CONFIGS["c5s_mx"] = dict(CONFIGS["c5s"], I=640, quant="mx_e4m3")
 CONFIGS["c2_mx"] = dict(CONFIGS["c2"], quant="mx_e4m3")
 CONFIGS["c3_mx"] = dict(CONFIGS["c3"], shared=0, quant="mx_e4m3")
+# MXFP4 weights: A8W4-FP (E4M3 activations) and A4W4-FP (E2M1 activations)
+CONFIGS["c2s_mx4"] = dict(CONFIGS["c2s_mx"], quant="mx_e4m3_e2m1")
+CONFIGS["c3s_mx4"] = dict(CONFIGS["c3s_mx"], quant="mx_e4m3_e2m1")
+CONFIGS["c3s_mxa4"] = dict(CONFIGS["c3s_mx"], quant="mx_e2m1")
+CONFIGS["c2_mx4"] = dict(CONFIGS["c2_mx"], quant="mx_e4m3_e2m1")
+CONFIGS["c3_mx4"] = dict(CONFIGS["c3_mx"], quant="mx_e4m3_e2m1")
+CONFIGS["c3_mxa4"] = dict(CONFIGS["c3_mx"], quant="mx_e2m1")
 # V4-Pro expert shapes at a size one ncu capture can take (4.2 GB of weights,
 # ~64 rows per expert as in c3, uniform load)
 CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
@@ -201,26 +208,47 @@ def _int8_weights(seed, tid, shape, std):
 # the code of 1.0 (E4M3: 0x38, eight codes per octave; E5M2: 0x3C, four per
 # octave), clipped to the finite codes; group scale codes 2^floor(log2 std)
 # or half of it.  Layout [E, N, K] with scales [E, N, K/32] (K contiguous).
-_MX_CODES = {"mx_e4m3": (56.0, 8.0, 126), "mx_e5m2": (60.0, 4.0, 123)}
+# FLOAT4_E2M1 weights (the A8W4-FP and A4W4-FP forms): magnitude code from a
+# rounded N(4.5, 1.5) over the eight codes (values 0 .. 6, mostly 2 and 3), a
+# random sign, two codes per byte with the even element in the low nibble;
+# group scales 2^floor(log2(std / 2.5)) or half of it.
+# quant name -> (activation format, weight format, code-space centre, width, top code)
+_MX_FORMS = {"mx_e4m3": ("e4m3", "e4m3", 56.0, 8.0, 126), "mx_e5m2": ("e5m2", "e5m2", 60.0, 4.0, 123),
+             "mx_e4m3_e2m1": ("e4m3", "e2m1", 4.5, 1.5, 7), "mx_e2m1": ("e2m1", "e2m1", 4.5, 1.5, 7)}
 
 
 def mx_format(quant) -> str | None:
-    """'e4m3' / 'e5m2' for an MX workload, else None."""
-    return quant[3:] if quant in _MX_CODES else None
+    """Activation element format ('e4m3', 'e5m2', 'e2m1') of an MX workload, else None."""
+    return _MX_FORMS[quant][0] if quant in _MX_FORMS else None
 
 
-def _mx_scale_code(std) -> int:
-    return 127 + int(math.floor(math.log2(std)))
+def mx_weight_format(quant) -> str | None:
+    """Weight element format of an MX workload, else None."""
+    return _MX_FORMS[quant][1] if quant in _MX_FORMS else None
+
+
+def _mx_scale_code(std, wfmt="e4m3") -> int:
+    return 127 + int(math.floor(math.log2(std / 2.5 if wfmt == "e2m1" else std)))
+
+
+def _pack_nibbles(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
 
 
 def _mx_weights(seed, tid, shape, std, quant):
+    """Codes [.., K] (E2M1: packed [.., K/2]) and E8M0 scales [.., K/32]."""
     rng = _rng(seed, 200 + tid)
-    c0, w, top = _MX_CODES[quant]
+    _, wfmt, c0, w, top = _MX_FORMS[quant]
     mag = np.clip(np.rint(rng.standard_normal(size=shape, dtype=np.float32) * w + c0), 0, top)
-    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << 7
-    s0 = _mx_scale_code(std)
+    sbit = 3 if wfmt == "e2m1" else 7
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << sbit
+    s0 = _mx_scale_code(std, wfmt)
     scales = rng.integers(s0 - 1, s0 + 1, size=shape[:-1] + (shape[-1] // 32,), dtype=np.int32)
-    return (mag.astype(np.uint8) | sign), scales.astype(np.uint8)
+    codes = mag.astype(np.uint8) | sign
+    if wfmt == "e2m1":
+        codes = _pack_nibbles(codes)
+    return codes, scales.astype(np.uint8)
 
 
 def _distinct_rows(rng: np.random.Generator, n: int, E: int, k: int) -> np.ndarray:
@@ -339,13 +367,18 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
 
     def mx_weights(tid, shape, std):
         g = gen(200 + tid)
-        c0, w, top = _MX_CODES[cfg["quant"]]
-        codes = torch.empty(shape, dtype=torch.uint8, device=dev)
+        _, wfmt, c0, w, top = _MX_FORMS[cfg["quant"]]
+        packed = wfmt == "e2m1"
+        cshape = shape[:-1] + (shape[-1] // 2,) if packed else shape
+        codes = torch.empty(cshape, dtype=torch.uint8, device=dev)
         for i in range(shape[0]):
             mag = (torch.randn(shape[1:], generator=g, device=dev) * w + c0).round_().clamp_(0, top)
-            sign = torch.randint(0, 2, shape[1:], generator=g, device=dev, dtype=torch.int32) * 128
-            codes[i] = (mag.to(torch.int32) + sign).to(torch.uint8)
-        s0 = _mx_scale_code(std)
+            sign = torch.randint(0, 2, shape[1:], generator=g, device=dev, dtype=torch.int32) * (8 if packed else 128)
+            c = mag.to(torch.int32) + sign
+            if packed:
+                c = c[..., 0::2] | (c[..., 1::2] << 4)
+            codes[i] = c.to(torch.uint8)
+        s0 = _mx_scale_code(std, wfmt)
         scales = torch.randint(s0 - 1, s0 + 1, shape[:-1] + (shape[-1] // 32,), generator=g,
                                device=dev, dtype=torch.int32).to(torch.uint8)
         return codes, scales

@@ -445,13 +445,40 @@ def test_mx_quantize_worked_group():
     assert list(oracle.mx_dequantize(q, s, "e4m3")) == want
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+# FLOAT4_E2M1 values of the OCP Microscaling formats table, codes 0..7
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_codes_match_the_format_table():
+    v = oracle.fp8_decode(np.arange(16), "e2m1")
+    assert list(v[:8]) == E2M1_TABLE
+    assert list(-v[8:]) == E2M1_TABLE and all(np.signbit(v[8:]))
+
+
+def test_e2m1_rounding_ties_and_saturation():
+    """Halfway cases go to the even code (mantissa bit 0): 0.25 -> 0,
+    0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4; beyond 6
+    saturates; the sign of zero is kept."""
+    v = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 100.0, -5.0, -0.0, 0.3])
+    want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, 6.0, -4.0, -0.0, 0.5]
+    got = oracle.fp8_decode(oracle.fp8_encode(v, "e2m1"), "e2m1")
+    assert list(got) == want
+    assert np.signbit(got[10])
+
+
+def test_e2m1_unpacking_order():
+    """Two codes per byte, the even element in the low nibble."""
+    b = np.array([[0x21, 0xF0, 0x7A]], dtype=np.uint8)
+    assert oracle.unpack_e2m1(b).tolist() == [[1, 2, 0, 15, 10, 7]]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
 def test_mx_quantize_closed_forms(fmt):
     """The shared exponent from frexp (an independent route to floor(log2)),
     the rounding error bound of each element, exact round trips of values
     already on the MX grid, and a group of zeros."""
     eb, mb, bias, vmax = oracle.FP8_FORMATS[fmt]
-    emax = {"e4m3": 8, "e5m2": 15}[fmt]
+    emax = {"e4m3": 8, "e5m2": 15, "e2m1": 2}[fmt]
     rng = np.random.default_rng(3)
     G = 400
     x = rng.standard_normal((G, 32)) * np.exp(rng.uniform(-20, 20, (G, 1)))
@@ -476,16 +503,41 @@ def test_mx_quantize_closed_forms(fmt):
     assert list(sz[0]) == [0, 0] and not qz.any()
 
 
-def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt):
-    """Per token, per expert, scalar loops: FP8 codes decoded by torch's float8
-    type, scales 2^(code-127) by ldexp, shared exponents by frexp, element
-    rounding by torch's conversion after clamping to the finite range."""
+def _scalar_fp(fmt):
+    """(decode(code), round(value)) for scalar brute force: FP8 through torch's
+    float8 types; E2M1 through the format table, rounding by a search for the
+    nearest table value with ties to the even code."""
+    if fmt == "e2m1":
+        def dec(code):
+            v = E2M1_TABLE[code & 7]
+            return -v if code & 8 else v
+
+        def rnd(c):
+            a = abs(c)
+            best = min(range(8), key=lambda i: (abs(E2M1_TABLE[i] - a), i & 1))
+            return math.copysign(E2M1_TABLE[best], c)
+        return dec, rnd
     torch, dt = _torch_fp8(fmt)
-    vmax = oracle.FP8_FORMATS[fmt][3]
-    emax = {"e4m3": 8, "e5m2": 15}[fmt]
 
     def dec(code):
         return torch.tensor([int(code)], dtype=torch.uint8).view(dt).to(torch.float64).item()
+
+    def rnd(c):
+        code = torch.tensor([c], dtype=torch.float32).to(dt).view(torch.uint8).item()
+        return dec(code)
+    return dec, rnd
+
+
+def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt, wfmt=None):
+    """Per token, per expert, scalar loops: codes decoded by torch's float8
+    types (E2M1 by the format table), scales 2^(code-127) by ldexp, shared
+    exponents by frexp, element rounding by torch's conversion (E2M1 by a
+    table search) after clamping to the finite range."""
+    wfmt = fmt if wfmt is None else wfmt
+    dec, rnd = _scalar_fp(fmt)
+    wdec, _ = _scalar_fp(wfmt)
+    vmax = oracle.FP8_FORMATS[fmt][3]
+    emax = {"e4m3": 8, "e5m2": 15, "e2m1": 2}[fmt]
 
     def quant_row(v):
         out = []
@@ -495,8 +547,7 @@ def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt):
             X = max(-127, math.frexp(amax)[1] - 1 - emax) if amax > 0 else -127
             for t in grp:
                 c = min(max(t / 2.0 ** X, -vmax), vmax)
-                code = torch.tensor([c], dtype=torch.float32).to(dt).view(torch.uint8).item()
-                out.append(math.ldexp(dec(code), X))
+                out.append(math.ldexp(rnd(c), X))
         return out
 
     T, k = E_ids.shape
@@ -511,7 +562,7 @@ def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt):
             for n in range(2 * I):
                 acc = 0.0
                 for h in range(H):
-                    w = math.ldexp(dec(W1q[e, n, h]), int(S1[e, n, h // 32]) - 127)
+                    w = math.ldexp(wdec(W1q[e, n, h]), int(S1[e, n, h // 32]) - 127)
                     acc += xd[h] * w
                 z.append(acc)
             u = [z[i] / (1.0 + math.exp(-z[i])) * z[I + i] for i in range(I)]
@@ -519,18 +570,19 @@ def _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt):
             for hh in range(H):
                 acc = 0.0
                 for i in range(I):
-                    acc += ud[i] * math.ldexp(dec(W2q[e, hh, i]), int(S2[e, hh, i // 32]) - 127)
+                    acc += ud[i] * math.ldexp(wdec(W2q[e, hh, i]), int(S2[e, hh, i // 32]) - 127)
                 Y[t, hh] += float(G[t, j]) * acc
     return Y
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_mx_layer_matches_scalar_bruteforce(fmt):
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1"),
+                                      ("e2m1", "e2m1")])
+def test_mx_layer_matches_scalar_bruteforce(fmt, wfmt):
     rng = np.random.default_rng(21)
     T, H, I, E, k = 4, 64, 32, 3, 2
     X = oracle.round_to_bf16(rng.standard_normal((T, H)))
-    codes = np.arange(256)
-    vals = oracle.fp8_decode(codes, fmt)
+    codes = np.arange(16 if wfmt == "e2m1" else 256)
+    vals = oracle.fp8_decode(codes, wfmt)
     finite = codes[np.isfinite(vals) & (np.abs(vals) <= 4.0)]
     W1q = rng.choice(finite, (E, 2 * I, H)).astype(np.uint8)
     W2q = rng.choice(finite, (E, H, I)).astype(np.uint8)
@@ -539,8 +591,8 @@ def test_mx_layer_matches_scalar_bruteforce(fmt):
     E_ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1]])
     G = rng.uniform(0.1, 1.0, (T, k))
     got = oracle.forward_mx_tokens(np.arange(T), oracle.f64_to_bf16_bits(X), E_ids, G,
-                                   W1q, S1, W2q, S2, E, fmt)
-    want = _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt)
+                                   W1q, S1, W2q, S2, E, fmt, wfmt)
+    want = _bruteforce_mx_layer(X, E_ids, G, W1q, S1, W2q, S2, fmt, wfmt)
     scale = np.abs(want).max()
     assert np.allclose(got, want, rtol=1e-9, atol=1e-12 * scale)
 
