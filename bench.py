@@ -47,13 +47,21 @@ WORKLOAD_TEXT = {
     "c3_mx": "V4-Pro-shaped layer, MXFP8 form (E4M3 codes, E8M0 scales per 32), no shared expert",
     "c2_mx": "given-routing layer, MXFP8 form (E4M3)",
     "c3p_mx": "V4-Pro expert shapes, T=512 E=48, MXFP8 form (profiling size)",
+    "c3_mx4": "V4-Pro-shaped layer, A8W4-FP form (E4M3 activations, E2M1 weights, E8M0 scales), no shared expert",
+    "c3_mxa4": "V4-Pro-shaped layer, A4W4-FP form (E2M1 activations and weights), no shared expert",
+    "c2_mx4": "given-routing layer, A8W4-FP form",
 }
 
 
 def synth_mx_format(cfg):
-    """'e4m3' / 'e5m2' for an MX workload, else None."""
-    q = cfg.get("quant") or ""
-    return q[3:] if q.startswith("mx_") else None
+    """Activation element format of an MX workload ('e4m3', 'e5m2', 'e2m1'), else None."""
+    import synth
+    return synth.mx_format(cfg.get("quant"))
+
+
+def synth_mx_weight_format(cfg):
+    import synth
+    return synth.mx_weight_format(cfg.get("quant"))
 
 
 def peaks():
@@ -163,7 +171,8 @@ def build_step(moe, dd, p, ws, stage_events=None):
                                  dd["_ws_q"], stage_events)
         elif synth_mx_format(c):
             moe.moe_forward_mx(p, moe.MX_FORMATS[synth_mx_format(c)], X, E_ids, G, dd["W1"], dd["S1"],
-                               dd["W2"], dd["S2"], Y, dd["_ws_q"], stage_events)
+                               dd["W2"], dd["S2"], Y, dd["_ws_q"], stage_events,
+                               wfmt=moe.MX_FORMATS[synth_mx_weight_format(c)])
         elif stage_events is not None:
             moe.moe_forward_timed(p, X, E_ids, G, dd["W1"], dd["W2"], dd["Ws1"], dd["Ws2"], Y, ws,
                                   stage_events)
@@ -316,10 +325,10 @@ def run_ours(args, rank, world, local_rank):
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=1, x_bytes=2, act_bytes=4)
         g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=1, act_bytes=2)
     elif mx:
-        g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=accounting.MX8,
-                                          x_bytes=accounting.MX8, act_bytes=accounting.MX8)
-        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=accounting.MX8,
-                                          act_bytes=accounting.MX8)
+        ab = accounting.MX4 if mx == "e2m1" else accounting.MX8
+        wb = accounting.MX4 if synth_mx_weight_format(c) == "e2m1" else accounting.MX8
+        g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=wb, x_bytes=ab, act_bytes=ab)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=wb, act_bytes=ab)
     else:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
         g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T)
@@ -364,15 +373,18 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8" if quant else (mx if mx else "bf16"),
+        "dtype": "int8" if quant else (f"{mx} x {synth_mx_weight_format(c)}" if mx else "bf16"),
         "data": "synthetic (seeded; random-init weights of the workload's shapes)",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
                    "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": has_shared,
                    "routing": c["routing"], "score": c["score"],
                    "l2": "inputs larger than L2: %.1f GB of expert weights per step"
-                         % ((E + has_shared) * 3 * H * I * (1 if quant else (accounting.MX8 if mx else 2)) / 1e9),
+                         % ((E + has_shared) * 3 * H * I * (1 if quant else (
+                             (accounting.MX4 if synth_mx_weight_format(c) == "e2m1" else accounting.MX8)
+                             if mx else 2)) / 1e9),
                    "weights": ("int8 + per-channel fp32 scales (A8W8-INT)" if quant else
-                               (f"{mx} codes + E8M0 scales per 32 (MX)" if mx else "bf16")),
+                               (f"{synth_mx_weight_format(c)} codes + E8M0 scales per 32 (MX), "
+                                f"{mx} activations" if mx else "bf16")),
                    "parallelism": f"replicas x{world} (token batches, no collective)"},
         "stages_ms": {k_: round(v, 4) for k_, v in stages.items()},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1),

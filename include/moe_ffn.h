@@ -228,24 +228,28 @@ moe_status moe_backward(const moe_params* p, const uint16_t* X, const uint16_t* 
                         void* stream, void* const* stage_events);
 
 /* Element formats of the MX forms ("mega_moe" page, section 约束说明:
- * dispatch_quant_out_dtype FLOAT8_E4M3FN or FLOAT8_E5M2, group size 32,
- * FLOAT8_E8M0 scales).  The values are also the tensor cores' format codes. */
+ * dispatch_quant_out_dtype FLOAT8_E4M3FN, FLOAT8_E5M2 or FLOAT4_E2M1, group
+ * size 32, FLOAT8_E8M0 scales).  The values are also the tensor cores'
+ * format codes.  E2M1 codes are stored two per byte, the even element in the
+ * low nibble, so an E2M1 tensor [rows, cols] occupies [rows, cols / 2] bytes. */
 typedef enum moe_mx_format {
   MOE_MX_E4M3 = 0, /* 1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448   */
-  MOE_MX_E5M2 = 1  /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; max 57344 */
+  MOE_MX_E5M2 = 1, /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; max 57344 */
+  MOE_MX_E2M1 = 5  /* 1 sign, 2 exponent (bias 1), 1 mantissa bit; max 6      */
 } moe_mx_format;
 
 /* Q_MX of bf16 rows, the MX quantisation of the "mega_moe" page (section
  * 计算过程, MXFP scenario): for each group of 32 consecutive values v of a
  * row, the shared exponent e = floor(log2 max|v|) - emax (emax 8 for E4M3,
- * 15 for E5M2; clamped below at -127, and -127 for a group of zeros) is
+ * 15 for E5M2, 2 for E2M1; clamped below at -127, and -127 for a group of zeros) is
  * stored as the E8M0 code e + 127, and each element as the FP8 code of
  * v / 2^e rounded to nearest, ties to even, saturating at the largest finite
  * value.  (The pages name the operation; these details follow the OCP
  * Microscaling formats definition.)  Use it to prepare MX weights from bf16
  * ones, or to inspect the token quantisation of moe_forward_mx.
  *   X [rows, cols] bf16 (16-byte aligned), cols a multiple of 32;
- *   Q [rows, cols] codes out (16-byte aligned); S [rows, cols / 32] out.
+ *   Q [rows, cols] codes out ([rows, cols / 2] for E2M1; 16-byte aligned);
+ *   S [rows, cols / 32] out.
  * Asynchronous on `stream`; errors are host-checked only. */
 moe_status moe_quantize_mx(int32_t fmt, const uint16_t* X, int32_t rows, int32_t cols,
                            uint8_t* Q, uint8_t* S, void* stream);
@@ -253,18 +257,22 @@ moe_status moe_quantize_mx(int32_t fmt, const uint16_t* X, int32_t rows, int32_t
 /* Bytes of workspace moe_forward_mx needs for these parameters. */
 size_t moe_workspace_size_mx(const moe_params* p);
 
-/* Layer forward in the MX (A8W8-FP) form of the "mega_moe" page (section
- * 计算过程, MXFP scenario), no shared expert (has_shared must be 0), combine
- * unquantised:
+/* Layer forward in the MX forms of the "mega_moe" page (section 计算过程,
+ * MXFP scenario; section 约束说明: A8W8-FP, A8W4-FP, A4W4-FP), no shared expert
+ * (has_shared must be 0), combine unquantised.  fmt is the activations'
+ * element format, wfmt the weights': (E4M3, E4M3), (E5M2, E5M2) (A8W8-FP),
+ * (E4M3 or E5M2, E2M1) (A8W4-FP), (E2M1, E2M1) (A4W4-FP); other pairs give
+ * MOE_ERR_UNSUPPORTED:
  *   (Xq, SX) = Q_MX(X) per token row (see moe_quantize_mx);
  *   per expert e with rows R_e: Z = DQ(Xq[R_e]) DQ(W1[e])^T [n_e, 2I];
  *   U = Z[:, :I] * sigmoid(Z[:, :I]) * Z[:, I:]; (Uq, SU) = Q_MX(U);
  *   O = DQ(Uq) DQ(W2[e])^T [n_e, H];  y_t = sum_j G[t, j] O[row(t, j)] (bf16).
  * DQ multiplies each code by its group's scale 2^(code - 127).
- *   W1 [E, 2I, H] FP8 codes (H contiguous; the first I rows are the SiLU
- *      branch), S1 [E, 2I, H / 32] E8M0 codes: the pages' weight1 and
- *      weightScales1 [E, 2I, H / 64, 2] read as one group per 32 of H;
- *   W2 [E, H, I] codes, S2 [E, H, I / 32];
+ *   W1 [E, 2I, H] codes (H contiguous; E2M1 packed: [E, 2I, H / 2] bytes;
+ *      the first I rows are the SiLU branch), S1 [E, 2I, H / 32] E8M0 codes:
+ *      the pages' weight1 and weightScales1 [E, 2I, H / 64, 2] read as one
+ *      group per 32 of H;
+ *   W2 [E, H, I] codes (E2M1: [E, H, I / 2] bytes), S2 [E, H, I / 32];
  *   X [T, H] bf16, E_ids [T, k], G [T, k] fp32, Y [T, H] bf16 out.
  * H and I must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise); S1 and
  * S2 must be 4-byte aligned, the other pointers 16-byte aligned.  The
@@ -272,7 +280,7 @@ size_t moe_workspace_size_mx(const moe_params* p);
  * stage_events: NULL, or 5 caller-created cudaEvent_t recorded at: start,
  * after dispatch and token quantisation, after Linear1 (+ SwiGLU and
  * re-quantisation), after Linear2, after combine. */
-moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
+moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const uint16_t* X,
                           const int32_t* E_ids, const float* G, const uint8_t* W1,
                           const uint8_t* S1, const uint8_t* W2, const uint8_t* S2, uint16_t* Y,
                           void* ws, size_t ws_bytes, void* stream, void* const* stage_events);

@@ -25,7 +25,8 @@ SCORE_SOFTMAX = 2
 
 MOE_MX_E4M3 = 0
 MOE_MX_E5M2 = 1
-MX_FORMATS = {"e4m3": MOE_MX_E4M3, "e5m2": MOE_MX_E5M2}
+MOE_MX_E2M1 = 5
+MX_FORMATS = {"e4m3": MOE_MX_E4M3, "e5m2": MOE_MX_E5M2, "e2m1": MOE_MX_E2M1}
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -71,7 +72,7 @@ SIGNATURES = {
                                     _P, _P, _SZ, _P, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_quantize_mx": (ctypes.c_int, [_I32, _P, _I32, _I32, _P, _P, _P]),
     "moe_workspace_size_mx": (_SZ, [_PP]),
-    "moe_forward_mx": (ctypes.c_int, [_PP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+    "moe_forward_mx": (ctypes.c_int, [_PP, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                       ctypes.POINTER(ctypes.c_void_p)]),
     "moe_sync_status": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
@@ -261,7 +262,8 @@ def moe_backward(p, X, Wg, E_ids, G, W1, W2, Ws1, Ws2, dY, dX, dWg, dW1, dW2, dW
 
 
 def moe_quantize_mx(fmt: int, X, Q, S, stream=None):
-    """Q_MX of the bf16 rows of X [rows, cols] into codes Q and E8M0 scales S."""
+    """Q_MX of the bf16 rows of X [rows, cols] into codes Q (E2M1: packed,
+    [rows, cols / 2]) and E8M0 scales S."""
     rows, cols = X.shape
     return _check(lib().moe_quantize_mx(int(fmt), _ptr(X), int(rows), int(cols), _ptr(Q), _ptr(S),
                                         _stream(stream)), "moe_quantize_mx")
@@ -282,12 +284,15 @@ def alloc_workspace_mx(p: MoeParams, device="cuda", stream=None):
     return ws
 
 
-def moe_forward_mx(p, fmt: int, X, E_ids, G, W1, S1, W2, S2, Y, ws, stage_events=None, stream=None):
-    """MX (FP8 codes + E8M0 group scales) layer forward."""
+def moe_forward_mx(p, fmt: int, X, E_ids, G, W1, S1, W2, S2, Y, ws, stage_events=None, stream=None,
+                   wfmt: int | None = None):
+    """MX (FP8 / FP4 codes + E8M0 group scales) layer forward; fmt is the
+    activations' element format, wfmt the weights' (default: fmt)."""
     arr = None
     if stage_events is not None:
         arr = (ctypes.c_void_p * 5)(*[(ev.cuda_event if ev is not None else None) for ev in stage_events])
-    return _check(lib().moe_forward_mx(ctypes.byref(p), int(fmt), _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1),
+    wf = int(fmt) if wfmt is None else int(wfmt)
+    return _check(lib().moe_forward_mx(ctypes.byref(p), int(fmt), wf, _ptr(X), _ptr(E_ids), _ptr(G), _ptr(W1),
                                        _ptr(S1), _ptr(W2), _ptr(S2), _ptr(Y), _ptr(ws), ws.numel(),
                                        _stream(stream), arr), "moe_forward_mx")
 

@@ -13,6 +13,7 @@ BF16 = 2
 F32 = 4
 I32 = 4
 MX8 = 1 + 1 / 32  # an FP8 code plus its share of the E8M0 scale of its group of 32
+MX4 = 0.5 + 1 / 32  # an E2M1 code (half a byte) plus its share of the scale
 
 
 def _counts(counts, has_shared, T):

@@ -788,7 +788,7 @@ moe_status moe_backward(const moe_params* p, const uint16_t* X, const uint16_t* 
 
 moe_status moe_quantize_mx(int32_t fmt, const uint16_t* X, int32_t rows, int32_t cols,
                            uint8_t* Q, uint8_t* S, void* stream) {
-  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E5M2) return MOE_ERR_INVALID_ARG;
+  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E5M2 && fmt != MOE_MX_E2M1) return MOE_ERR_INVALID_ARG;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!X || !Q || !S || !aligned16(X) || !aligned16(Q)) return MOE_ERR_INVALID_ARG;
@@ -801,13 +801,16 @@ size_t moe_workspace_size_mx(const moe_params* p) {
   return layout_mx(*p).total;
 }
 
-moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
+moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const uint16_t* X,
                           const int32_t* E_ids, const float* G, const uint8_t* W1,
                           const uint8_t* S1, const uint8_t* W2, const uint8_t* S2, uint16_t* Y,
                           void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
   moe_status st = check_params(p);
   if (st != MOE_OK) return st;
-  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E5M2) return MOE_ERR_INVALID_ARG;
+  auto known = [](int f) { return f == MOE_MX_E4M3 || f == MOE_MX_E5M2 || f == MOE_MX_E2M1; };
+  if (!known(fmt) || !known(wfmt)) return MOE_ERR_INVALID_ARG;
+  if (!mx_pair_supported(fmt, wfmt)) return MOE_ERR_UNSUPPORTED;
+  const bool a4 = fmt == MOE_MX_E2M1, w4 = wfmt == MOE_MX_E2M1;
   if (p->has_shared) return MOE_ERR_UNSUPPORTED;
   if (p->H % kMxBK != 0 || p->I % kMxBK != 0) return MOE_ERR_UNSUPPORTED;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
@@ -852,7 +855,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
   // Linear1 + SwiGLU + Q_MX on the token codes in expert order
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Xq, A, H) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 128))
+    if (!make_map_mx_rows(&maps.a, Xq, A, H, a4) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 128, w4))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -867,7 +870,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
     g.n_out = I;
     g.up_off = I;
     g.out = Uq;
-    g.ldo = I;
+    g.ldo = a4 ? I / 2 : I;  // bytes per code row
     g.out_sf = SU;
     g.out_sf_ld = I / 32;
     g.sfa = SX;
@@ -877,13 +880,13 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm_mx(true, fmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_mx(true, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // Linear2 on the re-quantised SwiGLU rows, fp32 out
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Uq, A, I) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256))
+    if (!make_map_mx_rows(&maps.a, Uq, A, I, a4) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256, w4))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -905,7 +908,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, const uint16_t* X,
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm_mx(false, fmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_mx(false, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);

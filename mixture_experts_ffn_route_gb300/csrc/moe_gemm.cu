@@ -583,14 +583,15 @@ bool make_map_weights_i8(CUtensorMap* m, const void* base, int64_t groups, int64
 
 // [rows, cols] FP8 codes (bytes, cols contiguous), box = 128 columns x 128
 // rows, 128-byte swizzle.
-bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool fp4) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(fp4 ? cols / 2 : cols)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(kBM)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -598,15 +599,17 @@ bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t co
 // [groups, N, K] FP8 codes (K contiguous), box = 128 k x box_rows n x 1,
 // 128-byte swizzle: the K-major B tiles of the MX forms.
 bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K,
-                         int box_rows) {
+                         int box_rows, bool fp4) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(groups)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
+  const int64_t rb = fp4 ? K / 2 : K;  // bytes per weight row
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N * rb)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+  return fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -33,6 +33,7 @@
 // of A row m (lane m, column m / 32) and of B row n (lane n % 32 of each lane
 // quarter, column n / 32; rows 128..255 from the second atom, 4 columns on);
 // the byte inside the word is the MMA's scale id.
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "moe_common.cuh"
@@ -99,23 +100,28 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // Instruction descriptor of the block-scaled kind: bits 4-5 B scale id,
-// 7-9 A format, 10-12 B format (0 = E4M3, 1 = E5M2), 15/16 A/B major
+// 7-9 A format, 10-12 B format (0 = E4M3, 1 = E5M2, 5 = E2M1), 15/16 A/B major
 // (0 = K-major), 17-22 N >> 3, 23 scale type (1 = E8M0), 24-28 M >> 4,
 // 29-30 A scale id.
-__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t fmt) {
-  return (fmt << 7) | (fmt << 10) | ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) |
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t afmt, uint32_t bfmt) {
+  return (afmt << 7) | (bfmt << 10) | ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
   return (a_id << 29) | (b_id << 4);
 }
 
-// Largest power-of-two exponent of the element format: E4M3 448 = 1.75 * 2^8,
-// E5M2 57344 = 1.75 * 2^15.
+// Element formats, by their tensor-core codes: 0 = E4M3, 1 = E5M2 (one code
+// per byte), 5 = E2M1 (two codes per byte in memory, even element in the low
+// nibble; TMA's 16U4_ALIGN16B type spreads each 16 of them over 16 bytes of
+// shared memory, the layout the MMA reads).  EMAX: the largest power-of-two
+// exponent of the format (448 = 1.75 * 2^8, 57344 = 1.75 * 2^15, 6 = 1.5 * 2^2).
 template <int FMT>
-struct Fp8 {
-  static constexpr int EMAX = FMT == 0 ? 8 : 15;
-  static constexpr __nv_fp8_interpretation_t KIND = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+struct MxFmt {
+  static constexpr int EMAX = FMT == 0 ? 8 : (FMT == 1 ? 15 : 2);
+  static constexpr bool FP4 = FMT == 5;
+  static constexpr int GROUP_BYTES = FP4 ? 16 : 32;  // bytes of one group of 32 codes
+  static constexpr __nv_fp8_interpretation_t KIND = FMT == 1 ? __NV_E5M2 : __NV_E4M3;
 };
 
 // Shared exponent of a group with maximum magnitude `amax` (the OCP MX rule):
@@ -123,7 +129,7 @@ struct Fp8 {
 // field (a zero or subnormal maximum gives -127).
 template <int FMT>
 __device__ __forceinline__ int mx_exponent(float amax) {
-  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - Fp8<FMT>::EMAX;
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - MxFmt<FMT>::EMAX;
   return e < -127 ? -127 : e;
 }
 
@@ -131,27 +137,49 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 // nearest even with saturation, first value in the lowest byte.
 template <int FMT>
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, Fp8<FMT>::KIND);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, Fp8<FMT>::KIND);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, MxFmt<FMT>::KIND);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, MxFmt<FMT>::KIND);
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
-// Quantise 32 values of one group: 8 words of codes, returns the scale code.
+// Eight values -> eight E2M1 codes in one word, round to nearest even with
+// saturation, first value in the lowest nibble.
+__device__ __forceinline__ uint32_t fp4x8(const float* v) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w |= static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(v[2 * i], v[2 * i + 1]), __NV_E2M1,
+                                                        cudaRoundNearest) & 0xFFu) << (8 * i);
+  return w;
+}
+
+// Quantise 32 values of one group: GROUP_BYTES / 4 words of codes (8 for
+// FP8, 4 for E2M1), returns the scale code.
 template <int FMT>
 __device__ __forceinline__ uint32_t mx_group(const float (&v)[32], uint32_t (&w)[8]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const int X = mx_exponent<FMT>(amax);
-  // 2^-X, exact: X is in [-127, 120] so 127 - X is a normal exponent field
+  // 2^-X, exact: X is in [-127, 125] so 127 - X is a normal exponent field
   const float inv = __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
+  if (MxFmt<FMT>::FP4) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = fp8x4<FMT>(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    for (int i = 0; i < 4; ++i) {
+      float s[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[j] = v[8 * i + j] * inv;
+      w[i] = fp4x8(s);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = fp8x4<FMT>(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  }
   return static_cast<uint32_t>(X + 127);
 }
 
-template <bool SWIGLU, int FMT>
+template <bool SWIGLU, int AF, int BF>
 __global__ void __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -207,7 +235,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sa = tiles0 + stage * kMxStageBytes;
           const uint32_t sb = sa + kMxA;
           const int kx = kb * kMxBK;
-          mbar_arrive_expect_tx(fb, kMxA + kMxB);
+          // an E2M1 tile arrives as half as many bytes as it fills
+          mbar_arrive_expect_tx(fb, (MxFmt<AF>::FP4 ? kMxA / 2 : kMxA) + (MxFmt<BF>::FP4 ? kMxB / 2 : kMxB));
           tma_load_2d(sa, &tmA, fb, kx, t.row0);
           if (SWIGLU) {
             tma_load_3d(sb, &tmB, fb, kx, t.n * 128, t.group);
@@ -267,7 +296,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN, FMT);
+      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN, AF, BF);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -323,7 +352,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
       if (SWIGLU) {
         // 128 SwiGLU columns = four scale groups, each held whole by this
-        // thread: codes staged as 128 bytes per row, scales as one word
+        // thread: codes staged as 128 (FP8) or 64 (E2M1) bytes per row,
+        // scales as one word
+        constexpr int GB = MxFmt<AF>::GROUP_BYTES;
         uint8_t* out = static_cast<uint8_t*>(p.out);
         const int col = t.n * 128;
         uint32_t sc = 0;
@@ -337,25 +368,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           // exceeds 2^126, the limit of g / (1 + e^-g) there
           for (int i = 0; i < 32; ++i) g[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
           uint32_t w[8];
-          sc |= mx_group<FMT>(g, w) << (8 * h);
-          uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords + 8 * h);
+          sc |= mx_group<AF>(g, w) << (8 * h);
+          uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords + (GB / 4) * h);
           srow4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          srow4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          if (GB == 32) srow4[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
         // the accumulator has been read: the next tile's MMAs may start
         tc_fence_before();
         mbar_arrive(tempty);
         __syncwarp();
-        // 4 rows x 128 bytes per store instruction
-        const int qd = lane & 7;
-        if (col + 16 * qd < p.n_out) {
+        // one store instruction: 4 rows x 128 bytes (FP8) or 8 rows x 64 bytes
+        // (E2M1); p.ldo is the row pitch in bytes
+        constexpr int LPR = GB / 4;  // lanes per row
+        const int qd = lane % LPR;
+        const long long cbytes = static_cast<long long>(col) * GB / 32;
+        if (col < p.n_out) {
 #pragma unroll
-          for (int rr = 0; rr < 32; rr += 4) {
-            const int r = rr + (lane >> 3);
+          for (int rr = 0; rr < 32; rr += 32 / LPR) {
+            const int r = rr + lane / LPR;
             const uint4 v = reinterpret_cast<const uint4*>(stg + r * kMxStgWords)[qd];
             const int grow = wrow0 + r;
             if (grow < t.row_end)
-              *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 16 * qd) = v;
+              *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + cbytes + 16 * qd) = v;
           }
         }
         if (row < t.row_end) {
@@ -420,8 +454,10 @@ __global__ void __launch_bounds__(256)
     mx_quant_rows_kernel(const uint16_t* __restrict__ x, int rows, int cols,
                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                          const int* __restrict__ inv, int k) {
+  constexpr int GB = MxFmt<FMT>::GROUP_BYTES;
   const int lane = threadIdx.x & 31;
   const int groups = cols / 32;
+  const long long row_bytes = static_cast<long long>(groups) * GB;
   const int wpb = blockDim.x >> 5;
   for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpb) {
     const uint16_t* xr = x + static_cast<long long>(row) * cols;
@@ -451,31 +487,46 @@ __global__ void __launch_bounds__(256)
       uint32_t w[8];
       const uint32_t sc = mx_group<FMT>(v, w);
       for (int d = 0; d < ndst; ++d) {
-        uint4* out = reinterpret_cast<uint4*>(codes + static_cast<long long>(dst[d]) * cols + 32 * g);
+        uint4* out = reinterpret_cast<uint4*>(codes + static_cast<long long>(dst[d]) * row_bytes + GB * g);
         out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (GB == 32) out[1] = make_uint4(w[4], w[5], w[6], w[7]);
         scales[static_cast<long long>(dst[d]) * groups + g] = static_cast<uint8_t>(sc);
       }
     }
   }
 }
 
-template <bool SWIGLU, int FMT>
+template <bool SWIGLU, int AF, int BF>
 cudaError_t launch_mx(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  auto kern = gemm_mx_kernel<SWIGLU, FMT>;
+  auto kern = gemm_mx_kernel<SWIGLU, AF, BF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kMxThreads, kMxSmem, s>>>(m.a, m.b, p);
   return cudaGetLastError();
 }
 
+template <bool SWIGLU>
+cudaError_t launch_mx_pair(int afmt, int bfmt, const GemmMaps& m, const GemmParams& p, int grid,
+                           cudaStream_t s) {
+  if (afmt == 0 && bfmt == 0) return launch_mx<SWIGLU, 0, 0>(m, p, grid, s);
+  if (afmt == 1 && bfmt == 1) return launch_mx<SWIGLU, 1, 1>(m, p, grid, s);
+  if (afmt == 0 && bfmt == 5) return launch_mx<SWIGLU, 0, 5>(m, p, grid, s);
+  if (afmt == 1 && bfmt == 5) return launch_mx<SWIGLU, 1, 5>(m, p, grid, s);
+  if (afmt == 5 && bfmt == 5) return launch_mx<SWIGLU, 5, 5>(m, p, grid, s);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_mx(bool swiglu, int fmt, const GemmMaps& maps, const GemmParams& p,
+bool mx_pair_supported(int afmt, int bfmt) {
+  return (afmt == bfmt && (afmt == 0 || afmt == 1 || afmt == 5)) || ((afmt == 0 || afmt == 1) && bfmt == 5);
+}
+
+cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, const GemmMaps& maps, const GemmParams& p,
                            int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  if (swiglu) return fmt == 0 ? launch_mx<true, 0>(maps, p, grid, s) : launch_mx<true, 1>(maps, p, grid, s);
-  return fmt == 0 ? launch_mx<false, 0>(maps, p, grid, s) : launch_mx<false, 1>(maps, p, grid, s);
+  return swiglu ? launch_mx_pair<true>(afmt, bfmt, maps, p, grid, s)
+                : launch_mx_pair<false>(afmt, bfmt, maps, p, grid, s);
 }
 
 cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols, uint8_t* codes,
@@ -485,10 +536,15 @@ cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols,
   const int wpb = 8;
   long long blocks = (rows + wpb - 1) / wpb;
   if (blocks > 8LL * num_sms()) blocks = 8LL * num_sms();
+  const int b = static_cast<int>(blocks);
   if (fmt == 0)
-    mx_quant_rows_kernel<0><<<static_cast<int>(blocks), 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+    mx_quant_rows_kernel<0><<<b, 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+  else if (fmt == 1)
+    mx_quant_rows_kernel<1><<<b, 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+  else if (fmt == 5)
+    mx_quant_rows_kernel<5><<<b, 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
   else
-    mx_quant_rows_kernel<1><<<static_cast<int>(blocks), 32 * wpb, 0, s>>>(x, rows, cols, codes, scales, inv, k);
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

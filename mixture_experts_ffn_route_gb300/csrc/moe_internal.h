@@ -84,20 +84,26 @@ cudaError_t launch_quant_rows_bf16(const uint16_t* x, int rows, int cols, uint16
 cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_max, int cols,
                                   uint16_t* codes, float* scales, cudaStream_t s);
 
-// MX forms ("mega_moe" MXFP scenario).  fmt: 0 = FLOAT8_E4M3FN, 1 = FLOAT8_E5M2.
-// Rows quantised per group of 32 (cols a multiple of 32): codes [rows, cols],
-// scales [rows, cols / 32]; with inv (the dispatch's inverse permutation,
-// k <= 16) row t is written to rows inv[t k + j] instead of row t.
+// MX forms ("mega_moe" MXFP scenario).  Formats by tensor-core code:
+// 0 = FLOAT8_E4M3FN, 1 = FLOAT8_E5M2, 5 = FLOAT4_E2M1 (two codes per byte).
+// Rows quantised per group of 32 (cols a multiple of 32): codes [rows, cols]
+// bytes (E2M1: [rows, cols / 2]), scales [rows, cols / 32]; with inv (the
+// dispatch's inverse permutation, k <= 16) row t is written to rows
+// inv[t k + j] instead of row t.
 cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols, uint8_t* codes,
                                  uint8_t* scales, const int* inv, int k, cudaStream_t s);
-// [rows, cols] FP8 codes, box 128 columns x box_rows rows, 128-byte swizzle;
-// the weights [groups, N, K] as a 3-D map with box 128 k x box_rows n x 1.
-bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
+// [rows, cols] codes, box 128 columns x 128 rows, 128-byte swizzle; the
+// weights [groups, N, K] as a 3-D map with box 128 k x box_rows n x 1.  With
+// fp4 the codes are packed E2M1 and the map type spreads them to the MMA's
+// shared-memory layout (16 codes per 16 bytes).
+bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool fp4);
 bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K,
-                         int box_rows);
-// Linear1 (SwiGLU, re-quantised FP8 out) or Linear2 (fp32 out); A rows in
-// expert order (map a), their scales at sfa.  K must be a multiple of 128.
-cudaError_t launch_gemm_mx(bool swiglu, int fmt, const GemmMaps& maps, const GemmParams& p,
+                         int box_rows, bool fp4);
+// Linear1 (SwiGLU, re-quantised to the activation format) or Linear2 (fp32
+// out); A rows in expert order (map a), their scales at sfa.  K must be a
+// multiple of 128.  afmt / bfmt: activation / weight formats.
+bool mx_pair_supported(int afmt, int bfmt);
+cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, const GemmMaps& maps, const GemmParams& p,
                            int grid, cudaStream_t s);
 constexpr int kMxBK = 128;  // MX k-block: 128 FP8 codes (one 128-byte swizzle row) = 4 groups
 

@@ -106,19 +106,23 @@ def test_argument_errors_return_before_any_launch(lib):
     assert fwd_q(_p(), ws_bytes=1024) == moe.MOE_ERR_WORKSPACE
     assert fwd_q(_p(T=0)) == moe.MOE_OK
 
-    def fwd_mx(p, fmt=0, ws_bytes=None, s1=16):
+    def fwd_mx(p, fmt=0, ws_bytes=None, s1=16, wfmt=None):
         n = moe.moe_workspace_size_mx(p) if ws_bytes is None else ws_bytes
-        return lib.moe_forward_mx(ctypes.byref(p), fmt, 16, 16, 16, 16, s1, 16, 16, 16, fake_ws, n,
-                                  None, None)
+        return lib.moe_forward_mx(ctypes.byref(p), fmt, fmt if wfmt is None else wfmt, 16, 16, 16, 16, s1,
+                                  16, 16, 16, fake_ws, n, None, None)
     assert fwd_mx(_p(has_shared=1)) == moe.MOE_ERR_UNSUPPORTED  # the MX form has no shared expert
     assert fwd_mx(_p(H=192)) == moe.MOE_ERR_UNSUPPORTED        # H, I multiples of 128
     assert fwd_mx(_p(I=320)) == moe.MOE_ERR_UNSUPPORTED
     assert fwd_mx(_p(), fmt=2) == moe.MOE_ERR_INVALID_ARG
+    assert fwd_mx(_p(), fmt=5, wfmt=0) == moe.MOE_ERR_UNSUPPORTED   # E2M1 activations need E2M1 weights
+    assert fwd_mx(_p(T=0), fmt=0, wfmt=5) == moe.MOE_OK
+    assert fwd_mx(_p(T=0), fmt=5) == moe.MOE_OK
     assert fwd_mx(_p(), ws_bytes=1024) == moe.MOE_ERR_WORKSPACE
     assert fwd_mx(_p(), s1=18) == moe.MOE_ERR_INVALID_ARG      # scales 4-byte aligned
     assert fwd_mx(_p(T=0)) == moe.MOE_OK
     assert lib.moe_quantize_mx(0, 16, 4, 48, 16, 16, None) == moe.MOE_ERR_INVALID_ARG  # cols % 32
     assert lib.moe_quantize_mx(3, 16, 4, 64, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_mx(5, 16, 0, 64, 16, 16, None) == moe.MOE_OK
     assert lib.moe_quantize_mx(0, 16, 0, 64, 16, 16, None) == moe.MOE_OK
 
 

@@ -1,6 +1,7 @@
-"""Parity of the MX forms (FP8 codes with E8M0 group scales, the MXFP
-scenario of the "mega_moe" page) with the oracle's restatement: the token
-quantisation bit-exact, the layer output within the Y tolerance."""
+"""Parity of the MX forms (FP8 / FP4 codes with E8M0 group scales, the MXFP
+scenario of the "mega_moe" page: A8W8-FP, A8W4-FP, A4W4-FP) with the oracle's
+restatement: the token quantisation bit-exact, the layer output within the Y
+tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -23,10 +24,20 @@ def _fmt(cfg):
     return synth.mx_format(cfg["quant"])
 
 
-def _run(p, fmt, dd, E_ids, G):
+def _wfmt(cfg):
+    return synth.mx_weight_format(cfg["quant"])
+
+
+def _codes(w, wfmt):
+    """Weight codes as the oracle takes them: one code per element."""
+    return oracle.unpack_e2m1(w) if wfmt == "e2m1" else w
+
+
+def _run(p, fmt, dd, E_ids, G, wfmt=None):
     ws = moe.alloc_workspace_mx(p, DEV)
     Y = torch.full((p.T, p.H), float("nan"), dtype=torch.bfloat16, device=DEV)
-    moe.moe_forward_mx(p, moe.MX_FORMATS[fmt], dd["X"], E_ids, G, dd["W1"], dd["S1"], dd["W2"], dd["S2"], Y, ws)
+    moe.moe_forward_mx(p, moe.MX_FORMATS[fmt], dd["X"], E_ids, G, dd["W1"], dd["S1"], dd["W2"], dd["S2"], Y, ws,
+                       wfmt=moe.MX_FORMATS[wfmt or fmt])
     moe.moe_sync_status(ws)
     return Y
 
@@ -41,31 +52,32 @@ def _quant_rows(fmt):
     x[1, 3] = 0.0
     x[2, 5] = rng.standard_normal(32) * 1e-9
     x[2, 5, 0] = 300.0
-    grid = oracle.fp8_decode(np.arange(128), fmt)
+    grid = oracle.fp8_decode(np.arange(8 if fmt == "e2m1" else 128), fmt)
     grid = grid[np.isfinite(grid)]
     mids = (grid[:-1] + grid[1:]) / 2
-    emax = {"e4m3": 8, "e5m2": 15}[fmt]
+    emax = {"e4m3": 8, "e5m2": 15, "e2m1": 2}[fmt]
     top = mids[(mids >= 1.0) & (mids < 2.0 ** emax)]
     g = rng.choice(top, 31)
     x[3, 0] = np.concatenate([[2.0 ** emax], g * rng.choice([-1, 1], 31)])   # shared exponent 0
     return oracle.f64_to_bf16_bits(x.reshape(R, C))
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
 def test_mx_token_quantisation_is_bit_exact(fmt):
     xb = _quant_rows(fmt)
     R, C = xb.shape
     X = bf(xb)
-    Q = torch.full((R, C), 0xAB, dtype=torch.uint8, device=DEV)
+    Cb = C // 2 if fmt == "e2m1" else C
+    Q = torch.full((R, Cb), 0xAB, dtype=torch.uint8, device=DEV)
     S = torch.full((R, C // 32), 0xAB, dtype=torch.uint8, device=DEV)
     moe.moe_quantize_mx(moe.MX_FORMATS[fmt], X, Q, S)
     torch.cuda.synchronize()
     q_ref, s_ref = oracle.mx_quantize(oracle.bf16_to_f64(xb).astype(np.float32), fmt, np.float32)
     assert np.array_equal(S.cpu().numpy(), s_ref)
-    assert np.array_equal(Q.cpu().numpy(), q_ref)
+    assert np.array_equal(_codes(Q.cpu().numpy(), fmt), q_ref)
 
 
-@pytest.mark.parametrize("name", ["c2s_mx", "c3s_mx", "c3s_mx5", "c5s_mx"])
+@pytest.mark.parametrize("name", ["c2s_mx", "c3s_mx", "c3s_mx5", "c5s_mx", "c2s_mx4", "c3s_mx4", "c3s_mxa4"])
 def test_mx_forward_matches_oracle(name):
     h = synth.make_inputs(name)
     c = h["cfg"]
@@ -81,9 +93,10 @@ def test_mx_forward_matches_oracle(name):
         ids, _, _ = oracle.route(h["X"], h["Wg"], h["bias"], c["score_fn"], c["k"], c["alpha"], c["renorm"])
         assert np.array_equal(E_ids.cpu().numpy(), ids)
         G = Gd.cpu().numpy().astype(np.float64)
-    Y = _run(p, _fmt(c), dd, E_ids, Gd)
-    Y_ref = oracle.forward_mx_tokens(np.arange(c["T"]), h["X"], ids, G, h["W1"], h["S1"], h["W2"], h["S2"],
-                                     E=c["E"], fmt=_fmt(c))
+    Y = _run(p, _fmt(c), dd, E_ids, Gd, _wfmt(c))
+    wf = _wfmt(c)
+    Y_ref = oracle.forward_mx_tokens(np.arange(c["T"]), h["X"], ids, G, _codes(h["W1"], wf), h["S1"],
+                                     _codes(h["W2"], wf), h["S2"], E=c["E"], fmt=_fmt(c), wfmt=wf)
     check_y(Y, Y_ref, name)
 
 
@@ -102,7 +115,7 @@ def test_mx_is_deterministic_and_rejects_a_shared_expert():
     assert ex.value.code == moe.MOE_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("name,n_rows", [("c3_mx", 6), ("c2_mx", 6)])
+@pytest.mark.parametrize("name,n_rows", [("c3_mx", 6), ("c2_mx", 6), ("c3_mx4", 4), ("c3_mxa4", 4)])
 def test_mx_full_size_sampled(name, n_rows):
     dd = synth.make_inputs_torch(name, device=DEV)
     c = dd["cfg"]
@@ -114,15 +127,17 @@ def test_mx_full_size_sampled(name, n_rows):
         ws_r = moe.alloc_workspace(p, DEV)
         E_ids, G = run_route(p, dd, ws_r)
         moe.moe_sync_status(ws_r)
-    Y = _run(p, _fmt(c), dd, E_ids, G)
+    wf = _wfmt(c)
+    Y = _run(p, _fmt(c), dd, E_ids, G, wf)
     rng = np.random.default_rng(7)
     rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, n_rows, replace=False)]))
     hX = host_bits(dd["X"])
     ids = E_ids.cpu().numpy()
     Gh = G.cpu().numpy().astype(np.float64)
-    W1 = lambda e: dd["W1"][e].cpu().numpy()  # noqa: E731
-    W2 = lambda e: dd["W2"][e].cpu().numpy()  # noqa: E731
+    W1 = lambda e: _codes(dd["W1"][e].cpu().numpy(), wf)  # noqa: E731
+    W2 = lambda e: _codes(dd["W2"][e].cpu().numpy(), wf)  # noqa: E731
     S1 = lambda e: dd["S1"][e].cpu().numpy()  # noqa: E731
     S2 = lambda e: dd["S2"][e].cpu().numpy()  # noqa: E731
-    Y_ref = oracle.forward_mx_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E, fmt=_fmt(c))
+    Y_ref = oracle.forward_mx_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E, fmt=_fmt(c),
+                                     wfmt=wf)
     check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
