@@ -359,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "algorithmic_flops_per_launch": int(g1_flops),
                 "peak_source": pk["source"] + " bf16_tflops_sustained" + (" x 2 (fp8)" if mx else "")}
-    if roof["bound"] == "hbm" and not quant and not mx:
+    if roof["bound"] == "hbm" and not quant:
         roof["traffic"] = load_traffic(args.workload, g1_bytes)
     if quant:
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_tc_kernel<3>)"
@@ -537,18 +537,37 @@ def run_train(args, rank, world, local_rank):
 
 
 def load_traffic(workload, algorithmic_bytes):
-    """DRAM bytes of one Linear1 launch from the committed ncu summary: the
-    traffic / algorithmic-bytes ratio captured on the c3p shapes, applied to
-    this launch (the c3 and c4 layers share those expert shapes)."""
-    if workload not in ("c3", "c4", "c3p"):
-        return None
-    path = os.path.join(ROOT, "profiles", "gemm1_swiglu_c3p.md")
-    if not os.path.exists(path):
-        return None
+    """DRAM bytes of one Linear1 launch from the committed ncu summaries: for
+    c3, the full-size capture itself (the mean of two launches); for c4 (the
+    same expert shapes and load recipe) that capture scaled by the ratio of
+    algorithmic bytes; for c3p its own small-size capture."""
     import re
-    with open(path) as f:
-        m = re.search(r"dram_bytes_per_launch_c3_scaled_ratio:\s*([0-9.]+)", f.read())
-    return int(float(m.group(1)) * algorithmic_bytes) if m else None
+    if workload in ("c3", "c4"):
+        path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
+        key, c3_alg = r"dram_bytes_per_launch_c3_gemm1:\s*([0-9]+)", 23135780864
+        if not os.path.exists(path):
+            return None
+        with open(path) as f:
+            m = re.search(key, f.read())
+        if not m:
+            return None
+        t = int(m.group(1))
+        return t if workload == "c3" else int(t * algorithmic_bytes / c3_alg)
+    if workload == "c3_mx":
+        path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
+        if not os.path.exists(path):
+            return None
+        with open(path) as f:
+            m = re.search(r"dram_bytes_per_launch_c3mx_gemm1:\s*([0-9]+)", f.read())
+        return int(m.group(1)) if m else None
+    if workload == "c3p":
+        path = os.path.join(ROOT, "profiles", "gemm1_swiglu_c3p.md")
+        if not os.path.exists(path):
+            return None
+        with open(path) as f:
+            m = re.search(r"dram_bytes_per_launch_c3_scaled_ratio:\s*([0-9.]+)", f.read())
+        return int(float(m.group(1)) * algorithmic_bytes) if m else None
+    return None
 
 
 # ------------------------------------------------------------------ oracle (CPU)
