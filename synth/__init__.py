@@ -100,6 +100,7 @@ CONFIGS["c3_mx"] = dict(CONFIGS["c3"], shared=0, quant="mx_e4m3")
 CONFIGS["c2s_mx4"] = dict(CONFIGS["c2s_mx"], quant="mx_e4m3_e2m1")
 CONFIGS["c3s_mx4"] = dict(CONFIGS["c3s_mx"], quant="mx_e4m3_e2m1")
 CONFIGS["c3s_mxa4"] = dict(CONFIGS["c3s_mx"], quant="mx_e2m1")
+CONFIGS["c3s_mx54"] = dict(CONFIGS["c3s_mx"], quant="mx_e5m2_e2m1")
 CONFIGS["c2_mx4"] = dict(CONFIGS["c2_mx"], quant="mx_e4m3_e2m1")
 CONFIGS["c3_mx4"] = dict(CONFIGS["c3_mx"], quant="mx_e4m3_e2m1")
 CONFIGS["c3_mxa4"] = dict(CONFIGS["c3_mx"], quant="mx_e2m1")
@@ -214,7 +215,8 @@ def _int8_weights(seed, tid, shape, std):
 # group scales 2^floor(log2(std / 2.5)) or half of it.
 # quant name -> (activation format, weight format, code-space centre, width, top code)
 _MX_FORMS = {"mx_e4m3": ("e4m3", "e4m3", 56.0, 8.0, 126), "mx_e5m2": ("e5m2", "e5m2", 60.0, 4.0, 123),
-             "mx_e4m3_e2m1": ("e4m3", "e2m1", 4.5, 1.5, 7), "mx_e2m1": ("e2m1", "e2m1", 4.5, 1.5, 7)}
+             "mx_e4m3_e2m1": ("e4m3", "e2m1", 4.5, 1.5, 7), "mx_e5m2_e2m1": ("e5m2", "e2m1", 4.5, 1.5, 7),
+             "mx_e2m1": ("e2m1", "e2m1", 4.5, 1.5, 7)}
 
 
 def mx_format(quant) -> str | None:

@@ -77,7 +77,8 @@ def test_mx_token_quantisation_is_bit_exact(fmt):
     assert np.array_equal(_codes(Q.cpu().numpy(), fmt), q_ref)
 
 
-@pytest.mark.parametrize("name", ["c2s_mx", "c3s_mx", "c3s_mx5", "c5s_mx", "c2s_mx4", "c3s_mx4", "c3s_mxa4"])
+@pytest.mark.parametrize("name", ["c2s_mx", "c3s_mx", "c3s_mx5", "c5s_mx", "c2s_mx4", "c3s_mx4", "c3s_mxa4",
+                                  "c3s_mx54"])
 def test_mx_forward_matches_oracle(name):
     h = synth.make_inputs(name)
     c = h["cfg"]
