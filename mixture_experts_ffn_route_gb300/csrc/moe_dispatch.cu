@@ -12,8 +12,12 @@
 //   count   : per chunk of kChunk assignments, per-expert counts (smem atomics)
 //   scan    : per-expert exclusive prefix over chunks, then over experts
 //             (row offsets) and over 128-row tiles (tile offsets for the GEMMs)
-//   place   : one warp per (expert, chunk): ballot-prefix ranks give each
-//             assignment its row; writes perm[row] = f and inv[f] = row
+//   place   : one block per chunk: each warp ranks its 128 ids among equal
+//             ids (match_any), per-warp counts are prefix-summed per expert,
+//             and each assignment gets row = row_off[e] + (rows of e in
+//             earlier chunks, warps, and earlier in its warp); writes
+//             perm[row] = f and inv[f] = row.  (Experts beyond 1024: one warp
+//             per (expert, chunk) with ballot-prefix ranks.)
 // The permuted token rows themselves are never written: Linear1 copies them
 // from X by perm while it loads its A tiles.
 //   combine : "mega_moe" page, section Token Combine: y_t = sum_j G[t, j] *
@@ -158,6 +162,63 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+constexpr int kPlaceMaxE = 1024;  // per-warp expert counts in shared memory: 32 * E ints
+
+// One block per chunk of kChunk assignments; warp w takes ids [128 w, 128 w +
+// 128) in four rounds of 32.  In a round, the lanes holding the same expert
+// find each other (match_any): a lane's rank is the number of equal ids in
+// lower lanes plus the warp's running count of that expert, which the lowest
+// of them then advances.  The per-warp counts become an exclusive prefix over
+// the warps, so rows follow ascending flat index inside each expert.
+__global__ void __launch_bounds__(kThreads)
+    dispatch_place_match_kernel(const int32_t* __restrict__ E_ids, int A, int E,
+                                const int* __restrict__ chunk_base, const int* __restrict__ row_off,
+                                int* __restrict__ perm, int* __restrict__ inv) {
+  extern __shared__ int sm[];
+  int* ids = sm;                // [kChunk]
+  int* rank = sm + kChunk;      // [kChunk] rank among equal ids of the same warp
+  int* cnt = sm + 2 * kChunk;   // [32][E]  per-warp counts, then their prefix over warps
+  const int c = blockIdx.x;
+  const int f0 = c * kChunk;
+  const int n = min(A - f0, kChunk);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ids[i] = E_ids[f0 + i];
+  __syncthreads();
+  int* wcnt = cnt + warp * E;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = 128 * warp + 32 * r + lane;
+    int e = i < n ? ids[i] : -1;
+    if (e >= E) e = -1;  // ids outside [0, E) are not placed (the count flagged them)
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int below = __popc(peers & ((1u << lane) - 1u));
+    const int base = e >= 0 ? wcnt[e] : 0;
+    __syncwarp();
+    if (e >= 0 && below == 0) wcnt[e] = base + __popc(peers);
+    __syncwarp();
+    if (i < n) rank[i] = base + below;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  const int* cb = chunk_base + static_cast<long long>(c) * E;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) continue;
+    const int row = __ldg(row_off + e) + __ldg(cb + e) + cnt[(i >> 7) * E + e] + rank[i];
+    perm[row] = f0 + i;
+    inv[f0 + i] = row;
+  }
+}
+
 cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,
                             const DispatchBufs& b, int* status, cudaStream_t s) {
   const int A = T * k;
@@ -173,7 +234,14 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
   }
   dispatch_scan_kernel<<<1, kThreads, 0, s>>>(b.chunk_cnt, b.nchunk, E, T, has_shared, b.counts,
                                               b.row_off, b.tile_off);
-  if (A > 0) {
+  if (A > 0 && E <= kPlaceMaxE) {
+    const int sh = (2 * kChunk + 32 * E) * static_cast<int>(sizeof(int));
+    cudaError_t e = cudaFuncSetAttribute(dispatch_place_match_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, sh);
+    if (e != cudaSuccess) return e;
+    dispatch_place_match_kernel<<<b.nchunk, kThreads, sh, s>>>(E_ids, A, E, b.chunk_cnt, b.row_off,
+                                                               b.perm, b.inv);
+  } else if (A > 0) {
     dispatch_place_kernel<<<dim3((E + 31) / 32, b.nchunk), kThreads, 0, s>>>(E_ids, A, E, b.nchunk,
                                                                  b.chunk_cnt, b.counts, b.row_off,
                                                                  b.perm, b.inv);
