@@ -485,15 +485,18 @@ def quantize_rows_int8(x, dtype=np.float64):
 
 
 def swiglu_expert_a8w8(q_rows, sx_rows, W1q, S1, W2q, S2) -> np.ndarray:
-    """[MM] A8W8 Expert Compute for one expert: C = Q W1q (int32, exact);
-    H = (C * s^W1) * s^X; A = SiLU(H[:, :I]) * H[:, I:]; s^A, A8 =
-    quantize(A) per row; D = A8 W2q (int32, exact); Y = (D * s^W2) * s^A."""
-    C = np.asarray(q_rows, np.int64) @ np.asarray(W1q, np.int64)
+    """[MM] A8W8 Expert Compute for one expert.  The weights are stored as the
+    operator's weight1 [2I, H] and weight2 [H, I] (one row per output channel,
+    the contraction contiguous), with one scale per output channel.
+    C = Q W1q^T (int32, exact); H = (C * s^W1) * s^X; A = SiLU(H[:, :I]) *
+    H[:, I:]; s^A, A8 = quantize(A) per row; D = A8 W2q^T (int32, exact);
+    Y = (D * s^W2) * s^A."""
+    C = np.asarray(q_rows, np.int64) @ np.asarray(W1q, np.int64).T
     Hm = (C.astype(np.float64) * np.asarray(S1, np.float64)[None, :]) * np.asarray(sx_rows, np.float64)[:, None]
-    I = np.asarray(W2q).shape[0]
+    I = np.asarray(W2q).shape[1]
     A = _silu(Hm[:, :I]) * Hm[:, I:]
     A8, sA = quantize_rows_int8(A, np.float64)
-    D = A8.astype(np.int64) @ np.asarray(W2q, np.int64)
+    D = A8.astype(np.int64) @ np.asarray(W2q, np.int64).T
     return (D.astype(np.float64) * np.asarray(S2, np.float64)[None, :]) * sA[:, None]
 
 

@@ -193,14 +193,16 @@ def _normal_bf16(seed, tid, shape, std) -> np.ndarray:
 
 # int8 weights: codes drawn as round(N(0, 40^2)) clipped to [-127, 127] and a
 # per-output-channel scale near std / 40 (times U(0.75, 1.25)), so that
-# code * scale has the spread of the bf16 weights of the same layer.
+# code * scale has the spread of the bf16 weights of the same layer.  Layout
+# [E, N, K]: one row per output channel, the contraction contiguous (the
+# operator's weight1 [E, 2I, H] and weight2 [E, H, I]); scales [E, N].
 _CODE_STD = 40.0
 
 
 def _int8_weights(seed, tid, shape, std):
     rng = _rng(seed, 100 + tid)
     codes = np.clip(np.rint(rng.standard_normal(size=shape, dtype=np.float32) * _CODE_STD), -127, 127)
-    scales = (std / _CODE_STD) * rng.uniform(0.75, 1.25, size=(shape[0], shape[2]))
+    scales = (std / _CODE_STD) * rng.uniform(0.75, 1.25, size=(shape[0], shape[1]))
     return codes.astype(np.int8), scales.astype(np.float32)
 
 
@@ -279,8 +281,8 @@ def make_inputs(name_or_cfg, seed: int = 1234, **overrides) -> dict:
     d["bias"] = (_rng(seed, 3).standard_normal(size=E, dtype=np.float32) * np.float32(0.1)
                  if cfg["bias"] else None)
     if cfg.get("quant") == "a8w8":
-        d["W1"], d["S1"] = _int8_weights(seed, 4, (E, H, 2 * I), 1.0 / math.sqrt(H))
-        d["W2"], d["S2"] = _int8_weights(seed, 5, (E, I, H), 1.0 / math.sqrt(I))
+        d["W1"], d["S1"] = _int8_weights(seed, 4, (E, 2 * I, H), 1.0 / math.sqrt(H))
+        d["W2"], d["S2"] = _int8_weights(seed, 5, (E, H, I), 1.0 / math.sqrt(I))
     elif mx_format(cfg.get("quant")):
         d["W1"], d["S1"] = _mx_weights(seed, 4, (E, 2 * I, H), 1.0 / math.sqrt(H), cfg["quant"])
         d["W2"], d["S2"] = _mx_weights(seed, 5, (E, H, I), 1.0 / math.sqrt(I), cfg["quant"])
@@ -364,7 +366,7 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
         codes = torch.empty(shape, dtype=torch.int8, device=dev)
         for i in range(shape[0]):
             codes[i] = (torch.randn(shape[1:], generator=g, device=dev) * _CODE_STD).round_().clamp_(-127, 127).to(torch.int8)
-        u = torch.rand((shape[0], shape[2]), generator=g, device=dev) * 0.5 + 0.75
+        u = torch.rand((shape[0], shape[1]), generator=g, device=dev) * 0.5 + 0.75
         return codes, (u * (std / _CODE_STD)).float().contiguous()
 
     def mx_weights(tid, shape, std):
@@ -386,8 +388,8 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
         return codes, scales
 
     if weights and cfg.get("quant") == "a8w8":
-        d["W1"], d["S1"] = int8_weights(4, (E, H, 2 * I), 1.0 / math.sqrt(H))
-        d["W2"], d["S2"] = int8_weights(5, (E, I, H), 1.0 / math.sqrt(I))
+        d["W1"], d["S1"] = int8_weights(4, (E, 2 * I, H), 1.0 / math.sqrt(H))
+        d["W2"], d["S2"] = int8_weights(5, (E, H, I), 1.0 / math.sqrt(I))
     elif weights and mx_format(cfg.get("quant")):
         d["W1"], d["S1"] = mx_weights(4, (E, 2 * I, H), 1.0 / math.sqrt(H))
         d["W2"], d["S2"] = mx_weights(5, (E, H, I), 1.0 / math.sqrt(I))

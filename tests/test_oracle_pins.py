@@ -339,18 +339,18 @@ def test_a8w8_expert_matches_integer_brute_force():
     N, H, I = 3, 8, 4
     q = rng.integers(-127, 128, size=(N, H))
     sx = rng.uniform(0.01, 0.1, size=N)
-    W1q = rng.integers(-127, 128, size=(H, 2 * I))
+    W1q = rng.integers(-127, 128, size=(2 * I, H))   # weight1: one row per output channel
     S1 = rng.uniform(0.001, 0.01, size=2 * I)
-    W2q = rng.integers(-127, 128, size=(I, H))
+    W2q = rng.integers(-127, 128, size=(H, I))       # weight2
     S2 = rng.uniform(0.001, 0.01, size=H)
     Y = oracle.swiglu_expert_a8w8(q, sx, W1q, S1, W2q, S2)
     for n in range(N):
-        C = [sum(int(q[n, h]) * int(W1q[h, c]) for h in range(H)) for c in range(2 * I)]
+        C = [sum(int(q[n, h]) * int(W1q[c, h]) for h in range(H)) for c in range(2 * I)]
         Hv = [C[c] * S1[c] * sx[n] for c in range(2 * I)]
         A = [Hv[c] / (1 + math.exp(-Hv[c])) * Hv[I + c] for c in range(I)]
         sA = max(abs(a) for a in A) / 127
         A8 = [int(math.copysign(math.floor(abs(a / sA) + 0.5), a)) for a in A]
-        D = [sum(A8[i] * int(W2q[i, o]) for i in range(I)) for o in range(H)]
+        D = [sum(A8[i] * int(W2q[o, i]) for i in range(I)) for o in range(H)]
         np.testing.assert_allclose(Y[n], [D[o] * S2[o] * sA for o in range(H)], rtol=1e-12)
 
 
@@ -372,8 +372,8 @@ def test_a8w8_layer_within_the_activation_quantisation_bound():
         bound = np.zeros(c["H"])
         for j in range(k):
             e = ids[t, j]
-            W1 = d["W1"][e].astype(np.float64) * d["S1"][e][None, :].astype(np.float64)
-            W2 = d["W2"][e].astype(np.float64) * d["S2"][e][None, :].astype(np.float64)
+            W1 = d["W1"][e].T.astype(np.float64) * d["S1"][e][None, :].astype(np.float64)
+            W2 = d["W2"][e].T.astype(np.float64) * d["S2"][e][None, :].astype(np.float64)
             h = Xd[t] @ W1
             a = h[:I] / (1 + np.exp(-h[:I])) * h[I:]
             want += G[t, j] * (a @ W2)
