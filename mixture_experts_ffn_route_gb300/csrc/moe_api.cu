@@ -521,14 +521,11 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
   if (e == cudaSuccess) e = launch_quant_rows_bf16(X, T, H, Xq, sX, s);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // Linear1: C = Q_e W1q[e] (token codes gathered by the permutation),
-  // dequantised, SwiGLU, fp32 out
+  // Linear1: C = Q_e W1q[e]^T (token codes gathered by the permutation),
+  // dequantised, SwiGLU, fp32 out; the weights are the MMA's A operand in TMEM
   {
-    GemmMaps maps;
-    if (!make_map_rows(&maps.a, Xq, T, H) || !make_map_weights_i8(&maps.b, W1q, E, H, 2 * I))
-      return MOE_ERR_CUDA;
-    maps.a2 = maps.a;
-    maps.b2 = maps.b;
+    CUtensorMap mw;
+    if (!make_map_i8_rows(&mw, W1q, E, 2LL * I, H)) return MOE_ERR_CUDA;
     GemmParams g;
     memset(&g, 0, sizeof(g));
     g.row_off = b.row_off;
@@ -551,17 +548,14 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm(kGemmSwiGLU_Q8, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_q8(true, mw, mw, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // per-row re-quantisation of the SwiGLU output, then Linear2
   if (launch_quant_rows_f32(Act, b.row_off + E, A, I, Aq, sA, s) != cudaSuccess) return MOE_ERR_CUDA;
   {
-    GemmMaps maps;
-    if (!make_map_rows(&maps.a, Aq, A, I) || !make_map_weights_i8(&maps.b, W2q, E, I, H))
-      return MOE_ERR_CUDA;
-    maps.a2 = maps.a;
-    maps.b2 = maps.b;
+    CUtensorMap mw, mb;
+    if (!make_map_rows(&mb, Aq, A, I) || !make_map_i8_rows(&mw, W2q, E, H, I)) return MOE_ERR_CUDA;
     GemmParams g;
     memset(&g, 0, sizeof(g));
     g.row_off = b.row_off;
@@ -579,7 +573,7 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm(kGemmPlain_Q8, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_q8(false, mw, mb, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);

@@ -1,0 +1,362 @@
+// Persistent grouped GEMM of the A8W8-INT form with the weights as the tensor
+// cores' A operand in TMEM: the output channels are the MMA's M, the tokens
+// its N ("mega_moe" page, section 计算过程, A8W8 scenario).
+//
+//   Linear1: D[c][m] = sum_k W1q[e][c][k] q[m][k] for the gate channels c and
+//            the matching up channels I + c; epilogue Act[m][c] = SiLU(Hg) * Hu
+//            with H = (D * s1[c]) * sx[m] (fp32 out, re-quantised per row later)
+//   Linear2: D[h][m] = sum_k W2q[e][h][k] a8[m][k]; Yp[m][h] = (D * s2[h]) * sa[m]
+//
+// GB300's tensor cores have no int8 form for sm_103a, so the int8 codes are
+// multiplied as fp16: |code| <= 127 is exact in fp16, a product is exact in
+// fp32, and the fp32 accumulator holds the int32 sum exactly while every
+// partial sum stays below 2^24 in magnitude.  Converting a weight tile to fp16
+// in shared memory doubles its bytes and the MMA then reads it back, so shared
+// memory rather than HBM set the pace of a kernel doing that.  Here each weight
+// row (the operator's layout: one row per output channel, K contiguous) is
+// converted by one thread straight into its TMEM lane with tcgen05.st, which
+// the MMA reads as A (row m in lane m, element k in column k / 2).
+//
+// Structure (one CTA per SM, 576 threads):
+//   warp 0       TMA: int8 weight rows, two blocks of 128 rows x 64 k per stage
+//                (Linear1: gate rows and the matching up rows; Linear2: 256
+//                output channels), and for Linear2 the token-code tile
+//                [128 rows x 64 k] (fp16, K-major, 128-byte swizzle)
+//   warp 1       TMEM (512 columns: two accumulators of 128 tokens, four weight
+//                slots of 2 x 32 columns); one lane issues tcgen05.mma
+//                (M 128, N 128, K 16) with A from TMEM
+//   warps 2..5   epilogue: thread = output channel, looping over the tile's tokens
+//   warps 6..9   Linear1: the token-code rows gathered by the permutation (cp.async)
+//   warps 10..17 converters, two groups of four taking alternate stages: thread
+//                j turns row j of both weight blocks (64 int8 each) into 32
+//                words of fp16 pairs in the stage's TMEM slot.  One group alone
+//                is bound by its own latency (load, convert, store to TMEM, wait
+//                for the store, signal) rather than by issue.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "moe_tile.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQ8Tok = 128;                   // tokens per tile (MMA N)
+constexpr int kQ8Raw = 2 * 128 * kBK;         // int8 weight rows of a stage: 16 KB
+constexpr int kQ8B = kQ8Tok * kBK * 2;        // fp16 token codes of a stage: 16 KB
+constexpr int kQ8StageBytes = kQ8Raw + kQ8B;  // 32 KB
+constexpr int kQ8Stages = 4;                  // = TMEM weight slots
+constexpr int kQ8Ring = kQ8Stages * kQ8StageBytes;
+constexpr int kQ8BarBytes = 256;
+constexpr int kQ8ScaleBytes = 4 * kQ8Tok * 4;  // per epilogue warp: the tile's token scales
+constexpr int kQ8Smem = kQ8Ring + 1024 + kQ8BarBytes + kQ8ScaleBytes;
+constexpr int kQ8Threads = 576;
+constexpr int kQ8ConvGroups = 2;
+constexpr int kQ8Slot0 = 256;                  // TMEM: accumulators 0..255, slots 256 + 64 s
+static_assert(kQ8Slot0 + 64 * kQ8Stages <= 512, "TMEM columns");
+static_assert(8 * (3 * kQ8Stages + 2) + 8 <= kQ8BarBytes, "barrier area");
+static_assert(kQ8Smem <= 232448, "shared memory");
+
+// 4 int8 (one 32-bit word) -> 4 fp16, exactly: with b = x + 128 in [0, 255],
+// the fp16 bit pattern 0x6400 | b is 1024 + b, and subtracting 1152 leaves x.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);
+  const __half2 k = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), k);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), k);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns: thread i writes lane (base + i).
+__device__ __forceinline__ void tmem_st_32x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], fp16 inputs, fp32 accumulator.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kQ8Threads, 1)
+    gemm_q8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + kQ8Ring;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * kQ8Stages + 2));
+  float* scale_area = reinterpret_cast<float*>(bar_area + kQ8BarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t tiles0 = smem_u32(smem);
+  const uint32_t rawfull0 = smem_u32(bar_area);          // weight rows (+ Linear2 codes) landed
+  const uint32_t full0 = rawfull0 + 8 * kQ8Stages;        // TMEM slot and token codes ready
+  const uint32_t empty0 = full0 + 8 * kQ8Stages;          // the stage's MMAs are done
+  const uint32_t tfull = empty0 + 8 * kQ8Stages;
+  const uint32_t tempty = tfull + 8;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQ8Stages; ++s) {
+      mbar_init(rawfull0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 0));  // converters (+ gather threads)
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    if (!SWIGLU) tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = __ldg(p.tile_off + p.num_groups) * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo t = decode_tile(p, tile);
+        const int r0 = SWIGLU ? t.n * 128 : t.n * 256;
+        const int r1 = SWIGLU ? p.up_off + t.n * 128 : t.n * 256 + 128;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
+          const uint32_t fb = rawfull0 + 8 * stage;
+          const uint32_t sw = tiles0 + stage * kQ8StageBytes;
+          mbar_arrive_expect_tx(fb, kQ8Raw + (SWIGLU ? 0 : kQ8B));
+          tma_load_3d(sw, &tmW, fb, kb * kBK, r0, t.group);
+          tma_load_3d(sw + kQ8Raw / 2, &tmW, fb, kb * kBK, r1, t.group);
+          if (!SWIGLU) tma_load_2d(sw + kQ8Raw, &tmB, fb, kb * kBK, t.row0);
+          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp >= 6 && warp < 10) {
+    // ------------------------------------------------------------ token-code gather
+    // Linear1: the 128 token rows of the tile (row r -> token perm[r] / k) in
+    // the 128-byte-swizzled K-major layout, 16-byte cp.async chunks, eight lanes
+    // per 128-byte row segment; rows past the group's end are not copied (their
+    // stale products reach accumulator columns that are never stored).
+    if (SWIGLU) {
+      const int gw = warp - 6;
+      const int c = lane & 7;
+      const int rq = lane >> 3;
+      const long long ld = static_cast<long long>(p.num_kb) * kBK;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+        const TileInfo t = decode_tile(p, tile);
+        int tok[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = t.row0 + 32 * gw + 4 * i + rq;
+          tok[i] = row < t.row_end ? __ldg(p.gather_perm + row) / p.gather_k : -1;
+        }
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+          const uint32_t sb = tiles0 + stage * kQ8StageBytes + kQ8Raw;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 32 * gw + 4 * i + rq;
+            if (tok[i] >= 0)
+              cp_async16(sb + r * 128 + ((c ^ (r & 7)) << 4), p.gather_src + tok[i] * ld + kb * kBK + c * 8);
+          }
+          cp_async_arrive(full0 + 8 * stage);
+          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ converters
+    // TMEM lane quarter (warp % 4) -> weight rows 32 (warp % 4) .. + 31 of both
+    // blocks; thread row j reads its 64 int8 of the block (4 x 16 bytes) and
+    // writes 32 columns of fp16 pairs (k = 2c, 2c + 1 in column c).  Group g
+    // takes the k-blocks whose running index is g modulo kQ8ConvGroups.
+    const int q = warp & 3;
+    const int grp = (warp - 10) >> 2;
+    const int j = 32 * q + lane;
+    unsigned it = 0;  // running k-block index of this CTA
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        if (static_cast<int>(it % kQ8ConvGroups) != grp) continue;
+        const int stage = static_cast<int>(it % kQ8Stages);
+        const uint32_t phase = (it / kQ8Stages) & 1u;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(rawfull0 + 8 * stage, phase, p.status, abort_flag);
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const uint8_t* sw = smem + stage * kQ8StageBytes;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const uint4* row = reinterpret_cast<const uint4*>(sw + b * (kQ8Raw / 2) + j * kBK);
+          uint32_t h[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = row[c];
+            i8x4_to_f16x4(v.x, h[8 * c + 0], h[8 * c + 1]);
+            i8x4_to_f16x4(v.y, h[8 * c + 2], h[8 * c + 3]);
+            i8x4_to_f16x4(v.z, h[8 * c + 4], h[8 * c + 5]);
+            i8x4_to_f16x4(v.w, h[8 * c + 6], h[8 * c + 7]);
+          }
+          tmem_st_32x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kQ8Slot0 + 64 * stage + 32 * b, h);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(full0 + 8 * stage);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f32acc(128, kQ8Tok, kFmtF16, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+        if (!mbar_wait(tempty, (local & 1) ^ 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
+          // the gather warps' copies went through the generic proxy
+          if (SWIGLU) fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t sb = tiles0 + stage * kQ8StageBytes + kQ8Raw;
+          const uint32_t slot = tmem_base + kQ8Slot0 + 64 * stage;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // B: the token codes, K-major rows of 128 B; a 16-wide k step is 32 B
+              const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
+              mma_f16_tmem_a(tmem_base + kQ8Tok * b, slot + 32 * b + 8 * kk, bd, idesc,
+                             (kb | kk) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(tfull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Thread = output channel (TMEM lane): channel j of both accumulators,
+    // the tile's tokens in chunks of 32 columns; each store instruction of a
+    // warp writes 32 consecutive channels of one token row.
+    const int q = warp & 3;
+    const int j = 32 * q + lane;
+    float* sc = scale_area + q * kQ8Tok;  // this warp's copy of the token scales
+    float* out = static_cast<float*>(p.out);
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const TileInfo t = decode_tile(p, tile);
+      // the token (Linear1) or row (Linear2) scale of each of the tile's rows
+#pragma unroll
+      for (int i = 0; i < kQ8Tok / 32; ++i) {
+        const int row = t.row0 + 32 * i + lane;
+        float s = 0.0f;
+        if (row < t.row_end)
+          s = SWIGLU ? __ldg(p.scale_row + __ldg(p.gather_perm + row) / p.gather_k) : __ldg(p.scale_row + row);
+        sc[32 * i + lane] = s;
+      }
+      __syncwarp();
+      const float* scol = p.scale_col + static_cast<long long>(t.group) * p.scale_ld;
+      const int c0 = SWIGLU ? t.n * 128 + j : t.n * 256 + j;        // block 0 channel
+      const int c1 = SWIGLU ? p.up_off + t.n * 128 + j : c0 + 128;  // block 1 channel
+      const bool in0 = c0 < p.n_out;
+      const bool in1 = SWIGLU ? in0 : c1 < p.n_out;
+      const float s0 = in0 ? __ldg(scol + c0) : 0.0f;
+      const float s1 = in1 ? __ldg(scol + c1) : 0.0f;
+      const bool got = mbar_wait(tfull, local & 1, p.status, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < kQ8Tok; c += 32) {
+        float a[32], b[32];
+        tmem_ld_32x32(tb + c, a);
+        tmem_ld_32x32(tb + kQ8Tok + c, b);
+        if (c + 32 == kQ8Tok) {
+          tc_fence_before();
+          mbar_arrive(tempty);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int row = t.row0 + c + i;
+          if (row >= t.row_end) continue;
+          const float sr = sc[c + i];
+          if (SWIGLU) {
+            // H = (C * s^W1) * s^X, then SwiGLU
+            const float hg = (a[i] * s0) * sr;
+            const float hu = (b[i] * s1) * sr;
+            if (in0) out[static_cast<long long>(row) * p.ldo + c0] = __fdividef(hg, 1.0f + __expf(-hg)) * hu;
+          } else {
+            if (in0) out[static_cast<long long>(row) * p.ldo + c0] = (a[i] * s0) * sr;
+            if (in1) out[static_cast<long long>(row) * p.ldo + c1] = (b[i] * s1) * sr;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <bool SWIGLU>
+cudaError_t launch_q8(const CUtensorMap& w, const CUtensorMap& b, const GemmParams& p, int grid,
+                      cudaStream_t s) {
+  auto kern = gemm_q8_kernel<SWIGLU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kQ8Threads, kQ8Smem, s>>>(w, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q8(bool swiglu, const CUtensorMap& w, const CUtensorMap& b,
+                           const GemmParams& p, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  return swiglu ? launch_q8<true>(w, b, p, grid, s) : launch_q8<false>(w, b, p, grid, s);
+}
+
+}  // namespace moe

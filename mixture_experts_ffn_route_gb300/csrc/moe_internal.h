@@ -153,6 +153,16 @@ cudaError_t launch_router_bwd(const float* logits, const int32_t* E_ids, const f
                               int E, int k, int score_fn, float alpha, int renorm, uint16_t* dl,
                               cudaStream_t s);
 
+// A8W8 GEMMs with the int8 weights converted into TMEM as the MMA's A operand
+// (moe_gemm_q8.cu).  w: int8 weight rows [groups, N, K] (K contiguous), box
+// 64 k x 128 rows x 1, no swizzle; b (Linear2 only): fp16 codes [rows, K] as
+// make_map_rows.  Linear1 gathers the token codes (gather_src / gather_perm).
+// p.scale_col / scale_ld: per-channel weight scales; p.scale_row: token
+// (Linear1) or row (Linear2) scales; p.out fp32 [rows, ldo].
+bool make_map_i8_rows(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K);
+cudaError_t launch_gemm_q8(bool swiglu, const CUtensorMap& w, const CUtensorMap& b,
+                           const GemmParams& p, int grid, cudaStream_t s);
+
 // Launch the tcgen05 GEMM of the given kind on `grid` persistent CTAs.
 cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p, int grid,
                         cudaStream_t s);
