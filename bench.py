@@ -47,6 +47,7 @@ WORKLOAD_TEXT = {
     "c3_mx": "V4-Pro-shaped layer, MXFP8 form (E4M3 codes, E8M0 scales per 32), no shared expert",
     "c2_mx": "given-routing layer, MXFP8 form (E4M3)",
     "c3p_mx": "V4-Pro expert shapes, T=512 E=48, MXFP8 form (profiling size)",
+    "c3p_q": "V4-Pro expert shapes, T=512 E=48, A8W8-INT form (profiling size)",
     "c3_mx4": "V4-Pro-shaped layer, A8W4-FP form (E4M3 activations, E2M1 weights, E8M0 scales), no shared expert",
     "c3_mxa4": "V4-Pro-shaped layer, A4W4-FP form (E2M1 activations and weights), no shared expert",
     "c2_mx4": "given-routing layer, A8W4-FP form",
@@ -362,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
     if roof["bound"] == "hbm" and not quant:
         roof["traffic"] = load_traffic(args.workload, g1_bytes)
     if quant:
-        roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_tc_kernel<3>)"
+        roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_q8_kernel<true>)"
     if mx:
         roof["kernel"] = "grouped MX Linear1 + SwiGLU + Q_MX (gemm_mx_kernel<true, %d>)" % moe.MX_FORMATS[mx]
     # route: transpose Wg, gating GEMM, select, recheck, reselect (hash: GEMM, select);

@@ -17,21 +17,27 @@
 // converted by one thread straight into its TMEM lane with tcgen05.st, which
 // the MMA reads as A (row m in lane m, element k in column k / 2).
 //
-// Structure (one CTA per SM, 576 threads):
-//   warp 0       TMA: int8 weight rows, two blocks of 128 rows x 64 k per stage
+// Structure (one CTA per SM, 576 threads).  Two rings run on one running
+// k-block index per CTA: the int8 weight rows in shared memory (eight deep,
+// freed as soon as they are converted, so the weight stream runs well ahead),
+// and the operand stages (four deep): a TMEM slot of converted weights plus the
+// shared-memory tile of token codes, made ready by one barrier and released by
+// one MMA commit.  The MMA thread's own work per k-block (one wait, eight MMAs,
+// one commit) bounds the kernel at these shapes, so it is kept to that.
+//   warp 0       TMA: int8 weight rows, two blocks of 128 rows x 64 k per k-block
 //                (Linear1: gate rows and the matching up rows; Linear2: 256
-//                output channels), and for Linear2 the token-code tile
-//                [128 rows x 64 k] (fp16, K-major, 128-byte swizzle)
+//                output channels)
 //   warp 1       TMEM (512 columns: two accumulators of 128 tokens, four weight
 //                slots of 2 x 32 columns); one lane issues tcgen05.mma
-//                (M 128, N 128, K 16) with A from TMEM
+//                (M 128, N = the tile's token count rounded up to 16, K 16)
+//                with A from TMEM
 //   warps 2..5   epilogue: thread = output channel, looping over the tile's tokens
-//   warps 6..9   Linear1: the token-code rows gathered by the permutation (cp.async)
-//   warps 10..17 converters, two groups of four taking alternate stages: thread
+//   warps 6..9   token codes, K-major with 128-byte swizzle: Linear1 gathers the
+//                rows by the permutation (cp.async); Linear2 loads the tile of
+//                expert-ordered rows by TMA (one lane of warp 6)
+//   warps 10..17 converters, two groups of four taking alternate k-blocks: thread
 //                j turns row j of both weight blocks (64 int8 each) into 32
-//                words of fp16 pairs in the stage's TMEM slot.  One group alone
-//                is bound by its own latency (load, convert, store to TMEM, wait
-//                for the store, signal) rather than by issue.
+//                words of fp16 pairs in the k-block's TMEM slot
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "moe_tile.cuh"
@@ -39,21 +45,25 @@
 namespace moe {
 namespace {
 
-constexpr int kQ8Tok = 128;                   // tokens per tile (MMA N)
-constexpr int kQ8Raw = 2 * 128 * kBK;         // int8 weight rows of a stage: 16 KB
-constexpr int kQ8B = kQ8Tok * kBK * 2;        // fp16 token codes of a stage: 16 KB
-constexpr int kQ8StageBytes = kQ8Raw + kQ8B;  // 32 KB
-constexpr int kQ8Stages = 4;                  // = TMEM weight slots
-constexpr int kQ8Ring = kQ8Stages * kQ8StageBytes;
-constexpr int kQ8BarBytes = 256;
-constexpr int kQ8ScaleBytes = 4 * kQ8Tok * 4;  // per epilogue warp: the tile's token scales
+constexpr int kQ8Tok = 128;                      // tokens per tile (largest MMA N)
+constexpr int kQ8RawBytes = 2 * 128 * kBK;       // int8 weight rows of a k-block: 16 KB
+constexpr int kQ8CodeBytes = kQ8Tok * kBK * 2;   // fp16 token codes of a k-block: 16 KB
+constexpr int kQ8RawStages = 8;
+constexpr int kQ8Slots = 4;                      // operand stages = TMEM weight slots
+constexpr int kQ8CodeStages = kQ8Slots;
+constexpr int kQ8ConvGroups = 2;
+constexpr int kQ8CodeRing = kQ8CodeStages * kQ8CodeBytes;  // first: 1024-aligned for the swizzle
+constexpr int kQ8Ring = kQ8CodeRing + kQ8RawStages * kQ8RawBytes;
+constexpr int kQ8Bars = 2 * (kQ8RawStages + kQ8Slots) + 2;
+constexpr int kQ8BarBytes = 512;
+constexpr int kQ8ScaleBytes = 4 * kQ8Tok * 4;    // per epilogue warp: the tile's token scales
 constexpr int kQ8Smem = kQ8Ring + 1024 + kQ8BarBytes + kQ8ScaleBytes;
 constexpr int kQ8Threads = 576;
-constexpr int kQ8ConvGroups = 2;
-constexpr int kQ8Slot0 = 256;                  // TMEM: accumulators 0..255, slots 256 + 64 s
-static_assert(kQ8Slot0 + 64 * kQ8Stages <= 512, "TMEM columns");
-static_assert(8 * (3 * kQ8Stages + 2) + 8 <= kQ8BarBytes, "barrier area");
+constexpr int kQ8Slot0 = 256;                    // TMEM: accumulators 0..255, slots 256 + 64 s
+static_assert(kQ8Slot0 + 64 * kQ8Slots <= 512, "TMEM columns");
+static_assert(8 * kQ8Bars + 8 <= kQ8BarBytes, "barrier area");
 static_assert(kQ8Smem <= 232448, "shared memory");
+static_assert(kQ8Slots % kQ8ConvGroups == 0, "a slot belongs to one converter group");
 
 // 4 int8 (one 32-bit word) -> 4 fp16, exactly: with b = x + 128 in [0, 255],
 // the fp16 bit pattern 0x6400 | b is 1024 + b, and subtracting 1152 leaves x.
@@ -93,6 +103,10 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// Stage and phase parity of running k-block `it` in a ring of `n` stages.
+__device__ __forceinline__ uint32_t ring_stage(unsigned it, int n) { return it % n; }
+__device__ __forceinline__ uint32_t ring_phase(unsigned it, int n) { return (it / n) & 1u; }
+
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kQ8Threads, 1)
     gemm_q8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmB,
@@ -101,23 +115,29 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + kQ8Ring;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * kQ8Stages + 2));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * kQ8Bars);
   float* scale_area = reinterpret_cast<float*>(bar_area + kQ8BarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t tiles0 = smem_u32(smem);
-  const uint32_t rawfull0 = smem_u32(bar_area);          // weight rows (+ Linear2 codes) landed
-  const uint32_t full0 = rawfull0 + 8 * kQ8Stages;        // TMEM slot and token codes ready
-  const uint32_t empty0 = full0 + 8 * kQ8Stages;          // the stage's MMAs are done
-  const uint32_t tfull = empty0 + 8 * kQ8Stages;
+  const uint32_t codes0 = smem_u32(smem);
+  const uint32_t raw0 = codes0 + kQ8CodeRing;
+  const uint32_t rawfull0 = smem_u32(bar_area);                // weight rows landed
+  const uint32_t rawempty0 = rawfull0 + 8 * kQ8RawStages;      // weight rows converted
+  const uint32_t full0 = rawempty0 + 8 * kQ8RawStages;         // TMEM slot written, codes landed
+  const uint32_t empty0 = full0 + 8 * kQ8Slots;                // the stage's MMAs are done
+  const uint32_t tfull = empty0 + 8 * kQ8Slots;
   const uint32_t tempty = tfull + 8;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kQ8Stages; ++s) {
+    for (int s = 0; s < kQ8RawStages; ++s) {
       mbar_init(rawfull0 + 8 * s, 1);
-      mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 0));  // converters (+ gather threads)
+      mbar_init(rawempty0 + 8 * s, 128);
+    }
+    for (int s = 0; s < kQ8Slots; ++s) {
+      // converters, and the gather threads or the codes' TMA
+      mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 1));
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(tfull, 1);
@@ -137,41 +157,42 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
   const int total = __ldg(p.tile_off + p.num_groups) * p.n_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight TMA
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      unsigned it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo t = decode_tile(p, tile);
         const int r0 = SWIGLU ? t.n * 128 : t.n * 256;
         const int r1 = SWIGLU ? p.up_off + t.n * 128 : t.n * 256 + 128;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
-          const uint32_t fb = rawfull0 + 8 * stage;
-          const uint32_t sw = tiles0 + stage * kQ8StageBytes;
-          mbar_arrive_expect_tx(fb, kQ8Raw + (SWIGLU ? 0 : kQ8B));
-          tma_load_3d(sw, &tmW, fb, kb * kBK, r0, t.group);
-          tma_load_3d(sw + kQ8Raw / 2, &tmW, fb, kb * kBK, r1, t.group);
-          if (!SWIGLU) tma_load_2d(sw + kQ8Raw, &tmB, fb, kb * kBK, t.row0);
-          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t st = ring_stage(it, kQ8RawStages);
+          if (!mbar_wait(rawempty0 + 8 * st, ring_phase(it, kQ8RawStages) ^ 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = rawfull0 + 8 * st;
+          const uint32_t dst = raw0 + st * kQ8RawBytes;
+          mbar_arrive_expect_tx(fb, kQ8RawBytes);
+          tma_load_3d(dst, &tmW, fb, kb * kBK, r0, t.group);
+          tma_load_3d(dst + kQ8RawBytes / 2, &tmW, fb, kb * kBK, r1, t.group);
         }
       }
     }
   } else if (warp >= 6 && warp < 10) {
-    // ------------------------------------------------------------ token-code gather
-    // Linear1: the 128 token rows of the tile (row r -> token perm[r] / k) in
-    // the 128-byte-swizzled K-major layout, 16-byte cp.async chunks, eight lanes
-    // per 128-byte row segment; rows past the group's end are not copied (their
-    // stale products reach accumulator columns that are never stored).
+    // ------------------------------------------------------------ token codes
     if (SWIGLU) {
+      // Linear1: the tile's 128 token rows (row r -> token perm[r] / k),
+      // 16-byte cp.async chunks, eight lanes per 128-byte row segment; rows
+      // past the group's end are not copied (their stale products reach
+      // accumulator columns that are never stored).
       const int gw = warp - 6;
       const int c = lane & 7;
       const int rq = lane >> 3;
       const long long ld = static_cast<long long>(p.num_kb) * kBK;
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+      unsigned it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo t = decode_tile(p, tile);
         int tok[8];
 #pragma unroll
@@ -179,22 +200,39 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
           const int row = t.row0 + 32 * gw + 4 * i + rq;
           tok[i] = row < t.row_end ? __ldg(p.gather_perm + row) / p.gather_k : -1;
         }
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t st = ring_stage(it, kQ8CodeStages);
           bool w = true;
-          if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+          if (lane == 0)
+            w = mbar_wait(empty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag);
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-          const uint32_t sb = tiles0 + stage * kQ8StageBytes + kQ8Raw;
+          const uint32_t sb = codes0 + st * kQ8CodeBytes;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = 32 * gw + 4 * i + rq;
             if (tok[i] >= 0)
               cp_async16(sb + r * 128 + ((c ^ (r & 7)) << 4), p.gather_src + tok[i] * ld + kb * kBK + c * 8);
           }
-          cp_async_arrive(full0 + 8 * stage);
-          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+          cp_async_arrive(full0 + 8 * st);
         }
-        if (!ok) break;
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 6 && lane == 0) {
+      // Linear2: the tile of expert-ordered rows [128 x 64] by TMA
+      unsigned it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo t = decode_tile(p, tile);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t st = ring_stage(it, kQ8CodeStages);
+          if (!mbar_wait(empty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * st;
+          mbar_arrive_expect_tx(fb, kQ8CodeBytes);
+          tma_load_2d(codes0 + st * kQ8CodeBytes, &tmB, fb, kb * kBK, t.row0);
+        }
       }
     }
   } else if (warp >= 10) {
@@ -206,67 +244,84 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     const int q = warp & 3;
     const int grp = (warp - 10) >> 2;
     const int j = 32 * q + lane;
-    unsigned it = 0;  // running k-block index of this CTA
+    const int sx = (j >> 1) & 3;
+    unsigned it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         if (static_cast<int>(it % kQ8ConvGroups) != grp) continue;
-        const int stage = static_cast<int>(it % kQ8Stages);
-        const uint32_t phase = (it / kQ8Stages) & 1u;
+        const uint32_t rs = ring_stage(it, kQ8RawStages);
+        const uint32_t sl = ring_stage(it, kQ8Slots);
         bool w = true;
-        if (lane == 0) w = mbar_wait(rawfull0 + 8 * stage, phase, p.status, abort_flag);
+        if (lane == 0)
+          w = mbar_wait(rawfull0 + 8 * rs, ring_phase(it, kQ8RawStages), p.status, abort_flag) &&
+              mbar_wait(empty0 + 8 * sl, ring_phase(it, kQ8Slots) ^ 1, p.status, abort_flag);
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        const uint8_t* sw = smem + stage * kQ8StageBytes;
+        tc_fence_after();
+        const uint8_t* sw = smem + kQ8CodeRing + rs * kQ8RawBytes;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-          const uint4* row = reinterpret_cast<const uint4*>(sw + b * (kQ8Raw / 2) + j * kBK);
+          const uint4* row = reinterpret_cast<const uint4*>(sw + b * (kQ8RawBytes / 2) + j * kBK);
           uint32_t h[32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 v = row[c];
+            const uint4 v = row[c ^ sx];  // the TMA's 64-byte swizzle
             i8x4_to_f16x4(v.x, h[8 * c + 0], h[8 * c + 1]);
             i8x4_to_f16x4(v.y, h[8 * c + 2], h[8 * c + 3]);
             i8x4_to_f16x4(v.z, h[8 * c + 4], h[8 * c + 5]);
             i8x4_to_f16x4(v.w, h[8 * c + 6], h[8 * c + 7]);
           }
-          tmem_st_32x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kQ8Slot0 + 64 * stage + 32 * b, h);
+          tmem_st_32x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kQ8Slot0 + 64 * sl + 32 * b, h);
         }
+        // the shared-memory rows were consumed by the conversions above
+        mbar_arrive(rawempty0 + 8 * rs);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
-        mbar_arrive(full0 + 8 * stage);
+        mbar_arrive(full0 + 8 * sl);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread; per k-block one wait, eight MMAs and one commit (ring
+    // position as a wrapping counter, descriptors as increments).
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f32acc(128, kQ8Tok, kFmtF16, false, false);
-      int stage = 0;
-      uint32_t phase = 0;
+      int sl = 0;
+      uint32_t ph = 0;
       int local = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+      bool ok = true;
+      const uint64_t bd0 = smem_desc_sw128(codes0, 16, 1024);
+      const uint32_t slot0 = tmem_base + kQ8Slot0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+        const TileInfo t = decode_tile(p, tile);
+        const int rows = t.row_end - t.row0;
+        const int n = rows <= 16 ? 16 : (rows >= kQ8Tok ? kQ8Tok : (rows + 15) & ~15);
+        const uint32_t idesc = idesc_f32acc(128, n, kFmtF16, false, false);
         if (!mbar_wait(tempty, (local & 1) ^ 1, p.status, abort_flag)) break;
         tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
+          if (!mbar_wait(full0 + 8 * sl, ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
           // the gather warps' copies went through the generic proxy
           if (SWIGLU) fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t sb = tiles0 + stage * kQ8StageBytes + kQ8Raw;
-          const uint32_t slot = tmem_base + kQ8Slot0 + 64 * stage;
+          // B: the token codes, K-major rows of 128 B; a 16-wide k step is 32 B
+          // (+2 in the descriptor's address field)
+          const uint64_t bd = bd0 + static_cast<uint64_t>(sl * (kQ8CodeBytes >> 4));
+          const uint32_t slot = slot0 + 64 * sl;
+          const uint32_t acc = kb != 0 ? 1u : 0u;
+          mma_f16_tmem_a(tmem_base, slot, bd, idesc, acc);
+          mma_f16_tmem_a(tmem_base + kQ8Tok, slot + 32, bd, idesc, acc);
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // B: the token codes, K-major rows of 128 B; a 16-wide k step is 32 B
-              const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
-              mma_f16_tmem_a(tmem_base + kQ8Tok * b, slot + 32 * b + 8 * kk, bd, idesc,
-                             (kb | kk) != 0 ? 1u : 0u);
-            }
+          for (int kk = 1; kk < kBK / 16; ++kk) {
+            mma_f16_tmem_a(tmem_base, slot + 8 * kk, bd + 2 * kk, idesc, 1u);
+            mma_f16_tmem_a(tmem_base + kQ8Tok, slot + 32 + 8 * kk, bd + 2 * kk, idesc, 1u);
           }
-          mma_commit(empty0 + 8 * stage);
-          if (++stage == kQ8Stages) { stage = 0; phase ^= 1; }
+          mma_commit(empty0 + 8 * sl);
+          if (++sl == kQ8Slots) { sl = 0; ph ^= 1; }
         }
+        if (!ok) break;
         mma_commit(tfull);
       }
     }
@@ -282,6 +337,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const TileInfo t = decode_tile(p, tile);
+      const int rows = t.row_end - t.row0;
+      const int ncol = rows <= 32 ? 32 : (rows >= kQ8Tok ? kQ8Tok : (rows + 31) & ~31);
       // the token (Linear1) or row (Linear2) scale of each of the tile's rows
 #pragma unroll
       for (int i = 0; i < kQ8Tok / 32; ++i) {
@@ -304,11 +361,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < kQ8Tok; c += 32) {
+      for (int c = 0; c < ncol; c += 32) {
         float a[32], b[32];
         tmem_ld_32x32(tb + c, a);
         tmem_ld_32x32(tb + kQ8Tok + c, b);
-        if (c + 32 == kQ8Tok) {
+        if (c + 32 == ncol) {
           tc_fence_before();
           mbar_arrive(tempty);
         }

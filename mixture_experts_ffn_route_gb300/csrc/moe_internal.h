@@ -155,7 +155,9 @@ cudaError_t launch_router_bwd(const float* logits, const int32_t* E_ids, const f
 
 // A8W8 GEMMs with the int8 weights converted into TMEM as the MMA's A operand
 // (moe_gemm_q8.cu).  w: int8 weight rows [groups, N, K] (K contiguous), box
-// 64 k x 128 rows x 1, no swizzle; b (Linear2 only): fp16 codes [rows, K] as
+// 64 k x 128 rows x 1, 64-byte swizzle (the 16-byte chunk c of row r lands at
+// chunk c ^ ((r >> 1) & 3), so that a warp reading one row per thread hits
+// every bank once); b (Linear2 only): fp16 codes [rows, K] as
 // make_map_rows.  Linear1 gathers the token codes (gather_src / gather_perm).
 // p.scale_col / scale_ld: per-channel weight scales; p.scale_row: token
 // (Linear1) or row (Linear2) scales; p.out fp32 [rows, ldo].
