@@ -168,12 +168,16 @@ size_t moe_workspace_size_a8w8(const moe_params* p);
  * A8W8 scenario), no shared expert (has_shared must be 0):
  *   each token row is quantised, s^X_t = max|x_t| / 127, q_t = round(x_t / s^X_t)
  *   (nearest integer, halves away from zero; float32);
- *   per expert: C = Q_e W1q[e] (int32), H = (C * S1[e]) * s^X, A = SiLU(H[:, :I])
- *   * H[:, I:], each row of A re-quantised the same way (s^A, A8), D = A8 W2q[e]
- *   (int32), Y_e = (D * S2[e]) * s^A;  y_t = sum_j G[t, j] Y[row(t, j)].
- *   W1q [E, H, 2I] int8, S1 [E, 2I] fp32 (per output channel)
- *   W2q [E, I, H]  int8, S2 [E, H]  fp32
+ *   per expert: C = Q_e W1q[e]^T (int32), H = (C * S1[e]) * s^X,
+ *   A = SiLU(H[:, :I]) * H[:, I:], each row of A re-quantised the same way
+ *   (s^A, A8), D = A8 W2q[e]^T (int32), Y_e = (D * S2[e]) * s^A;
+ *   y_t = sum_j G[t, j] Y[row(t, j)].
+ *   The weights keep the operator's layout, one row per output channel with
+ *   K contiguous (rows 0..I-1 of W1q are the SiLU branch):
+ *   W1q [E, 2I, H] int8, S1 [E, 2I] fp32 (per output channel)
+ *   W2q [E, H, I]  int8, S2 [E, H]  fp32
  *   X [T, H] bf16, E_ids [T, k], G [T, k] fp32, Y [T, H] bf16 out.
+ * H and I must be multiples of 64 (MOE_ERR_UNSUPPORTED otherwise).
  * The int8 products run on the fp16 tensor-core path (GB300's int8 tensor rate
  * is far lower): codes are exact in fp16 and the fp32 accumulator holds each
  * int32 sum exactly while every partial sum stays below 2^24 in magnitude

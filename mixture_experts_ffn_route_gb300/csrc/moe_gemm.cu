@@ -4,34 +4,24 @@
 //   router     : logits[T, E] = X[T, H] Wg[H, E]                          (fp32 out)
 //   Linear1    : Act[rows, I] = SiLU(X_e W1[e][:, :I]) * (X_e W1[e][:, I:])   (bf16 out)
 //   Linear2    : Yp[rows, H]  = Act W2[e]                                  (fp32 out)
-//   Linear1 A8W8: Act = SiLU(Hg) * Hu,  H = (Q_e W1q[e] * s^W1) * s^X      (fp32 out)
-//   Linear2 A8W8: Yp  = (A8 W2q[e] * s^W2) * s^A                            (fp32 out)
 // The expert FFN is the "Expert Compute" step of the "mega_moe" page
 // (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
-// projection; its A8W8 scenario for the int8 forms); the router product is the
+// projection); the router product is the
 // gating linear of "Megatron-LM 的 MoE 并行：以 DeepSeek-V4 为例" (section 路由张量).
 //
 // Structure (one CTA per SM):
 //   warp 0      TMA producer: A tile [128 rows x 64 k] K-major and B tile
 //               [64 k x BN cols] MN-major (the weights keep their [K][N] row-major
 //               layout), both with 128-byte swizzle, into a STAGES-deep ring.
-//               For the int8 forms warp 0 streams raw int8 B tiles through a
-//               ring of their own, and A (Linear2) comes from warp 6.
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16)
 //               into one of two TMEM accumulators and commits to mbarriers.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
-//               dequantise / fuse SwiGLU, stage through shared memory for
+//               fuse SwiGLU, stage through shared memory for
 //               full-line stores, free the accumulator so the next tile's MMAs
 //               overlap this epilogue.
-//   warps 6..9  Linear1 only: copy the A rows straight from the token rows (X,
-//               or its int8 codes held as fp16) by the dispatch permutation
-//               (cp.async), so the permuted rows are never written to memory.
-//   warps 10..13 int8 forms only: convert each raw int8 B tile to fp16 in the
-//               swizzled MN-major layout.  GB300's int8 tensor rate is far below
-//               its fp16 rate, so the int8 x int8 products run as fp16 x fp16:
-//               |code| <= 127 is exact in fp16, a product is exact in fp32, and
-//               the fp32 accumulator holds the int32 sum exactly while partial
-//               sums stay below 2^24 in magnitude.
+//   warps 6..9  Linear1 only: copy the A rows straight from the token rows X
+//               by the dispatch permutation (cp.async), so the permuted rows are
+//               never written to memory.
 // Tiles are walked in (group, column tile, 128-row tile) order, striding by
 // gridDim.x.  Group row ranges come from device memory.
 #include "moe_common.cuh"
@@ -47,54 +37,33 @@ constexpr int kStgWords = 36;
 
 template <int KIND>
 struct KindInfo {
-  static constexpr bool Q8 = (KIND == kGemmSwiGLU_Q8 || KIND == kGemmPlain_Q8);
-  static constexpr bool SWIGLU = (KIND == kGemmSwiGLU || KIND == kGemmSwiGLU_Q8);
+  static constexpr bool SWIGLU = (KIND == kGemmSwiGLU);
   static constexpr int BN = (KIND == kGemmRouter) ? 128 : 256;
-  static constexpr int THREADS = Q8 ? 448 : 320;
+  static constexpr int THREADS = 320;
 };
 
-template <int BN, bool Q8>
+template <int BN>
 struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;   // 16 KB
   static constexpr int B_BYTES = BN * kBK * 2;    // 8 KB per 64 columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = Q8 ? 3 : ((BN == 256) ? 4 : 6);
-  // int8 forms: a ring of raw int8 B tiles of its own, refilled as soon as the
-  // converters have read a slot (not when the MMA frees a stage)
-  static constexpr int RAW_BYTES = Q8 ? BN * kBK : 0;
-  static constexpr int RAW_STAGES = Q8 ? 3 : 0;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES + RAW_STAGES * RAW_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
   // epilogue staging: per epilogue warp 32 rows x kStgWords 32-bit words
   static constexpr int STG_BYTES = 4 * 32 * kStgWords * 4;
   static constexpr int SMEM_BYTES = RING_BYTES + 1024 + BAR_BYTES + STG_BYTES;
-  static_assert(8 * (2 * STAGES + 2 * RAW_STAGES + 4) + 8 <= BAR_BYTES, "barrier area");
+  static_assert(8 * (2 * STAGES + 4) + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// First weight column of 64-wide B box j (bf16 forms) or 128-wide raw box j
-// (int8 forms) of column tile n.  SwiGLU tiles hold 128 gate columns followed
-// by the matching 128 up columns.
+// First weight column of 64-wide B box j of column tile n.  SwiGLU tiles hold
+// 128 gate columns followed by the matching 128 up columns.
 template <int KIND>
 __device__ __forceinline__ int b_box_col(const GemmParams& p, int n, int j) {
   if (KIND == kGemmSwiGLU) return (j < 2) ? n * 128 + j * 64 : p.up_off + n * 128 + (j - 2) * 64;
-  if (KIND == kGemmSwiGLU_Q8) return (j == 0) ? n * 128 : p.up_off + n * 128;
-  if (KIND == kGemmPlain_Q8) return n * 256 + j * 128;
   return n * KindInfo<KIND>::BN + j * 64;
-}
-
-// 4 int8 (one 32-bit word) -> 4 fp16, exactly: with b = x + 128 in [0, 255],
-// the fp16 bit pattern 0x6400 | b is 1024 + b, and subtracting 1152 leaves x.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);
-  const uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);
-  const __half2 k = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), k);
-  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), k);
-  lo = *reinterpret_cast<const uint32_t*>(&ha);
-  hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
 template <int KIND>
@@ -102,16 +71,14 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                    const GemmParams p) {
-  constexpr bool Q8 = KindInfo<KIND>::Q8;
   constexpr bool SWIGLU = KindInfo<KIND>::SWIGLU;
   constexpr int BN = KindInfo<KIND>::BN;
-  using C = GemmCfg<BN, Q8>;
+  using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + C::RING_BYTES;
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 2 * C::RAW_STAGES + 4));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 4));
   uint32_t* stg_area = reinterpret_cast<uint32_t*>(bar_area + C::BAR_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -122,22 +89,14 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
   const uint32_t empty0 = full0 + 8 * C::STAGES;
   const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
-  const uint32_t rawfull0 = tempty0 + 16;                   // int8 forms: raw tile landed
-  const uint32_t rawempty0 = rawfull0 + 8 * C::RAW_STAGES;  // raw slot read by the converters
-  const uint32_t raws0 = tiles0 + C::STAGES * C::STAGE_BYTES;  // raw ring
 
   const bool gather = SWIGLU && (p.gather_src != nullptr);
   if (threadIdx.x == 0) {
-    // arrivals completing a stage: the TMA producer's (when it loads A or the
-    // bf16 B), one per gather thread, one per converter warp
-    const int full_count = (Q8 ? 4 : 0) + (gather ? 128 : 0) + (!gather ? 1 : 0) + ((!Q8 && gather) ? 1 : 0);
+    // arrivals completing a stage: the TMA producer's and one per gather thread
+    const int full_count = 1 + (gather ? 128 : 0);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, full_count);
       mbar_init(empty0 + 8 * s, 1);
-    }
-    for (int r = 0; r < C::RAW_STAGES; ++r) {
-      mbar_init(rawfull0 + 8 * r, 1);
-      mbar_init(rawempty0 + 8 * r, 4);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -166,9 +125,8 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // bf16 forms: lane 0 waits for a free stage, posts the byte count and
-    // loads B, and A too unless the gather warps copy the A rows.  int8 forms:
-    // lane 0 streams the raw int8 B tiles through their own ring.
+    // Lane 0 waits for a free stage, posts the byte count and loads B, and A
+    // too unless the gather warps copy the A rows.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -178,17 +136,6 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
         const CUtensorMap* mB = t.second ? &tmB2 : &tmB;
         const int bz = t.second ? 0 : t.group;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (Q8) {
-            if (!mbar_wait(rawempty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
-            const uint32_t rb = rawfull0 + 8 * stage;
-            const uint32_t sr = raws0 + stage * C::RAW_BYTES;
-            mbar_arrive_expect_tx(rb, C::RAW_BYTES);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_3d(sr + j * (128 * kBK), mB, rb, b_box_col<KIND>(p, t.n, j), kb * kBK, bz);
-            if (++stage == C::RAW_STAGES) { stage = 0; phase ^= 1; }
-            continue;
-          }
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
@@ -202,24 +149,6 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_3d(sb + j * (64 * kBK * 2), mB, fb, b_box_col<KIND>(p, t.n, j), kb * kBK, bz);
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-        }
-      }
-    }
-  } else if (Q8 && !gather && warp == 6) {
-    // ------------------------------------------------------------ A loader
-    // int8 Linear2: the A tiles (fp16 codes of the re-quantised activations)
-    // by TMA into the fp16 ring, in step with the MMA's stages.
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const TileInfo t = decode_tile(p, tile);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag)) break;
-          const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, C::A_BYTES);
-          tma_load_2d(tiles0 + stage * C::STAGE_BYTES, &tmA, fb, kb * kBK, t.a_row0);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -276,73 +205,10 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
         if (!ok) break;
       }
     }
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ int8 -> fp16
-    // Thread v of 128 converts raw 16-byte vectors v, v + 128, ...: raw half j
-    // (128 columns), k-row, 16-column group q.  The raw tile arrives with the
-    // 128-byte swizzle (vector q of row k at chunk q ^ (k % 8)).  The 16 fp16
-    // values land in two 16-byte chunks of N-block 2j + q/4 (64 columns, 8 KB),
-    // row k, at chunk positions (2 (q % 4) + 0/1) ^ (k % 8): the MN-major
-    // 128-byte swizzle.  The 8 lanes of one shared-memory phase take one column
-    // group in 8 consecutive k-rows, so the XOR with k % 8 sends their 16-byte
-    // reads and writes to 8 distinct bank quads.
-    if (Q8) {
-      const int tid = threadIdx.x - 10 * 32;
-      int stage = 0, rstage = 0;
-      uint32_t phase = 0, rphase = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          bool w = true;
-          if (lane == 0)
-            w = mbar_wait(rawfull0 + 8 * rstage, rphase, p.status, abort_flag) &&
-                mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-          uint8_t* sbp = smem + stage * C::STAGE_BYTES + C::A_BYTES;   // fp16 B
-          const uint8_t* srp = smem + C::STAGES * C::STAGE_BYTES + rstage * C::RAW_BYTES;  // raw
-          // all eight 16-byte loads first (one latency), then convert and store
-          uint4 raw[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int v = tid + 128 * i;
-            const int j = v >> 9;                      // raw half
-            const int k = 8 * ((v >> 6) & 7) + (v & 7);  // k-row
-            const int q = (v >> 3) & 7;                // 16-column group
-            raw[i] = *reinterpret_cast<const uint4*>(srp + j * 8192 + k * 128 + ((q ^ (k & 7)) << 4));
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int v = tid + 128 * i;
-            const int j = v >> 9;
-            const int k = 8 * ((v >> 6) & 7) + (v & 7);
-            const int q = (v >> 3) & 7;
-            uint32_t h[8];
-            i8x4_to_f16x4(raw[i].x, h[0], h[1]);
-            i8x4_to_f16x4(raw[i].y, h[2], h[3]);
-            i8x4_to_f16x4(raw[i].z, h[4], h[5]);
-            i8x4_to_f16x4(raw[i].w, h[6], h[7]);
-            uint8_t* row = sbp + (2 * j + (q >> 2)) * 8192 + k * 128;
-            const int c0 = 2 * (q & 3);
-            *reinterpret_cast<uint4*>(row + ((c0 ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (k & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(full0 + 8 * stage);
-            mbar_arrive(rawempty0 + 8 * rstage);
-          }
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-          if (++rstage == C::RAW_STAGES) { rstage = 0; rphase ^= 1; }
-        }
-        if (!ok) break;
-      }
-    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f32acc(kBM, BN, Q8 ? kFmtF16 : kFmtBF16, false, true);
+      constexpr uint32_t idesc = idesc_f32acc(kBM, BN, kFmtBF16, false, true);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -354,10 +220,9 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
-          // rows copied by the gather warps and tiles written by the converter
-          // warps went through the generic proxy; order them before the
-          // tensor cores read the stage
-          if (gather || Q8) fence_proxy_async_smem();
+          // rows copied by the gather warps went through the generic proxy;
+          // order them before the tensor cores read the stage
+          if (gather) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = tiles0 + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
@@ -399,17 +264,6 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(tempty0 + 8 * acc);
         continue;
-      }
-      // int8 forms: this row's activation scale (token scale for Linear1, row
-      // scale for Linear2) and the group's per-column weight scales
-      float srow = 0.0f;
-      const float* scol = nullptr;
-      if (Q8) {
-        const int row = wrow0 + lane;
-        if (row < t.row_end)
-          srow = (KIND == kGemmSwiGLU_Q8) ? __ldg(p.scale_row + __ldg(p.gather_perm + row) / p.gather_k)
-                                          : __ldg(p.scale_row + row);
-        scol = p.scale_col + static_cast<long long>(t.group) * p.scale_ld;
       }
       if (KIND == kGemmSwiGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -461,31 +315,13 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
           __syncwarp();
         }
       } else {
-        // fp32 outputs: router logits, Linear2 (bf16 or int8 form), and the
-        // int8 Linear1 (dequantised, SwiGLU, kept in fp32 for re-quantisation)
+        // fp32 outputs: router logits and Linear2
         float* out = static_cast<float*>(p.out);
-        constexpr int NCOL = (KIND == kGemmSwiGLU_Q8) ? 128 : BN;
 #pragma unroll 1
-        for (int c = 0; c < NCOL; c += 32) {
+        for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld_32x32(tb + c, v);
-          const int col = t.n * NCOL + c;
-          if (KIND == kGemmSwiGLU_Q8) {
-            // H = (C * s^W1) * s^X for the gate and up halves, then SwiGLU
-            float u[32];
-            tmem_ld_32x32(tb + 128 + c, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const bool in = col + i < p.n_out;
-              const float hg = (v[i] * (in ? __ldg(scol + col + i) : 0.0f)) * srow;
-              const float hu = (u[i] * (in ? __ldg(scol + p.up_off + col + i) : 0.0f)) * srow;
-              v[i] = __fdividef(hg, 1.0f + __expf(-hg)) * hu;
-            }
-          } else if (KIND == kGemmPlain_Q8) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              v[i] = (v[i] * (col + i < p.n_out ? __ldg(scol + col + i) : 0.0f)) * srow;
-          }
+          const int col = t.n * BN + c;
           float4* srow4 = reinterpret_cast<float4*>(stg + lane * kStgWords);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -566,21 +402,6 @@ bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [groups, K, N] int8 row-major (N contiguous), box = 128 n x 64 k x 1,
-// 128-byte swizzle.
-bool make_map_weights_i8(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
-                        static_cast<cuuint64_t>(groups)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(N * K)};
-  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kBK), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // [rows, cols] FP8 codes (bytes, cols contiguous), box = 128 columns x 128
 // rows, 128-byte swizzle.
 bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool fp4) {
@@ -644,6 +465,8 @@ bool make_map_bf16_kmajor_b(CUtensorMap* m, const void* base, int64_t groups, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [groups, N, K] int8 row-major (K contiguous: one row per output channel),
+// box = 64 k x 128 rows x 1, 64-byte swizzle.
 bool make_map_i8_rows(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -662,7 +485,7 @@ int gemm_block_n(GemmKind kind) { return kind == kGemmRouter ? 128 : 256; }
 template <int KIND>
 static cudaError_t launch_one(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
   using I = KindInfo<KIND>;
-  using C = GemmCfg<I::BN, I::Q8>;
+  using C = GemmCfg<I::BN>;
   auto kern = gemm_tc_kernel<KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
@@ -677,9 +500,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
   switch (kind) {
     case kGemmRouter: return launch_one<kGemmRouter>(maps, p, grid, s);
     case kGemmSwiGLU: return launch_one<kGemmSwiGLU>(maps, p, grid, s);
-    case kGemmPlain: return launch_one<kGemmPlain>(maps, p, grid, s);
-    case kGemmSwiGLU_Q8: return launch_one<kGemmSwiGLU_Q8>(maps, p, grid, s);
-    default: return launch_one<kGemmPlain_Q8>(maps, p, grid, s);
+    default: return launch_one<kGemmPlain>(maps, p, grid, s);
   }
 }
 

@@ -14,9 +14,7 @@ constexpr int kBK = 64;   // GEMM k-block (one 128-byte swizzle row of bf16)
 enum GemmKind {
   kGemmRouter = 0,     // fp32 logits
   kGemmSwiGLU = 1,     // Linear1 + SwiGLU, bf16 out
-  kGemmPlain = 2,      // Linear2, fp32 out
-  kGemmSwiGLU_Q8 = 3,  // A8W8 Linear1 + dequantisation + SwiGLU, fp32 out
-  kGemmPlain_Q8 = 4    // A8W8 Linear2 + dequantisation, fp32 out
+  kGemmPlain = 2       // Linear2, fp32 out
 };
 
 // One grouped GEMM launch.  Groups are row ranges [row_off[g], row_off[g+1])
@@ -74,7 +72,6 @@ struct GemmMaps {
 // Tensor-map helpers (host).  Return false if the driver rejects the map.
 bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
 bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N);
-bool make_map_weights_i8(CUtensorMap* m, const void* base, int64_t groups, int64_t K, int64_t N);
 
 // Per-row int8 quantisation ("mega_moe" A8W8): s = max|x| / 127 and codes
 // round(x / s) (halves away from zero), written as fp16 values.  rows_dev,
