@@ -17,20 +17,20 @@
 // converted by one thread straight into its TMEM lane with tcgen05.st, which
 // the MMA reads as A (row m in lane m, element k in column k / 2).
 //
-// Structure (one CTA per SM, 576 threads).  Two rings run on one running
+// Structure (one CTA per SM, 608 threads).  Two rings run on one running
 // k-block index per CTA: the int8 weight rows in shared memory (eight deep,
 // freed as soon as they are converted, so the weight stream runs well ahead),
 // and the operand stages (four deep): a TMEM slot of converted weights plus the
 // shared-memory tile of token codes, made ready by one barrier and released by
-// one MMA commit.  The MMA thread's own work per k-block (one wait, eight MMAs,
-// one commit) bounds the kernel at these shapes, so it is kept to that.
+// two MMA commits.  The MMA threads' own work per k-block (one wait, four MMAs,
+// one commit each) bounds the kernel at these shapes, so it is kept to that.
 //   warp 0       TMA: int8 weight rows, two blocks of 128 rows x 64 k per k-block
 //                (Linear1: gate rows and the matching up rows; Linear2: 256
 //                output channels)
-//   warp 1       TMEM (512 columns: two accumulators of 128 tokens, four weight
-//                slots of 2 x 32 columns); one lane issues tcgen05.mma
-//                (M 128, N = the tile's token count rounded up to 16, K 16)
-//                with A from TMEM
+//   warps 1, 18  MMA: warp 1 allocates TMEM (512 columns: two accumulators of
+//                128 tokens, four weight slots of 2 x 32 columns); one lane of
+//                each issues tcgen05.mma (M 128, N = the tile's token count
+//                rounded up to 16, K 16, A from TMEM) into its own accumulator
 //   warps 2..5   epilogue: thread = output channel, looping over the tile's tokens
 //   warps 6..9   token codes, K-major with 128-byte swizzle: Linear1 gathers the
 //                rows by the permutation (cp.async); Linear2 loads the tile of
@@ -58,7 +58,8 @@ constexpr int kQ8Bars = 2 * (kQ8RawStages + kQ8Slots) + 2;
 constexpr int kQ8BarBytes = 512;
 constexpr int kQ8ScaleBytes = 4 * kQ8Tok * 4;    // per epilogue warp: the tile's token scales
 constexpr int kQ8Smem = kQ8Ring + 1024 + kQ8BarBytes + kQ8ScaleBytes;
-constexpr int kQ8Threads = 576;
+constexpr int kQ8Threads = 608;
+constexpr int kQ8MmaWarp2 = 18;                  // the second MMA thread's warp
 constexpr int kQ8Slot0 = 256;                    // TMEM: accumulators 0..255, slots 256 + 64 s
 static_assert(kQ8Slot0 + 64 * kQ8Slots <= 512, "TMEM columns");
 static_assert(8 * kQ8Bars + 8 <= kQ8BarBytes, "barrier area");
@@ -138,9 +139,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     for (int s = 0; s < kQ8Slots; ++s) {
       // converters, and the gather threads or the codes' TMA
       mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 1));
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 2);  // one commit per MMA thread
     }
-    mbar_init(tfull, 1);
+    mbar_init(tfull, 2);
     mbar_init(tempty, 128);
     *abort_flag = 0;
     fence_mbar_init();
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         }
       }
     }
-  } else if (warp >= 10) {
+  } else if (warp >= 10 && warp < 18) {
     // ------------------------------------------------------------ converters
     // TMEM lane quarter (warp % 4) -> weight rows 32 (warp % 4) .. + 31 of both
     // blocks; thread row j reads its 64 int8 of the block (4 x 16 bytes) and
@@ -280,17 +281,22 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         mbar_arrive(full0 + 8 * sl);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread; per k-block one wait, eight MMAs and one commit (ring
-    // position as a wrapping counter, descriptors as increments).
+  } else if (warp == 1 || warp == kQ8MmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads on different schedulers, one per accumulator (Linear1: gate
+    // and up; Linear2: the two 128-channel blocks); each does one wait, four
+    // MMAs and one commit per k-block (ring position as a wrapping counter,
+    // descriptors as increments).  The pace of this loop, not the tensor core,
+    // bounds the kernel at these shapes, hence the split.
     if (lane == 0) {
+      const int b = warp == 1 ? 0 : 1;
       int sl = 0;
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
       const uint64_t bd0 = smem_desc_sw128(codes0, 16, 1024);
       const uint32_t slot0 = tmem_base + kQ8Slot0;
+      const uint32_t dacc = tmem_base + kQ8Tok * b;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
         const TileInfo t = decode_tile(p, tile);
         const int rows = t.row_end - t.row0;
@@ -310,14 +316,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
           // (+2 in the descriptor's address field)
           const uint64_t bd = bd0 + static_cast<uint64_t>(sl * (kQ8CodeBytes >> 4));
           const uint32_t slot = slot0 + 64 * sl;
-          const uint32_t acc = kb != 0 ? 1u : 0u;
-          mma_f16_tmem_a(tmem_base, slot, bd, idesc, acc);
-          mma_f16_tmem_a(tmem_base + kQ8Tok, slot + 32, bd, idesc, acc);
+          mma_f16_tmem_a(dacc, slot + 32 * b, bd, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < kBK / 16; ++kk) {
-            mma_f16_tmem_a(tmem_base, slot + 8 * kk, bd + 2 * kk, idesc, 1u);
-            mma_f16_tmem_a(tmem_base + kQ8Tok, slot + 32 + 8 * kk, bd + 2 * kk, idesc, 1u);
-          }
+          for (int kk = 1; kk < kBK / 16; ++kk)
+            mma_f16_tmem_a(dacc, slot + 32 * b + 8 * kk, bd + 2 * kk, idesc, 1u);
           mma_commit(empty0 + 8 * sl);
           if (++sl == kQ8Slots) { sl = 0; ph ^= 1; }
         }
