@@ -10,16 +10,21 @@
 // pages' K-contiguous layout ([E, 2I, H] and [E, H, I]) with their scales
 // [E, N, K/32].
 //
-// Structure (one CTA per SM, 320 threads):
+// Structure (one CTA per SM, 352 threads):
 //   warp 0      TMA producer: A tile [128 rows x 128 k] and B tile
 //               [256 n x 128 k], both K-major with 128-byte swizzle (Linear1:
 //               128 gate rows of W1 and the matching 128 up rows; Linear2: 256
 //               rows of W2).  Linear1's A rows are the token codes already laid
 //               out in expert order by the quantisation kernel.
-//   warp 1      allocates TMEM (one 256-column accumulator and the scale slots
-//               of every stage); one lane copies the stage's scale atoms into
-//               TMEM (tcgen05.cp 32x128b.warpx4) and issues four MMAs
-//               (M 128, N 256, K 32) whose scale byte is the k step.
+//   warps 1, 10 MMA: warp 1 allocates TMEM (one 256-column accumulator and the
+//               scale slots of every stage); one lane of each takes one half of
+//               the accumulator (B rows 0..127 or 128..255): it copies the
+//               stage's A scale atom and its B scale atom into TMEM slots of its
+//               own (tcgen05.cp 32x128b.warpx4, ordered before its own MMAs)
+//               and issues four MMAs (M 128, N 128, K 32) whose scale byte is
+//               the k step.  Splitting the issue over two threads on different
+//               schedulers shortens the per-k-block issue path, which bounds the
+//               kernel when a k-block carries few weight bytes (E2M1).
 //   warps 2..5  epilogue (one accumulator row per thread).
 //   warps 6..9  per k-block, the 4 scale bytes of each of the 128 A rows and
 //               256 B rows into the stage's three 512-byte atoms (cp.async).
@@ -31,7 +36,8 @@
 // at byte (r % 32) * 16 + (r / 32) * 4.  Copied with warpx4, TMEM lane l then
 // holds rows l % 32 + 32 c in column c, which is where the MMA reads the scale
 // of A row m (lane m, column m / 32) and of B row n (lane n % 32 of each lane
-// quarter, column n / 32; rows 128..255 from the second atom, 4 columns on);
+// quarter, column n / 32 of the B slot of the MMA thread that owns row n: rows
+// 128..255 are rows 0..127 of the second B atom, in the second thread's slot);
 // the byte inside the word is the MMA's scale id.
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -55,10 +61,12 @@ constexpr int kMxBarBytes = 256;
 constexpr int kMxStgWords = 36;       // staging row pitch (32 data words + 4 pad)
 constexpr int kMxStg = 4 * 32 * kMxStgWords * 4;
 constexpr int kMxSmem = kMxRing + 1024 + kMxBarBytes + kMxStg;
-constexpr int kMxThreads = 320;
+constexpr int kMxThreads = 352;
+constexpr int kMxMmaWarp2 = 10;       // the second MMA thread's warp
 constexpr int kMxTmemCols = 512;
-constexpr int kMxSfCol = kMxBN;       // stage s: A scales at kMxSfCol + 12 s, B at + 4
-constexpr int kMxSfStride = 4 * kMxAtoms;
+// stage s, MMA thread b: A scales at kMxSfCol + 16 s + 8 b, its B scales 4 on
+constexpr int kMxSfCol = kMxBN;
+constexpr int kMxSfStride = 16;
 static_assert(kMxSfCol + kMxSfStride * kMxStages <= kMxTmemCols, "TMEM columns");
 static_assert(8 * (2 * kMxStages + 2) + 8 <= kMxBarBytes, "barrier area");
 static_assert(kMxSmem <= 232448, "shared memory");
@@ -204,9 +212,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // byte count) and each of the 128 row threads' copies have (one each)
     for (int s = 0; s < kMxStages; ++s) {
       mbar_init(full0 + 8 * s, 1 + 128);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 2);  // one commit per MMA thread
     }
-    mbar_init(tfull, 1);
+    mbar_init(tfull, 2);
     mbar_init(tempty, 128);
     *abort_flag = 0;
     fence_mbar_init();
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ row threads
     // Thread (gw, lane) copies the 4 scale bytes of A row r and of B rows r
     // and r + 128, r = 8 gw + lane / 4 + 32 (lane % 4), for each k-block: the
@@ -293,31 +301,31 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMxMmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN, AF, BF);
+      const int b = warp == 1 ? 0 : 1;  // accumulator half = B rows 128 b ..
+      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN / 2, AF, BF);
+      const uint32_t d = tmem_base + (kMxBN / 2) * b;
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
         if (!mbar_wait(tempty, (local & 1) ^ 1, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, p.status, abort_flag)) break;
           // the row threads' copies went through the generic proxy
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = tiles0 + stage * kMxStageBytes;
-          const uint32_t sb = sa + kMxA;
-          const uint32_t atoms = sb + kMxB;
-          const uint32_t tsa = tmem_base + kMxSfCol + kMxSfStride * stage;
+          const uint32_t sb = sa + kMxA + b * (kMxBN / 2) * kMxBK;
+          const uint32_t atoms = sa + kMxA + kMxB;
+          const uint32_t tsa = tmem_base + kMxSfCol + kMxSfStride * stage + 8 * b;
           const uint32_t tsb = tsa + 4;
-          // scale atoms -> TMEM; executes before the MMAs issued after it
-#pragma unroll
-          for (int a = 0; a < kMxAtoms; ++a)
-            tmem_cp_atom(tsa + 4 * a, smem_desc_plain(atoms + a * kMxAtom, 128, 128));
+          // scale atoms -> TMEM; executes before the MMAs this thread issues after it
+          tmem_cp_atom(tsa, smem_desc_plain(atoms, 128, 128));
+          tmem_cp_atom(tsb, smem_desc_plain(atoms + (1 + b) * kMxAtom, 128, 128));
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk) {
             // K-major rows of 128 B; a 32-wide k step is 32 B along the row
