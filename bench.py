@@ -332,7 +332,8 @@ def run_ours(args, rank, world, local_rank):
         g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=wb, act_bytes=ab)
     else:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
-        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T)
+        # the inference forward writes Linear2's rows in bf16
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, out_bytes=accounting.BF16)
     g1_flops = accounting.gemm1_flops(counts, H, I, has_shared, T)
     g2_flops = accounting.gemm2_flops(counts, H, I, has_shared, T)
     g1_s = stages["gemm1_swiglu_quant" if mx else "gemm1_swiglu"] / 1e3

@@ -45,11 +45,11 @@ def gemm1_bytes(counts, H, I, has_shared=0, T=0, w_bytes=BF16, x_bytes=BF16, act
     return n_active * H * 2 * I * w_bytes + rows * H * x_bytes + rows * I * act_bytes
 
 
-def gemm2_bytes(counts, H, I, has_shared=0, T=0, w_bytes=BF16, act_bytes=BF16):
+def gemm2_bytes(counts, H, I, has_shared=0, T=0, w_bytes=BF16, act_bytes=BF16, out_bytes=F32):
     """W2 of every active expert (I x H), Act rows in (bf16, or fp16 codes),
-    expert output rows out (fp32)."""
+    expert output rows out (fp32; bf16 in the bf16 inference forward)."""
     rows, n_active = _counts(counts, has_shared, T)
-    return n_active * I * H * w_bytes + rows * I * act_bytes + rows * H * F32
+    return n_active * I * H * w_bytes + rows * I * act_bytes + rows * H * out_bytes
 
 
 def dispatch_bytes(T, H, k):
@@ -64,10 +64,10 @@ def dispatch_payload_bytes(T, H, k):
     return T * k * H * BF16
 
 
-def combine_bytes(T, H, k, has_shared=0):
-    """k fp32 expert rows (+ the shared row) in, gates and row ids in, one bf16
-    row out."""
-    return (T * k + (T if has_shared else 0)) * H * F32 + T * k * (F32 + I32) + T * H * BF16
+def combine_bytes(T, H, k, has_shared=0, row_bytes=F32):
+    """k expert rows (+ the shared row; fp32, or bf16 in the bf16 inference
+    forward) in, gates and row ids in, one bf16 row out."""
+    return (T * k + (T if has_shared else 0)) * H * row_bytes + T * k * (F32 + I32) + T * H * BF16
 
 
 def route_bytes(T, H, E, k):
@@ -87,5 +87,6 @@ def layer_flops(counts, T, H, E, I, has_shared=0, with_router=True):
 
 def layer_bytes(counts, T, H, E, k, I, has_shared=0, with_router=True):
     b = (dispatch_bytes(T, H, k) + gemm1_bytes(counts, H, I, has_shared, T)
-         + gemm2_bytes(counts, H, I, has_shared, T) + combine_bytes(T, H, k, has_shared))
+         + gemm2_bytes(counts, H, I, has_shared, T, out_bytes=BF16)
+         + combine_bytes(T, H, k, has_shared, row_bytes=BF16))
     return b + (route_bytes(T, H, E, k) if with_router else 0)

@@ -424,7 +424,10 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     if ((e = launch_gemm(kGemmSwiGLU, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // Linear2:  Yp = Act W2[e] in fp32 (shared group uses Ws2)
+  // Linear2:  Yp = Act W2[e] (shared group uses Ws2), rounded to bf16 for the
+  // inference forward; the training forward keeps fp32 rows, which the
+  // backward's gate gradient reads
+  const bool yp_bf16 = h_out == nullptr;
   {
     GemmMaps maps;
     bool ok = make_map_rows(&maps.a, Act, A + Tsh, I) && make_map_weights(&maps.b, W2, E, I, H);
@@ -447,10 +450,13 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if ((e = launch_gemm(kGemmPlain, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_gemm(yp_bf16 ? kGemmPlainBf16 : kGemmPlain, maps, g, grid, s)) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
+  e = yp_bf16 ? launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k,
+                                    H, E, p->has_shared, Y, s)
+              : launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }

@@ -252,8 +252,21 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
 // ---------------------------------------------------------------------- combine
 constexpr int kCombineThreads = 128;
 
+// 8 consecutive elements of an expert output row (fp32 or bf16) as fp32.
+__device__ __forceinline__ void load_row8(const float* row, int c, float (&x)[8]) {
+  const float4* src = reinterpret_cast<const float4*>(row) + 2 * c;
+  const float4 u = __ldcs(src), v = __ldcs(src + 1);  // read once
+  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w; x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+}
+__device__ __forceinline__ void load_row8(const uint16_t* row, int c, float (&x)[8]) {
+  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(row) + c);
+  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+  x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+
+template <typename In>
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const float* __restrict__ Yp, const int* __restrict__ inv,
+    combine_kernel(const In* __restrict__ Yp, const int* __restrict__ inv,
                    const float* __restrict__ G, const int* __restrict__ row_off, int k, int H,
                    int E, int has_shared, uint16_t* __restrict__ Y) {
   __shared__ int rows[17];
@@ -277,11 +290,11 @@ __global__ void __launch_bounds__(kCombineThreads)
     for (int j = 0; j < n; ++j) {
       const int p = rows[j];
       if (p < 0) continue;
-      const float4* src = reinterpret_cast<const float4*>(Yp + static_cast<long long>(p) * H) + 2 * c;
-      const float4 u = __ldcs(src), v = __ldcs(src + 1);  // read once
+      float x[8];
+      load_row8(Yp + static_cast<long long>(p) * H, c, x);
       const float g = w[j];
-      acc[0] += g * u.x; acc[1] += g * u.y; acc[2] += g * u.z; acc[3] += g * u.w;
-      acc[4] += g * v.x; acc[5] += g * v.y; acc[6] += g * v.z; acc[7] += g * v.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += g * x[i];
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
@@ -295,7 +308,15 @@ __global__ void __launch_bounds__(kCombineThreads)
 cudaError_t launch_combine(const float* Yp, const int* inv, const float* G, const int* row_off,
                            int T, int k, int H, int E, int has_shared, uint16_t* Y, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  combine_kernel<<<T, kCombineThreads, 0, s>>>(Yp, inv, G, row_off, k, H, E, has_shared, Y);
+  combine_kernel<float><<<T, kCombineThreads, 0, s>>>(Yp, inv, G, row_off, k, H, E, has_shared, Y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bf16(const uint16_t* Yp, const int* inv, const float* G,
+                                const int* row_off, int T, int k, int H, int E, int has_shared,
+                                uint16_t* Y, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_kernel<uint16_t><<<T, kCombineThreads, 0, s>>>(Yp, inv, G, row_off, k, H, E, has_shared, Y);
   return cudaGetLastError();
 }
 

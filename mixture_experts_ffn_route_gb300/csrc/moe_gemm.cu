@@ -3,7 +3,7 @@
 // Serves the contractions of the layer:
 //   router     : logits[T, E] = X[T, H] Wg[H, E]                          (fp32 out)
 //   Linear1    : Act[rows, I] = SiLU(X_e W1[e][:, :I]) * (X_e W1[e][:, I:])   (bf16 out)
-//   Linear2    : Yp[rows, H]  = Act W2[e]                                  (fp32 out)
+//   Linear2    : Yp[rows, H]  = Act W2[e]                     (fp32 or bf16 out)
 // The expert FFN is the "Expert Compute" step of the "mega_moe" page
 // (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
 // projection); the router product is the
@@ -314,6 +314,36 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
           }
           __syncwarp();
         }
+      } else if (KIND == kGemmPlainBf16) {
+        // Linear2 rows rounded once to bf16 (RNE) for the combine
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld_32x32(tb + c, v);
+          const int col = t.n * BN + c;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kStgWords);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            srow4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          __syncwarp();
+          if (col < p.n_out) {
+            // 8 rows x 64 bytes per instruction: lane -> row rr + lane/4, quad lane%4
+            const int qd = lane & 3;
+#pragma unroll
+            for (int rr = 0; rr < 32; rr += 8) {
+              const int r = rr + (lane >> 2);
+              const uint4 x = reinterpret_cast<const uint4*>(stg + r * kStgWords)[qd];
+              const int grow = wrow0 + r;
+              if (grow < t.row_end)
+                *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 8 * qd) = x;
+            }
+          }
+          __syncwarp();
+        }
       } else {
         // fp32 outputs: router logits and Linear2
         float* out = static_cast<float*>(p.out);
@@ -500,7 +530,8 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
   switch (kind) {
     case kGemmRouter: return launch_one<kGemmRouter>(maps, p, grid, s);
     case kGemmSwiGLU: return launch_one<kGemmSwiGLU>(maps, p, grid, s);
-    default: return launch_one<kGemmPlain>(maps, p, grid, s);
+    case kGemmPlain: return launch_one<kGemmPlain>(maps, p, grid, s);
+    default: return launch_one<kGemmPlainBf16>(maps, p, grid, s);
   }
 }
 

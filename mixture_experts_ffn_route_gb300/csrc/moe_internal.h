@@ -14,7 +14,8 @@ constexpr int kBK = 64;   // GEMM k-block (one 128-byte swizzle row of bf16)
 enum GemmKind {
   kGemmRouter = 0,     // fp32 logits
   kGemmSwiGLU = 1,     // Linear1 + SwiGLU, bf16 out
-  kGemmPlain = 2       // Linear2, fp32 out
+  kGemmPlain = 2,      // Linear2, fp32 out
+  kGemmPlainBf16 = 3   // Linear2, bf16 out (the inference forward)
 };
 
 // One grouped GEMM launch.  Groups are row ranges [row_off[g], row_off[g+1])
@@ -196,6 +197,9 @@ int dispatch_chunks(int A);
 cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,
                             const DispatchBufs& b, int* status, cudaStream_t s);
 cudaError_t launch_combine(const float* Yp, const int* inv, const float* G,
+                           const int* row_off, int T, int k, int H, int E, int has_shared,
+                           uint16_t* Y, cudaStream_t s);
+cudaError_t launch_combine_bf16(const uint16_t* Yp, const int* inv, const float* G,
                            const int* row_off, int T, int k, int H, int E, int has_shared,
                            uint16_t* Y, cudaStream_t s);
 
