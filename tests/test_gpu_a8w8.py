@@ -87,3 +87,43 @@ def test_a8w8_full_size_sampled(name, n_rows):
     S2 = lambda e: dd["S2"][e].cpu().numpy()  # noqa: E731
     Y_ref = oracle.forward_a8w8_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E)
     check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
+
+
+# Ragged and degenerate shapes: one token, k = E, every token on one expert
+# (several 128-token tiles, the last partial, other experts empty), H and I
+# that are not multiples of 128 (partial channel tiles).
+EDGE_Q = [
+    dict(T=1, H=64, E=4, k=2, I=64),
+    dict(T=17, H=128, E=5, k=5, I=192),
+    dict(T=129, H=192, E=3, k=1, I=64),
+    dict(T=300, H=128, E=6, k=1, I=320, hot=True),
+    dict(T=260, H=320, E=9, k=3, I=448),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_Q, ids=lambda s: "T{T}_H{H}_E{E}_k{k}_I{I}".format(**s))
+def test_a8w8_edge_shapes(shape):
+    shape = dict(shape)
+    hot = shape.pop("hot", False)
+    h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0, quant="a8w8"), seed=99)
+    if hot:
+        h["E_ids"][:] = 0
+    c = h["cfg"]
+    dd = to_device(h)
+    p = params(c)
+    Y = _run(p, dd, dd["E_ids"], dd["G"])
+    Y_ref = oracle.forward_a8w8_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
+                                       h["W1"], h["S1"], h["W2"], h["S2"], E=c["E"])
+    check_y(Y, Y_ref, str(shape))
+
+
+def test_a8w8_with_no_tokens_writes_nothing():
+    h = synth.make_inputs("c3s_q")
+    dd = to_device(h)
+    p = params(h["cfg"], T=0)
+    ws = moe.alloc_workspace_a8w8(p, DEV)
+    Y = torch.full((4, h["cfg"]["H"]), 3.0, dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward_a8w8(p, dd["X"], dd["E_ids"] if "E_ids" in dd else dd["X"], dd["X"], dd["W1"], dd["S1"],
+                         dd["W2"], dd["S2"], Y, ws)
+    moe.moe_sync_status(ws)
+    assert (Y == 3.0).all()

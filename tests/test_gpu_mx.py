@@ -142,3 +142,44 @@ def test_mx_full_size_sampled(name, n_rows):
     Y_ref = oracle.forward_mx_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E, fmt=_fmt(c),
                                      wfmt=wf)
     check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
+
+
+# Ragged and degenerate shapes (H and I multiples of 128, as the MX forms
+# need): one token, k = E, every token on one expert (several 128-row tiles,
+# the last partial, other experts empty), for FP8 and FP4 weights.
+EDGE_MX = [
+    dict(T=1, H=128, E=4, k=2, I=128),
+    dict(T=17, H=256, E=5, k=5, I=128),
+    dict(T=300, H=128, E=6, k=1, I=256, hot=True),
+    dict(T=260, H=384, E=9, k=3, I=384),
+]
+
+
+@pytest.mark.parametrize("quant", ["mx_e4m3", "mx_e4m3_e2m1"])
+@pytest.mark.parametrize("shape", EDGE_MX, ids=lambda s: "T{T}_H{H}_E{E}_k{k}_I{I}".format(**s))
+def test_mx_edge_shapes(shape, quant):
+    shape = dict(shape)
+    hot = shape.pop("hot", False)
+    h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0, quant=quant), seed=99)
+    if hot:
+        h["E_ids"][:] = 0
+    c = h["cfg"]
+    dd = to_device(h)
+    p = params(c)
+    wf = _wfmt(c)
+    Y = _run(p, _fmt(c), dd, dd["E_ids"], dd["G"], wf)
+    Y_ref = oracle.forward_mx_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
+                                     _codes(h["W1"], wf), h["S1"], _codes(h["W2"], wf), h["S2"], E=c["E"],
+                                     fmt=_fmt(c), wfmt=wf)
+    check_y(Y, Y_ref, f"{shape} {quant}")
+
+
+def test_mx_with_no_tokens_writes_nothing():
+    h = synth.make_inputs("c2s_mx")
+    dd = to_device(h)
+    p = params(h["cfg"], T=0)
+    ws = moe.alloc_workspace_mx(p, DEV)
+    Y = torch.full((4, h["cfg"]["H"]), 3.0, dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward_mx(p, 0, dd["X"], dd["E_ids"], dd["G"], dd["W1"], dd["S1"], dd["W2"], dd["S2"], Y, ws)
+    moe.moe_sync_status(ws)
+    assert (Y == 3.0).all()
