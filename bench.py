@@ -324,12 +324,14 @@ def run_ours(args, rank, world, local_rank):
     pk = peaks()
     if quant:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=1, x_bytes=2, act_bytes=4)
-        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=1, act_bytes=2)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=1, act_bytes=2,
+                                          out_bytes=accounting.BF16)
     elif mx:
         ab = accounting.MX4 if mx == "e2m1" else accounting.MX8
         wb = accounting.MX4 if synth_mx_weight_format(c) == "e2m1" else accounting.MX8
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T, w_bytes=wb, x_bytes=ab, act_bytes=ab)
-        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=wb, act_bytes=ab)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, w_bytes=wb, act_bytes=ab,
+                                          out_bytes=accounting.BF16)
     else:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
         # the inference forward writes Linear2's rows in bf16

@@ -571,7 +571,8 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     g.n_tiles = (H + 255) / 256;
     g.num_kb = I / kBK;
     g.n_out = H;
-    g.out = Yp;
+    g.out = Yp;  // bf16 rows
+    g.out_bf16 = 1;
     g.ldo = H;
     g.scale_col = S2;
     g.scale_ld = H;
@@ -582,7 +583,7 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     if (launch_gemm_q8(false, mw, mb, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
+  e = launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }
@@ -883,7 +884,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     if (launch_gemm_mx(true, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // Linear2 on the re-quantised SwiGLU rows, fp32 out
+  // Linear2 on the re-quantised SwiGLU rows, bf16 rows out
   {
     GemmMaps maps;
     if (!make_map_mx_rows(&maps.a, Uq, A, I, a4) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256, w4))
@@ -900,6 +901,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.num_kb = I / kMxBK;
     g.n_out = H;
     g.out = Yp;
+    g.out_bf16 = 1;
     g.ldo = H;
     g.sfa = SU;
     g.sfb = S2;
@@ -911,7 +913,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     if (launch_gemm_mx(false, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
+  e = launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k, H, E, 0, Y, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }

@@ -4,7 +4,7 @@
 //
 //   Linear1: Z = DQ(Xq_e) DQ(W1[e])^T, U = Z_g * sigma(Z_g) * Z_u, and U
 //            re-quantised per 32 columns: FP8 codes + E8M0 scales out
-//   Linear2: O = DQ(Uq) DQ(W2[e])^T, fp32 out
+//   Linear2: O = DQ(Uq) DQ(W2[e])^T, bf16 (or fp32) out
 // These are the stages GMM1 + SwiGLU + MX quantisation and GMM2 of the MXFP
 // scenario on the "mega_moe" page (section 计算过程).  The weights keep the
 // pages' K-contiguous layout ([E, 2I, H] and [E, H, I]) with their scales
@@ -410,6 +410,40 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sc);
         }
         __syncwarp();
+      } else if (p.out_bf16) {
+        // rows rounded once to bf16 (RNE) for the combine
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < kMxBN; c += 32) {
+          float v[32];
+          tmem_ld_32x32(tb + c, v);
+          if (c + 32 == kMxBN) {
+            tc_fence_before();
+            mbar_arrive(tempty);
+          }
+          const int col = t.n * kMxBN + c;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kMxStgWords);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            srow4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          __syncwarp();
+          // 8 rows x 64 bytes per store instruction
+          const int qd = lane & 3;
+          if (col < p.n_out) {
+#pragma unroll
+            for (int rr = 0; rr < 32; rr += 8) {
+              const int r = rr + (lane >> 2);
+              const uint4 x = reinterpret_cast<const uint4*>(stg + r * kMxStgWords)[qd];
+              const int grow = wrow0 + r;
+              if (grow < t.row_end)
+                *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 8 * qd) = x;
+            }
+          }
+          __syncwarp();
+        }
       } else {
         float* out = static_cast<float*>(p.out);
 #pragma unroll 1

@@ -6,6 +6,7 @@
 //            the matching up channels I + c; epilogue Act[m][c] = SiLU(Hg) * Hu
 //            with H = (D * s1[c]) * sx[m] (fp32 out, re-quantised per row later)
 //   Linear2: D[h][m] = sum_k W2q[e][h][k] a8[m][k]; Yp[m][h] = (D * s2[h]) * sa[m]
+//            (bf16 or fp32 out)
 //
 // GB300's tensor cores have no int8 form for sm_103a, so the int8 codes are
 // multiplied as fp16: |code| <= 127 is exact in fp16, a product is exact in
@@ -381,6 +382,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             const float hg = (a[i] * s0) * sr;
             const float hu = (b[i] * s1) * sr;
             if (in0) out[static_cast<long long>(row) * p.ldo + c0] = __fdividef(hg, 1.0f + __expf(-hg)) * hu;
+          } else if (p.out_bf16) {
+            // rows rounded once to bf16 (RNE) for the combine
+            uint16_t* o16 = static_cast<uint16_t*>(p.out) + static_cast<long long>(row) * p.ldo;
+            if (in0) o16[c0] = __bfloat16_as_ushort(__float2bfloat16_rn((a[i] * s0) * sr));
+            if (in1) o16[c1] = __bfloat16_as_ushort(__float2bfloat16_rn((b[i] * s1) * sr));
           } else {
             if (in0) out[static_cast<long long>(row) * p.ldo + c0] = (a[i] * s0) * sr;
             if (in1) out[static_cast<long long>(row) * p.ldo + c1] = (b[i] * s1) * sr;

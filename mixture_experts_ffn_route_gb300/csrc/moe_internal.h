@@ -64,6 +64,9 @@ struct GemmParams {
   // Linear1 (bf16): when set, the pre-activations (gate and up halves, bf16)
   // are also written to h_out [rows, 2 up_off], kept for the backward
   uint16_t* h_out;
+  // Linear2 of the quantised forms: 1 = write the rows to out as bf16 (RNE)
+  // instead of fp32
+  int out_bf16;
 };
 
 struct GemmMaps {
