@@ -542,9 +542,10 @@ def run_train(args, rank, world, local_rank):
 
 def load_traffic(workload, algorithmic_bytes):
     """DRAM bytes of one Linear1 launch from the committed ncu summaries: for
-    c3, the full-size capture itself (the mean of two launches); for c4 (the
-    same expert shapes and load recipe) that capture scaled by the ratio of
-    algorithmic bytes; for c3p its own small-size capture."""
+    c3, c3_mx and c3_q, the full-size captures themselves (the mean of two
+    launches); for c4 (the same expert shapes and load recipe) the c3 capture
+    scaled by the ratio of algorithmic bytes; for c3p its own small-size
+    capture."""
     import re
     if workload in ("c3", "c4"):
         path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
@@ -557,12 +558,13 @@ def load_traffic(workload, algorithmic_bytes):
             return None
         t = int(m.group(1))
         return t if workload == "c3" else int(t * algorithmic_bytes / c3_alg)
-    if workload == "c3_mx":
+    if workload in ("c3_mx", "c3_q"):
         path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
         if not os.path.exists(path):
             return None
+        key = "c3mx" if workload == "c3_mx" else "c3q"
         with open(path) as f:
-            m = re.search(r"dram_bytes_per_launch_c3mx_gemm1:\s*([0-9]+)", f.read())
+            m = re.search(r"dram_bytes_per_launch_%s_gemm1:\s*([0-9]+)" % key, f.read())
         return int(m.group(1)) if m else None
     if workload == "c3p":
         path = os.path.join(ROOT, "profiles", "gemm1_swiglu_c3p.md")
