@@ -814,6 +814,12 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
   const bool a4 = fmt == MOE_MX_E2M1, w4 = wfmt == MOE_MX_E2M1;
   if (p->has_shared) return MOE_ERR_UNSUPPORTED;
   if (p->H % kMxBK != 0 || p->I % kMxBK != 0) return MOE_ERR_UNSUPPORTED;
+  // E2M1 x E2M1 runs kind::mxf4 on packed tiles when both K dims fill whole
+  // 256-code k-blocks; otherwise kind::mxf8f6f4 on spread tiles
+  const bool packed = a4 && w4 && p->H % kMxBKPacked == 0 && p->I % kMxBKPacked == 0;
+  const int la = packed ? kMxFp4Packed : (a4 ? kMxFp4Spread : kMxFp8);
+  const int lw = packed ? kMxFp4Packed : (w4 ? kMxFp4Spread : kMxFp8);
+  const int kbk = packed ? kMxBKPacked : kMxBK;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
       ws_bytes < layout_mx(*p).total)
     return MOE_ERR_WORKSPACE;
@@ -856,7 +862,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
   // Linear1 + SwiGLU + Q_MX on the token codes in expert order
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Xq, A, H, a4) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 128, w4))
+    if (!make_map_mx_rows(&maps.a, Xq, A, H, la) || !make_map_mx_weights(&maps.b, W1, E, 2LL * I, H, 128, lw))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -867,7 +873,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.num_groups = E;
     g.shared_group = -1;
     g.n_tiles = (I + 127) / 128;
-    g.num_kb = H / kMxBK;
+    g.num_kb = H / kbk;
     g.n_out = I;
     g.up_off = I;
     g.out = Uq;
@@ -881,13 +887,13 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm_mx(true, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_mx(true, fmt, wfmt, packed, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // Linear2 on the re-quantised SwiGLU rows, bf16 rows out
   {
     GemmMaps maps;
-    if (!make_map_mx_rows(&maps.a, Uq, A, I, a4) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256, w4))
+    if (!make_map_mx_rows(&maps.a, Uq, A, I, la) || !make_map_mx_weights(&maps.b, W2, E, H, I, 256, lw))
       return MOE_ERR_CUDA;
     maps.a2 = maps.a;
     maps.b2 = maps.b;
@@ -898,7 +904,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.num_groups = E;
     g.shared_group = -1;
     g.n_tiles = (H + 255) / 256;
-    g.num_kb = I / kMxBK;
+    g.num_kb = I / kbk;
     g.n_out = H;
     g.out = Yp;
     g.out_bf16 = 1;
@@ -910,7 +916,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm_mx(false, fmt, wfmt, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_mx(false, fmt, wfmt, packed, maps, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k, H, E, 0, Y, s);

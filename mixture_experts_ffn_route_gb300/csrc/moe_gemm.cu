@@ -432,36 +432,44 @@ bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows, cols] FP8 codes (bytes, cols contiguous), box = 128 columns x 128
-// rows, 128-byte swizzle.
-bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool fp4) {
+// MX codes, [rows, cols] (cols contiguous): one 128-byte row segment per box
+// row, 128 rows, 128-byte swizzle.  kMxFp8: bytes; kMxFp4Spread: packed E2M1
+// spread by the map type to 16 codes per 16 bytes of shared memory (the box
+// counts codes); kMxFp4Packed: the packed bytes as they are.
+static CUtensorMapDataType mx_map_type(int layout) {
+  return layout == kMxFp4Spread ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+}
+
+bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int layout) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(fp4 ? cols / 2 : cols)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(kBM)};
+  const bool packed = layout == kMxFp4Packed;
+  const int64_t row_bytes = layout == kMxFp8 ? cols : cols / 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(packed ? row_bytes : cols),
+                        static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(packed ? 128 : kMxBK), static_cast<cuuint32_t>(kBM)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-            const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, mx_map_type(layout), 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [groups, N, K] FP8 codes (K contiguous), box = 128 k x box_rows n x 1,
-// 128-byte swizzle: the K-major B tiles of the MX forms.
+// MX weight codes [groups, N, K] (K contiguous), box = one 128-byte row
+// segment x box_rows n x 1, 128-byte swizzle: the K-major B tiles.
 bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K,
-                         int box_rows, bool fp4) {
+                         int box_rows, int layout) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+  const bool packed = layout == kMxFp4Packed;
+  const int64_t rb = layout == kMxFp8 ? K : K / 2;  // bytes per weight row
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(packed ? rb : K), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(groups)};
-  const int64_t rb = fp4 ? K / 2 : K;  // bytes per weight row
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N * rb)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kMxBK), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(packed ? 128 : kMxBK), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-            const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, mx_map_type(layout), 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -53,7 +53,11 @@ constexpr int kMxBN = 256;
 constexpr int kMxA = kBM * kMxBK;     // 16 KB
 constexpr int kMxB = kMxBN * kMxBK;   // 32 KB
 constexpr int kMxAtom = 512;          // 128 rows x 4 scale bytes
-constexpr int kMxAtoms = 1 + kMxBN / 128;
+// scale words per row per k-block: 1 (a k-block of 128 codes), or 2 for the
+// packed E2M1 x E2M1 form (kind::mxf4, a k-block of 256 codes in the same
+// 128-byte rows); a stage holds that many A atoms and B atoms per 128 B rows
+constexpr int kMxWordsMax = 2;
+constexpr int kMxAtoms = kMxWordsMax * (1 + kMxBN / 128);
 constexpr int kMxStageBytes = ((kMxA + kMxB + kMxAtoms * kMxAtom + 1023) / 1024) * 1024;
 constexpr int kMxStages = 4;
 constexpr int kMxRing = kMxStages * kMxStageBytes;
@@ -64,9 +68,10 @@ constexpr int kMxSmem = kMxRing + 1024 + kMxBarBytes + kMxStg;
 constexpr int kMxThreads = 352;
 constexpr int kMxMmaWarp2 = 10;       // the second MMA thread's warp
 constexpr int kMxTmemCols = 512;
-// stage s, MMA thread b: A scales at kMxSfCol + 16 s + 8 b, its B scales 4 on
+// stage s, MMA thread b, scale word w: A scales at kMxSfCol + 32 s + 16 b + 4 w,
+// its B scales 8 on
 constexpr int kMxSfCol = kMxBN;
-constexpr int kMxSfStride = 16;
+constexpr int kMxSfStride = 32;
 static_assert(kMxSfCol + kMxSfStride * kMxStages <= kMxTmemCols, "TMEM columns");
 static_assert(8 * (2 * kMxStages + 2) + 8 <= kMxBarBytes, "barrier area");
 static_assert(kMxSmem <= 232448, "shared memory");
@@ -107,6 +112,21 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= (A * sA)(B * sB)^T with packed E2M1 A, B (two codes per byte,
+// even element in the low nibble), K 64, and two E8M0 scales per row (one per
+// 32 codes) read from bytes sid and sid + 1 of the row's scale word.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor of the block-scaled kind: bits 4-5 B scale id,
 // 7-9 A format, 10-12 B format (0 = E4M3, 1 = E5M2, 5 = E2M1), 15/16 A/B major
 // (0 = K-major), 17-22 N >> 3, 23 scale type (1 = E8M0), 24-28 M >> 4,
@@ -115,6 +135,9 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t afmt, uin
   return (afmt << 7) | (bfmt << 10) | ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
+// kind::mxf4: E2M1 is format 1 for both operands (probe-confirmed: all-ones
+// tiles and random codes against a CPU product)
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) { return idesc_mx(M, N, 1, 1); }
 __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
   return (a_id << 29) | (b_id << 4);
 }
@@ -187,10 +210,13 @@ __device__ __forceinline__ uint32_t mx_group(const float (&v)[32], uint32_t (&w)
   return static_cast<uint32_t>(X + 127);
 }
 
-template <bool SWIGLU, int AF, int BF>
+template <bool SWIGLU, int AF, int BF, bool PACKED>
 __global__ void __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
+  static_assert(!PACKED || (AF == 5 && BF == 5), "the packed form is E2M1 x E2M1");
+  constexpr int WORDS = PACKED ? 2 : 1;        // scale words per row per k-block
+  constexpr int KBX = PACKED ? 128 : kMxBK;   // TMA x step per k-block: bytes, or codes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -242,9 +268,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = tiles0 + stage * kMxStageBytes;
           const uint32_t sb = sa + kMxA;
-          const int kx = kb * kMxBK;
-          // an E2M1 tile arrives as half as many bytes as it fills
-          mbar_arrive_expect_tx(fb, (MxFmt<AF>::FP4 ? kMxA / 2 : kMxA) + (MxFmt<BF>::FP4 ? kMxB / 2 : kMxB));
+          const int kx = kb * KBX;
+          // an unpacked E2M1 tile arrives as half as many bytes as it fills;
+          // a packed one fills its tile
+          if (PACKED)
+            mbar_arrive_expect_tx(fb, kMxA + kMxB);
+          else
+            mbar_arrive_expect_tx(fb, (MxFmt<AF>::FP4 ? kMxA / 2 : kMxA) + (MxFmt<BF>::FP4 ? kMxB / 2 : kMxB));
           tma_load_2d(sa, &tmA, fb, kx, t.row0);
           if (SWIGLU) {
             tma_load_3d(sb, &tmB, fb, kx, t.n * 128, t.group);
@@ -292,10 +322,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         const uint32_t atoms = tiles0 + stage * kMxStageBytes + kMxA + kMxB;
-        if (sfa_src != nullptr) cp_async4(atoms + atom_off, sfa_src + kb * 4);
+        // word w of the k-block's scales: A atom w, B atoms WORDS (1 + h) + w
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (sfb_src[h] != nullptr) cp_async4(atoms + (1 + h) * kMxAtom + atom_off, sfb_src[h] + kb * 4);
+        for (int w = 0; w < WORDS; ++w) {
+          const int off = (kb * WORDS + w) * 4;
+          if (sfa_src != nullptr) cp_async4(atoms + w * kMxAtom + atom_off, sfa_src + off);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (sfb_src[h] != nullptr)
+              cp_async4(atoms + (WORDS * (1 + h) + w) * kMxAtom + atom_off, sfb_src[h] + off);
+        }
         cp_async_arrive(full0 + 8 * stage);
         if (++stage == kMxStages) { stage = 0; phase ^= 1; }
       }
@@ -305,7 +341,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const int b = warp == 1 ? 0 : 1;  // accumulator half = B rows 128 b ..
-      constexpr uint32_t idesc = idesc_mx(kBM, kMxBN / 2, AF, BF);
+      constexpr uint32_t idesc = PACKED ? idesc_mxf4(kBM, kMxBN / 2) : idesc_mx(kBM, kMxBN / 2, AF, BF);
       const uint32_t d = tmem_base + (kMxBN / 2) * b;
       int stage = 0;
       uint32_t phase = 0;
@@ -321,17 +357,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sa = tiles0 + stage * kMxStageBytes;
           const uint32_t sb = sa + kMxA + b * (kMxBN / 2) * kMxBK;
           const uint32_t atoms = sa + kMxA + kMxB;
-          const uint32_t tsa = tmem_base + kMxSfCol + kMxSfStride * stage + 8 * b;
-          const uint32_t tsb = tsa + 4;
+          const uint32_t tsa = tmem_base + kMxSfCol + kMxSfStride * stage + 16 * b;
+          const uint32_t tsb = tsa + 8;
           // scale atoms -> TMEM; executes before the MMAs this thread issues after it
-          tmem_cp_atom(tsa, smem_desc_plain(atoms, 128, 128));
-          tmem_cp_atom(tsb, smem_desc_plain(atoms + (1 + b) * kMxAtom, 128, 128));
 #pragma unroll
-          for (int kk = 0; kk < kMxBK / 32; ++kk) {
-            // K-major rows of 128 B; a 32-wide k step is 32 B along the row
+          for (int w = 0; w < WORDS; ++w) {
+            tmem_cp_atom(tsa + 4 * w, smem_desc_plain(atoms + w * kMxAtom, 128, 128));
+            tmem_cp_atom(tsb + 4 * w, smem_desc_plain(atoms + (WORDS * (1 + b) + w) * kMxAtom, 128, 128));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // K-major rows of 128 B; a k step (32 FP8 codes, or 64 packed E2M1
+            // codes) is 32 B along the row
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
-            mma_mx(d, ad, bd, idesc | idesc_sf_ids(kk, kk), tsa, tsb, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            if (PACKED) {
+              // two groups of 32 per MMA: scale bytes 2 (kk % 2) and + 1 of word kk / 2
+              const uint32_t w = static_cast<uint32_t>(kk >> 1), sid = 2u * static_cast<uint32_t>(kk & 1);
+              mma_mxf4(d, ad, bd, idesc | idesc_sf_ids(sid, sid), tsa + 4 * w, tsb + 4 * w, acc);
+            } else {
+              mma_mx(d, ad, bd, idesc | idesc_sf_ids(kk, kk), tsa, tsb, acc);
+            }
           }
           mma_commit(empty0 + 8 * stage);
           if (++stage == kMxStages) { stage = 0; phase ^= 1; }
@@ -538,9 +585,9 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <bool SWIGLU, int AF, int BF>
+template <bool SWIGLU, int AF, int BF, bool PACKED = false>
 cudaError_t launch_mx(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  auto kern = gemm_mx_kernel<SWIGLU, AF, BF>;
+  auto kern = gemm_mx_kernel<SWIGLU, AF, BF, PACKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kMxThreads, kMxSmem, s>>>(m.a, m.b, p);
@@ -548,8 +595,9 @@ cudaError_t launch_mx(const GemmMaps& m, const GemmParams& p, int grid, cudaStre
 }
 
 template <bool SWIGLU>
-cudaError_t launch_mx_pair(int afmt, int bfmt, const GemmMaps& m, const GemmParams& p, int grid,
-                           cudaStream_t s) {
+cudaError_t launch_mx_pair(int afmt, int bfmt, bool packed, const GemmMaps& m, const GemmParams& p,
+                           int grid, cudaStream_t s) {
+  if (packed) return afmt == 5 && bfmt == 5 ? launch_mx<SWIGLU, 5, 5, true>(m, p, grid, s) : cudaErrorInvalidValue;
   if (afmt == 0 && bfmt == 0) return launch_mx<SWIGLU, 0, 0>(m, p, grid, s);
   if (afmt == 1 && bfmt == 1) return launch_mx<SWIGLU, 1, 1>(m, p, grid, s);
   if (afmt == 0 && bfmt == 5) return launch_mx<SWIGLU, 0, 5>(m, p, grid, s);
@@ -564,11 +612,11 @@ bool mx_pair_supported(int afmt, int bfmt) {
   return (afmt == bfmt && (afmt == 0 || afmt == 1 || afmt == 5)) || ((afmt == 0 || afmt == 1) && bfmt == 5);
 }
 
-cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, const GemmMaps& maps, const GemmParams& p,
-                           int grid, cudaStream_t s) {
+cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, bool packed, const GemmMaps& maps,
+                           const GemmParams& p, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  return swiglu ? launch_mx_pair<true>(afmt, bfmt, maps, p, grid, s)
-                : launch_mx_pair<false>(afmt, bfmt, maps, p, grid, s);
+  return swiglu ? launch_mx_pair<true>(afmt, bfmt, packed, maps, p, grid, s)
+                : launch_mx_pair<false>(afmt, bfmt, packed, maps, p, grid, s);
 }
 
 cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols, uint8_t* codes,

@@ -93,20 +93,26 @@ cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_
 // inv[t k + j] instead of row t.
 cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols, uint8_t* codes,
                                  uint8_t* scales, const int* inv, int k, cudaStream_t s);
-// [rows, cols] codes, box 128 columns x 128 rows, 128-byte swizzle; the
-// weights [groups, N, K] as a 3-D map with box 128 k x box_rows n x 1.  With
-// fp4 the codes are packed E2M1 and the map type spreads them to the MMA's
-// shared-memory layout (16 codes per 16 bytes).
-bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool fp4);
+// [rows, cols] codes, box of one 128-byte row segment x 128 rows, 128-byte
+// swizzle; the weights [groups, N, K] as a 3-D map with box 128 bytes x
+// box_rows n x 1.  Layouts: kMxFp8 one code per byte (box 128 codes);
+// kMxFp4Spread packed E2M1 in memory, which the map type spreads to the
+// shared-memory layout of kind::mxf8f6f4 (16 codes per 16 bytes, box 128
+// codes); kMxFp4Packed packed E2M1 kept packed for kind::mxf4 (box 256 codes).
+enum MxLayout { kMxFp8 = 0, kMxFp4Spread = 1, kMxFp4Packed = 2 };
+bool make_map_mx_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int layout);
 bool make_map_mx_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K,
-                         int box_rows, bool fp4);
-// Linear1 (SwiGLU, re-quantised to the activation format) or Linear2 (fp32
-// out); A rows in expert order (map a), their scales at sfa.  K must be a
-// multiple of 128.  afmt / bfmt: activation / weight formats.
+                         int box_rows, int layout);
+// Linear1 (SwiGLU, re-quantised to the activation format) or Linear2 (bf16 or
+// fp32 out); A rows in expert order (map a), their scales at sfa.  K must be a
+// multiple of 128 (of kMxBKPacked when packed).  afmt / bfmt: activation /
+// weight formats; packed (E2M1 x E2M1 only): kind::mxf4 on packed tiles, maps
+// of layout kMxFp4Packed, p.num_kb = K / kMxBKPacked.
 bool mx_pair_supported(int afmt, int bfmt);
-cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, const GemmMaps& maps, const GemmParams& p,
-                           int grid, cudaStream_t s);
-constexpr int kMxBK = 128;  // MX k-block: 128 FP8 codes (one 128-byte swizzle row) = 4 groups
+cudaError_t launch_gemm_mx(bool swiglu, int afmt, int bfmt, bool packed, const GemmMaps& maps,
+                           const GemmParams& p, int grid, cudaStream_t s);
+constexpr int kMxBK = 128;        // MX k-block: 128 FP8 codes (one 128-byte swizzle row) = 4 groups
+constexpr int kMxBKPacked = 256;  // packed E2M1 k-block: 256 codes in the same row = 8 groups
 
 // Backward GEMMs (bf16 operands, fp32 accumulation).  Groups split the rows
 // (M) as in the forward (row_off / tile_off, shared group on map b2), or, for
