@@ -150,12 +150,14 @@ def test_mx_full_size_sampled(name, n_rows):
 EDGE_MX = [
     dict(T=1, H=128, E=4, k=2, I=128),
     dict(T=17, H=256, E=5, k=5, I=128),
-    dict(T=300, H=128, E=6, k=1, I=256, hot=True),
+    dict(T=300, H=256, E=6, k=1, I=256, hot=True),
     dict(T=260, H=384, E=9, k=3, I=384),
 ]
 
 
-@pytest.mark.parametrize("quant", ["mx_e4m3", "mx_e4m3_e2m1"])
+# mx_e2m1 takes the packed kind::mxf4 path where H and I are multiples of 256
+# (the T=300 shape) and the spread kind::mxf8f6f4 path elsewhere
+@pytest.mark.parametrize("quant", ["mx_e4m3", "mx_e4m3_e2m1", "mx_e2m1"])
 @pytest.mark.parametrize("shape", EDGE_MX, ids=lambda s: "T{T}_H{H}_E{E}_k{k}_I{I}".format(**s))
 def test_mx_edge_shapes(shape, quant):
     shape = dict(shape)
