@@ -48,6 +48,7 @@ WORKLOAD_TEXT = {
     "c2_mx": "given-routing layer, MXFP8 form (E4M3)",
     "c3p_mx": "V4-Pro expert shapes, T=512 E=48, MXFP8 form (profiling size)",
     "c3p_q": "V4-Pro expert shapes, T=512 E=48, A8W8-INT form (profiling size)",
+    "c3p_mxa4": "V4-Pro expert shapes, T=512 E=48, A4W4-FP form (profiling size)",
     "c3_mx4": "V4-Pro-shaped layer, A8W4-FP form (E4M3 activations, E2M1 weights, E8M0 scales), no shared expert",
     "c3_mxa4": "V4-Pro-shaped layer, A4W4-FP form (E2M1 activations and weights), no shared expert",
     "c2_mx4": "given-routing layer, A8W4-FP form",
@@ -542,7 +543,7 @@ def run_train(args, rank, world, local_rank):
 
 def load_traffic(workload, algorithmic_bytes):
     """DRAM bytes of one Linear1 launch from the committed ncu summaries: for
-    c3, c3_mx and c3_q, the full-size captures themselves (the mean of two
+    c3, c3_mx, c3_mxa4 and c3_q, the full-size captures themselves (the mean of two
     launches); for c4 (the same expert shapes and load recipe) the c3 capture
     scaled by the ratio of algorithmic bytes; for c3p its own small-size
     capture."""
@@ -558,11 +559,11 @@ def load_traffic(workload, algorithmic_bytes):
             return None
         t = int(m.group(1))
         return t if workload == "c3" else int(t * algorithmic_bytes / c3_alg)
-    if workload in ("c3_mx", "c3_q"):
+    if workload in ("c3_mx", "c3_q", "c3_mxa4"):
         path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
         if not os.path.exists(path):
             return None
-        key = "c3mx" if workload == "c3_mx" else "c3q"
+        key = {"c3_mx": "c3mx", "c3_q": "c3q", "c3_mxa4": "c3mxa4"}[workload]
         with open(path) as f:
             m = re.search(r"dram_bytes_per_launch_%s_gemm1:\s*([0-9]+)" % key, f.read())
         return int(m.group(1)) if m else None

@@ -109,6 +109,7 @@ CONFIGS["c3_mxa4"] = dict(CONFIGS["c3_mx"], quant="mx_e2m1")
 CONFIGS["c3p"] = dict(_BASE, T=512, H=7168, E=48, k=6, I=2048, shared=1, alpha=2.5, bias=True)
 CONFIGS["c3p_mx"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e4m3")
 CONFIGS["c3p_q"] = dict(CONFIGS["c3p"], shared=0, quant="a8w8")
+CONFIGS["c3p_mxa4"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e2m1")
 # the V4-Pro router at full size with a token-sized FFN (I = 64): a workload
 # whose routing kernels one ncu capture can take (1.1 GB of weights)
 CONFIGS["c3r"] = dict(CONFIGS["c3"], I=64)
