@@ -18,13 +18,15 @@
 // converted by one thread straight into its TMEM lane with tcgen05.st, which
 // the MMA reads as A (row m in lane m, element k in column k / 2).
 //
-// Structure (one CTA per SM, 608 threads).  Two rings run on one running
+// Structure (one CTA per SM, 608 threads).  Three rings run on one running
 // k-block index per CTA: the int8 weight rows in shared memory (eight deep,
 // freed as soon as they are converted, so the weight stream runs well ahead),
-// and the operand stages (four deep): a TMEM slot of converted weights plus the
-// shared-memory tile of token codes, made ready by one barrier and released by
-// two MMA commits.  The MMA threads' own work per k-block (one wait, four MMAs,
-// one commit each) bounds the kernel at these shapes, so it is kept to that.
+// the TMEM slots of converted weights (four) and the shared-memory tiles of
+// token codes (five: the codes' latency, not the MMAs, set the pace with four).
+// A k-block is made ready by one barrier, its code stage's, on which both the
+// converters and the code loaders arrive, and released by one, on which the
+// code loaders and (kQ8Slots k-blocks later) the converters wait, so each MMA
+// thread does one wait, four MMAs and one commit per k-block.
 //   warp 0       TMA: int8 weight rows, two blocks of 128 rows x 64 k per k-block
 //                (Linear1: gate rows and the matching up rows; Linear2: 256
 //                output channels)
@@ -50,12 +52,15 @@ constexpr int kQ8Tok = 128;                      // tokens per tile (largest MMA
 constexpr int kQ8RawBytes = 2 * 128 * kBK;       // int8 weight rows of a k-block: 16 KB
 constexpr int kQ8CodeBytes = kQ8Tok * kBK * 2;   // fp16 token codes of a k-block: 16 KB
 constexpr int kQ8RawStages = 8;
-constexpr int kQ8Slots = 4;                      // operand stages = TMEM weight slots
-constexpr int kQ8CodeStages = kQ8Slots;
+constexpr int kQ8Slots = 4;                      // TMEM weight slots
+// token-code stages: deeper than the slots, since the codes' latency (gathered
+// rows or TMA, ~1.3 us under the weight stream) sets the pace otherwise; a
+// k-block's "ready" barrier is the code stage's
+constexpr int kQ8CodeStages = 5;
 constexpr int kQ8ConvGroups = 2;
 constexpr int kQ8CodeRing = kQ8CodeStages * kQ8CodeBytes;  // first: 1024-aligned for the swizzle
 constexpr int kQ8Ring = kQ8CodeRing + kQ8RawStages * kQ8RawBytes;
-constexpr int kQ8Bars = 2 * (kQ8RawStages + kQ8Slots) + 2;
+constexpr int kQ8Bars = 2 * kQ8RawStages + 2 * kQ8CodeStages + 2;
 constexpr int kQ8BarBytes = 512;
 constexpr int kQ8ScaleBytes = 4 * kQ8Tok * 4;    // per epilogue warp: the tile's token scales
 constexpr int kQ8Smem = kQ8Ring + 1024 + kQ8BarBytes + kQ8ScaleBytes;
@@ -66,6 +71,14 @@ static_assert(kQ8Slot0 + 64 * kQ8Slots <= 512, "TMEM columns");
 static_assert(8 * kQ8Bars + 8 <= kQ8BarBytes, "barrier area");
 static_assert(kQ8Smem <= 232448, "shared memory");
 static_assert(kQ8Slots % kQ8ConvGroups == 0, "a slot belongs to one converter group");
+// A TMEM slot's previous user, k-block it - kQ8Slots, signals its end on its
+// code stage's release barrier, so the converters wait there (no barrier of
+// the slots' own).  That wait cannot alias: the next completion of the same
+// barrier is the MMAs of k-block it - kQ8Slots + kQ8CodeStages > it - 1, which
+// need this converter's slot first.  And the converter of k-block
+// it + kQ8CodeStages, which waits for the MMAs of it + kQ8CodeStages - kQ8Slots
+// >= it, never arrives on a ready barrier whose previous phase is still open.
+static_assert(kQ8CodeStages >= kQ8Slots, "code ring at least as deep as the slots");
 
 // 4 int8 (one 32-bit word) -> 4 fp16, exactly: with b = x + 128 in [0, 255],
 // the fp16 bit pattern 0x6400 | b is 1024 + b, and subtracting 1152 leaves x.
@@ -127,9 +140,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
   const uint32_t raw0 = codes0 + kQ8CodeRing;
   const uint32_t rawfull0 = smem_u32(bar_area);                // weight rows landed
   const uint32_t rawempty0 = rawfull0 + 8 * kQ8RawStages;      // weight rows converted
-  const uint32_t full0 = rawempty0 + 8 * kQ8RawStages;         // TMEM slot written, codes landed
-  const uint32_t empty0 = full0 + 8 * kQ8Slots;                // the stage's MMAs are done
-  const uint32_t tfull = empty0 + 8 * kQ8Slots;
+  const uint32_t full0 = rawempty0 + 8 * kQ8RawStages;         // k-block ready: slot written, codes landed
+  const uint32_t cempty0 = full0 + 8 * kQ8CodeStages;          // the k-block's MMAs are done
+  const uint32_t tfull = cempty0 + 8 * kQ8CodeStages;
   const uint32_t tempty = tfull + 8;
 
   if (threadIdx.x == 0) {
@@ -137,10 +150,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
       mbar_init(rawfull0 + 8 * s, 1);
       mbar_init(rawempty0 + 8 * s, 128);
     }
-    for (int s = 0; s < kQ8Slots; ++s) {
+    for (int s = 0; s < kQ8CodeStages; ++s) {
       // converters, and the gather threads or the codes' TMA
       mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 1));
-      mbar_init(empty0 + 8 * s, 2);  // one commit per MMA thread
+      mbar_init(cempty0 + 8 * s, 2);  // one commit per MMA thread
     }
     mbar_init(tfull, 2);
     mbar_init(tempty, 128);
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
           const uint32_t st = ring_stage(it, kQ8CodeStages);
           bool w = true;
           if (lane == 0)
-            w = mbar_wait(empty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag);
+            w = mbar_wait(cempty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag);
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
           const uint32_t sb = codes0 + st * kQ8CodeBytes;
 #pragma unroll
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         const TileInfo t = decode_tile(p, tile);
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t st = ring_stage(it, kQ8CodeStages);
-          if (!mbar_wait(empty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag)) {
+          if (!mbar_wait(cempty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -256,8 +269,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         const uint32_t sl = ring_stage(it, kQ8Slots);
         bool w = true;
         if (lane == 0)
-          w = mbar_wait(rawfull0 + 8 * rs, ring_phase(it, kQ8RawStages), p.status, abort_flag) &&
-              mbar_wait(empty0 + 8 * sl, ring_phase(it, kQ8Slots) ^ 1, p.status, abort_flag);
+          w = mbar_wait(rawfull0 + 8 * rs, ring_phase(it, kQ8RawStages), p.status, abort_flag);
+          if (w && it >= static_cast<unsigned>(kQ8Slots)) {
+            // the slot's previous user, k-block it - kQ8Slots, is done
+            const unsigned j = it - kQ8Slots;
+            w = mbar_wait(cempty0 + 8 * ring_stage(j, kQ8CodeStages), ring_phase(j, kQ8CodeStages), p.status,
+                          abort_flag);
+          }
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         tc_fence_after();
         const uint8_t* sw = smem + kQ8CodeRing + rs * kQ8RawBytes;
@@ -279,7 +297,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         mbar_arrive(rawempty0 + 8 * rs);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
-        mbar_arrive(full0 + 8 * sl);
+        mbar_arrive(full0 + 8 * ring_stage(it, kQ8CodeStages));
       }
     }
   } else if (warp == 1 || warp == kQ8MmaWarp2) {
@@ -291,8 +309,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     // bounds the kernel at these shapes, hence the split.
     if (lane == 0) {
       const int b = warp == 1 ? 0 : 1;
-      int sl = 0;
-      uint32_t ph = 0;
+      int sl = 0, cs = 0;   // TMEM slot and code stage of the k-block
+      uint32_t ph = 0;      // phase of the code stage's ready barrier
       int local = 0;
       bool ok = true;
       const uint64_t bd0 = smem_desc_sw128(codes0, 16, 1024);
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         if (!mbar_wait(tempty, (local & 1) ^ 1, p.status, abort_flag)) break;
         tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(full0 + 8 * sl, ph, p.status, abort_flag)) {
+          if (!mbar_wait(full0 + 8 * cs, ph, p.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -315,14 +333,15 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
           tc_fence_after();
           // B: the token codes, K-major rows of 128 B; a 16-wide k step is 32 B
           // (+2 in the descriptor's address field)
-          const uint64_t bd = bd0 + static_cast<uint64_t>(sl * (kQ8CodeBytes >> 4));
+          const uint64_t bd = bd0 + static_cast<uint64_t>(cs * (kQ8CodeBytes >> 4));
           const uint32_t slot = slot0 + 64 * sl;
           mma_f16_tmem_a(dacc, slot + 32 * b, bd, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 1; kk < kBK / 16; ++kk)
             mma_f16_tmem_a(dacc, slot + 32 * b + 8 * kk, bd + 2 * kk, idesc, 1u);
-          mma_commit(empty0 + 8 * sl);
-          if (++sl == kQ8Slots) { sl = 0; ph ^= 1; }
+          mma_commit(cempty0 + 8 * cs);
+          if (++sl == kQ8Slots) sl = 0;
+          if (++cs == kQ8CodeStages) { cs = 0; ph ^= 1; }
         }
         if (!ok) break;
         mma_commit(tfull);
