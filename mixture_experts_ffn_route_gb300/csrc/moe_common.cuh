@@ -78,6 +78,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
                                           volatile int* abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
+#pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
