@@ -246,6 +246,33 @@ def run_ours(args, rank, world, local_rank):
         moe.moe_sync_status(dd["_ws_q"])
     ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world, dev)
 
+    # optionally, the same step captured once in a CUDA graph and replayed K
+    # times (what a launch-bound small batch gains from it)
+    graph_ms = None
+    if args.graph:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            plain_step()
+        torch.cuda.current_stream().wait_stream(gs)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            plain_step()
+        for _ in range(args.warmup):
+            graph.replay()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(K):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        moe.moe_sync_status(ws)
+        graph_ms = max_over_ranks(g0.elapsed_time(g1) / K, world, dev)
+
     def avg(evs, a, b):
         return sum(e[a].elapsed_time(e[b]) for e in evs) / len(evs)
     stages = {"dispatch": avg(st_ev, 0, 1), "gemm1_swiglu": avg(st_ev, 1, 2),
@@ -406,6 +433,9 @@ def run_ours(args, rank, world, local_rank):
         "load": {"max_expert_rows": int(counts.max()), "min_expert_rows": int(counts.min()),
                  "active_experts": int((counts > 0).sum())},
     }
+    if graph_ms is not None:
+        out["graph_replay"] = {"ms_per_step": round(graph_ms, 4),
+                               "value": round(T * world / (graph_ms / 1e3), 1), "unit": UNIT}
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(dd, budget_s=args.cpu_budget)
     return out
@@ -700,6 +730,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once in a CUDA graph and replayed")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (route + forward + backward) instead of the forward")
     args = ap.parse_args(argv)
