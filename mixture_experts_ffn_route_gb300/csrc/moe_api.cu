@@ -884,6 +884,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.sfb = S1;
     g.sf_ld = H / 32;
     g.sfb_ld = 2LL * I * (H / 32);
+    g.sf_vec = (g.sf_ld % 16 == 0 && g.sfb_ld % 16 == 0 && aligned16(g.sfa) && aligned16(g.sfb)) ? 1 : 0;
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
@@ -913,6 +914,7 @@ moe_status moe_forward_mx(const moe_params* p, int32_t fmt, int32_t wfmt, const 
     g.sfb = S2;
     g.sf_ld = I / 32;
     g.sfb_ld = static_cast<long long>(H) * (I / 32);
+    g.sf_vec = (g.sf_ld % 16 == 0 && g.sfb_ld % 16 == 0 && aligned16(g.sfa) && aligned16(g.sfb)) ? 1 : 0;
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ row threads
-    // Thread (gw, lane) copies the 4 scale bytes of A row r and of B rows r
+    // Thread (gw, lane) places the scale word(s) of A row r and of B rows r
     // and r + 128, r = 8 gw + lane / 4 + 32 (lane % 4), for each k-block: the
     // 32 lanes of a warp then write 32 consecutive words of an atom.  A rows
     // past the group's end and B rows past the output's end are not copied:
@@ -297,45 +297,116 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int gw = warp - 6;
     const int sr = 8 * gw + (lane >> 2) + 32 * (lane & 3);
     const uint32_t atom_off = static_cast<uint32_t>(128 * gw + 4 * lane);
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+    // this thread's scale rows in a tile: A row sr, B rows sr and sr + 128
+    // (Linear1: 128 gate rows, then the matching up rows); nullptr past the
+    // group's end or the output's end
+    auto row_ptrs = [&](int tile, const uint8_t* (&src)[3]) {
       const TileInfo t = decode_tile(p, tile);
       const int row = t.row0 + sr;
-      const uint8_t* sfa_src =
-          row < t.row_end ? p.sfa + static_cast<long long>(row) * p.sf_ld : nullptr;
-      const uint8_t* sfb_src[2];
+      src[0] = row < t.row_end ? p.sfa + static_cast<long long>(row) * p.sf_ld : nullptr;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        // B row sr + 128 h of the tile: Linear1 holds 128 gate rows, then the
-        // matching up rows
         const int c = SWIGLU ? t.n * 128 + sr : t.n * kMxBN + 128 * h + sr;
         const int nr = SWIGLU ? (h == 0 ? c : p.up_off + c) : c;
-        sfb_src[h] = c < p.n_out
-                         ? p.sfb + t.group * p.sfb_ld + static_cast<long long>(nr) * p.sf_ld
-                         : nullptr;
+        src[1 + h] = c < p.n_out ? p.sfb + t.group * p.sfb_ld + static_cast<long long>(nr) * p.sf_ld
+                                 : nullptr;
       }
-      bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        const uint32_t atoms = tiles0 + stage * kMxStageBytes + kMxA + kMxB;
-        // word w of the k-block's scales: A atom w, B atoms WORDS (1 + h) + w
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    if (p.sf_vec) {
+      // Scale rows are whole 16-byte chunks (4 FP8 k-blocks, or 2 packed
+      // ones): each is loaded once into registers, a chunk ahead of its use
+      // and across tiles, and each k-block's words are stored into the atoms.
+      // A quarter of the 4-byte gathers' requests, and their latency is off
+      // the stage's path.
+      constexpr int KPC = 4 / WORDS;  // k-blocks per chunk
+      const int nchunks = p.num_kb / KPC;
+      int ltile = blockIdx.x, lchunk = 0;  // load cursor
+      const uint8_t* lsrc[3] = {nullptr, nullptr, nullptr};
+      if (ltile < total) row_ptrs(ltile, lsrc);
+      auto load_next = [&](uint4 (&v)[3]) {
 #pragma unroll
-        for (int w = 0; w < WORDS; ++w) {
-          const int off = (kb * WORDS + w) * 4;
-          if (sfa_src != nullptr) cp_async4(atoms + w * kMxAtom + atom_off, sfa_src + off);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            if (sfb_src[h] != nullptr)
-              cp_async4(atoms + (WORDS * (1 + h) + w) * kMxAtom + atom_off, sfb_src[h] + off);
+        for (int i = 0; i < 3; ++i)
+          v[i] = (ltile < total && lsrc[i] != nullptr)
+                     ? __ldg(reinterpret_cast<const uint4*>(lsrc[i] + 16 * lchunk))
+                     : make_uint4(0u, 0u, 0u, 0u);
+        if (++lchunk == nchunks) {
+          lchunk = 0;
+          ltile += gridDim.x;
+          if (ltile < total) row_ptrs(ltile, lsrc);
         }
-        cp_async_arrive(full0 + 8 * stage);
-        if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+      };
+      auto word = [](const uint4& v, int i) -> uint32_t {
+        return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+      };
+      uint4 cur[3], nxt[3];
+      load_next(cur);
+      load_next(nxt);
+      bool fresh = true, ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+        const uint8_t* src[3];
+        row_ptrs(tile, src);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          const int j = kb % KPC;
+          if (j == 0) {
+            if (!fresh) {
+#pragma unroll
+              for (int i = 0; i < 3; ++i) cur[i] = nxt[i];
+              load_next(nxt);
+            }
+            fresh = false;
+          }
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+          uint8_t* atoms = smem + stage * kMxStageBytes + kMxA + kMxB;
+#pragma unroll
+          for (int w2 = 0; w2 < WORDS; ++w2) {
+            const int wi = j * WORDS + w2;
+            if (src[0] != nullptr)
+              *reinterpret_cast<uint32_t*>(atoms + w2 * kMxAtom + atom_off) = word(cur[0], wi);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (src[1 + h] != nullptr)
+                *reinterpret_cast<uint32_t*>(atoms + (WORDS * (1 + h) + w2) * kMxAtom + atom_off) =
+                    word(cur[1 + h], wi);
+          }
+          // the tcgen05.cp that reads the atoms goes through the async proxy
+          fence_proxy_async_smem();
+          mbar_arrive(full0 + 8 * stage);
+          if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+        }
       }
-      if (!ok) break;
+    } else {
+      // Scale rows that are not whole 16-byte chunks: 4-byte cp.async per row
+      // and k-block, each thread arriving when its copies have landed.
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
+        const uint8_t* src[3];
+        row_ptrs(tile, src);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, abort_flag);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+          const uint32_t atoms = tiles0 + stage * kMxStageBytes + kMxA + kMxB;
+          // word w of the k-block's scales: A atom w, B atoms WORDS (1 + h) + w
+#pragma unroll
+          for (int w2 = 0; w2 < WORDS; ++w2) {
+            const int off = (kb * WORDS + w2) * 4;
+            if (src[0] != nullptr) cp_async4(atoms + w2 * kMxAtom + atom_off, src[0] + off);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (src[1 + h] != nullptr)
+                cp_async4(atoms + (WORDS * (1 + h) + w2) * kMxAtom + atom_off, src[1 + h] + off);
+          }
+          cp_async_arrive(full0 + 8 * stage);
+          if (++stage == kMxStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
     }
   } else if (warp == 1 || warp == kMxMmaWarp2) {
     // ------------------------------------------------------------ MMA issuers

@@ -61,6 +61,7 @@ struct GemmParams {
   long long sfb_ld;
   uint8_t* out_sf;
   int out_sf_ld;
+  int sf_vec;        // 1: sf_ld, sfb_ld and both scale bases are 16-byte multiples
   // Linear1 (bf16): when set, the pre-activations (gate and up halves, bf16)
   // are also written to h_out [rows, 2 up_off], kept for the backward
   uint16_t* h_out;
