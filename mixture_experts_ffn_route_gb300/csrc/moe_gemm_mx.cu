@@ -235,9 +235,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
   if (threadIdx.x == 0) {
     // a stage is complete when the TMA bytes have landed (one arrival with the
-    // byte count) and each of the 128 row threads' copies have (one each)
+    // byte count) and the row threads' scales have: one arrival per row warp
+    // (chunked loads) or per row thread (4-byte copies)
     for (int s = 0; s < kMxStages; ++s) {
-      mbar_init(full0 + 8 * s, 1 + 128);
+      mbar_init(full0 + 8 * s, 1 + (p.sf_vec ? 4 : 128));
       mbar_init(empty0 + 8 * s, 2);  // one commit per MMA thread
     }
     mbar_init(tfull, 2);
@@ -373,9 +374,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 *reinterpret_cast<uint32_t*>(atoms + (WORDS * (1 + h) + w2) * kMxAtom + atom_off) =
                     word(cur[1 + h], wi);
           }
-          // the tcgen05.cp that reads the atoms goes through the async proxy
+          // the tcgen05.cp that reads the atoms goes through the async proxy;
+          // one arrival per warp once all its lanes have written and fenced
           fence_proxy_async_smem();
-          mbar_arrive(full0 + 8 * stage);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * stage);
           if (++stage == kMxStages) { stage = 0; phase ^= 1; }
         }
       }
