@@ -81,8 +81,8 @@ static WsLayoutQ layout_a8w8(const moe_params& p) {
   L.tile_off = take((E + 2) * sizeof(int));
   L.perm = take(A * sizeof(int));
   L.inv = take(A * sizeof(int));
-  L.xq = take(T * H * 2);
-  L.sx = take(T * sizeof(float));
+  L.xq = take(A * H * 2);          // token codes in expert order (one row per assignment)
+  L.sx = take(A * sizeof(float));
   L.act = take(A * I * sizeof(float));
   L.aq = take(A * I * 2);
   L.sa = take(A * sizeof(float));
@@ -524,24 +524,20 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
 
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = launch_dispatch(E_ids, T, k, E, 0, b, status, s);
-  if (e == cudaSuccess) e = launch_quant_rows_bf16(X, T, H, Xq, sX, s);
+  if (e == cudaSuccess) e = launch_quant_rows_bf16(X, T, H, Xq, sX, b.inv, k, s);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // Linear1: C = Q_e W1q[e]^T (token codes gathered by the permutation),
+  // Linear1: C = Q_e W1q[e]^T on the token codes in expert order (TMA),
   // dequantised, SwiGLU, fp32 out; the weights are the MMA's A operand in TMEM
   {
-    CUtensorMap mw;
-    if (!make_map_i8_rows(&mw, W1q, E, 2LL * I, H)) return MOE_ERR_CUDA;
+    CUtensorMap mw, mb;
+    if (!make_map_rows(&mb, Xq, A, H) || !make_map_i8_rows(&mw, W1q, E, 2LL * I, H)) return MOE_ERR_CUDA;
     GemmParams g;
     memset(&g, 0, sizeof(g));
     g.row_off = b.row_off;
     g.tile_off = b.tile_off;
     g.num_groups = E;
     g.shared_group = -1;
-    g.gather_src = Xq;
-    g.gather_perm = b.perm;
-    g.gather_k = k;
-    g.gather_rows = T;
     g.n_tiles = (I + 127) / 128;
     g.num_kb = H / kBK;
     g.n_out = I;
@@ -554,7 +550,7 @@ moe_status moe_forward_a8w8(const moe_params* p, const uint16_t* X, const int32_
     g.status = status;
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if (launch_gemm_q8(true, mw, mw, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm_q8(true, mw, mb, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // per-row re-quantisation of the SwiGLU output, then Linear2

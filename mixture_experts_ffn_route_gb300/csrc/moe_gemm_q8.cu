@@ -35,9 +35,9 @@
 //                each issues tcgen05.mma (M 128, N = the tile's token count
 //                rounded up to 16, K 16, A from TMEM) into its own accumulator
 //   warps 2..5   epilogue: thread = output channel, looping over the tile's tokens
-//   warps 6..9   token codes, K-major with 128-byte swizzle: Linear1 gathers the
-//                rows by the permutation (cp.async); Linear2 loads the tile of
-//                expert-ordered rows by TMA (one lane of warp 6)
+//   warp 6       token codes: the tile of expert-ordered code rows (the token
+//                quantiser writes each token's codes to its k rows) by TMA, K-major
+//                with 128-byte swizzle, for Linear1 and Linear2 alike
 //   warps 10..17 converters, two groups of four taking alternate k-blocks: thread
 //                j turns row j of both weight blocks (64 int8 each) into 32
 //                words of fp16 pairs in the k-block's TMEM slot
@@ -53,9 +53,9 @@ constexpr int kQ8RawBytes = 2 * 128 * kBK;       // int8 weight rows of a k-bloc
 constexpr int kQ8CodeBytes = kQ8Tok * kBK * 2;   // fp16 token codes of a k-block: 16 KB
 constexpr int kQ8RawStages = 8;
 constexpr int kQ8Slots = 4;                      // TMEM weight slots
-// token-code stages: deeper than the slots, since the codes' latency (gathered
-// rows or TMA, ~1.3 us under the weight stream) sets the pace otherwise; a
-// k-block's "ready" barrier is the code stage's
+// token-code stages: deeper than the slots, since the codes' latency (~1.3 us
+// under the weight stream) sets the pace otherwise; a k-block's "ready"
+// barrier is the code stage's
 constexpr int kQ8CodeStages = 5;
 constexpr int kQ8ConvGroups = 2;
 constexpr int kQ8CodeRing = kQ8CodeStages * kQ8CodeBytes;  // first: 1024-aligned for the swizzle
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
       mbar_init(rawempty0 + 8 * s, 128);
     }
     for (int s = 0; s < kQ8CodeStages; ++s) {
-      // converters, and the gather threads or the codes' TMA
-      mbar_init(full0 + 8 * s, 128 + (SWIGLU ? 128 : 1));
+      // converters, and the codes' TMA
+      mbar_init(full0 + 8 * s, 128 + 1);
       mbar_init(cempty0 + 8 * s, 2);  // one commit per MMA thread
     }
     mbar_init(tfull, 2);
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
-    if (!SWIGLU) tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
@@ -196,44 +196,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
   } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ token codes
-    if (SWIGLU) {
-      // Linear1: the tile's 128 token rows (row r -> token perm[r] / k),
-      // 16-byte cp.async chunks, eight lanes per 128-byte row segment; rows
-      // past the group's end are not copied (their stale products reach
-      // accumulator columns that are never stored).
-      const int gw = warp - 6;
-      const int c = lane & 7;
-      const int rq = lane >> 3;
-      const long long ld = static_cast<long long>(p.num_kb) * kBK;
-      unsigned it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo t = decode_tile(p, tile);
-        int tok[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = t.row0 + 32 * gw + 4 * i + rq;
-          tok[i] = row < t.row_end ? __ldg(p.gather_perm + row) / p.gather_k : -1;
-        }
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-          const uint32_t st = ring_stage(it, kQ8CodeStages);
-          bool w = true;
-          if (lane == 0)
-            w = mbar_wait(cempty0 + 8 * st, ring_phase(it, kQ8CodeStages) ^ 1, p.status, abort_flag);
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-          const uint32_t sb = codes0 + st * kQ8CodeBytes;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 32 * gw + 4 * i + rq;
-            if (tok[i] >= 0)
-              cp_async16(sb + r * 128 + ((c ^ (r & 7)) << 4), p.gather_src + tok[i] * ld + kb * kBK + c * 8);
-          }
-          cp_async_arrive(full0 + 8 * st);
-        }
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 6 && lane == 0) {
-      // Linear2: the tile of expert-ordered rows [128 x 64] by TMA
+    // One lane of warp 6 loads the tile of expert-ordered code rows [128 x 64]
+    // by TMA (rows past the group's end are the next group's or zero fill:
+    // their products reach accumulator columns that are never stored); warps
+    // 7..9 have no role (the converters' warp numbers fix their TMEM quarters).
+    if (warp == 6 && lane == 0) {
       unsigned it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -328,8 +295,6 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             ok = false;
             break;
           }
-          // the gather warps' copies went through the generic proxy
-          if (SWIGLU) fence_proxy_async_smem();
           tc_fence_after();
           // B: the token codes, K-major rows of 128 B; a 16-wide k step is 32 B
           // (+2 in the descriptor's address field)
@@ -366,8 +331,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
       for (int i = 0; i < kQ8Tok / 32; ++i) {
         const int row = t.row0 + 32 * i + lane;
         float s = 0.0f;
-        if (row < t.row_end)
-          s = SWIGLU ? __ldg(p.scale_row + __ldg(p.gather_perm + row) / p.gather_k) : __ldg(p.scale_row + row);
+        if (row < t.row_end) s = __ldg(p.scale_row + row);
         sc[32 * i + lane] = s;
       }
       __syncwarp();

@@ -81,8 +81,10 @@ bool make_map_weights(CUtensorMap* m, const void* base, int64_t groups, int64_t 
 // Per-row int8 quantisation ("mega_moe" A8W8): s = max|x| / 127 and codes
 // round(x / s) (halves away from zero), written as fp16 values.  rows_dev,
 // when set, gives the row count on the device (rows is then an upper bound).
+// With inv (k <= 16), row t's codes and scale go to rows inv[t * k + j] of the
+// outputs (the token rows in expert order), each token quantised once.
 cudaError_t launch_quant_rows_bf16(const uint16_t* x, int rows, int cols, uint16_t* codes,
-                                   float* scales, cudaStream_t s);
+                                   float* scales, const int* inv, int k, cudaStream_t s);
 cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_max, int cols,
                                   uint16_t* codes, float* scales, cudaStream_t s);
 
@@ -165,10 +167,10 @@ cudaError_t launch_router_bwd(const float* logits, const int32_t* E_ids, const f
 // (moe_gemm_q8.cu).  w: int8 weight rows [groups, N, K] (K contiguous), box
 // 64 k x 128 rows x 1, 64-byte swizzle (the 16-byte chunk c of row r lands at
 // chunk c ^ ((r >> 1) & 3), so that a warp reading one row per thread hits
-// every bank once); b (Linear2 only): fp16 codes [rows, K] as
-// make_map_rows.  Linear1 gathers the token codes (gather_src / gather_perm).
-// p.scale_col / scale_ld: per-channel weight scales; p.scale_row: token
-// (Linear1) or row (Linear2) scales; p.out fp32 [rows, ldo].
+// every bank once); b: fp16 codes [rows, K] in expert order (one row per
+// assignment) as make_map_rows.  p.scale_col / scale_ld: per-channel weight
+// scales; p.scale_row: per-row activation scales; p.out [rows, ldo], fp32 (or
+// bf16 for Linear2 with p.out_bf16).
 bool make_map_i8_rows(CUtensorMap* m, const void* base, int64_t groups, int64_t N, int64_t K);
 cudaError_t launch_gemm_q8(bool swiglu, const CUtensorMap& w, const CUtensorMap& b,
                            const GemmParams& p, int grid, cudaStream_t s);

@@ -39,13 +39,26 @@ __device__ __forceinline__ uint32_t code_pair(float a, float b, float s) {
 template <typename In>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_rows_kernel(const In* __restrict__ x, const int* __restrict__ rows_dev, int rows_max,
-                      int cols, uint16_t* __restrict__ codes, float* __restrict__ scales) {
+                      int cols, uint16_t* __restrict__ codes, float* __restrict__ scales,
+                      const int* __restrict__ inv, int k) {
   const int rows = rows_dev != nullptr ? *rows_dev : rows_max;
   const int lane = threadIdx.x & 31;
   const int vecs = cols / 8;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
     const In* row = x + static_cast<long long>(r) * cols;
+    // destination rows: r itself, or with inv the k rows of token r in expert
+    // order (dropped assignments, inv = -1, skipped)
+    int dst[16];
+    int ndst = 1;
+    dst[0] = r;
+    if (inv != nullptr) {
+      ndst = 0;
+      for (int j = 0; j < k; ++j) {
+        const int d = __ldg(inv + static_cast<long long>(r) * k + j);
+        if (d >= 0) dst[ndst++] = d;
+      }
+    }
     float amax = 0.0f;
     for (int v = lane; v < vecs; v += 32) {
       float e[8];
@@ -55,14 +68,16 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     }
     amax = warp_max_f(amax);
     const float s = __fdiv_rn(amax, 127.0f);
-    uint4* out = reinterpret_cast<uint4*>(codes + static_cast<long long>(r) * cols);
     for (int v = lane; v < vecs; v += 32) {
       float e[8];
       load8(row, v, e);
-      out[v] = make_uint4(code_pair(e[0], e[1], s), code_pair(e[2], e[3], s),
-                          code_pair(e[4], e[5], s), code_pair(e[6], e[7], s));
+      const uint4 c = make_uint4(code_pair(e[0], e[1], s), code_pair(e[2], e[3], s),
+                                 code_pair(e[4], e[5], s), code_pair(e[6], e[7], s));
+      for (int d = 0; d < ndst; ++d)
+        reinterpret_cast<uint4*>(codes + static_cast<long long>(dst[d]) * cols)[v] = c;
     }
-    if (lane == 0) scales[r] = s;
+    if (lane == 0)
+      for (int d = 0; d < ndst; ++d) scales[dst[d]] = s;
   }
 }
 
@@ -73,18 +88,19 @@ static int quant_grid(int rows) {
 }
 
 cudaError_t launch_quant_rows_bf16(const uint16_t* x, int rows, int cols, uint16_t* codes,
-                                   float* scales, cudaStream_t s) {
+                                   float* scales, const int* inv, int k, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  if (inv != nullptr && (k < 1 || k > 16)) return cudaErrorInvalidValue;
   quant_rows_kernel<uint16_t><<<quant_grid(rows), kQuantWarps * 32, 0, s>>>(x, nullptr, rows, cols,
-                                                                             codes, scales);
+                                                                             codes, scales, inv, k);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_max, int cols,
                                   uint16_t* codes, float* scales, cudaStream_t s) {
   if (rows_max <= 0) return cudaSuccess;
-  quant_rows_kernel<float><<<quant_grid(rows_max), kQuantWarps * 32, 0, s>>>(x, rows_dev, rows_max,
-                                                                             cols, codes, scales);
+  quant_rows_kernel<float><<<quant_grid(rows_max), kQuantWarps * 32, 0, s>>>(
+      x, rows_dev, rows_max, cols, codes, scales, nullptr, 0);
   return cudaGetLastError();
 }
 
