@@ -126,9 +126,14 @@ moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* coun
  *   W1   [E, H, 2I]  bf16   Linear1; columns [0, I) gate, [I, 2I) up
  *   W2   [E, I, H]   bf16   Linear2
  *   Ws1  [H, 2I], Ws2 [I, H]  bf16 shared expert (has_shared = 1), else NULL
- *   Y    [T, H]      bf16   out; float32 accumulation, one rounding
+ *   Y    [T, H]      bf16   out
+ * Precision: float32 accumulation in both GEMMs and in the combine; the SwiGLU
+ * rows and each expert's output rows are kept in bf16 (round to nearest even)
+ * between the kernels, and Y is rounded to bf16 once at the end.
  * Every step (dispatch, Linear1 with SwiGLU, Linear2, combine) runs in this
- * library's kernels, with no host synchronisation. */
+ * library's kernels, with no host synchronisation: sizes come from device
+ * memory, so a call (with moe_route before it) can be captured in a CUDA graph
+ * and replayed. */
 moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_ids,
                        const float* G, const uint16_t* W1, const uint16_t* W2,
                        const uint16_t* Ws1, const uint16_t* Ws2, uint16_t* Y, void* ws,
