@@ -175,8 +175,8 @@ size_t moe_workspace_size_a8w8(const moe_params* p);
  *   (nearest integer, halves away from zero; float32);
  *   per expert: C = Q_e W1q[e]^T (int32), H = (C * S1[e]) * s^X,
  *   A = SiLU(H[:, :I]) * H[:, I:], each row of A re-quantised the same way
- *   (s^A, A8), D = A8 W2q[e]^T (int32), Y_e = (D * S2[e]) * s^A;
- *   y_t = sum_j G[t, j] Y[row(t, j)].
+ *   (s^A, A8), D = A8 W2q[e]^T (int32), Y_e = (D * S2[e]) * s^A kept in bf16;
+ *   y_t = sum_j G[t, j] Y[row(t, j)] (fp32 sum, bf16 out).
  *   The weights keep the operator's layout, one row per output channel with
  *   K contiguous (rows 0..I-1 of W1q are the SiLU branch):
  *   W1q [E, 2I, H] int8, S1 [E, 2I] fp32 (per output channel)
@@ -275,7 +275,8 @@ size_t moe_workspace_size_mx(const moe_params* p);
  *   (Xq, SX) = Q_MX(X) per token row (see moe_quantize_mx);
  *   per expert e with rows R_e: Z = DQ(Xq[R_e]) DQ(W1[e])^T [n_e, 2I];
  *   U = Z[:, :I] * sigmoid(Z[:, :I]) * Z[:, I:]; (Uq, SU) = Q_MX(U);
- *   O = DQ(Uq) DQ(W2[e])^T [n_e, H];  y_t = sum_j G[t, j] O[row(t, j)] (bf16).
+ *   O = DQ(Uq) DQ(W2[e])^T [n_e, H], kept in bf16;
+ *   y_t = sum_j G[t, j] O[row(t, j)] (fp32 sum, bf16 out).
  * DQ multiplies each code by its group's scale 2^(code - 127).
  *   W1 [E, 2I, H] codes (H contiguous; E2M1 packed: [E, 2I, H / 2] bytes;
  *      the first I rows are the SiLU branch), S1 [E, 2I, H / 32] E8M0 codes:
@@ -284,8 +285,12 @@ size_t moe_workspace_size_mx(const moe_params* p);
  *   W2 [E, H, I] codes (E2M1: [E, H, I / 2] bytes), S2 [E, H, I / 32];
  *   X [T, H] bf16, E_ids [T, k], G [T, k] fp32, Y [T, H] bf16 out.
  * H and I must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise); S1 and
- * S2 must be 4-byte aligned, the other pointers 16-byte aligned.  The
- * products run on the block-scaled FP8 tensor cores with fp32 accumulation.
+ * S2 must be 4-byte aligned, the other pointers 16-byte aligned (scales at
+ * 16-byte aligned addresses whose rows are 16-byte multiples, H and I
+ * multiples of 512, are read in wider chunks).  The products run on the
+ * block-scaled tensor cores with fp32 accumulation: kind::mxf8f6f4, or
+ * kind::mxf4 on packed tiles for E2M1 x E2M1 when H and I are multiples of
+ * 256.
  * stage_events: NULL, or 5 caller-created cudaEvent_t recorded at: start,
  * after dispatch and token quantisation, after Linear1 (+ SwiGLU and
  * re-quantisation), after Linear2, after combine. */
