@@ -87,10 +87,13 @@ __device__ int block_exclusive_scan(int v, int* out, int* warp_tot) {
 // Single block.  After it: chunk_cnt[c][e] = rows of expert e in chunks < c;
 // counts[e]; row_off[e] (exclusive, row_off[E] = valid assignments); tile_off.
 // With a shared expert, group E is the T shared rows placed after all
-// routed rows: counts[E] = T, row_off[E + 1] = row_off[E] + T.
+// routed rows: counts[E] = T, row_off[E + 1] = row_off[E] + T.  With tile_doff
+// set, tile_doff and tile_soff are the same running count of row tiles taken
+// over the groups of at least dense_mt row tiles and over the rest.
 __global__ void __launch_bounds__(kThreads)
     dispatch_scan_kernel(int* __restrict__ chunk_cnt, int nchunk, int E, int T, int has_shared,
-                         int* __restrict__ counts, int* __restrict__ row_off, int* __restrict__ tile_off) {
+                         int* __restrict__ counts, int* __restrict__ row_off, int* __restrict__ tile_off,
+                         int* __restrict__ tile_doff, int* __restrict__ tile_soff, int dense_mt) {
   __shared__ int warp_tot[32];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
@@ -104,27 +107,46 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   // exclusive scans over experts, kThreads experts per pass
-  int row_carry = 0, tile_carry = 0;
+  const bool split = tile_doff != nullptr;
+  int row_carry = 0, tile_carry = 0, dense_carry = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
     const int n = (e < E) ? counts[e] : 0;
-    int rb, tb;
+    const int mt = (n + kBM - 1) / kBM;
+    int rb, tb, db = 0;
     const int rt = block_exclusive_scan(n, &rb, warp_tot);
-    const int tt = block_exclusive_scan((n + kBM - 1) / kBM, &tb, warp_tot);
+    const int tt = block_exclusive_scan(mt, &tb, warp_tot);
+    const int dt = split ? block_exclusive_scan(mt >= dense_mt ? mt : 0, &db, warp_tot) : 0;
     if (e < E) {
       row_off[e] = row_carry + rb;
       tile_off[e] = tile_carry + tb;
+      if (split) {
+        tile_doff[e] = dense_carry + db;
+        tile_soff[e] = (tile_carry + tb) - (dense_carry + db);
+      }
     }
     row_carry += rt;
     tile_carry += tt;
+    dense_carry += dt;
   }
   if (threadIdx.x == 0) {
     row_off[E] = row_carry;
     tile_off[E] = tile_carry;
+    int dense_end = dense_carry;
     if (has_shared) {
+      const int mt = (T + kBM - 1) / kBM;
       counts[E] = T;
       row_off[E + 1] = row_carry + T;
-      tile_off[E + 1] = tile_carry + (T + kBM - 1) / kBM;
+      tile_off[E + 1] = tile_carry + mt;
+      if (mt >= dense_mt) dense_end += mt;
+    }
+    if (split) {
+      tile_doff[E] = dense_carry;
+      tile_soff[E] = tile_carry - dense_carry;
+      if (has_shared) {
+        tile_doff[E + 1] = dense_end;
+        tile_soff[E + 1] = tile_off[E + 1] - dense_end;
+      }
     }
   }
 }
@@ -233,7 +255,8 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
     dispatch_count_kernel<<<b.nchunk, kThreads, sh, s>>>(E_ids, A, E, b.chunk_cnt, b.inv, status);
   }
   dispatch_scan_kernel<<<1, kThreads, 0, s>>>(b.chunk_cnt, b.nchunk, E, T, has_shared, b.counts,
-                                              b.row_off, b.tile_off);
+                                              b.row_off, b.tile_off, b.tile_doff, b.tile_soff,
+                                              b.dense_mt);
   if (A > 0 && E <= kPlaceMaxE) {
     const int sh = (2 * kChunk + 32 * E) * static_cast<int>(sizeof(int));
     cudaError_t e = cudaFuncSetAttribute(dispatch_place_match_kernel,

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
     // Lane 0 waits for a free stage, posts the byte count and loads B, and A
     // too unless the gather warps copy the A rows.
     if (lane == 0) {
+      const uint64_t evict_first = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
@@ -146,9 +147,16 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
           } else {
             mbar_arrive_expect_tx(fb, C::B_BYTES);
           }
+          if (p.l2_hint && t.stream) {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_3d(sb + j * (64 * kBK * 2), mB, fb, b_box_col<KIND>(p, t.n, j), kb * kBK, bz);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d_hint(sb + j * (64 * kBK * 2), mB, fb, b_box_col<KIND>(p, t.n, j), kb * kBK,
+                               bz, evict_first);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * (64 * kBK * 2), mB, fb, b_box_col<KIND>(p, t.n, j), kb * kBK, bz);
+          }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }

@@ -76,6 +76,8 @@ __device__ __forceinline__ BwdTile decode_bwd(const BwdParams& p, int tile) {
     q.shared_group = p.shared_group;
     q.a2_shared = 0;
     q.n_tiles = p.n_tiles;
+    q.tile_doff = nullptr;  // plain group order
+    q.tile_soff = nullptr;
     const TileInfo t = decode_tile(q, tile);
     b.group = t.group;
     b.m = t.m;

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t evict_first = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
@@ -277,7 +278,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           else
             mbar_arrive_expect_tx(fb, (MxFmt<AF>::FP4 ? kMxA / 2 : kMxA) + (MxFmt<BF>::FP4 ? kMxB / 2 : kMxB));
           tma_load_2d(sa, &tmA, fb, kx, t.row0);
-          if (SWIGLU) {
+          if (p.l2_hint && t.stream) {
+            if (SWIGLU) {
+              tma_load_3d_hint(sb, &tmB, fb, kx, t.n * 128, t.group, evict_first);
+              tma_load_3d_hint(sb + 128 * kMxBK, &tmB, fb, kx, p.up_off + t.n * 128, t.group,
+                               evict_first);
+            } else {
+              tma_load_3d_hint(sb, &tmB, fb, kx, t.n * kMxBN, t.group, evict_first);
+            }
+          } else if (SWIGLU) {
             tma_load_3d(sb, &tmB, fb, kx, t.n * 128, t.group);
             tma_load_3d(sb + 128 * kMxBK, &tmB, fb, kx, p.up_off + t.n * 128, t.group);
           } else {

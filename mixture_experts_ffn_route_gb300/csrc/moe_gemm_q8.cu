@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ weight TMA
     if (lane == 0) {
+      const uint64_t evict_first = l2_policy_evict_first();
       unsigned it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -189,8 +190,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
           const uint32_t fb = rawfull0 + 8 * st;
           const uint32_t dst = raw0 + st * kQ8RawBytes;
           mbar_arrive_expect_tx(fb, kQ8RawBytes);
-          tma_load_3d(dst, &tmW, fb, kb * kBK, r0, t.group);
-          tma_load_3d(dst + kQ8RawBytes / 2, &tmW, fb, kb * kBK, r1, t.group);
+          if (p.l2_hint && t.stream) {
+            tma_load_3d_hint(dst, &tmW, fb, kb * kBK, r0, t.group, evict_first);
+            tma_load_3d_hint(dst + kQ8RawBytes / 2, &tmW, fb, kb * kBK, r1, t.group, evict_first);
+          } else {
+            tma_load_3d(dst, &tmW, fb, kb * kBK, r0, t.group);
+            tma_load_3d(dst + kQ8RawBytes / 2, &tmW, fb, kb * kBK, r1, t.group);
+          }
         }
       }
     }

@@ -68,6 +68,17 @@ struct GemmParams {
   // Linear2 of the quantised forms: 1 = write the rows to out as bf16 (RNE)
   // instead of fp32
   int out_bf16;
+  // Interleaved tile order (optional): tile_doff and tile_soff are tile_off
+  // counted over the dense groups only (those of at least dense_mt row tiles,
+  // whose weights are reused across row tiles) and over the others; the
+  // dense groups' tiles are then spread evenly through the sparse groups'
+  // weight stream (decode_tile).  Null: plain group order.
+  const int* tile_doff;
+  const int* tile_soff;
+  // 1: the weight loads of sparse-group tiles (read once) carry an L2
+  // evict_first policy, so that they pass through L2 without displacing the
+  // token rows and the dense groups' weight blocks that are read again
+  int l2_hint;
 };
 
 struct GemmMaps {
@@ -201,9 +212,12 @@ struct DispatchBufs {
   int* counts;       // [E + 1]
   int* row_off;      // [E + 2]
   int* tile_off;     // [E + 2]
+  int* tile_doff;    // [E + 2] dense groups' tile offsets, or null
+  int* tile_soff;    // [E + 2] sparse groups' tile offsets, or null
   int* perm;         // [T * k]
   int* inv;          // [T * k]
   int nchunk;
+  int dense_mt;      // row tiles from which a group counts as dense
 };
 int dispatch_chunks(int A);
 cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_shared,

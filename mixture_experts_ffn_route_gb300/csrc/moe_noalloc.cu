@@ -74,6 +74,9 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_params* p, const int32_t* E
   DispatchBufs b;
   b.chunk_cnt = reinterpret_cast<int*>(base);
   b.tile_off = reinterpret_cast<int*>(base + kChunkCntBytes);
+  b.tile_doff = nullptr;  // no GEMM follows: the interleaved order is not needed
+  b.tile_soff = nullptr;
+  b.dense_mt = 0;
   b.inv = reinterpret_cast<int*>(base + kChunkCntBytes + kTileOffBytes);
   b.counts = counts;    // the scan writes counts[0, E) and offsets[0, E]
   b.row_off = offsets;  // straight into the caller's outputs

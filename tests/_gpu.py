@@ -62,6 +62,19 @@ def to_host(dd: dict) -> dict:
     return out
 
 
+def mixed_load_ids(T, E):
+    """Top-2 expert ids [T, 2] under which some groups span several 128-row
+    tiles and the rest one partial tile: expert 0 takes the first min(T, 450)
+    tokens, expert 3 the first 260 and every fifth token after 450, experts
+    1-5 share the rest of column 0 and experts 6 to E-1 the rest of column 1.
+    The grouped GEMMs then interleave dense and sparse groups in one launch."""
+    assert E >= 12
+    t = np.arange(T)
+    first = np.where(t < 450, 0, 1 + t % 5)
+    second = np.where(t < 260, 3, 6 + t % (E - 6))
+    return np.stack([first, second], axis=1).astype(np.int32)
+
+
 def params(cfg, **kw):
     c = dict(cfg)
     c.update(kw)

@@ -7,7 +7,7 @@ import torch
 import mixture_experts_ffn_route_gb300 as moe
 import oracle
 import synth
-from _gpu import DEV, check_y, host_bits, params, run_route, to_device
+from _gpu import DEV, check_y, host_bits, mixed_load_ids, params, run_route, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -98,6 +98,7 @@ EDGE_Q = [
     dict(T=129, H=192, E=3, k=1, I=64),
     dict(T=300, H=128, E=6, k=1, I=320, hot=True),
     dict(T=260, H=320, E=9, k=3, I=448),
+    dict(T=700, H=128, E=12, k=2, I=320, mixed=True),
 ]
 
 
@@ -105,9 +106,12 @@ EDGE_Q = [
 def test_a8w8_edge_shapes(shape):
     shape = dict(shape)
     hot = shape.pop("hot", False)
+    mixed = shape.pop("mixed", False)
     h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0, quant="a8w8"), seed=99)
     if hot:
         h["E_ids"][:] = 0
+    if mixed:
+        h["E_ids"][:] = mixed_load_ids(shape["T"], shape["E"])
     c = h["cfg"]
     dd = to_device(h)
     p = params(c)

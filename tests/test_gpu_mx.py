@@ -9,7 +9,7 @@ import torch
 import mixture_experts_ffn_route_gb300 as moe
 import oracle
 import synth
-from _gpu import DEV, bf, check_y, host_bits, params, run_route, to_device
+from _gpu import DEV, bf, check_y, host_bits, mixed_load_ids, params, run_route, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -152,6 +152,7 @@ EDGE_MX = [
     dict(T=17, H=256, E=5, k=5, I=128),
     dict(T=300, H=256, E=6, k=1, I=256, hot=True),
     dict(T=260, H=384, E=9, k=3, I=384),
+    dict(T=700, H=256, E=12, k=2, I=256, mixed=True),
 ]
 
 
@@ -162,9 +163,12 @@ EDGE_MX = [
 def test_mx_edge_shapes(shape, quant):
     shape = dict(shape)
     hot = shape.pop("hot", False)
+    mixed = shape.pop("mixed", False)
     h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0, quant=quant), seed=99)
     if hot:
         h["E_ids"][:] = 0
+    if mixed:
+        h["E_ids"][:] = mixed_load_ids(shape["T"], shape["E"])
     c = h["cfg"]
     dd = to_device(h)
     p = params(c)

@@ -12,8 +12,8 @@ import torch
 import mixture_experts_ffn_route_gb300 as moe
 import oracle
 import synth
-from _gpu import (DEV, bf, check_gates, check_y, host_bits, params, run_forward, run_route,
-                  to_device, to_host)
+from _gpu import (DEV, bf, check_gates, check_y, host_bits, mixed_load_ids, params, run_forward,
+                  run_route, to_device, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -227,6 +227,7 @@ EDGE = [
     dict(T=40, H=256, E=40, k=2, I=64),
     dict(T=600, H=128, E=6, k=1, I=192, hot=True),
     dict(T=260, H=320, E=9, k=3, I=448, shared=1),
+    dict(T=700, H=192, E=12, k=2, I=320, shared=1, mixed=True),
 ]
 
 
@@ -234,9 +235,12 @@ EDGE = [
 def test_forward_edge_shapes(shape):
     shape = dict(shape)
     hot = shape.pop("hot", False)
+    mixed = shape.pop("mixed", False)
     h = synth.make_inputs(dict(shape, routing="given", score="softmax", renorm=0), seed=99)
     if hot:
         h["E_ids"][:] = 0  # every token to expert 0: several 128-row tiles, other experts empty
+    if mixed:
+        h["E_ids"][:] = mixed_load_ids(shape["T"], shape["E"])
     c = h["cfg"]
     dd = to_device(h)
     p = params(c)
