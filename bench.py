@@ -598,7 +598,7 @@ def load_traffic(workload, algorithmic_bytes):
             m = re.search(r"dram_bytes_per_launch_%s_gemm1:\s*([0-9]+)" % key, f.read())
         return int(m.group(1)) if m else None
     if workload == "c3p":
-        path = os.path.join(ROOT, "profiles", "gemm1_swiglu_c3p.md")
+        path = os.path.join(ROOT, "profiles", "gemm_bf16_c2_c3p.md")
         if not os.path.exists(path):
             return None
         with open(path) as f:
