@@ -71,9 +71,11 @@ def _run(p, dd, E_ids, G, dY):
     return out
 
 
-@pytest.mark.parametrize("name", ["c1s", "c3s", "c3s_sp", "c4s", "c5s"])
-def test_backward_matches_oracle(name):
-    h = synth.make_inputs(name)
+# c5s at T = 1040 averages 260 routed rows per expert (several row tiles each)
+@pytest.mark.parametrize("name,T", [("c1s", None), ("c3s", None), ("c3s_sp", None), ("c4s", None),
+                                    ("c5s", None), ("c5s", 1040)])
+def test_backward_matches_oracle(name, T):
+    h = synth.make_inputs(name, **({"T": T} if T else {}))
     c = h["cfg"]
     dd = to_device(h)
     p = params(c)

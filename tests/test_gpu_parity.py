@@ -228,6 +228,11 @@ EDGE = [
     dict(T=600, H=128, E=6, k=1, I=192, hot=True),
     dict(T=260, H=320, E=9, k=3, I=448, shared=1),
     dict(T=700, H=192, E=12, k=2, I=320, shared=1, mixed=True),
+    # experts of several hundred rows (every group dense in the tile order),
+    # partial last row tiles and partial column tiles
+    dict(T=700, H=192, E=2, k=2, I=320, shared=1),
+    dict(T=520, H=256, E=4, k=2, I=128),
+    dict(T=300, H=128, E=1, k=1, I=64),
 ]
 
 
@@ -250,6 +255,23 @@ def test_forward_edge_shapes(shape):
     Y_ref, _ = oracle.forward(h["X"], h["E_ids"], h["G"].astype(np.float64), h["W1"], h["W2"],
                               h["Ws1"], h["Ws2"])
     check_y(Y, Y_ref, str(shape))
+
+
+def test_routed_forward_dense_experts():
+    """The c5s layer with T = 1040 (260 routed rows per expert on average: every
+    expert spans several 128-row tiles): routing and Y."""
+    h = synth.make_inputs("c5s", T=1040)
+    c = h["cfg"]
+    dd = to_device(h)
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    Y = run_forward(p, dd, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref = _reference_ids(h)
+    assert np.array_equal(E_ids.cpu().numpy(), ids_ref)
+    Y_ref, _ = oracle.forward(h["X"], ids_ref, G_ref, h["W1"], h["W2"], h["Ws1"], h["Ws2"])
+    check_y(Y, Y_ref, "c5s T=1040")
 
 
 def test_forward_with_no_tokens_writes_nothing():
