@@ -453,6 +453,9 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
   // inference forward; the training forward keeps fp32 rows, which the
   // backward's gate gradient reads
   const bool yp_bf16 = h_out == nullptr;
+  // top-1 without a shared expert: the combine is one gate-scaled row per
+  // token, written by Linear2's epilogue straight into Y (no Yp round trip)
+  const bool fuse_k1 = yp_bf16 && k == 1 && !p->has_shared;
   {
     GemmMaps maps;
     bool ok = make_map_rows(&maps.a, Act, A + Tsh, I) && make_map_weights(&maps.b, W2, E, I, H);
@@ -471,18 +474,26 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     g.num_kb = I / kBK;
     g.n_out = H;
     g.up_off = 0;
-    g.out = Yp;
+    g.out = fuse_k1 ? static_cast<void*>(Y) : static_cast<void*>(Yp);
     g.ldo = H;
     g.status = status;
+    if (fuse_k1) {
+      g.gather_perm = b.perm;
+      g.gate = G;
+    }
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    if ((e = launch_gemm(yp_bf16 ? kGemmPlainBf16 : kGemmPlain, maps, g, grid, s)) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    const GemmKind kind = fuse_k1 ? kGemmCombineK1 : (yp_bf16 ? kGemmPlainBf16 : kGemmPlain);
+    if ((e = launch_gemm(kind, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  e = yp_bf16 ? launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k,
-                                    H, E, p->has_shared, Y, s)
-              : launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
+  if (fuse_k1)
+    e = launch_zero_dropped_rows(b.inv, T, H, Y, s);
+  else if (yp_bf16)
+    e = launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k, H, E,
+                            p->has_shared, Y, s);
+  else
+    e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }

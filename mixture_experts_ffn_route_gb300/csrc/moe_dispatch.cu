@@ -328,6 +328,23 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
+// One warp per token: a token whose single assignment was dropped has no
+// Linear2 row, so its output row is written here as zeros.
+__global__ void __launch_bounds__(256)
+    zero_dropped_kernel(const int* __restrict__ inv, int T, int H, uint16_t* __restrict__ Y) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T || __ldg(inv + t) >= 0) return;
+  uint4* row = reinterpret_cast<uint4*>(Y + static_cast<long long>(t) * H);
+  for (int c = lane; c < H / 8; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+cudaError_t launch_zero_dropped_rows(const int* inv, int T, int H, uint16_t* Y, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  zero_dropped_kernel<<<(T + 7) / 8, 256, 0, s>>>(inv, T, H, Y);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float* Yp, const int* inv, const float* G, const int* row_off,
                            int T, int k, int H, int E, int has_shared, uint16_t* Y, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;

@@ -437,6 +437,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
     case kGemmRouter: return launch_one<kGemmRouter>(maps, p, grid, s);
     case kGemmSwiGLU: return launch_one<kGemmSwiGLU>(maps, p, grid, s);
     case kGemmPlain: return launch_one<kGemmPlain>(maps, p, grid, s);
+    case kGemmCombineK1: return launch_one<kGemmCombineK1>(maps, p, grid, s);
     default: return launch_one<kGemmPlainBf16>(maps, p, grid, s);
   }
 }

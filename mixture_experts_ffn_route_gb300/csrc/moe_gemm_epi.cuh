@@ -3,7 +3,8 @@
 // row per lane) -> a padded shared staging block -> global memory, with every
 // store instruction writing whole 128-byte lines (4 rows of fp32 or 8 rows of
 // bf16).  KIND selects SwiGLU (gate columns 0-127 and up columns 128-255 of
-// the accumulator, bf16 out), bf16 rows, or fp32 rows.
+// the accumulator, bf16 out), bf16 rows (plain, or gate-scaled into the
+// tokens' rows of Y: the top-1 combine), or fp32 rows.
 #pragma once
 
 #include "moe_common.cuh"
@@ -70,9 +71,24 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, uint32_t tb,
       }
       __syncwarp();
     }
-  } else if (KIND == kGemmPlainBf16) {
-    // Linear2 rows rounded once to bf16 (RNE) for the combine
+  } else if (KIND == kGemmPlainBf16 || KIND == kGemmCombineK1) {
+    // Linear2 rows rounded once to bf16 (RNE) for the combine; or, with the
+    // top-1 combine fused here, each row scaled by its token's gate, rounded
+    // once and stored to that token's row of Y (with k = 1 the permutation
+    // entry of an assignment row is its token)
+    constexpr bool K1 = (KIND == kGemmCombineK1);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    float g = 1.0f;
+    if (K1) {
+      const int my = wrow0 + lane;
+      g = my < row_end ? __ldg(p.gate + __ldg(p.gather_perm + my)) : 0.0f;
+    }
+    int dst[4];  // output row of each of the four rows this lane stores, or -1
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int grow = wrow0 + 8 * i + (lane >> 2);
+      dst[i] = grow < row_end ? (K1 ? __ldg(p.gather_perm + grow) : grow) : -1;
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       float v[32];
@@ -80,7 +96,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, uint32_t tb,
       const int col = n * BN + c;
       uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(g * v[2 * i], g * v[2 * i + 1]);
       uint4* srow4 = reinterpret_cast<uint4*>(stg + lane * kStgWords);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -93,9 +109,9 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, uint32_t tb,
         for (int rr = 0; rr < 32; rr += 8) {
           const int r = rr + (lane >> 2);
           const uint4 x = reinterpret_cast<const uint4*>(stg + r * kStgWords)[qd];
-          const int grow = wrow0 + r;
-          if (grow < row_end)
-            *reinterpret_cast<uint4*>(out + static_cast<long long>(grow) * p.ldo + col + 8 * qd) = x;
+          const int d = dst[rr >> 3];
+          if (d >= 0)
+            *reinterpret_cast<uint4*>(out + static_cast<long long>(d) * p.ldo + col + 8 * qd) = x;
         }
       }
       __syncwarp();

@@ -15,7 +15,9 @@ enum GemmKind {
   kGemmRouter = 0,     // fp32 logits
   kGemmSwiGLU = 1,     // Linear1 + SwiGLU, bf16 out
   kGemmPlain = 2,      // Linear2, fp32 out
-  kGemmPlainBf16 = 3   // Linear2, bf16 out (the inference forward)
+  kGemmPlainBf16 = 3,  // Linear2, bf16 out (the inference forward)
+  kGemmCombineK1 = 4   // Linear2 with the top-1 combine: gate-scaled bf16 rows
+                       // written to their tokens' rows of Y
 };
 
 // One grouped GEMM launch.  Groups are row ranges [row_off[g], row_off[g+1])
@@ -68,6 +70,8 @@ struct GemmParams {
   // Linear2 of the quantised forms: 1 = write the rows to out as bf16 (RNE)
   // instead of fp32
   int out_bf16;
+  // kGemmCombineK1: the gates G [T] (k = 1); gather_perm maps a row to its token
+  const float* gate;
   // Interleaved tile order (optional): tile_doff and tile_soff are tile_off
   // counted over the dense groups only (those of at least dense_mt row tiles,
   // whose weights are reused across row tiles) and over the others; the
@@ -225,6 +229,9 @@ cudaError_t launch_dispatch(const int32_t* E_ids, int T, int k, int E, int has_s
 cudaError_t launch_combine(const float* Yp, const int* inv, const float* G,
                            const int* row_off, int T, int k, int H, int E, int has_shared,
                            uint16_t* Y, cudaStream_t s);
+// Top-1 forward with the combine fused into Linear2: zero the rows of Y whose
+// token's one id was dropped (inv < 0), as the combine would.
+cudaError_t launch_zero_dropped_rows(const int* inv, int T, int H, uint16_t* Y, cudaStream_t s);
 cudaError_t launch_combine_bf16(const uint16_t* Yp, const int* inv, const float* G,
                            const int* row_off, int T, int k, int H, int E, int has_shared,
                            uint16_t* Y, cudaStream_t s);

@@ -87,6 +87,8 @@ CONFIGS["c2s_q"] = dict(CONFIGS["c2s"], quant="a8w8")
 CONFIGS["c3s_q"] = dict(CONFIGS["c3s"], shared=0, quant="a8w8")
 CONFIGS["c5s_q"] = dict(CONFIGS["c5s"], quant="a8w8")
 CONFIGS["c2_q"] = dict(CONFIGS["c2"], quant="a8w8")
+# top-1 variant of the given-routing layer: the combine fuses into Linear2
+CONFIGS["c2k1"] = dict(CONFIGS["c2"], k=1)
 CONFIGS["c3_q"] = dict(CONFIGS["c3"], shared=0, quant="a8w8")
 # MXFP forms: FP8 weight codes with E8M0 group scales (no shared expert).
 # H and I are multiples of 128 (one block of 128 FP8 elements = 4 groups).

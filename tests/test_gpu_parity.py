@@ -299,6 +299,29 @@ def test_bad_expert_ids_are_skipped_and_reported():
     check_y(Y, Y_ref, "dropped assignments")
 
 
+def test_top1_combine_in_the_linear2_epilogue():
+    """k = 1 without a shared expert: Linear2's epilogue writes each gate-scaled
+    row straight into its token's row of Y (no combine pass); a token whose one
+    id is bad gets a zero row, as the combine would give it."""
+    h = synth.make_inputs(dict(T=300, H=192, E=5, k=1, I=128, routing="given", score="softmax", renorm=0),
+                          seed=7)
+    c = h["cfg"]
+    # a softmax over one logit is 1: draw gates that make the scaling visible
+    h["G"] = np.random.default_rng(11).uniform(0.25, 2.0, size=h["G"].shape).astype(np.float32)
+    ids = h["E_ids"].copy()
+    bad = [0, 17, 299]
+    ids[bad, 0] = [-1, c["E"], 2 * c["E"]]
+    dd = to_device(h)
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    Y = torch.full((c["T"], c["H"]), float("nan"), dtype=torch.bfloat16, device=DEV)
+    run_forward(p, dd, torch.from_numpy(ids).to(DEV), dd["G"], ws, Y=Y)
+    assert moe.moe_sync_status(ws, raise_on_error=False) == moe.MOE_ERR_BAD_EXPERT_ID
+    assert torch.equal(Y[bad].float(), torch.zeros((len(bad), c["H"]), device=DEV))
+    Y_ref, _ = oracle.forward(h["X"], ids, h["G"].astype(np.float64), h["W1"], h["W2"])
+    check_y(Y, Y_ref, "top-1, fused combine")
+
+
 def test_bad_hash_token_ids_are_reported():
     h, dd = host_inputs("c4s")
     c = h["cfg"]
