@@ -129,7 +129,10 @@ moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* coun
  *   Y    [T, H]      bf16   out
  * Precision: float32 accumulation in both GEMMs and in the combine; the SwiGLU
  * rows and each expert's output rows are kept in bf16 (round to nearest even)
- * between the kernels, and Y is rounded to bf16 once at the end.
+ * between the kernels, and Y is rounded to bf16 once at the end.  With k = 1
+ * and no shared expert the combine is done by Linear2's epilogue: each
+ * float32 row times its gate is rounded once into Y (the expert rows are not
+ * kept), and tokens whose id was dropped get zero rows, as in the combine.
  * Every step (dispatch, Linear1 with SwiGLU, Linear2, combine) runs in this
  * library's kernels, with no host synchronisation: sizes come from device
  * memory, so a call (with moe_route before it) can be captured in a CUDA graph
