@@ -1,10 +1,20 @@
 // Tile walk of the persistent grouped GEMMs: which group, row tile and column
-// tile a linear tile index names.
+// tile a linear tile index names.  Host-callable as well, so that the walk can
+// be checked on the CPU against the tile counts it is given.
 #pragma once
 
 #include "moe_internal.h"
 
 namespace moe {
+
+// Read-only load: through the non-coherent cache on the device.
+__host__ __device__ __forceinline__ int ld_ro(const int* p) {
+#ifdef __CUDA_ARCH__
+  return __ldg(p);
+#else
+  return *p;
+#endif
+}
 
 struct TileInfo {
   int group, m, n;
@@ -16,11 +26,11 @@ struct TileInfo {
 
 // Largest g in [0, G) with off[g] * n_tiles <= j (groups without tiles share
 // their start with the next group, so the search lands on the one holding j).
-__device__ __forceinline__ int find_group(const int* off, int G, int n_tiles, long long j) {
+__host__ __device__ __forceinline__ int find_group(const int* off, int G, int n_tiles, long long j) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<long long>(__ldg(off + mid)) * n_tiles <= j) lo = mid; else hi = mid - 1;
+    if (static_cast<long long>(ld_ro(off + mid)) * n_tiles <= j) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -39,7 +49,7 @@ __device__ __forceinline__ int find_group(const int* off, int G, int n_tiles, lo
 // holds the two lists in the ratio nd : total - nd, so the dense groups'
 // tensor-bound tiles overlap the sparse groups' HBM-bound weight stream
 // instead of running in phases of their own.
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
+__host__ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
   TileInfo t;
   t.stream = false;
   if (p.row_off == nullptr) {
@@ -54,7 +64,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
     const int* off = p.tile_off;
     long long j = tile;
     if (p.tile_doff != nullptr) {
-      const int mt_all = __ldg(p.tile_off + G), mt_dense = __ldg(p.tile_doff + G);
+      const int mt_all = ld_ro(p.tile_off + G), mt_dense = ld_ro(p.tile_doff + G);
       if (mt_dense == 0) {
         t.stream = true;  // all sparse: the plain walk, every tile streamed
       } else if (mt_dense < mt_all) {
@@ -72,14 +82,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
       }  // all dense: the plain walk
     }
     const int g = find_group(off, G, p.n_tiles, j);
-    const int t0 = __ldg(off + g);
-    const int mt = __ldg(off + g + 1) - t0;
+    const int t0 = ld_ro(off + g);
+    const int mt = ld_ro(off + g + 1) - t0;
     const int local = static_cast<int>(j - static_cast<long long>(t0) * p.n_tiles);
     t.group = g;
     t.n = local / mt;
     t.m = local - t.n * mt;
-    t.row0 = __ldg(p.row_off + g) + t.m * kBM;
-    t.row_end = __ldg(p.row_off + g + 1);
+    t.row0 = ld_ro(p.row_off + g) + t.m * kBM;
+    t.row_end = ld_ro(p.row_off + g + 1);
   }
   t.second = (t.group == p.shared_group);
   t.a_row0 = (t.second && p.a2_shared) ? t.m * kBM : t.row0;
