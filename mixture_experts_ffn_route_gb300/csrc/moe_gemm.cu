@@ -213,10 +213,15 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f32acc(kBM, BN, kFmtBF16, false, true);
+      // tiles of at most 64 rows (short experts) run M = 64 MMAs: half the
+      // tensor work on rows that are padding
+      constexpr uint32_t idesc64 = idesc_f32acc(64, BN, kFmtBF16, false, true);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+        const TileInfo t = decode_tile(p, tile);
+        const uint32_t id = (t.row_end - t.row0 <= 64) ? idesc64 : idesc;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, p.status, abort_flag)) break;
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
             // B: MN-major; rows of 128 B hold 64 n-values of one k; 8-row groups
             // are 1024 B apart (SBO) and 64-column blocks 8 KB apart (LBO).
             const uint64_t bd = smem_desc_sw128(sb + kk * 16 * 128, 64 * kBK * 2, 1024);
-            mma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_f16(d, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
           }
           mma_commit(empty0 + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -247,10 +252,12 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Each warp owns 32 accumulator rows (its TMEM lane quarter).  A chunk of
-    // 32 columns goes TMEM -> registers (one row per lane) -> a padded shared
-    // staging block -> global memory with every store instruction writing
-    // whole 128-byte lines (4 rows of fp32 or 8 rows of bf16 per instruction).
+    // Each warp owns 32 accumulator rows (its TMEM lane quarter), or 16 after
+    // an M = 64 MMA, which leaves row 16q + l in lane l < 16 of quarter q.  A
+    // chunk of 32 columns goes TMEM -> registers (one row per lane) -> a
+    // padded shared staging block -> global memory with every store
+    // instruction writing whole 128-byte lines (4 rows of fp32 or 8 rows of
+    // bf16 per instruction).
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t* stg = stg_area + q * 32 * kStgWords;
     int local = 0;
@@ -262,14 +269,16 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int wrow0 = t.row0 + q * 32;  // first output row of this warp
-      if (wrow0 >= t.row_end) {
-        // all 32 rows of this warp lie past the group's end: nothing to store
+      const bool m64 = t.row_end - t.row0 <= 64;
+      const int wrow0 = t.row0 + q * (m64 ? 16 : 32);  // first output row of this warp
+      const int wend = m64 ? min(t.row_end, wrow0 + 16) : t.row_end;
+      if (wrow0 >= wend) {
+        // all rows of this warp lie past the group's end: nothing to store
         tc_fence_before();
         mbar_arrive(tempty0 + 8 * acc);
         continue;
       }
-      epilogue_store<KIND, BN>(p, tb, wrow0, t.row_end, t.n, stg, lane);
+      epilogue_store<KIND, BN>(p, tb, wrow0, wend, t.n, stg, lane);
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
