@@ -3,7 +3,8 @@
 // Serves the contractions of the layer:
 //   router     : logits[T, E] = X[T, H] Wg[H, E]                          (fp32 out)
 //   Linear1    : Act[rows, I] = SiLU(X_e W1[e][:, :I]) * (X_e W1[e][:, I:])   (bf16 out)
-//   Linear2    : Yp[rows, H]  = Act W2[e]                     (fp32 or bf16 out)
+//   Linear2    : Yp[rows, H]  = Act W2[e]                     (fp32 or bf16 out;
+//                top-1: the gate-scaled rows straight into Y)
 // The expert FFN is the "Expert Compute" step of the "mega_moe" page
 // (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
 // projection); the router product is the
@@ -13,16 +14,18 @@
 //   warp 0      TMA producer: A tile [128 rows x 64 k] K-major and B tile
 //               [64 k x BN cols] MN-major (the weights keep their [K][N] row-major
 //               layout), both with 128-byte swizzle, into a STAGES-deep ring.
-//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16)
-//               into one of two TMEM accumulators and commits to mbarriers.
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, or M=64
+//               for a tile of at most 64 rows; N=BN, K=16) into one of two
+//               TMEM accumulators and commits to mbarriers.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
-//               fuse SwiGLU, stage through shared memory for
-//               full-line stores, free the accumulator so the next tile's MMAs
-//               overlap this epilogue.
+//               fuse SwiGLU (or the top-1 combine), stage through shared
+//               memory for full-line stores, free the accumulator so the next
+//               tile's MMAs overlap this epilogue.
 //   warps 6..9  Linear1 only: copy the A rows straight from the token rows X
 //               by the dispatch permutation (cp.async), so the permuted rows are
 //               never written to memory.
-// Tiles are walked in (group, column tile, 128-row tile) order, striding by
+// Tiles are walked in (group, column tile, 128-row tile) order, or with the
+// dense groups' tiles interleaved into the others' (moe_tile.cuh), striding by
 // gridDim.x.  Group row ranges come from device memory.
 #include "moe_common.cuh"
 #include "moe_internal.h"
