@@ -1,14 +1,16 @@
 """Throughput of the routed MoE FFN layer forward on GB300.
 
 One step = one pass of the whole layer over one batch of synthetic tokens:
-router (gating GEMM, scores, biased top-k, gates), dispatch (counts, scan,
-permutation, row gather), Linear1 + SwiGLU, Linear2 (routed experts and the
-shared expert), gate-weighted combine.  Default workload: the V4-Pro-shaped
-layer (T=4096, H=7168, E=384, top-6, I=2048, one shared expert, sigmoid
-affinity with selection bias, alpha = 2.5, Zipf(1.1) expert load), the only
-one of the pages' workloads that runs every step of the path.
+router (gating GEMM, scores, top-k, gates), dispatch (counts, scan,
+permutation), Linear1 + SwiGLU (rows gathered by the permutation), Linear2
+(routed experts and, where the layer has one, the shared expert),
+gate-weighted combine.  Default workload: the largest layer, T=16384 (B=2,
+S=8192), H=8192, 64 experts top-2 with softmax gates, I=22016; then, on the
+same GPU, the V4-Pro-shaped layer (T=4096, H=7168, 384 experts top-6, I=2048,
+one shared expert, sigmoid affinity with selection bias, alpha 2.5, Zipf(1.1)
+load), reported under "other_workloads".
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--also c3]
     python bench.py --impl reference ...   # the CPU oracle on this host's cores
 
 Under torchrun each rank runs its own batch (weak scaling, no collective in
@@ -183,17 +185,18 @@ def build_step(moe, dd, p, ws, stage_events=None):
     return step
 
 
-def run_ours(args, rank, world, local_rank):
+def run_ours(args, rank, world, local_rank, workload=None, with_cpu=True):
     import torch
     import mixture_experts_ffn_route_gb300 as moe
     from mixture_experts_ffn_route_gb300 import accounting
     import synth
 
+    workload = workload or args.workload
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.lib()
     wseed, tseed = rank_seeds(rank)
-    dd = synth.make_inputs_torch(args.workload, seed=wseed, token_seed=tseed, device=dev)
+    dd = synth.make_inputs_torch(workload, seed=wseed, token_seed=tseed, device=dev)
     c = dd["cfg"]
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     has_shared = c["shared"]
@@ -362,8 +365,9 @@ def run_ours(args, rank, world, local_rank):
                                           out_bytes=accounting.BF16)
     else:
         g1_bytes = accounting.gemm1_bytes(counts, H, I, has_shared, T)
-        # the inference forward writes Linear2's rows in bf16
-        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T, out_bytes=accounting.BF16)
+        # Linear2 writes fp32 rows (top-1 without a shared expert: bf16 rows of Y)
+        g2_bytes = accounting.gemm2_bytes(counts, H, I, has_shared, T,
+                                          out_bytes=accounting.BF16 if (k == 1 and not has_shared) else 4)
     g1_flops = accounting.gemm1_flops(counts, H, I, has_shared, T)
     g2_flops = accounting.gemm2_flops(counts, H, I, has_shared, T)
     g1_s = stages["gemm1_swiglu_quant" if mx else "gemm1_swiglu"] / 1e3
@@ -392,7 +396,7 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_flops_per_launch": int(g1_flops),
                 "peak_source": pk["source"] + " bf16_tflops_sustained" + (" x 2 (fp8)" if mx else "")}
     if roof["bound"] == "hbm" and not quant:
-        roof["traffic"] = load_traffic(args.workload, g1_bytes)
+        roof["traffic"] = load_traffic(workload, g1_bytes)
     if quant:
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_q8_kernel<true>)"
     if mx:
@@ -407,7 +411,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8" if quant else (f"{mx} x {synth_mx_weight_format(c)}" if mx else "bf16"),
         "data": "synthetic (seeded; random-init weights of the workload's shapes)",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
+        "config": {"workload": f"{workload}: {WORKLOAD_TEXT.get(workload, '')}",
                    "T": T, "H": H, "E": E, "k": k, "I": I, "shared_experts": has_shared,
                    "routing": c["routing"], "score": c["score"],
                    "l2": "inputs larger than L2: %.1f GB of expert weights per step"
@@ -436,8 +440,8 @@ def run_ours(args, rank, world, local_rank):
     if graph_ms is not None:
         out["graph_replay"] = {"ms_per_step": round(graph_ms, 4),
                                "value": round(T * world / (graph_ms / 1e3), 1), "unit": UNIT}
-    if world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(dd, budget_s=args.cpu_budget)
+    if world == 1 and with_cpu and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(dd, args.cpu_tokens, args.cpu_tokens_1core)
     return out
 
 
@@ -609,9 +613,10 @@ def load_traffic(workload, algorithmic_bytes):
 
 # ------------------------------------------------------------------ oracle (CPU)
 class OracleRunner:
-    """The CPU oracle, as it stands, over successive token slices of the
-    workload.  Inputs come from the same seeded device drawing; expert weights
-    are fetched to the host one expert at a time when a slice needs them."""
+    """The CPU oracle, as it stands, on the bench's workload.  Inputs come from
+    the same seeded device drawing, copied to the host; expert weights are
+    fetched to the host (bf16 bits) one expert at a time when the oracle asks
+    for them, and the oracle decodes them itself."""
 
     def __init__(self, dd):
         import torch
@@ -632,14 +637,13 @@ class OracleRunner:
         if c["routing"] == "hash":
             self.tok = dd["token_ids"].cpu().numpy()
             self.tab = dd["tid2eid"].cpu().numpy()
-        self.pos = 0
 
-    def run(self, n):
+    def route(self, rows=None):
+        """The oracle's routing and dispatch of the given tokens (all by
+        default): returns (ids, G) of those tokens."""
         import oracle
         c = self.c
-        T = c["T"]
-        rows = (np.arange(n) + self.pos) % T
-        self.pos = (self.pos + n) % T
+        rows = np.arange(c["T"]) if rows is None else rows
         X = self.X[rows]
         if c["routing"] == "given":
             ids, G = self.E_ids[rows], self.G[rows]
@@ -648,6 +652,15 @@ class OracleRunner:
                                           c["alpha"], c["renorm"])
         else:
             ids, G, _ = oracle.route(X, self.Wg, self.bias, c["score_fn"], c["k"], c["alpha"], c["renorm"])
+        oracle.dispatch(ids, c["E"])
+        return ids, G
+
+    def ffn(self, rows, ids, G):
+        """The oracle's expert FFNs and combine of the given tokens (their ids
+        and gates given), rounded to bf16."""
+        import oracle
+        c = self.c
+        X = self.X[rows]
         dd = self.dd
         raw = lambda key: (lambda e: dd[key][e].cpu().numpy())  # noqa: E731
         if c.get("quant") == "a8w8":
@@ -660,38 +673,100 @@ class OracleRunner:
             W1 = lambda e: self.bits(dd["W1"][e])  # noqa: E731
             W2 = lambda e: self.bits(dd["W2"][e])  # noqa: E731
             Y = oracle.forward_tokens(rows, X, ids, G, W1, W2, self.Ws1, self.Ws2, E=c["E"])
-        oracle.f64_to_bf16_bits(Y)
-        return n
+        return oracle.f64_to_bf16_bits(Y)
 
 
-def _threads():
+def _blas_threads(n=None):
+    """Read (and, with n, set) the thread count of the BLAS library numpy
+    loaded: threadpoolctl where installed, else the library's own
+    set/get calls found through /proc/self/maps."""
     try:
         import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        n = [i.get("num_threads") for i in info if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
+        info = [i for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            old = int(max(i["num_threads"] for i in info))
+            if n is not None:
+                threadpoolctl.threadpool_limits(n, user_api="blas")
+            return old
     except Exception:
         pass
-    return os.cpu_count()
+    import ctypes
+    import re
+    libs = set()
+    try:
+        with open("/proc/self/maps") as f:
+            for line in f:
+                m = re.search(r"(/\S*openblas\S*\.so\S*)", line)
+                if m:
+                    libs.add(m.group(1))
+    except OSError:
+        return None
+    old = None
+    for path in sorted(libs):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for suffix in ("", "64_", "_64_"):
+            for pre in ("openblas", "scipy_openblas"):
+                get = getattr(lib, f"{pre}_get_num_threads{suffix}", None)
+                put = getattr(lib, f"{pre}_set_num_threads{suffix}", None)
+                if get is None or put is None:
+                    continue
+                old = int(get())
+                if n is not None:
+                    put(ctypes.c_int(n))
+                return old
+    return old
 
 
-def cpu_baseline(dd, budget_s=15.0, tokens_per_slice=2):
-    r = OracleRunner(dd)
-    r.run(1)  # first-call costs (BLAS thread start-up) stay outside the timing
+def oracle_leg(r, n_tokens, seed=0):
+    """One timing of the oracle on the workload: routing and dispatch of all T
+    tokens, then the expert FFNs and combine of a seeded set of n_tokens tokens
+    that reaches every routed expert (each expert's weights fetched and decoded
+    once), scaled to T tokens (rows are independent).  Returns (tokens/s of the
+    whole layer, route seconds, FFN seconds, tokens in the FFN sample)."""
+    import synth
+    c = r.c
+    T = c["T"]
     t0 = time.time()
-    done = 0
-    while time.time() - t0 < budget_s:
-        done += r.run(tokens_per_slice)
-    dt = time.time() - t0
-    return {"value": round(done / dt, 4), "unit": UNIT, "cores": _threads(), "kind": "oracle",
-            "sample": f"{done} tokens of the workload in slices of {tokens_per_slice} "
-                      f"(route, dispatch, fp64 SwiGLU FFN of every expert a slice touches, "
-                      f"combine), {dt:.1f} s of host time"}
+    ids, G = r.route()
+    t_route = time.time() - t0
+    rows = synth.covering_tokens(ids, c["E"], n_tokens, 0, seed=seed)
+    t0 = time.time()
+    r.ffn(rows, ids[rows], G[rows])
+    t_ffn = time.time() - t0
+    return T / (t_route + t_ffn * T / len(rows)), t_route, t_ffn, len(rows)
+
+
+def cpu_baseline(dd, n_all=512, n_one=128):
+    """The oracle on this host's cores (all, then one) at the bench's workload."""
+    r = OracleRunner(dd)
+    r.route(np.arange(2))  # first-call costs (BLAS start-up) outside the timing
+    cores = os.cpu_count()
+    v_all, tr_all, tf_all, n_a = oracle_leg(r, n_all)
+    old = _blas_threads(1)
+    try:
+        v_one, tr_one, tf_one, n_o = oracle_leg(r, n_one, seed=1)
+    finally:
+        if old:
+            _blas_threads(old)
+    T = r.c["T"]
+    return {"value": round(v_all, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cores_all": cores, "value_all": round(v_all, 4), "value_1core": round(v_one, 4),
+            "blas_threads_all": old, "extrapolated": True,
+            "sample": (f"routing and dispatch of all {T} tokens ({tr_all:.1f} s on all cores, "
+                       f"{tr_one:.1f} s on one), then the fp64 expert FFNs and combine of {n_a} "
+                       f"tokens chosen to reach every routed expert ({tf_all:.1f} s, all cores; "
+                       f"{n_o} tokens, {tf_one:.1f} s, one core), each expert's weights decoded "
+                       f"once per call, extrapolated x T/{n_a} (x T/{n_o}): token rows are "
+                       f"independent")}
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, timed on this host's cores (rank 0 only)."""
+    """The oracle as it stands on this host's cores (rank 0 only), the leg of
+    cpu_baseline with a smaller FFN sample per step so that --steps K
+    --warmup W end within a few minutes."""
     if rank != 0:
         return None
     import torch
@@ -700,22 +775,26 @@ def run_reference(args, rank, world):
     dd = synth.make_inputs_torch(args.workload, seed=1234, device=dev)
     r = OracleRunner(dd)
     n = args.ref_tokens
-    for _ in range(args.warmup):
-        r.run(n)
-    t0 = time.time()
-    for _ in range(args.steps):
-        r.run(n)
-    dt = (time.time() - t0) / args.steps
-    v = n / dt
-    sample = (f"each step: {n} tokens of the {args.workload} workload (route, dispatch, fp64 "
-              f"SwiGLU FFN of every expert they touch, combine)")
+    for i in range(args.warmup):
+        oracle_leg(r, n, seed=100 + i)
+    vals, secs = [], []
+    for i in range(args.steps):
+        t0 = time.time()
+        v, _, _, n_used = oracle_leg(r, n, seed=i)
+        secs.append(time.time() - t0)
+        vals.append(v)
+    v = len(vals) / sum(1.0 / x for x in vals)  # tokens/s over the K steps (harmonic mean)
+    sample = (f"each step: routing and dispatch of all {dd['cfg']['T']} tokens, then the fp64 "
+              f"expert FFNs and combine of {n} tokens reaching as many experts as they route to "
+              f"(each expert's weights decoded once per step), extrapolated x T/{n}")
     return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "impl": "reference",
             "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}"},
-            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": _threads(),
-                             "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample, "extrapolated": True},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -726,10 +805,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c3")
+    ap.add_argument("--workload", default="c5")
+    ap.add_argument("--also", default="c3",
+                    help="comma-separated workloads measured after the main one (1 GPU), "
+                         "reported under other_workloads; empty for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="tokens of the oracle's FFN sample on all cores")
+    ap.add_argument("--cpu-tokens-1core", type=int, default=128,
+                    help="tokens of the oracle's FFN sample on one core")
+    ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured once in a CUDA graph and replayed")
     ap.add_argument("--train", action="store_true",
@@ -751,6 +836,21 @@ def main(argv=None):
         out = run_train(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
+        extra = [w for w in args.also.split(",") if w and w != args.workload] if world == 1 else []
+        if extra:
+            import gc
+            import torch
+            gc.collect()
+            torch.cuda.empty_cache()
+            other = {}
+            for w in extra:
+                o = run_ours(args, rank, world, local_rank, workload=w, with_cpu=False)
+                gc.collect()
+                torch.cuda.empty_cache()
+                other[w] = {key: o[key] for key in ("value", "unit", "ms_per_step", "config", "stages_ms",
+                                                     "grouped_gemm", "roofline", "e2e", "gpu_launches",
+                                                     "clocks", "load") if key in o}
+            out["other_workloads"] = other
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     if world > 1 and args.impl == "ours":

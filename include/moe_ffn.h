@@ -128,11 +128,11 @@ moe_status moe_dispatch(const moe_params* p, const int32_t* E_ids, int32_t* coun
  *   Ws1  [H, 2I], Ws2 [I, H]  bf16 shared expert (has_shared = 1), else NULL
  *   Y    [T, H]      bf16   out
  * Precision: float32 accumulation in both GEMMs and in the combine; the SwiGLU
- * rows and each expert's output rows are kept in bf16 (round to nearest even)
- * between the kernels, and Y is rounded to bf16 once at the end.  With k = 1
- * and no shared expert the combine is done by Linear2's epilogue: each
- * float32 row times its gate is rounded once into Y (the expert rows are not
- * kept), and tokens whose id was dropped get zero rows, as in the combine.
+ * rows are kept in bf16 (round to nearest even) between the GEMMs, each
+ * expert's output rows in float32, and Y is rounded to bf16 once at the end.
+ * With k = 1 and no shared expert the combine is done by Linear2's epilogue:
+ * each float32 row times its gate is rounded once into Y (the expert rows are
+ * not kept), and tokens whose id was dropped get zero rows, as in the combine.
  * Every step (dispatch, Linear1 with SwiGLU, Linear2, combine) runs in this
  * library's kernels, with no host synchronisation: sizes come from device
  * memory, so a call (with moe_route before it) can be captured in a CUDA graph
@@ -151,11 +151,12 @@ moe_status moe_forward(const moe_params* p, const uint16_t* X, const int32_t* E_
  * but the scratch is a fixed array inside the library (about 1.2 MB, held on
  * every GPU that loads the library until the process exits).
  * Limits: T * k <= 262144 and E <= 512, else MOE_ERR_UNSUPPORTED before any
- * device work.  The call allocates nothing.  Its first call on each device
- * looks up the array's device address (cudaGetSymbolAddress); make that
- * first call before any stream capture.  All calls share the array: calls that
- * overlap on the GPU race, so serialise them.  Ids outside [0, E) are dropped
- * without a status report. */
+ * device work.  The call allocates nothing.  Its first call in each CUDA
+ * context (on each device, and again after a device reset) looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  All calls share the array: calls that overlap on the
+ * GPU race, so serialise them.  Ids outside [0, E) are dropped and there is no
+ * status word: a caller sees them only as offsets[E] < T * k. */
 moe_status moe_dispatch_noalloc(const moe_params* p, const int32_t* E_ids, int32_t* counts,
                                 int32_t* offsets, int32_t* perm, void* stream);
 

@@ -449,13 +449,12 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     if ((e = launch_gemm(kGemmSwiGLU, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // Linear2:  Yp = Act W2[e] (shared group uses Ws2), rounded to bf16 for the
-  // inference forward; the training forward keeps fp32 rows, which the
-  // backward's gate gradient reads
-  const bool yp_bf16 = h_out == nullptr;
-  // top-1 without a shared expert: the combine is one gate-scaled row per
-  // token, written by Linear2's epilogue straight into Y (no Yp round trip)
-  const bool fuse_k1 = yp_bf16 && k == 1 && !p->has_shared;
+  // Linear2:  Yp = Act W2[e] (shared group uses Ws2), fp32 rows: the layer
+  // output is rounded to bf16 once, in the combine.  Top-1 without a shared
+  // expert: the combine is one gate-scaled row per token, written by Linear2's
+  // epilogue straight into Y (no Yp round trip); the training forward keeps
+  // the rows, which the backward's gate gradient reads.
+  const bool fuse_k1 = h_out == nullptr && k == 1 && !p->has_shared;
   {
     GemmMaps maps;
     bool ok = make_map_rows(&maps.a, Act, A + Tsh, I) && make_map_weights(&maps.b, W2, E, I, H);
@@ -483,15 +482,12 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     }
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;
     const int grid = tiles < num_sms() ? static_cast<int>(tiles) : num_sms();
-    const GemmKind kind = fuse_k1 ? kGemmCombineK1 : (yp_bf16 ? kGemmPlainBf16 : kGemmPlain);
+    const GemmKind kind = fuse_k1 ? kGemmCombineK1 : kGemmPlain;
     if ((e = launch_gemm(kind, maps, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (fuse_k1)
     e = launch_zero_dropped_rows(b.inv, T, H, Y, s);
-  else if (yp_bf16)
-    e = launch_combine_bf16(reinterpret_cast<const uint16_t*>(Yp), b.inv, G, b.row_off, T, k, H, E,
-                            p->has_shared, Y, s);
   else
     e = launch_combine(Yp, b.inv, G, b.row_off, T, k, H, E, p->has_shared, Y, s);
   if (e == cudaSuccess) e = mark(4);

@@ -3,7 +3,7 @@
 // Serves the contractions of the layer:
 //   router     : logits[T, E] = X[T, H] Wg[H, E]                          (fp32 out)
 //   Linear1    : Act[rows, I] = SiLU(X_e W1[e][:, :I]) * (X_e W1[e][:, I:])   (bf16 out)
-//   Linear2    : Yp[rows, H]  = Act W2[e]                     (fp32 or bf16 out;
+//   Linear2    : Yp[rows, H]  = Act W2[e]                     (fp32 out;
 //                top-1: the gate-scaled rows straight into Y)
 // The expert FFN is the "Expert Compute" step of the "mega_moe" page
 // (section 计算公式: Linear1 projection, SwiGLU activation, Linear2
@@ -450,7 +450,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
     case kGemmSwiGLU: return launch_one<kGemmSwiGLU>(maps, p, grid, s);
     case kGemmPlain: return launch_one<kGemmPlain>(maps, p, grid, s);
     case kGemmCombineK1: return launch_one<kGemmCombineK1>(maps, p, grid, s);
-    default: return launch_one<kGemmPlainBf16>(maps, p, grid, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -3,8 +3,8 @@
 // row per lane) -> a padded shared staging block -> global memory, with every
 // store instruction writing whole 128-byte lines (4 rows of fp32 or 8 rows of
 // bf16).  KIND selects SwiGLU (gate columns 0-127 and up columns 128-255 of
-// the accumulator, bf16 out), bf16 rows (plain, or gate-scaled into the
-// tokens' rows of Y: the top-1 combine), or fp32 rows.
+// the accumulator, bf16 out), gate-scaled bf16 rows into the tokens' rows of
+// Y (the top-1 combine), or fp32 rows.
 #pragma once
 
 #include "moe_common.cuh"
@@ -71,12 +71,11 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, uint32_t tb,
       }
       __syncwarp();
     }
-  } else if (KIND == kGemmPlainBf16 || KIND == kGemmCombineK1) {
-    // Linear2 rows rounded once to bf16 (RNE) for the combine; or, with the
-    // top-1 combine fused here, each row scaled by its token's gate, rounded
-    // once and stored to that token's row of Y (with k = 1 the permutation
-    // entry of an assignment row is its token)
-    constexpr bool K1 = (KIND == kGemmCombineK1);
+  } else if (KIND == kGemmCombineK1) {
+    // the top-1 combine fused here: each row scaled by its token's gate,
+    // rounded once to bf16 (RNE) and stored to that token's row of Y (with
+    // k = 1 the permutation entry of an assignment row is its token)
+    constexpr bool K1 = true;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     float g = 1.0f;
     if (K1) {

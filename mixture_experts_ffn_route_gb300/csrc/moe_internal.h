@@ -15,7 +15,6 @@ enum GemmKind {
   kGemmRouter = 0,     // fp32 logits
   kGemmSwiGLU = 1,     // Linear1 + SwiGLU, bf16 out
   kGemmPlain = 2,      // Linear2, fp32 out
-  kGemmPlainBf16 = 3,  // Linear2, bf16 out (the inference forward)
   kGemmCombineK1 = 4   // Linear2 with the top-1 combine: gate-scaled bf16 rows
                        // written to their tokens' rows of Y
 };

@@ -32,26 +32,69 @@ constexpr size_t kNoAllocScratchBytes = kChunkCntBytes + kTileOffBytes + kInvByt
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array, looked up once per device with that device
-// current (in host code the array's name is only a stand-in, not an address).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime (no
+// link-time dependency on the driver library).
+static void context_fns(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
+  static CtxGetCurrentFn f_cur = nullptr;
+  static CtxGetIdFn f_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f_cur = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f_id = reinterpret_cast<CtxGetIdFn>(ptr);
+  });
+  *cur = f_cur;
+  *id = f_id;
+}
+
+// Unique id of the calling thread's current context, 0 if there is none (or
+// the driver calls are unavailable).  Ids are never reused within a process,
+// so a context created after a device reset gets a new one.
+static unsigned long long current_context_id() {
+  CtxGetCurrentFn cur;
+  CtxGetIdFn id;
+  context_fns(&cur, &id);
+  CUcontext ctx = nullptr;
+  unsigned long long v = 0;
+  if (cur == nullptr || id == nullptr || cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  return id(ctx, &v) == CUDA_SUCCESS ? v : 0;
+}
+
+// Device address of the array in the current context (in host code the
+// array's name is only a stand-in, not an address).  It is looked up with
+// cudaGetSymbolAddress the first time a context calls, with its device
+// current, and kept per context: a device reset ends the context, and the
+// next call, from the new context, looks the address up again.
 static void* noalloc_scratch_ptr(cudaError_t* err) {
+  constexpr int kSlots = 64;
   static std::mutex mu;
-  static void* ptrs[64] = {nullptr};
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
+  static unsigned long long ids[kSlots] = {0};
+  static void* ptrs[kSlots] = {nullptr};
+  static int next = 0;
   std::lock_guard<std::mutex> g(mu);
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
+  unsigned long long ctx = current_context_id();
+  if (ctx != 0)
+    for (int i = 0; i < kSlots; ++i)
+      if (ids[i] == ctx) return ptrs[i];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current
+  if (*err != cudaSuccess) return nullptr;
+  ctx = current_context_id();
+  if (ctx != 0) {
+    ids[next] = ctx;
+    ptrs[next] = p;
+    next = (next + 1) % kSlots;
   }
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace moe
@@ -83,8 +126,8 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_params* p, const int32_t* E
   b.perm = perm;
   b.nchunk = dispatch_chunks(static_cast<int>(A));
   // Nothing in the array has to start at zero: every word a call reads was
-  // written earlier in the same call.  Ids outside [0, E) are dropped (no
-  // status word here; the counts show them as missing).
+  // written earlier in the same call.  Ids outside [0, E) are dropped; there
+  // is no status word here, so they show only as offsets[E] < T * k.
   err = launch_dispatch(E_ids, p->T, p->k, p->E, 0, b, nullptr, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -41,7 +41,7 @@ import os
 
 import numpy as np
 
-__all__ = ["CONFIGS", "get_config", "make_inputs", "make_inputs_torch",
+__all__ = ["CONFIGS", "get_config", "make_inputs", "make_inputs_torch", "covering_tokens",
            "bf16_bits_from_f32", "f32_from_bf16_bits", "zipf_targets",
            "zipf_offsets"]
 
@@ -117,6 +117,9 @@ CONFIGS["c3p_mxa4"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e2m1")
 CONFIGS["c3r"] = dict(CONFIGS["c3"], I=64)
 # the pages' own V4-Pro routing rule (sqrt-softplus affinity) at the c3 shapes
 CONFIGS["c3_sp"] = dict(CONFIGS["c3"], score="sqrt_softplus", skew=None)
+# the V4-Pro layer at the pages' own expert width f = 3072 (the model table of
+# the Megatron DeepSeek-V4 page); the other recipes of c3 unchanged
+CONFIGS["c3_f3072"] = dict(CONFIGS["c3"], I=3072)
 
 
 def get_config(name_or_cfg, **overrides) -> dict:
@@ -419,3 +422,31 @@ def make_inputs_torch(name_or_cfg, seed: int = 1234, device="cuda", token_seed=N
         d["tid2eid"] = keys.topk(k, dim=1).indices.to(torch.int32).contiguous()
         d["token_ids"] = torch.randint(0, V, (T,), generator=gen(11, True), device=dev, dtype=torch.int32)
     return d
+
+
+# --------------------------------------------------------------------------- samples
+def covering_tokens(ids, E: int, n_min: int, n_extra: int = 0, seed: int = 5) -> np.ndarray:
+    """Sorted indices of a seeded token sample that reaches every expert some
+    token is routed to: for each expert in turn, the first token in a seeded
+    random order that is routed to it, unless a token already taken reaches
+    it; then random tokens up to n_min; then n_extra more random tokens.
+    ``ids`` [T, k] are the tokens' expert ids (ids outside [0, E) reach no
+    expert)."""
+    ids = np.asarray(ids)
+    rng = np.random.default_rng(seed)
+    T = ids.shape[0]
+    order = rng.permutation(T)
+    pos = np.empty(T, np.int64)
+    pos[order] = np.arange(T)
+    taken = np.zeros(T, bool)
+    for e in range(E):
+        hit = np.nonzero((ids == e).any(axis=1))[0]
+        if hit.size and not taken[hit].any():
+            taken[hit[np.argmin(pos[hit])]] = True
+
+    def fill(want):
+        free = order[~taken[order]]
+        taken[free[:max(0, min(want, T) - int(taken.sum()))]] = True
+    fill(n_min)
+    fill(int(taken.sum()) + n_extra)
+    return np.nonzero(taken)[0]

@@ -10,17 +10,24 @@ import mixture_experts_ffn_route_gb300 as moe
 
 DEV = torch.device("cuda:0")
 
-# Y tolerance.  The layer's stated bar is max |err| <= 2e-2 * RMS(Y_ref) with
-# fp32 accumulation and bf16 I/O.  The bf16 output format alone rounds each
-# element by up to 2^-8 of its magnitude, which exceeds 2e-2 * RMS on the
-# largest elements of a Gaussian-like output, so the bound is applied to the
-# error beyond that rounding: |y - y_ref| <= 2e-2 * RMS(Y_ref) + 2^-8 |y_ref|.
+# Y tolerance: the layer's stated bar, max |err| <= 2e-2 * RMS(Y_ref) with
+# fp32 accumulation and bf16 I/O, where Y_ref is the oracle's output rounded
+# once to bf16 (round to nearest even) and the oracle rounds to bf16 where the
+# path keeps bf16 numbers between its kernels (the SwiGLU rows of the bf16
+# forward; the quantised forms' oracles quantise their activations as the
+# path does).  Without that intermediate rounding in the oracle, the bf16
+# SwiGLU rows alone move y by about 1e-3 RMS before the final rounding, which
+# flips the final bf16 rounding of some of the largest outputs by one unit in
+# the last place (2^-7 of their size, 2-4% of RMS); those flips are counted
+# and reported against the exact oracle, not allowed for in the bar.
 Y_RTOL_RMS = 2e-2
-Y_OUT_ULP = 2.0 ** -8
-# Gates: g = alpha * a_e / sum a (or a softmax value) from fp32 tensor-core
-# logits.  d(log g) is a difference of logit errors weighted by slopes <= 1, so
-# |dg/g| <= 2 max|dl|; the router tests hold |dl| (score space) under 1e-4,
-# hence a relative tolerance of 2e-4.
+# Against the exact (unrounded-intermediate) oracle the error RMS stays under
+# this fraction of RMS: the bf16 SwiGLU rows contribute about 2^-9 / sqrt(3)
+# of RMS, the final rounding about 2^-9 / sqrt(3) of each element.
+Y_EXACT_RMS_ERR = 3e-3
+# (case, max|err|/RMS vs the rounded oracle, max|err|/RMS vs the exact
+# oracle or None, elements beyond the bar vs the exact oracle or None, size)
+Y_STATS = []
 G_RTOL = 2e-4
 
 
@@ -100,17 +107,50 @@ def run_forward(p, dd, E_ids, G, ws, Y=None):
     return Y
 
 
-def check_y(Y_gpu, Y_ref, what=""):
-    """Assert the output tolerance; return (max|err|/RMS, worst err/allowance)."""
+def _rne_bf16(y):
+    """float64 -> nearest bf16 value (ties to even), as float64."""
+    import oracle
+    return oracle.round_to_bf16(np.asarray(y, dtype=np.float64))
+
+
+def check_y(Y_gpu, Y_ref, what="", Y_exact=None):
+    """Assert max|y - bf16(Y_ref)| <= 2e-2 * RMS(bf16(Y_ref)) element by element.
+
+    Y_ref: the oracle's float64 output with the path's intermediate rounding
+    points.  Y_exact (optional): the oracle without them; the error against
+    its bf16 rounding is recorded (max, count beyond the bar) and its RMS is
+    held under Y_EXACT_RMS_ERR of RMS.  Returns max|err|/RMS."""
     y = Y_gpu.float().cpu().numpy().astype(np.float64) if isinstance(Y_gpu, torch.Tensor) else Y_gpu
     assert np.isfinite(y).all(), f"{what}: non-finite output"
-    rms = float(np.sqrt((Y_ref ** 2).mean()))
-    err = np.abs(y - Y_ref)
-    allow = Y_RTOL_RMS * rms + Y_OUT_ULP * np.abs(Y_ref)
-    worst = float((err / allow).max())
-    assert worst <= 1.0, (f"{what}: worst |err|/allowance = {worst:.3f} "
-                          f"(max|err|/RMS = {err.max() / rms:.3e})")
-    return float(err.max() / rms), worst
+    ref = _rne_bf16(Y_ref)
+    rms = float(np.sqrt((ref ** 2).mean()))
+    err = np.abs(y - ref)
+    ratio = float(err.max() / rms) if rms > 0 else float(err.max())
+    x_ratio = x_beyond = None
+    if Y_exact is not None:
+        xref = _rne_bf16(Y_exact)
+        xrms = float(np.sqrt((xref ** 2).mean()))
+        xerr = np.abs(y - xref)
+        x_ratio = float(xerr.max() / xrms)
+        x_beyond = int((xerr > Y_RTOL_RMS * xrms).sum())
+    Y_STATS.append((what, ratio, x_ratio, x_beyond, int(err.size)))
+    assert err.max() <= Y_RTOL_RMS * rms, (
+        f"{what}: max|err|/RMS = {ratio:.3e} > {Y_RTOL_RMS} "
+        f"({int((err > Y_RTOL_RMS * rms).sum())} of {err.size} elements)")
+    if Y_exact is not None:
+        xe = np.sqrt(((y - xref) ** 2).mean())
+        assert xe <= Y_EXACT_RMS_ERR * xrms, f"{what}: error RMS vs the exact oracle {xe / xrms:.3e}"
+    return ratio
+
+
+def check_y_layer(Y_gpu, what, X, ids, G, W1, W2, Ws1=None, Ws2=None):
+    """check_y for the bf16 forward of a whole small layer: the oracle with
+    the SwiGLU rows rounded to bf16 (the path's one intermediate rounding
+    point) sets the bar; the exact oracle is compared as well."""
+    import oracle
+    Y_r, _ = oracle.forward(X, ids, G, W1, W2, Ws1, Ws2, act_round_bf16=True)
+    Y_x, _ = oracle.forward(X, ids, G, W1, W2, Ws1, Ws2)
+    return check_y(Y_gpu, Y_r, what, Y_exact=Y_x)
 
 
 def check_gates(G_gpu, G_ref, what=""):

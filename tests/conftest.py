@@ -34,3 +34,18 @@ def built_lib():
     if _lib_is_stale():
         b.build()
     return b.LIB
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the Y parity of every checked case: max|err|/RMS against the
+    oracle rounded at the path's rounding points (the bar is 2e-2), and
+    against the exact oracle with the count of elements beyond 2e-2 RMS."""
+    mod = sys.modules.get("_gpu")
+    if mod is None or not mod.Y_STATS:
+        return
+    Y_STATS = mod.Y_STATS
+    tr = terminalreporter
+    tr.write_sep("-", "Y parity (max|err|/RMS; bar 2e-2)")
+    for what, r, xr, xb, n in Y_STATS:
+        extra = "" if xr is None else f"  exact oracle: {xr:.3e}, {xb} of {n} beyond the bar"
+        tr.write_line(f"{what[:60]:60s} {r:.3e}{extra}")

@@ -5,6 +5,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -60,3 +61,28 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--workload", "c3s", "--steps", "1", "--warmup", "3"],
                        capture_output=True, text=True, cwd=ROOT, timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_covering_tokens_reach_every_expert():
+    import synth
+    rng = np.random.default_rng(3)
+    T, E, k = 4096, 384, 6
+    ids = np.argsort(rng.random((T, E)) ** np.linspace(0.2, 3, E), axis=1)[:, :k]
+    rows = synth.covering_tokens(ids, E, 512, 256)
+    assert len(rows) == 768 and np.all(np.diff(rows) > 0)
+    assert np.unique(ids[rows]).size == np.unique(ids).size
+    assert np.array_equal(rows, synth.covering_tokens(ids, E, 512, 256))  # seeded
+    few = synth.covering_tokens(ids[:10], E, 4)
+    assert np.array_equal(few, np.arange(10))  # 10 tokens cannot reach 60 experts with fewer
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    import synth
+    dd = synth.make_inputs_torch("c3s", device="cpu")
+    before = bench._blas_threads()
+    b = bench.cpu_baseline(dd, 64, 16)
+    assert bench._blas_threads() == before  # restored
+    for key in ("value", "unit", "cores", "kind", "cores_all", "value_all", "value_1core", "sample"):
+        assert key in b
+    assert b["extrapolated"] is True and b["cores"] == os.cpu_count()
+    assert b["value"] > 0 and b["value_1core"] > 0 and "every routed expert" in b["sample"]

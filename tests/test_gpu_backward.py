@@ -30,6 +30,9 @@ pytestmark = pytest.mark.gpu
 RTOL_RMS = 2e-2
 FLIP_FRACTION = 1e-3
 RMS_ERR = 1e-2
+# RMS distance of the rounded oracle from the exact gradient, relative to the
+# exact gradient's RMS: five rounding points, each 2^-9 / sqrt(3)
+EXACT_RMS = 5 * 2.0 ** -9 / 3 ** 0.5
 
 
 def _check(got, ref, name, mass, bf16_out=False):
@@ -94,10 +97,19 @@ def test_backward_matches_oracle(name, T):
     for key in ("dWg", "dW1", "dW2", "dG") + (("dWs1", "dWs2") if c["shared"] else ()):
         got = out[key].cpu().numpy()
         _check(got, ref[key], f"{name} {key}", ref["mass_" + key])
-        # against the exact gradient: the bf16 operands move the oracle itself
-        # by up to 8% of RMS at these sizes (dW1 of c4s); bound at 15%
+        # against the exact gradient.  Each of the five bf16 rounding points
+        # moves its operand by a relative error of RMS 2^-9 / sqrt(3); a
+        # gradient depends on at most five of them with sensitivities of order
+        # one, so the rounded oracle's distance d = ref - exact has RMS at most
+        # EXACT_RMS (tests/test_oracle_pins.py checks this on the CPU).  The
+        # GPU is within the parity tolerance of ref, so element by element
+        # |got - exact| <= |d| + 2e-2 RMS + 2^-7 mass, and in RMS the two add.
+        d = np.abs(ref[key] - exact[key])
         rms = np.sqrt((exact[key] ** 2).mean())
-        assert np.abs(got - exact[key]).max() <= 0.15 * rms, (name, key)
+        e = np.abs(got - exact[key])
+        assert np.all(e <= d + RTOL_RMS * np.sqrt((ref[key] ** 2).mean()) + 2.0 ** -7 * ref["mass_" + key]), \
+            (name, key, "exact, per element")
+        assert np.sqrt((e ** 2).mean()) <= (EXACT_RMS + RMS_ERR) * rms, (name, key, "exact, RMS")
 
 
 def test_backward_is_deterministic():

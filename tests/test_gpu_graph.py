@@ -10,7 +10,7 @@ import torch
 import mixture_experts_ffn_route_gb300 as moe
 import oracle
 import synth
-from _gpu import DEV, bf, check_y, params, to_device
+from _gpu import DEV, bf, check_y_layer, params, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -106,5 +106,5 @@ def test_step_replays_as_a_graph(name, form):
                       if c["routing"] == "hash" else
                       oracle.route(x2, h["Wg"], h["bias"], c["score_fn"], k, c["alpha"], c["renorm"]))
         assert np.array_equal(ids_graph.cpu().numpy(), ids)
-        Y_ref, _ = oracle.forward(x2, ids, Gr, h["W1"], h["W2"], h.get("Ws1"), h.get("Ws2"))
-        check_y(Y_graph, Y_ref, f"{name} graph replay")
+        check_y_layer(Y_graph, f"{name} graph replay", x2, ids, Gr, h["W1"], h["W2"], h.get("Ws1"),
+                      h.get("Ws2"))

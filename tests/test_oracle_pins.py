@@ -245,6 +245,53 @@ def test_forward_bruteforce_tiny():
         np.testing.assert_allclose(Y[t], want, rtol=1e-12, atol=1e-12)
 
 
+def _bf16_scalar(v):
+    """Nearest bf16 value of a float, ties to even, written from the format:
+    v = m * 2^e with 0.5 <= |m| < 1 (frexp); bf16 keeps 8 significant bits,
+    so m * 2^8 is rounded to an integer (Python's round() takes halves to the
+    even neighbour) and scaled back."""
+    if v == 0.0:
+        return 0.0
+    m, e = math.frexp(v)
+    return math.ldexp(round(m * 256.0), e - 8)
+
+
+def test_bf16_scalar_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(16)
+    x = (rng.standard_normal(4000) * 2.0 ** rng.integers(-20, 20, 4000)).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert [_bf16_scalar(float(v)) for v in x] == want.tolist()
+
+
+def test_forward_with_bf16_swiglu_rows_matches_scalar_loops():
+    """The oracle's forward with its SwiGLU rows rounded to bf16 (the rounding
+    point of a path that keeps them in bf16 between the two GEMMs), against
+    per-token loops that round each activation with _bf16_scalar; the rounding
+    must also change the result, so the flag is not a no-op."""
+    rng = np.random.default_rng(17)
+    X, E_ids, G, W1, W2, Ws1, Ws2 = _tiny_layer(rng)
+    Y, _ = oracle.forward(X, E_ids, G, W1, W2, Ws1, Ws2, act_round_bf16=True)
+    Y0, _ = oracle.forward(X, E_ids, G, W1, W2, Ws1, Ws2)
+    f = lambda b: synth.f32_from_bf16_bits(b).astype(float).tolist()  # noqa: E731
+    x, w1, w2, s1, s2 = f(X), f(W1), f(W2), f(Ws1), f(Ws2)
+
+    def ffn_rounded(xt, a, b):
+        H, twoI = len(a), len(a[0])
+        I = twoI // 2
+        h = [sum(xt[r] * a[r][c] for r in range(H)) for c in range(twoI)]
+        act = [_bf16_scalar(h[c] / (1.0 + math.exp(-h[c])) * h[I + c]) for c in range(I)]
+        return [sum(act[c] * b[c][o] for c in range(I)) for o in range(len(b[0]))]
+
+    for t in range(X.shape[0]):
+        want = ffn_rounded(x[t], s1, s2)
+        for j in range(E_ids.shape[1]):
+            ye = ffn_rounded(x[t], w1[E_ids[t, j]], w2[E_ids[t, j]])
+            want = [a + G[t, j] * b for a, b in zip(want, ye)]
+        np.testing.assert_allclose(Y[t], want, rtol=1e-12, atol=1e-12)
+    assert np.abs(Y - Y0).max() > 1e-6 * np.abs(Y0).max()
+
+
 def _dense_ffn(X64, W1_64, W2_64):
     """Dense SwiGLU FFN with SiLU written through tanh: z*sigma(z) = z*(1+tanh(z/2))/2."""
     I = W2_64.shape[0]
@@ -673,3 +720,101 @@ def test_backward_matches_torch_autograd():
     (torch.tensor(dY) * Y).sum().backward()
     for n, key in dict(X="dX", Wg="dWg", W1="dW1", W2="dW2", Ws1="dWs1", Ws2="dWs2").items():
         assert np.allclose(g[key], t[n].grad.numpy(), rtol=1e-9, atol=1e-11), key
+
+
+def _backward_loops_bf16(X, Wg, ids, dY, W1, W2, Ws1, Ws2, alpha):
+    """Gradients of a tiny sigmoid-routed layer (renormalised gates, shared
+    expert) by scalar loops, rounding to bf16 (_bf16_scalar) at the five
+    points where a bf16 path keeps its tensors: the pre-activations H as the
+    backward reads them, the SwiGLU output A (from the unrounded H), the
+    gate-scaled row gradient g dY, the pre-activation gradient dH, and the
+    logit gradient before its two products."""
+    T, H = X.shape
+    E, k, I = Wg.shape[1], ids.shape[1], W2.shape[1]
+    bf, sig = _bf16_scalar, (lambda z: 1.0 / (1.0 + math.exp(-z)))
+    silu = lambda z: z * sig(z)  # noqa: E731
+    dsilu = lambda z: sig(z) * (1.0 + z * (1.0 - sig(z)))  # noqa: E731
+    dX = np.zeros((T, H))
+    dWg = np.zeros((H, E))
+    dW1, dW2 = np.zeros((E, H, 2 * I)), np.zeros((E, I, H))
+    dWs1, dWs2 = np.zeros((H, 2 * I)), np.zeros((I, H))
+    dG = np.zeros((T, k))
+
+    def branch(t, w1, w2, gate, dw1, dw2):
+        """One expert FFN branch of token t: accumulates dX, dw1, dw2 and
+        returns <dY_t, y> (y the branch output, A rounded)."""
+        h = [sum(X[t, r] * w1[r, c] for r in range(H)) for c in range(2 * I)]
+        hk = [bf(v) for v in h]
+        act = [bf(silu(h[c]) * h[I + c]) for c in range(I)]
+        y = [sum(act[c] * w2[c, o] for c in range(I)) for o in range(H)]
+        dout = [bf(gate * dY[t, o]) for o in range(H)]
+        dA = [sum(dout[o] * w2[c, o] for o in range(H)) for c in range(I)]
+        dh = ([bf(dA[c] * hk[I + c] * dsilu(hk[c])) for c in range(I)]
+              + [bf(dA[c] * silu(hk[c])) for c in range(I)])
+        for c in range(I):
+            for o in range(H):
+                dw2[c, o] += act[c] * dout[o]
+        for r in range(H):
+            for c in range(2 * I):
+                dw1[r, c] += X[t, r] * dh[c]
+            dX[t, r] += sum(dh[c] * w1[r, c] for c in range(2 * I))
+        return sum(dY[t, o] * y[o] for o in range(H))
+
+    for t in range(T):
+        l = [sum(X[t, r] * Wg[r, e] for r in range(H)) for e in range(E)]
+        a = [sig(v) for v in l]
+        S = sum(a[ids[t, j]] for j in range(k))
+        g = [alpha * a[ids[t, j]] / S for j in range(k)]
+        branch(t, Ws1, Ws2, 1.0, dWs1, dWs2)
+        for j in range(k):
+            e = ids[t, j]
+            dG[t, j] = branch(t, W1[e], W2[e], g[j], dW1[e], dW2[e])
+        # g_j = alpha a_j / S:  dL/da_i = alpha / S (dG_i - sum_j dG_j a_j / S)
+        da = [0.0] * E
+        ssum = sum(dG[t, j] * a[ids[t, j]] for j in range(k)) / S
+        for j in range(k):
+            da[ids[t, j]] += alpha / S * (dG[t, j] - ssum)
+        dl = [bf(da[e] * a[e] * (1.0 - a[e])) for e in range(E)]
+        for r in range(H):
+            for e in range(E):
+                dWg[r, e] += X[t, r] * dl[e]
+            dX[t, r] += sum(dl[e] * Wg[r, e] for e in range(E))
+    return dict(dX=dX, dWg=dWg, dW1=dW1, dW2=dW2, dWs1=dWs1, dWs2=dWs2, dG=dG)
+
+
+def test_backward_with_bf16_rounding_points_matches_scalar_loops():
+    X, Wg, W1, W2, Ws1, Ws2, ids, dY = _bwd_case(31, T=3, H=6, E=4, k=2, I=3, shared=True)
+    X = oracle.round_to_bf16(X)
+    alpha = 2.5
+    got = oracle.backward(X, Wg, ids, dY, W1, W2, Ws1, Ws2, 0, alpha, True, round_bf16=True)
+    want = _backward_loops_bf16(X, Wg, ids, dY, W1, W2, Ws1, Ws2, alpha)
+    exact = oracle.backward(X, Wg, ids, dY, W1, W2, Ws1, Ws2, 0, alpha, True)
+    for key, w in want.items():
+        scale = np.abs(w).max()
+        assert np.allclose(got[key], w, rtol=1e-12, atol=1e-12 * scale), key
+        # the rounding points move every gradient, so none of them is a no-op
+        assert np.abs(got[key] - exact[key]).max() > 1e-6 * scale, key
+
+
+@pytest.mark.parametrize("name", ["c1s", "c3s", "c4s", "c5s"])
+def test_backward_rounding_points_move_gradients_by_the_derived_rms(name):
+    """The five bf16 rounding points of the rounded backward each move an
+    operand by a relative error of RMS 2^-9 / sqrt(3) (uniform over half an
+    ulp of 8 significant bits); a gradient depends on at most five of them,
+    so its RMS distance from the exact gradient is at most 5 * 2^-9 / sqrt(3)
+    of its RMS.  This is the bound the GPU backward tests use."""
+    h = synth.make_inputs(name)
+    c = h["cfg"]
+    if c["routing"] == "hash":
+        ids = h["tid2eid"][h["token_ids"]]
+    else:
+        ids, _, _ = oracle.route(h["X"], h["Wg"], h["bias"], c["score_fn"], c["k"], c["alpha"], c["renorm"])
+    dY = oracle.bf16_to_f64(synth.upstream_grad(c["T"], c["H"]))
+    args = (h["X"], h["Wg"], ids, dY, h["W1"], h["W2"], h["Ws1"], h["Ws2"], c["score_fn"], c["alpha"],
+            c["renorm"])
+    ref = oracle.backward(*args, round_bf16=True)
+    exact = oracle.backward(*args)
+    bound = 5 * 2.0 ** -9 / math.sqrt(3)
+    for key in ("dX", "dWg", "dW1", "dW2", "dG") + (("dWs1", "dWs2") if c["shared"] else ()):
+        rms = np.sqrt((exact[key] ** 2).mean())
+        assert np.sqrt(((ref[key] - exact[key]) ** 2).mean()) <= bound * rms, key

@@ -1,9 +1,10 @@
 """moe_dispatch_noalloc, the dispatch for callers that cannot allocate device
 memory where they route tokens (their memory belongs to another allocator, or
 a cudaMalloc that may synchronise the device is not allowed on their path).
-Its scratch is a fixed array inside the library, so the test checks that two
-calls in a row, on different inputs, each match moe_dispatch exactly (the
-dispatch is integer work: bit-exact)."""
+Its scratch is a fixed array inside the library, so the test checks that
+calls in a row, on different inputs, each match moe_dispatch and the CPU
+oracle's dispatch exactly (the dispatch is integer work: bit-exact), one of
+them with ids outside [0, E), which are dropped and show as offsets[E] < T k."""
 import ctypes
 
 import numpy as np
@@ -11,6 +12,7 @@ import pytest
 import torch
 
 import mixture_experts_ffn_route_gb300 as moe
+import oracle
 
 DEV = torch.device("cuda:0")
 
@@ -41,21 +43,33 @@ def _without_workspace(p, E_ids):
 
 
 @pytest.mark.gpu
-def test_noalloc_dispatch_matches_the_workspace_dispatch_twice_in_a_row(built_lib):
+def test_noalloc_dispatch_matches_the_workspace_dispatch_and_the_oracle(built_lib):
     moe.lib()
     torch.cuda.set_device(DEV)
     # first call: V4-Pro-like routing (E 384, top-6, 4096 tokens: several chunks);
     # second call: a different, smaller problem whose results must not carry
-    # anything over from the first
-    cases = [(4096, 384, 6, 1), (1000, 40, 3, 2)]
-    for T, E, k, seed in cases:
+    # anything over from the first; third: ids outside [0, E) in two chunks
+    cases = [(4096, 384, 6, 1, False), (1000, 40, 3, 2, False), (5000, 24, 3, 3, True)]
+    for T, E, k, seed, bad in cases:
         p = moe.make_params(T, 64, E, k, 64)
-        E_ids = torch.from_numpy(_ids(T, E, k, seed)).to(DEV)
-        want = _with_workspace(p, E_ids)
+        ids = _ids(T, E, k, seed)
+        if bad:
+            ids[7, 1] = -1
+            ids[4100, 0] = E
+            ids[4999, 2] = 10 ** 6
+        E_ids = torch.from_numpy(ids).to(DEV)
         got = _without_workspace(p, E_ids)
-        for w, g in zip(want, got):
-            np.testing.assert_array_equal(g, w)
-        assert got[0].sum() == T * k
+        rc, ro, rp, _ = oracle.dispatch(ids, E)
+        n = int(ro[-1])
+        np.testing.assert_array_equal(got[0], rc)
+        np.testing.assert_array_equal(got[1], ro)
+        np.testing.assert_array_equal(got[2][:n], rp)
+        assert (got[2][n:] == -9).all()  # entries past offsets[E] are left untouched
+        assert n == T * k - (3 if bad else 0)
+        if not bad:
+            want = _with_workspace(p, E_ids)
+            for w, g in zip(want, got):
+                np.testing.assert_array_equal(g, w)
 
 
 def test_noalloc_dispatch_rejects_sizes_past_its_limits(built_lib):
