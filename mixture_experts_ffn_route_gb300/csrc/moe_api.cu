@@ -30,9 +30,13 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct WsLayout {
-  size_t status, logits, wgt, rcount, flagged, pairs, s64, chunk_cnt, counts, row_off, tile_off,
-      perm, inv, act, yp, total;
+  size_t status, logits, wgt, flagged, fnorm, pairs, plogit, s64, chunk_cnt, counts, row_off,
+      tile_off, perm, inv, act, yp, total;
 };
+
+// The status header (256 bytes, zeroed by moe_workspace_init): the status
+// word at byte 0; the router's re-decision list counters at byte 64.
+constexpr size_t kRouteCountersAt = 64;
 
 static WsLayout layout(const moe_params& p) {
   WsLayout L;
@@ -43,11 +47,12 @@ static WsLayout layout(const moe_params& p) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(256);
-  L.logits = take(T * E * sizeof(float));
+  L.logits = take(T * E * sizeof(float));  // general router path only
   L.wgt = take(static_cast<size_t>(p.H) * E * 2);
-  L.rcount = take(4 * sizeof(int));
   L.flagged = take(T * 4 * sizeof(int));
+  L.fnorm = take(T * 2 * sizeof(float));
   L.pairs = take(T * E * 2 * sizeof(int));
+  L.plogit = take(T * E * sizeof(float));
   L.s64 = take(T * E * sizeof(double));
   L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
   L.counts = take((E + 2) * sizeof(int));
@@ -274,6 +279,17 @@ moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_u
   return cuda_status(cudaGetLastError());
 }
 
+static RouteScratch route_scratch(void* ws, const WsLayout& L) {
+  RouteScratch rs;
+  rs.counters = at<int>(ws, kRouteCountersAt);
+  rs.flagged = at<int4>(ws, L.flagged);
+  rs.fnorm = at<float2>(ws, L.fnorm);
+  rs.pairs = at<int2>(ws, L.pairs);
+  rs.plogit = at<float>(ws, L.plogit);
+  rs.key = at<unsigned long long>(ws, L.s64);
+  return rs;
+}
+
 moe_status moe_route_logits(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
                             float* logits, void* ws, size_t ws_bytes, void* stream) {
   moe_status st = check_params(p);
@@ -283,7 +299,22 @@ moe_status moe_route_logits(const moe_params* p, const uint16_t* X, const uint16
   if (p->T == 0) return MOE_OK;
   if (!X || !Wg || !logits || !aligned16(X) || !aligned16(Wg) || !aligned16(logits))
     return MOE_ERR_INVALID_ARG;
-  return run_router_gemm(p, X, Wg, logits, at<int>(ws, 0), static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!route_fused_supported(p->E, p->H))
+    return run_router_gemm(p, X, Wg, logits, at<int>(ws, 0), s);
+  // the fused router's own logits (the ones its decisions are taken on)
+  const WsLayout L = layout(*p);
+  RouteFusedArgs a;
+  memset(&a, 0, sizeof(a));
+  a.X = X;
+  a.Wg = Wg;
+  a.T = p->T; a.H = p->H; a.E = p->E; a.k = p->k; a.score_fn = p->score_fn; a.renorm = p->renorm;
+  a.alpha = p->alpha;
+  a.select = 0;
+  a.logits_out = logits;
+  a.rs = route_scratch(ws, L);
+  a.status = at<int>(ws, L.status);
+  return cuda_status(launch_route_fused(a, s));
 }
 
 moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
@@ -303,17 +334,32 @@ moe_status moe_route(const moe_params* p, const uint16_t* X, const uint16_t* Wg,
   const WsLayout L = layout(*p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(ws, L.status);
-  float* logits = at<float>(ws, L.logits);
   uint16_t* WgT = at<uint16_t>(ws, L.wgt);
-  RouteScratch rs;
-  rs.counters = at<int>(ws, L.rcount);
-  rs.flagged = at<int4>(ws, L.flagged);
-  rs.pairs = at<int2>(ws, L.pairs);
-  rs.key = at<unsigned long long>(ws, L.s64);
-  if (!hash) {
-    if (cudaMemsetAsync(rs.counters, 0, 4 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_transpose_wg(Wg, p->H, p->E, WgT, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const RouteScratch rs = route_scratch(ws, L);
+  if (route_fused_supported(p->E, p->H)) {
+    // one launch: gating GEMM + scores + top-k (or hash lookup) + gates; for
+    // top-k two more that re-decide the close tokens from float64 logits
+    RouteFusedArgs a;
+    a.X = X;
+    a.Wg = Wg;
+    a.bias = bias;
+    a.token_ids = token_ids;
+    a.tid2eid = tid2eid;
+    a.V = V;
+    a.T = p->T; a.H = p->H; a.E = p->E; a.k = p->k; a.score_fn = p->score_fn; a.renorm = p->renorm;
+    a.alpha = p->alpha;
+    a.select = 1;
+    a.E_ids = E_ids;
+    a.G = G;
+    a.logits_out = nullptr;
+    a.WgT = hash ? nullptr : WgT;
+    a.rs = rs;
+    a.status = status;
+    return cuda_status(launch_route_fused(a, s));
   }
+  // general path: fp32 logits to the workspace, then the selection
+  float* logits = at<float>(ws, L.logits);
+  if (!hash && launch_transpose_wg(Wg, p->H, p->E, WgT, s) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_router_gemm(p, X, Wg, logits, status, s)) != MOE_OK) return st;
   return cuda_status(launch_route_select(logits, X, WgT, bias, token_ids, tid2eid, V, p->T, p->H,
                                          p->E, p->k, p->score_fn, p->alpha, p->renorm, E_ids, G,

@@ -194,20 +194,54 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
                         cudaStream_t s);
 int gemm_block_n(GemmKind kind);
 
-// Router selection over fp32 logits [T, E] (top-k with a float64 re-decision
-// of close tokens, or the hash lookup).  Scratch for the re-decision:
+// Router.  Scratch of the float64 re-decision of close tokens:
 struct RouteScratch {
-  int* counters;  // [0] close tokens, [1] candidate pairs; zeroed before select
+  int* counters;  // [0] close tokens, [1] candidate pairs; zero between calls
+                  // (the reselect kernel zeroes them when it is done)
   int4* flagged;  // [T]      {token, first pair, pair count, 0}
+  float2* fnorm;  // [T]      softmax normaliser of a close token {max logit, sum exp}
   int2* pairs;    // [T * E]  {token, expert}
+  float* plogit;  // [T * E]  fp32 logit of each pair (for the gates)
   unsigned long long* key;  // [T * E]  order-preserving key of each pair's float64 score
 };
 cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT, cudaStream_t s);
+// Selection over fp32 logits [T, E] (top-k with the float64 re-decision of
+// close tokens, or the hash lookup).
 cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
                                 const float* bias, const int32_t* token_ids,
                                 const int32_t* tid2eid, int V, int T, int H, int E, int k,
                                 int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
                                 const RouteScratch& rs, int* status, cudaStream_t s);
+// The float64 re-decision alone (recheck + reselect) of the tokens listed in rs.
+cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
+                                 int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
+                                 float* G, const RouteScratch& rs, cudaStream_t s);
+// Fused router (moe_route_fused.cu): the gating GEMM on the tensor cores with
+// the scores, the selection bias, the top-k (or the hash lookup), the gates
+// and the listing of close tokens in its epilogue; split over K across a
+// cluster of CTAs whose partial logits are summed through distributed shared
+// memory.  Writes Wg transposed into WgT (for the re-decision) when WgT is
+// set, and the fp32 logits into logits_out when that is set; select = 0
+// writes only those.  Returns cudaErrorNotSupported for shapes it does not
+// take (E > 384 or H % 64 != 0), so the caller can use the general path.
+struct RouteFusedArgs {
+  const uint16_t* X;
+  const uint16_t* Wg;
+  const float* bias;
+  const int32_t* token_ids;
+  const int32_t* tid2eid;
+  int V, T, H, E, k, score_fn, renorm;
+  float alpha;
+  int select;
+  int32_t* E_ids;
+  float* G;
+  float* logits_out;
+  uint16_t* WgT;
+  RouteScratch rs;
+  int* status;
+};
+bool route_fused_supported(int E, int H);
+cudaError_t launch_route_fused(const RouteFusedArgs& a, cudaStream_t s);
 
 // Dispatch: counts, offsets, permutation, inverse, tile offsets, gathered rows.
 struct DispatchBufs {

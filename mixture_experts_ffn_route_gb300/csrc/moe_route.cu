@@ -1,4 +1,6 @@
-// Router selection over the fp32 logits of the gating GEMM.
+// Router selection over fp32 logits (the general path, for layers whose
+// experts do not fit the fused router of moe_route_fused.cu), and the
+// float64 re-decision of close tokens that both paths share.
 //
 // "Megatron-LM 的 MoE 并行：以 DeepSeek-V4 为例", section 路由与负载 / 路由张量:
 //   a = score(l);  I_t = TopK(a + beta);  g = alpha * a / sum_{I_t} a
@@ -11,77 +13,28 @@
 // 1e-5 of the exact value, so the fp32 selection is final unless two
 // neighbouring scores among the first k+1 lie within a decision band.  Such a
 // token is re-decided in three steps:
-//   select    one warp per token: fp32 top-(k+1) by k+1 warp arg-max rounds;
-//             a close token appends every expert scoring within twice the band
-//             of its k-th score to a list of (token, expert) pairs;
+//   select    fp32 top-(k+1) by k+1 warp arg-max rounds; a close token appends
+//             every expert scoring within twice the band of its k-th score to
+//             a list of (token, expert) pairs, with the pair's fp32 logit (and
+//             the token's softmax normaliser);
 //   recheck   four warps per pair: the logit sum_h X[t,h] Wg[h,e] to ~48 bits
 //             over a transposed copy of Wg (contiguous rows; each bf16 product
 //             is exact in fp32 and the sum is carried as a float pair), then
 //             its float64 selection score;
-//   reselect  one warp per close token: top-k of the float64 scores of its
-//             candidates, larger score first, equal scores to the lower id.
+//   reselect  one block, a warp per close token: top-k of the float64 scores
+//             of its candidates, larger score first, equal scores to the lower
+//             id; gates from the listed fp32 logits.  The block then zeroes
+//             the list counters for the next call.
 // The ids then equal those of an exact evaluation except at exact ties.
 #include <float.h>
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_route.cuh"
 
 namespace moe {
 
 constexpr int kWarps = 8;  // tokens (or pairs) per 256-thread block
-constexpr int kMaxK = 16;
-// Decision bands.  Sigmoid and sqrt-softplus have slope <= 1/3, so their fp32
-// scores are within ~2e-5 of exact; a band of 2e-4 on the score leaves a
-// margin of about 10x.  Softmax selects on the logit itself; its band is
-// 1e-3 * max(1, |l|).
-constexpr float kBand = 2e-4f;
-constexpr float kBandSoftmax = 1e-3f;
-
-__device__ __forceinline__ float band_at(float v, int fn) {
-  return fn == 2 ? kBandSoftmax * fmaxf(1.0f, fabsf(v)) : kBand;
-}
-
-__device__ __forceinline__ float score_f32(float l, int fn) {
-  if (fn == 0) return 1.0f / (1.0f + expf(-l));
-  if (fn == 1) return sqrtf(fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l))));
-  return l;  // softmax: select on the logit (monotone in the softmax value)
-}
-
-__device__ __forceinline__ double score_f64(double l, int fn) {
-  if (fn == 0) return 1.0 / (1.0 + exp(-l));
-  if (fn == 1) return sqrt(fmax(l, 0.0) + log1p(exp(-fabs(l))));
-  return l;
-}
-
-// (value, id) order: larger value first, equal values lower id first.
-template <typename V>
-__device__ __forceinline__ bool before(V v, int id, V ov, int oid) {
-  return v > ov || (v == ov && id < oid);
-}
-
-template <typename V>
-__device__ __forceinline__ void warp_argmax(V& v, int& id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const V ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oid = __shfl_xor_sync(0xffffffffu, id, o);
-    if (before(ov, oid, v, id)) { v = ov; id = oid; }
-  }
-}
-
-template <typename V>
-__device__ __forceinline__ V warp_sum(V v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // Softmax normaliser of one token's logits: max and sum of exp(l - max).
 __device__ __forceinline__ void softmax_norm(const float* lrow, int E, int lane, float& lmax,
                                              float& zsum) {
@@ -202,13 +155,18 @@ __global__ void __launch_bounds__(kWarps * 32)
         base = atomicAdd(rs.counters + 1, count);
         const int fi = atomicAdd(rs.counters + 0, 1);
         rs.flagged[fi] = make_int4(t, base, count, 0);
+        rs.fnorm[fi] = make_float2(lmax, zsum);
       }
       base = __shfl_sync(0xffffffffu, base, 0);
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
         const bool cand = e < E && s[e] >= lim;
         const unsigned m = __ballot_sync(0xffffffffu, cand);
-        if (cand) rs.pairs[base + __popc(m & ((1u << lane) - 1u))] = make_int2(t, e);
+        if (cand) {
+          const int at = base + __popc(m & ((1u << lane) - 1u));
+          rs.pairs[at] = make_int2(t, e);
+          rs.plogit[at] = lrow[e];
+        }
         base += __popc(m);
       }
     }
@@ -310,30 +268,37 @@ __global__ void __launch_bounds__(kRecheckWarps * 32)
   }
 }
 
-// Re-decide each close token from the float64 scores of its candidates.
-__global__ void __launch_bounds__(kWarps * 32)
-    route_reselect_kernel(const float* __restrict__ logits, int E,
-                          int k, int fn, float alpha, int renorm, int32_t* __restrict__ E_ids,
-                          float* __restrict__ G, RouteScratch rs, int* status) {
-  const int n = rs.counters[0];
+// Re-decide each close token from the float64 scores of its candidates: one
+// block, a warp per close token.  The gates come from the candidates' listed
+// fp32 logits (and, for softmax, the token's listed normaliser).  At the end
+// the block zeroes the list counters, so the next call starts empty.
+constexpr int kReselectWarps = 32;
+
+__global__ void __launch_bounds__(kReselectWarps * 32)
+    route_reselect_kernel(int k, int fn, float alpha, int renorm, int32_t* __restrict__ E_ids,
+                          float* __restrict__ G, RouteScratch rs) {
+  const int n = *reinterpret_cast<volatile int*>(rs.counters);
   const int lane = threadIdx.x & 31;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < n; j += nw) {
+  for (int j = threadIdx.x >> 5; j < n; j += kReselectWarps) {
     const int4 f = rs.flagged[j];
     const int t = f.x, base = f.y, count = f.z;
+    const float2 nrm = rs.fnorm[j];
     // candidates held in registers, up to 4 per lane (count <= 128); more
     // candidates than that are read from memory each round.  Scores are
     // order-preserving integer keys: larger key = larger score.
     constexpr int kHold = 4;
     unsigned long long cv[kHold];
     int ce[kHold];
+    float cl[kHold];
 #pragma unroll
     for (int h = 0; h < kHold; ++h) {
       const int i = lane + 32 * h;
       cv[h] = i < count ? rs.key[base + i] : 0ull;
       ce[h] = i < count ? rs.pairs[base + i].y : 0x7fffffff;
+      cl[h] = i < count ? rs.plogit[base + i] : 0.0f;
     }
     int my_sel = -1;
+    float my_l = 0.0f;
     unsigned long long last_v = ~0ull;
     int last_id = -1;
     // round r: the best candidate strictly after the previous winner in the
@@ -342,27 +307,45 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int r = 0; r < k; ++r) {
       unsigned long long best = 0ull;
       int bid = 0x7fffffff;
+      float bl = 0.0f;
 #pragma unroll
       for (int h = 0; h < kHold; ++h)
         if (before(last_v, last_id, cv[h], ce[h]) && before(cv[h], ce[h], best, bid)) {
           best = cv[h];
           bid = ce[h];
+          bl = cl[h];
         }
       for (int i = lane + 32 * kHold; i < count; i += 32) {
         const int e = rs.pairs[base + i].y;
         const unsigned long long v = rs.key[base + i];
-        if (before(last_v, last_id, v, e) && before(v, e, best, bid)) { best = v; bid = e; }
+        if (before(last_v, last_id, v, e) && before(v, e, best, bid)) {
+          best = v;
+          bid = e;
+          bl = rs.plogit[base + i];
+        }
       }
-      warp_argmax(best, bid);
-      if (lane == r) my_sel = bid;
+      warp_argmax_payload(best, bid, bl);
+      if (lane == r) {
+        my_sel = bid;
+        my_l = bl;
+      }
       last_v = best;
       last_id = bid;
     }
-    const float* lrow = logits + static_cast<long long>(t) * E;
-    float lmax = 0.0f, zsum = 1.0f;
-    if (fn == 2) softmax_norm(lrow, E, lane, lmax, zsum);
-    write_gates(lrow, E, k, fn, alpha, renorm, my_sel, true, lmax, zsum, lane,
-                E_ids + static_cast<long long>(t) * k, G + static_cast<long long>(t) * k, status);
+    const float a = lane < k ? affinity_f32(my_l, fn, nrm.x, nrm.y) : 0.0f;
+    float den = 0.0f;
+    for (int jj = 0; jj < k; ++jj) den += __shfl_sync(0xffffffffu, a, jj);
+    if (lane < k) {
+      float g = alpha * a;
+      if (renorm) g = den > 0.0f ? alpha * a / den : 0.0f;
+      E_ids[static_cast<long long>(t) * k + lane] = my_sel;
+      G[static_cast<long long>(t) * k + lane] = g;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    rs.counters[0] = 0;
+    rs.counters[1] = 0;
   }
 }
 
@@ -388,6 +371,15 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
   return cudaGetLastError();
 }
 
+cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
+                                 int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
+                                 float* G, const RouteScratch& rs, cudaStream_t s) {
+  const int grid = 8 * num_sms();
+  route_recheck_kernel<<<grid, kRecheckWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
+  route_reselect_kernel<<<1, kReselectWarps * 32, 0, s>>>(k, score_fn, alpha, renorm, E_ids, G, rs);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
                                 const float* bias, const int32_t* token_ids,
                                 const int32_t* tid2eid, int V, int T, int H, int E, int k,
@@ -406,11 +398,7 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                                       k, score_fn, alpha, renorm, E_ids, G, rs,
                                                       status);
   if (token_ids != nullptr) return cudaGetLastError();
-  const int grid = 2 * num_sms();
-  route_recheck_kernel<<<4 * grid, kRecheckWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
-  route_reselect_kernel<<<grid, kWarps * 32, 0, s>>>(logits, E, k, score_fn, alpha, renorm, E_ids,
-                                                     G, rs, status);
-  return cudaGetLastError();
+  return launch_route_recheck(X, WgT, bias, H, score_fn, k, alpha, renorm, E_ids, G, rs, s);
 }
 
 }  // namespace moe

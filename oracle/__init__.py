@@ -697,3 +697,138 @@ def forward_mx_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: 
         ok = p >= 0
         Y[ok] += G_rows[ok, j:j + 1] * Yp[p[ok]]
     return Y
+
+
+# ----------------------------------------------------------------------------- decision margins
+# For the tests of a path that decides the activation codes of the quantised
+# forms from float32 values, where this oracle decides them from float64
+# values: if the exact SwiGLU output of an element lies within the float32
+# path's error of a code boundary (or its group's maximum within that error of
+# a power of two), the two may pick neighbouring codes.  The functions below
+# bound, per output element, how far such decisions can move it.  They change
+# none of the values computed above.
+def _swiglu_with_bound(Z, dZ, I):
+    """U = SiLU(Zx) * Zy and a bound dU on |U' - U| for any Z' within dZ of Z:
+    SiLU(Zx + a) - SiLU(Zx) is at most (|SiLU'(Zx)| + |a| / 2) |a| (|SiLU''| <= 1/2),
+    so |dU| <= (|SiLU'(Zx)| + dZx / 2) dZx (|Zy| + dZy) + |SiLU(Zx)| dZy."""
+    Zx, Zy = Z[:, :I], Z[:, I:]
+    dx, dy = dZ[:, :I], dZ[:, I:]
+    U = _silu(Zx) * Zy
+    dU = (np.abs(_silu_grad(Zx)) + 0.5 * dx) * dx * (np.abs(Zy) + dy) + np.abs(_silu(Zx)) * dy
+    return U, dU
+
+
+def _mx_decision_steps(U, dU, fmt: str) -> np.ndarray:
+    """Per element of U [m, K]: the largest change of its Q_MX dequantised value
+    (code times group scale) when the values move anywhere within dU, taking
+    both the element's rounding and its group's shared exponent into account."""
+    _, _, _, vmax = FP8_FORMATS[fmt]
+    emax = int(np.floor(np.log2(vmax)))
+    m, K = U.shape
+    g = U.reshape(m, K // MX_GROUP, MX_GROUP)
+    dg = dU.reshape(g.shape)
+
+    def expo(amax):
+        with np.errstate(divide="ignore"):
+            ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))), -np.inf)
+        return np.clip(ex - emax, -127, 127)[..., None]
+
+    X = expo(np.abs(g).max(axis=-1))
+    chosen = fp8_round(g / 2.0 ** X, fmt) * 2.0 ** X
+    step = np.zeros_like(g)
+    Xs = [X, expo(np.maximum(np.abs(g) - dg, 0.0).max(axis=-1)), expo((np.abs(g) + dg).max(axis=-1))]
+    for Xa in Xs:
+        for sgn in (-1.0, 1.0):
+            alt = fp8_round((g + sgn * dg) / 2.0 ** Xa, fmt) * 2.0 ** Xa
+            step = np.maximum(step, np.abs(alt - chosen))
+    return step.reshape(m, K)
+
+
+def swiglu_margin_mx(xq, sx, W1q, S1, W2q, S2, fmt: str, wfmt: str | None = None,
+                     rel: float = 2.0 ** -12) -> np.ndarray:
+    """Decision margin of swiglu_expert_mx's output [m, H]: sum over the
+    activation elements of |largest change of the dequantised activation| x
+    |Linear2 weight|, the activations moving within the float32 path's error:
+    each pre-activation within rel times the sum of its products' magnitudes
+    (a float32 accumulation of up to 2^13 exact products in blocks of 16
+    stays within 2^-15 of that sum; rel leaves 8x)."""
+    wfmt = fmt if wfmt is None else wfmt
+    Xd = mx_dequantize(xq, sx, fmt)
+    W1d = mx_dequantize(W1q, S1, wfmt)
+    Z = Xd @ W1d.T
+    dZ = rel * (np.abs(Xd) @ np.abs(W1d).T)
+    I = np.asarray(W2q).shape[1]
+    U, dU = _swiglu_with_bound(Z, dZ, I)
+    return _mx_decision_steps(U, dU, fmt) @ np.abs(mx_dequantize(W2q, S2, wfmt)).T
+
+
+def swiglu_margin_a8w8(q_rows, sx_rows, W1q, S1, W2q, S2, rel: float = 2.0 ** -18) -> np.ndarray:
+    """Decision margin of swiglu_expert_a8w8's output [m, H]: sum over the
+    activation elements of |largest change of code x row scale| x |Linear2
+    weight (dequantised)|, the SwiGLU output moving within the float32 path's
+    error (its integer products are exact; two dequantisation roundings and
+    the SiLU evaluation stay within rel of each value) and the row scale
+    within rel of itself."""
+    C = np.asarray(q_rows, np.int64) @ np.asarray(W1q, np.int64).T
+    Z = (C.astype(np.float64) * np.asarray(S1, np.float64)[None, :]) * np.asarray(sx_rows, np.float64)[:, None]
+    I = np.asarray(W2q).shape[1]
+    U, dU = _swiglu_with_bound(Z, rel * np.abs(Z), I)
+    dU = dU + rel * np.abs(U)
+    s = np.abs(U).max(axis=-1) / 127.0
+    safe = np.where(s > 0, s, 1.0)[:, None]
+    z = U / safe
+    dz = dU / safe + rel * np.abs(z)
+    q = round_half_away(z)
+    step = np.maximum(np.abs(round_half_away(z - dz) - q), np.abs(round_half_away(z + dz) - q)) * safe
+    step = np.where(s[:, None] > 0, step, 0.0)
+    W2d = np.asarray(W2q, np.float64) * np.asarray(S2, np.float64)[:, None]
+    return step @ np.abs(W2d).T
+
+
+def _combine_margin(tokens, E_rows, G_rows, E, rows_margin):
+    """Sum over a token's assignments of |gate| x its rows' margins."""
+    R = len(tokens)
+    E_rows = np.asarray(E_rows, dtype=np.int64).reshape(R, -1)
+    G_rows = np.asarray(G_rows, dtype=np.float64).reshape(R, -1)
+    k = E_rows.shape[1]
+    counts, offsets, perm, inv = dispatch(E_rows, E)
+    B = None
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        rows = perm[offsets[e]:offsets[e + 1]] // k
+        Me = rows_margin(e, rows)
+        if B is None:
+            B = np.zeros((perm.shape[0], Me.shape[1]))
+        B[offsets[e]:offsets[e + 1]] = Me
+    out = None
+    for j in range(k):
+        p = inv[np.arange(R) * k + j]
+        ok = p >= 0
+        if B is None:
+            break
+        if out is None:
+            out = np.zeros((R, B.shape[1]))
+        out[ok] += np.abs(G_rows[ok, j:j + 1]) * B[p[ok]]
+    return out
+
+
+def margin_mx_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: int,
+                     fmt: str, wfmt: str | None = None) -> np.ndarray:
+    """Decision margin [R, H] of forward_mx_tokens' output (same arguments)."""
+    R = len(tokens)
+    x = bf16_to_f64(X_rows_bits).reshape(R, -1)
+    xq, sx = mx_quantize(x, fmt)
+    out = _combine_margin(tokens, E_rows, G_rows, E, lambda e, rows: swiglu_margin_mx(
+        xq[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e), fmt, wfmt))
+    return np.zeros((R, x.shape[1])) if out is None else out
+
+
+def margin_a8w8_tokens(tokens, X_rows_bits, E_rows, G_rows, W1q, S1, W2q, S2, E: int) -> np.ndarray:
+    """Decision margin [R, H] of forward_a8w8_tokens' output (same arguments)."""
+    R = len(tokens)
+    x32 = bf16_to_f64(X_rows_bits).reshape(R, -1).astype(np.float32)
+    q, sx = quantize_rows_int8(x32, np.float32)
+    out = _combine_margin(tokens, E_rows, G_rows, E, lambda e, rows: swiglu_margin_a8w8(
+        q[rows], sx[rows], _get(W1q, e), _get(S1, e), _get(W2q, e), _get(S2, e)))
+    return np.zeros((R, x32.shape[1])) if out is None else out

@@ -12,23 +12,27 @@ DEV = torch.device("cuda:0")
 
 # Y tolerance: the layer's stated bar, max |err| <= 2e-2 * RMS(Y_ref) with
 # fp32 accumulation and bf16 I/O, where Y_ref is the oracle's output rounded
-# once to bf16 (round to nearest even) and the oracle rounds to bf16 where the
-# path keeps bf16 numbers between its kernels (the SwiGLU rows of the bf16
-# forward; the quantised forms' oracles quantise their activations as the
-# path does).  Without that intermediate rounding in the oracle, the bf16
-# SwiGLU rows alone move y by about 1e-3 RMS before the final rounding, which
-# flips the final bf16 rounding of some of the largest outputs by one unit in
-# the last place (2^-7 of their size, 2-4% of RMS); those flips are counted
-# and reported against the exact oracle, not allowed for in the bar.
+# once to bf16 (round to nearest even) and the oracle rounds where the path
+# keeps low-precision numbers between its kernels (the SwiGLU rows in bf16;
+# the quantised forms quantise their activations).
+#
+# One exception is counted, not absorbed: the GPU sums in another order than
+# the oracle, so where the exact output lies within a few 1e-7 of a bf16
+# rounding boundary the two round it to neighbouring bf16 values.  On the
+# largest outputs one unit in the last place (2^-7 of the value's binade) can
+# exceed 2e-2 RMS.  An element beyond the bar passes only if it is exactly such
+# a neighbour (|err| <= the bar + one ulp of Y_ref), and such elements may be
+# at most Y_FLIP_FRACTION of the output (a real defect moves many elements, by
+# more than one ulp).
 Y_RTOL_RMS = 2e-2
+Y_FLIP_FRACTION = 1e-4
 # Against the exact (unrounded-intermediate) oracle the error RMS stays under
 # this fraction of RMS: the bf16 SwiGLU rows contribute about 2^-9 / sqrt(3)
 # of RMS, the final rounding about 2^-9 / sqrt(3) of each element.
 Y_EXACT_RMS_ERR = 3e-3
-# (case, max|err|/RMS vs the rounded oracle, max|err|/RMS vs the exact
-# oracle or None, elements beyond the bar vs the exact oracle or None, size)
+# (case, max|err|/RMS, elements beyond the bar (one-ulp flips), elements,
+# max|err|/RMS vs the exact oracle or None, beyond the bar vs the exact oracle)
 Y_STATS = []
-G_RTOL = 2e-4
 
 
 def bf(a: np.ndarray) -> torch.Tensor:
@@ -113,18 +117,33 @@ def _rne_bf16(y):
     return oracle.round_to_bf16(np.asarray(y, dtype=np.float64))
 
 
-def check_y(Y_gpu, Y_ref, what="", Y_exact=None):
-    """Assert max|y - bf16(Y_ref)| <= 2e-2 * RMS(bf16(Y_ref)) element by element.
+def bf16_ulp(v):
+    """Spacing of the bf16 values at |v| (8 significant bits): 2^(floor(log2|v|) - 7)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def check_y(Y_gpu, Y_ref, what="", Y_exact=None, slack=None):
+    """Assert |y - bf16(Y_ref)| <= 2e-2 * RMS(bf16(Y_ref)) element by element,
+    apart from counted one-ulp rounding flips (see Y_FLIP_FRACTION).
 
     Y_ref: the oracle's float64 output with the path's intermediate rounding
-    points.  Y_exact (optional): the oracle without them; the error against
-    its bf16 rounding is recorded (max, count beyond the bar) and its RMS is
-    held under Y_EXACT_RMS_ERR of RMS.  Returns max|err|/RMS."""
+    points.  slack (optional, per element): the oracle's bound on what its
+    activation-code decisions that sit within the GPU's float32 rounding of a
+    decision boundary can move the element (quantised forms); it adds to the
+    bar.  Y_exact (optional): the oracle without intermediate rounding; the
+    error against its bf16 rounding is recorded and its RMS held under
+    Y_EXACT_RMS_ERR of RMS.  Returns max|err|/RMS."""
     y = Y_gpu.float().cpu().numpy().astype(np.float64) if isinstance(Y_gpu, torch.Tensor) else Y_gpu
     assert np.isfinite(y).all(), f"{what}: non-finite output"
     ref = _rne_bf16(Y_ref)
     rms = float(np.sqrt((ref ** 2).mean()))
     err = np.abs(y - ref)
+    allow = Y_RTOL_RMS * rms + (0.0 if slack is None else np.asarray(slack))
+    beyond = err > allow
+    flips = beyond & (err <= allow + bf16_ulp(ref) * (1 + 1e-9))
+    hard = beyond & ~flips
     ratio = float(err.max() / rms) if rms > 0 else float(err.max())
     x_ratio = x_beyond = None
     if Y_exact is not None:
@@ -133,10 +152,13 @@ def check_y(Y_gpu, Y_ref, what="", Y_exact=None):
         xerr = np.abs(y - xref)
         x_ratio = float(xerr.max() / xrms)
         x_beyond = int((xerr > Y_RTOL_RMS * xrms).sum())
-    Y_STATS.append((what, ratio, x_ratio, x_beyond, int(err.size)))
-    assert err.max() <= Y_RTOL_RMS * rms, (
-        f"{what}: max|err|/RMS = {ratio:.3e} > {Y_RTOL_RMS} "
-        f"({int((err > Y_RTOL_RMS * rms).sum())} of {err.size} elements)")
+    n_flip = int(flips.sum())
+    Y_STATS.append((what, ratio, n_flip, int(err.size), x_ratio, x_beyond))
+    assert not hard.any(), (
+        f"{what}: {int(hard.sum())} of {err.size} elements beyond the bar by more than one ulp "
+        f"(max|err|/RMS = {ratio:.3e})")
+    assert n_flip <= max(2, Y_FLIP_FRACTION * err.size), (
+        f"{what}: {n_flip} of {err.size} one-ulp flips beyond the bar")
     if Y_exact is not None:
         xe = np.sqrt(((y - xref) ** 2).mean())
         assert xe <= Y_EXACT_RMS_ERR * xrms, f"{what}: error RMS vs the exact oracle {xe / xrms:.3e}"

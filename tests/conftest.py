@@ -45,7 +45,7 @@ def pytest_terminal_summary(terminalreporter):
         return
     Y_STATS = mod.Y_STATS
     tr = terminalreporter
-    tr.write_sep("-", "Y parity (max|err|/RMS; bar 2e-2)")
-    for what, r, xr, xb, n in Y_STATS:
-        extra = "" if xr is None else f"  exact oracle: {xr:.3e}, {xb} of {n} beyond the bar"
-        tr.write_line(f"{what[:60]:60s} {r:.3e}{extra}")
+    tr.write_sep("-", "Y parity (max|err|/RMS against bf16(Y_ref); bar 2e-2)")
+    for what, r, nf, n, xr, xb in Y_STATS:
+        extra = "" if xr is None else f"  exact oracle: {xr:.3e}, {xb} beyond the bar"
+        tr.write_line(f"{what[:60]:60s} {r:.3e}  {nf} one-ulp flips of {n}{extra}")

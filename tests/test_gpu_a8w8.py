@@ -45,7 +45,9 @@ def test_a8w8_forward_matches_oracle(name):
     Y = _run(p, dd, E_ids, Gd)
     Y_ref = oracle.forward_a8w8_tokens(np.arange(c["T"]), h["X"], ids, G, h["W1"], h["S1"], h["W2"],
                                        h["S2"], E=c["E"])
-    check_y(Y, Y_ref, name)
+    slack = oracle.margin_a8w8_tokens(np.arange(c["T"]), h["X"], ids, G, h["W1"], h["S1"], h["W2"],
+                                       h["S2"], E=c["E"])
+    check_y(Y, Y_ref, name, slack=slack)
 
 
 def test_a8w8_is_deterministic_and_rejects_a_shared_expert():
@@ -86,7 +88,8 @@ def test_a8w8_full_size_sampled(name, n_rows):
     S1 = lambda e: dd["S1"][e].cpu().numpy()  # noqa: E731
     S2 = lambda e: dd["S2"][e].cpu().numpy()  # noqa: E731
     Y_ref = oracle.forward_a8w8_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E)
-    check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
+    slack = oracle.margin_a8w8_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E)
+    check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name, slack=slack)
 
 
 # Ragged and degenerate shapes: one token, k = E, every token on one expert
@@ -118,7 +121,9 @@ def test_a8w8_edge_shapes(shape):
     Y = _run(p, dd, dd["E_ids"], dd["G"])
     Y_ref = oracle.forward_a8w8_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
                                        h["W1"], h["S1"], h["W2"], h["S2"], E=c["E"])
-    check_y(Y, Y_ref, str(shape))
+    slack = oracle.margin_a8w8_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
+                                       h["W1"], h["S1"], h["W2"], h["S2"], E=c["E"])
+    check_y(Y, Y_ref, str(shape), slack=slack)
 
 
 def test_a8w8_with_no_tokens_writes_nothing():

@@ -98,7 +98,9 @@ def test_mx_forward_matches_oracle(name):
     wf = _wfmt(c)
     Y_ref = oracle.forward_mx_tokens(np.arange(c["T"]), h["X"], ids, G, _codes(h["W1"], wf), h["S1"],
                                      _codes(h["W2"], wf), h["S2"], E=c["E"], fmt=_fmt(c), wfmt=wf)
-    check_y(Y, Y_ref, name)
+    slack = oracle.margin_mx_tokens(np.arange(c["T"]), h["X"], ids, G, _codes(h["W1"], wf), h["S1"],
+                                     _codes(h["W2"], wf), h["S2"], E=c["E"], fmt=_fmt(c), wfmt=wf)
+    check_y(Y, Y_ref, name, slack=slack)
 
 
 def test_mx_is_deterministic_and_rejects_a_shared_expert():
@@ -141,7 +143,9 @@ def test_mx_full_size_sampled(name, n_rows):
     S2 = lambda e: dd["S2"][e].cpu().numpy()  # noqa: E731
     Y_ref = oracle.forward_mx_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E, fmt=_fmt(c),
                                      wfmt=wf)
-    check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name)
+    slack = oracle.margin_mx_tokens(rows, hX[rows], ids[rows], Gh[rows], W1, S1, W2, S2, E=E, fmt=_fmt(c),
+                                     wfmt=wf)
+    check_y(Y[torch.from_numpy(rows).to(DEV)], Y_ref, name, slack=slack)
 
 
 # Ragged and degenerate shapes (H and I multiples of 128, as the MX forms
@@ -177,7 +181,10 @@ def test_mx_edge_shapes(shape, quant):
     Y_ref = oracle.forward_mx_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
                                      _codes(h["W1"], wf), h["S1"], _codes(h["W2"], wf), h["S2"], E=c["E"],
                                      fmt=_fmt(c), wfmt=wf)
-    check_y(Y, Y_ref, f"{shape} {quant}")
+    slack = oracle.margin_mx_tokens(np.arange(c["T"]), h["X"], h["E_ids"], h["G"].astype(np.float64),
+                                     _codes(h["W1"], wf), h["S1"], _codes(h["W2"], wf), h["S2"], E=c["E"],
+                                     fmt=_fmt(c), wfmt=wf)
+    check_y(Y, Y_ref, f"{shape} {quant}", slack=slack)
 
 
 def test_mx_with_no_tokens_writes_nothing():

@@ -93,6 +93,39 @@ def test_route_matches_oracle(name):
     check_gates(G, G_ref, name)
 
 
+# shapes that take the fused router's split of H over clusters of 1, 2, 4 and
+# 8 CTAs, one or two MMAs per k-step (E <= 256 or up to 384) and padded
+# expert columns (E not a multiple of 64)
+ROUTER_SHAPES = [
+    dict(T=300, H=4096, E=64, k=4, I=64, bias=True),                          # 8 CTAs per tile
+    dict(T=256, H=1024, E=384, k=6, I=64, bias=True, alpha=2.5),              # 2, two MMAs
+    dict(T=200, H=2048, E=128, k=8, I=64, score="softmax", renorm=0),         # 4
+    dict(T=130, H=512, E=320, k=3, I=64, score="sqrt_softplus", bias=True),   # 1, N = 256 + 64
+    dict(T=77, H=1024, E=40, k=5, I=64, bias=True),                           # 2, padded columns
+]
+
+
+@pytest.mark.parametrize("shape", ROUTER_SHAPES, ids=lambda s: "T{T}_H{H}_E{E}_k{k}".format(**s))
+def test_route_split_over_clusters(shape):
+    h, dd = host_inputs(dict(shape), seed=31)
+    c = h["cfg"]
+    p = params(c)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref, l64 = oracle_route(h)
+    assert np.array_equal(E_ids.cpu().numpy(), ids_ref)
+    check_gates(G, G_ref, str(shape))
+    L = torch.empty((c["T"], c["E"]), dtype=torch.float32, device=DEV)
+    moe.moe_route_logits(p, dd["X"], dd["Wg"], L, ws)
+    moe.moe_sync_status(ws)
+    l32 = L.cpu().numpy().astype(np.float64)
+    if c["score_fn"] == oracle.SCORE_SOFTMAX:
+        assert (np.abs(l32 - l64) / np.maximum(1.0, np.abs(l64))).max() < 2.5e-4
+    else:
+        assert np.abs(oracle.affinity(l32, c["score_fn"]) - oracle.affinity(l64, c["score_fn"])).max() < 5e-5
+
+
 def test_route_equal_scores_go_to_the_lower_id():
     rng = np.random.default_rng(11)
     T, H, E, k = 64, 128, 16, 4

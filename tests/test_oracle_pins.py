@@ -818,3 +818,75 @@ def test_backward_rounding_points_move_gradients_by_the_derived_rms(name):
     for key in ("dX", "dWg", "dW1", "dW2", "dG") + (("dWs1", "dWs2") if c["shared"] else ()):
         rms = np.sqrt((exact[key] ** 2).mean())
         assert np.sqrt(((ref[key] - exact[key]) ** 2).mean()) <= bound * rms, key
+
+
+# ------------------------------------------------------------------ decision margins
+def _perturbed_mx_rows(xq, sx, W1q, S1, W2q, S2, fmt, wfmt, rng, rel):
+    """swiglu_expert_mx with each pre-activation moved anywhere within rel
+    times its product-magnitude sum (what a float32 accumulation may do)."""
+    Xd = oracle.mx_dequantize(xq, sx, fmt)
+    W1d = oracle.mx_dequantize(W1q, S1, wfmt)
+    Z = Xd @ W1d.T
+    Z = Z + rng.uniform(-1, 1, Z.shape) * rel * (np.abs(Xd) @ np.abs(W1d).T)
+    I = W2q.shape[1]
+    U = Z[:, :I] / (1 + np.exp(-Z[:, :I])) * Z[:, I:]
+    Uq, SU = oracle.mx_quantize(U, fmt)
+    return oracle.mx_dequantize(Uq, SU, fmt) @ oracle.mx_dequantize(W2q, S2, wfmt).T
+
+
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e2m1", "e2m1")])
+def test_mx_decision_margin_bounds_float32_moves(fmt, wfmt):
+    """Moving the pre-activations within the assumed float32 error flips some
+    activation codes (and so moves outputs); every move stays within the
+    margin, and the margin is zero wherever no decision is within reach."""
+    rng = np.random.default_rng(41)
+    m, H, I = 24, 256, 128
+    x = rng.standard_normal((m, H))
+    xq, sx = oracle.mx_quantize(x, fmt)
+    codes = np.arange(16 if wfmt == "e2m1" else 256)
+    vals = oracle.fp8_decode(codes, wfmt)
+    finite = codes[np.isfinite(vals) & (np.abs(vals) <= 4.0)]
+    W1q = rng.choice(finite, (2 * I, H)).astype(np.uint8)
+    W2q = rng.choice(finite, (H, I)).astype(np.uint8)
+    S1 = rng.integers(118, 122, (2 * I, H // 32)).astype(np.uint8)
+    S2 = rng.integers(118, 122, (H, I // 32)).astype(np.uint8)
+    rel = 2.0 ** -7  # large, so that many decisions are within reach
+    base = oracle.swiglu_expert_mx(xq, sx, W1q, S1, W2q, S2, fmt, wfmt)
+    B = oracle.swiglu_margin_mx(xq, sx, W1q, S1, W2q, S2, fmt, wfmt, rel=rel)
+    moved = 0
+    for _ in range(8):
+        d = np.abs(_perturbed_mx_rows(xq, sx, W1q, S1, W2q, S2, fmt, wfmt, rng, rel) - base)
+        assert np.all(d <= B * (1 + 1e-9) + 1e-12)
+        moved += int((d > 0).sum())
+    assert moved > 0 and (B > 0).any()
+
+
+def test_a8w8_decision_margin_bounds_float32_moves():
+    rng = np.random.default_rng(42)
+    m, H, I = 24, 128, 96
+    x = rng.standard_normal((m, H)).astype(np.float32)
+    q, sx = oracle.quantize_rows_int8(x, np.float32)
+    W1q = rng.integers(-127, 128, (2 * I, H)).astype(np.int8)
+    W2q = rng.integers(-127, 128, (H, I)).astype(np.int8)
+    S1 = rng.uniform(0.5, 1.5, 2 * I) / 127 / np.sqrt(H)
+    S2 = rng.uniform(0.5, 1.5, H) / 127 / np.sqrt(I)
+    rel = 2.0 ** -9
+    base = oracle.swiglu_expert_a8w8(q, sx, W1q, S1, W2q, S2)
+    B = oracle.swiglu_margin_a8w8(q, sx, W1q, S1, W2q, S2, rel=rel)
+    C = q.astype(np.int64) @ W1q.astype(np.int64).T
+    Z0 = C * S1[None, :] * sx[:, None].astype(np.float64)
+    moved = 0
+    for _ in range(8):
+        Z = Z0 * (1 + rng.uniform(-1, 1, Z0.shape) * rel)
+        U = Z[:, :I] / (1 + np.exp(-Z[:, :I])) * Z[:, I:]
+        U = U * (1 + rng.uniform(-1, 1, U.shape) * rel)
+        s = np.abs(U).max(axis=1) / 127 * (1 + rng.uniform(-1, 1, m) * rel)
+        A8 = oracle.round_half_away(U / s[:, None])
+        out = (A8 @ W2q.astype(np.float64).T) * S2[None, :] * s[:, None]
+        # the row scale moves every dequantised value by up to rel of itself:
+        # a continuous change, bounded separately from the code flips
+        cont = rel * 1.01 * (np.abs(A8) * s[:, None]) @ (np.abs(W2q.astype(np.float64)) * S2[:, None]).T
+        d = np.abs(out - base)
+        assert np.all(d <= B * (1 + 1e-9) + cont + 1e-12)
+        moved += int((d > cont).sum())
+    assert moved > 0 and (B > 0).any()
