@@ -152,6 +152,22 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 
 
 # ------------------------------------------------------------------ our arm
+def route_launches(c):
+    """Kernels moe_route launches: the fused router (gating GEMM with the
+    decision in its epilogue) and, for top-k, the float64 re-decision of close
+    tokens; layers of more than 384 experts take the general path (Wg
+    transpose, gating GEMM, selection, re-decision; hash: GEMM, selection).
+    The forward adds count, scan, place, Linear1 (row gather fused), Linear2
+    and combine; A8W8 adds the token and the activation quantisation, MX the
+    token one."""
+    if c["routing"] == "given":
+        return 0
+    fused = c["E"] <= 384 and c["E"] % 8 == 0
+    if c["routing"] == "hash":
+        return 1 if fused else 2
+    return 2 if fused else 4
+
+
 def build_step(moe, dd, p, ws, stage_events=None):
     c = dd["cfg"]
     routed = c["routing"] != "given"
@@ -401,10 +417,7 @@ def run_ours(args, rank, world, local_rank, workload=None, with_cpu=True):
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_q8_kernel<true>)"
     if mx:
         roof["kernel"] = "grouped MX Linear1 + SwiGLU + Q_MX (gemm_mx_kernel<true, %d>)" % moe.MX_FORMATS[mx]
-    # route: transpose Wg, gating GEMM, select, recheck, reselect (hash: GEMM, select);
-    # forward: count, scan, place, Linear1 (row gather fused), Linear2, combine;
-    # A8W8 adds the token and the activation quantisation, MX the token one
-    launches_per_step = {"given": 0, "hash": 2}.get(c["routing"], 5) + (8 if quant else (7 if mx else 6))
+    launches_per_step = route_launches(c) + (8 if quant else (7 if mx else 6))
     out = {
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -567,9 +580,9 @@ def run_train(args, rank, world, local_rank):
                      "peak_source": pk["source"] + " hbm_gbs"},
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(2 * T * H * 2), "d2h_bytes_per_step": int(2 * T * H * 2)},
-        # route 5 (hash 2) + forward 6 + backward: unpermute, gather, 2 dgrad,
-        # 2 wgrad, router GEMM, router backward, dWg, dXr, dX sum = 11
-        "gpu_launches": ({"hash": 2}.get(c["routing"], 5) + 6 + 11) * K,
+        # route + forward 6 + backward: unpermute, gather, 2 dgrad, 2 wgrad,
+        # router GEMM, router backward, dWg, dXr, dX sum = 11
+        "gpu_launches": (route_launches(c) + 6 + 11) * K,
         "clocks": sampler.summary() if sampler else None,
     }
     return out

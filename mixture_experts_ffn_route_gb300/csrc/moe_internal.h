@@ -196,8 +196,9 @@ int gemm_block_n(GemmKind kind);
 
 // Router.  Scratch of the float64 re-decision of close tokens:
 struct RouteScratch {
-  int* counters;  // [0] close tokens, [1] candidate pairs; zero between calls
-                  // (the reselect kernel zeroes them when it is done)
+  int* counters;  // [0] close tokens, [1] candidate pairs, [2] re-decision blocks
+                  // done; zero between calls (the re-decision's last block
+                  // zeroes them)
   int4* flagged;  // [T]      {token, first pair, pair count, 0}
   float2* fnorm;  // [T]      softmax normaliser of a close token {max logit, sum exp}
   int2* pairs;    // [T * E]  {token, expert}
@@ -212,7 +213,7 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                 const int32_t* tid2eid, int V, int T, int H, int E, int k,
                                 int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
                                 const RouteScratch& rs, int* status, cudaStream_t s);
-// The float64 re-decision alone (recheck + reselect) of the tokens listed in rs.
+// The float64 re-decision of the tokens listed in rs (one kernel).
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, cudaStream_t s);

@@ -12,19 +12,18 @@
 // Exact ids from inexact logits.  The fp32 tensor-core logit is within a few
 // 1e-5 of the exact value, so the fp32 selection is final unless two
 // neighbouring scores among the first k+1 lie within a decision band.  Such a
-// token is re-decided in three steps:
+// token is re-decided in two steps:
 //   select    fp32 top-(k+1) by k+1 warp arg-max rounds; a close token appends
 //             every expert scoring within twice the band of its k-th score to
 //             a list of (token, expert) pairs, with the pair's fp32 logit (and
 //             the token's softmax normaliser);
-//   recheck   four warps per pair: the logit sum_h X[t,h] Wg[h,e] to ~48 bits
-//             over a transposed copy of Wg (contiguous rows; each bf16 product
-//             is exact in fp32 and the sum is carried as a float pair), then
-//             its float64 selection score;
-//   reselect  one block, a warp per close token: top-k of the float64 scores
-//             of its candidates, larger score first, equal scores to the lower
-//             id; gates from the listed fp32 logits.  The block then zeroes
-//             the list counters for the next call.
+//   redecide  one block per close token: a warp per candidate recomputes the
+//             logit sum_h X[t,h] Wg[h,e] to ~48 bits over a transposed copy of
+//             Wg (contiguous rows; each bf16 product is exact in fp32 and the
+//             sum is carried as float pairs) and its float64 selection score;
+//             then the top-k of those scores, larger score first, equal scores
+//             to the lower id, with gates from the listed fp32 logits.  The
+//             last block zeroes the list counters for the next call.
 // The ids then equal those of an exact evaluation except at exact ties.
 #include <float.h>
 
@@ -199,153 +198,150 @@ __device__ __forceinline__ unsigned long long order_key(double v) {
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
-constexpr int kRecheckWarps = 4;  // warps that share one (token, expert) pair
+constexpr int kRedecideWarps = 8;
 
-// Float64 selection score of the listed (token, expert) pairs, four warps to a
-// pair.  Each bf16 x bf16 product is exact in fp32; the products are summed as
-// unevaluated float pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's
-// fp64 rate is low), folded as float pairs across the lanes of each warp, and
-// the four warps' sums added in float64 in a fixed order.  The logit is within ~1e-12 of
-// the exact value at the workload sizes.  The score is stored as an
-// order-preserving integer key so the reselection compares integers.
-__global__ void __launch_bounds__(kRecheckWarps * 32)
-    route_recheck_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
-                         const float* __restrict__ bias, int H, int fn, RouteScratch rs) {
-  __shared__ double part[kRecheckWarps];
-  const int n = rs.counters[1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Float64 selection score of one (token, expert) pair, one warp: each bf16 x
+// bf16 product is exact in fp32; the products are summed as unevaluated float
+// pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's fp64 rate is low),
+// eight pairs per lane, folded as float pairs across the lanes in a fixed
+// order, and converted to float64 once.  The logit is within ~1e-12 of the
+// exact value at the workload sizes.  Returned as an order-preserving integer
+// key of score + bias.
+__device__ __forceinline__ unsigned long long pair_key(const uint16_t* __restrict__ X,
+                                                       const uint16_t* __restrict__ WgT,
+                                                       const float* __restrict__ bias, int H, int fn,
+                                                       int t, int e, int lane) {
+  const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
+  const uint4* wr = reinterpret_cast<const uint4*>(WgT + static_cast<long long>(e) * H);
   const int vecs = H / 8;  // 16-byte vectors per row
-  for (int i = blockIdx.x; i < n; i += gridDim.x) {
-    const int2 pr = rs.pairs[i];
-    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(pr.x) * H);
-    const uint4* wr = reinterpret_cast<const uint4*>(WgT + static_cast<long long>(pr.y) * H);
-    // eight independent (hi, lo) accumulators, one per element of a vector
-    float hi[8], lo[8];
+  float hi[8], lo[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.0f;
-    for (int v0 = threadIdx.x; v0 < vecs; v0 += 8 * kRecheckWarps * 32) {
-      uint4 a[8], b[8];
+  for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.0f;
+  for (int v0 = lane; v0 < vecs; v0 += 8 * 32) {
+    uint4 a[8], b[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {  // all loads of this round first
-        const int v = v0 + u * kRecheckWarps * 32;
-        a[u] = v < vecs ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
-        b[u] = v < vecs ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
-      }
+    for (int u = 0; u < 8; ++u) {  // all loads of this round first
+      const int v = v0 + u * 32;
+      a[u] = v < vecs ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+      b[u] = v < vecs ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float p[8] = {bf16_lo(a[u].x) * bf16_lo(b[u].x), bf16_hi(a[u].x) * bf16_hi(b[u].x),
-                            bf16_lo(a[u].y) * bf16_lo(b[u].y), bf16_hi(a[u].y) * bf16_hi(b[u].y),
-                            bf16_lo(a[u].z) * bf16_lo(b[u].z), bf16_hi(a[u].z) * bf16_hi(b[u].z),
-                            bf16_lo(a[u].w) * bf16_lo(b[u].w), bf16_hi(a[u].w) * bf16_hi(b[u].w)};
+    for (int u = 0; u < 8; ++u) {
+      const float p[8] = {bf16_lo(a[u].x) * bf16_lo(b[u].x), bf16_hi(a[u].x) * bf16_hi(b[u].x),
+                          bf16_lo(a[u].y) * bf16_lo(b[u].y), bf16_hi(a[u].y) * bf16_hi(b[u].y),
+                          bf16_lo(a[u].z) * bf16_lo(b[u].z), bf16_hi(a[u].z) * bf16_hi(b[u].z),
+                          bf16_lo(a[u].w) * bf16_lo(b[u].w), bf16_hi(a[u].w) * bf16_hi(b[u].w)};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float sum, err;
-          two_sum(hi[q], p[q], sum, err);
-          hi[q] = sum;
-          lo[q] += err;
-        }
+      for (int q = 0; q < 8; ++q) {
+        float sum, err;
+        two_sum(hi[q], p[q], sum, err);
+        hi[q] = sum;
+        lo[q] += err;
       }
     }
-    // fold the eight pairs and then the warp's lanes as float pairs (fp32
-    // pipes); one conversion to float64 per warp
-    float H0 = hi[0], L0 = lo[0];
-#pragma unroll
-    for (int q = 1; q < 8; ++q) ff_add(H0, L0, hi[q], lo[q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      ff_add(H0, L0, __shfl_xor_sync(0xffffffffu, H0, o), __shfl_xor_sync(0xffffffffu, L0, o));
-    if (lane == 0) part[warp] = static_cast<double>(H0) + static_cast<double>(L0);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double l = 0.0;
-#pragma unroll
-      for (int w = 0; w < kRecheckWarps; ++w) l += part[w];
-      double v = score_f64(l, fn);
-      if (bias != nullptr) v += static_cast<double>(bias[pr.y]);
-      rs.key[i] = order_key(v);
-    }
-    __syncthreads();
   }
+  float H0 = hi[0], L0 = lo[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) ff_add(H0, L0, hi[q], lo[q]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    ff_add(H0, L0, __shfl_xor_sync(0xffffffffu, H0, o), __shfl_xor_sync(0xffffffffu, L0, o));
+  double v = score_f64(static_cast<double>(H0) + static_cast<double>(L0), fn);
+  if (bias != nullptr) v += static_cast<double>(bias[e]);
+  return order_key(v);
 }
 
-// Re-decide each close token from the float64 scores of its candidates: one
-// block, a warp per close token.  The gates come from the candidates' listed
-// fp32 logits (and, for softmax, the token's listed normaliser).  At the end
-// the block zeroes the list counters, so the next call starts empty.
-constexpr int kReselectWarps = 32;
-
-__global__ void __launch_bounds__(kReselectWarps * 32)
-    route_reselect_kernel(int k, int fn, float alpha, int renorm, int32_t* __restrict__ E_ids,
-                          float* __restrict__ G, RouteScratch rs) {
+// Re-decide the close tokens: one block per listed token (striding over the
+// list).  The block's warps score its candidates in float64 (one pair per warp
+// at a time, keys to rs.key); then warp 0 takes k arg-max rounds over the keys,
+// larger score first, equal scores to the lower id, and writes the ids and the
+// gates, computed from the candidates' listed fp32 logits (and, for softmax,
+// the token's listed normaliser).  The last block to finish zeroes the list
+// counters, so the next call starts with empty lists.
+__global__ void __launch_bounds__(kRedecideWarps * 32)
+    route_redecide_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
+                          const float* __restrict__ bias, int H, int k, int fn, float alpha, int renorm,
+                          int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs) {
   const int n = *reinterpret_cast<volatile int*>(rs.counters);
-  const int lane = threadIdx.x & 31;
-  for (int j = threadIdx.x >> 5; j < n; j += kReselectWarps) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = blockIdx.x; j < n; j += gridDim.x) {
     const int4 f = rs.flagged[j];
     const int t = f.x, base = f.y, count = f.z;
-    const float2 nrm = rs.fnorm[j];
-    // candidates held in registers, up to 4 per lane (count <= 128); more
-    // candidates than that are read from memory each round.  Scores are
-    // order-preserving integer keys: larger key = larger score.
-    constexpr int kHold = 4;
-    unsigned long long cv[kHold];
-    int ce[kHold];
-    float cl[kHold];
-#pragma unroll
-    for (int h = 0; h < kHold; ++h) {
-      const int i = lane + 32 * h;
-      cv[h] = i < count ? rs.key[base + i] : 0ull;
-      ce[h] = i < count ? rs.pairs[base + i].y : 0x7fffffff;
-      cl[h] = i < count ? rs.plogit[base + i] : 0.0f;
+    for (int i = warp; i < count; i += kRedecideWarps) {
+      const unsigned long long key = pair_key(X, WgT, bias, H, fn, t, rs.pairs[base + i].y, lane);
+      if (lane == 0) rs.key[base + i] = key;
     }
-    int my_sel = -1;
-    float my_l = 0.0f;
-    unsigned long long last_v = ~0ull;
-    int last_id = -1;
-    // round r: the best candidate strictly after the previous winner in the
-    // (larger score, lower id) order, so no candidate is taken twice
+    __syncthreads();
+    if (warp == 0) {
+      const float2 nrm = rs.fnorm[j];
+      // candidates held in registers, up to 4 per lane (count <= 128); more
+      // candidates than that are read from memory each round
+      constexpr int kHold = 4;
+      unsigned long long cv[kHold];
+      int ce[kHold];
+      float cl[kHold];
+#pragma unroll
+      for (int h = 0; h < kHold; ++h) {
+        const int i = lane + 32 * h;
+        cv[h] = i < count ? rs.key[base + i] : 0ull;
+        ce[h] = i < count ? rs.pairs[base + i].y : 0x7fffffff;
+        cl[h] = i < count ? rs.plogit[base + i] : 0.0f;
+      }
+      int my_sel = -1;
+      float my_l = 0.0f;
+      unsigned long long last_v = ~0ull;
+      int last_id = -1;
+      // round r: the best candidate strictly after the previous winner in the
+      // (larger score, lower id) order, so no candidate is taken twice
 #pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-      unsigned long long best = 0ull;
-      int bid = 0x7fffffff;
-      float bl = 0.0f;
+      for (int r = 0; r < k; ++r) {
+        unsigned long long best = 0ull;
+        int bid = 0x7fffffff;
+        float bl = 0.0f;
 #pragma unroll
-      for (int h = 0; h < kHold; ++h)
-        if (before(last_v, last_id, cv[h], ce[h]) && before(cv[h], ce[h], best, bid)) {
-          best = cv[h];
-          bid = ce[h];
-          bl = cl[h];
+        for (int h = 0; h < kHold; ++h)
+          if (before(last_v, last_id, cv[h], ce[h]) && before(cv[h], ce[h], best, bid)) {
+            best = cv[h];
+            bid = ce[h];
+            bl = cl[h];
+          }
+        for (int i = lane + 32 * kHold; i < count; i += 32) {
+          const int e = rs.pairs[base + i].y;
+          const unsigned long long v = rs.key[base + i];
+          if (before(last_v, last_id, v, e) && before(v, e, best, bid)) {
+            best = v;
+            bid = e;
+            bl = rs.plogit[base + i];
+          }
         }
-      for (int i = lane + 32 * kHold; i < count; i += 32) {
-        const int e = rs.pairs[base + i].y;
-        const unsigned long long v = rs.key[base + i];
-        if (before(last_v, last_id, v, e) && before(v, e, best, bid)) {
-          best = v;
-          bid = e;
-          bl = rs.plogit[base + i];
+        warp_argmax_payload(best, bid, bl);
+        if (lane == r) {
+          my_sel = bid;
+          my_l = bl;
         }
+        last_v = best;
+        last_id = bid;
       }
-      warp_argmax_payload(best, bid, bl);
-      if (lane == r) {
-        my_sel = bid;
-        my_l = bl;
+      const float a = lane < k ? affinity_f32(my_l, fn, nrm.x, nrm.y) : 0.0f;
+      float den = 0.0f;
+      for (int jj = 0; jj < k; ++jj) den += __shfl_sync(0xffffffffu, a, jj);
+      if (lane < k) {
+        float g = alpha * a;
+        if (renorm) g = den > 0.0f ? alpha * a / den : 0.0f;
+        E_ids[static_cast<long long>(t) * k + lane] = my_sel;
+        G[static_cast<long long>(t) * k + lane] = g;
       }
-      last_v = best;
-      last_id = bid;
     }
-    const float a = lane < k ? affinity_f32(my_l, fn, nrm.x, nrm.y) : 0.0f;
-    float den = 0.0f;
-    for (int jj = 0; jj < k; ++jj) den += __shfl_sync(0xffffffffu, a, jj);
-    if (lane < k) {
-      float g = alpha * a;
-      if (renorm) g = den > 0.0f ? alpha * a / den : 0.0f;
-      E_ids[static_cast<long long>(t) * k + lane] = my_sel;
-      G[static_cast<long long>(t) * k + lane] = g;
-    }
+    __syncthreads();
   }
-  __syncthreads();
+  // the last block to finish zeroes the counters (every block has read them)
   if (threadIdx.x == 0) {
-    rs.counters[0] = 0;
-    rs.counters[1] = 0;
+    __threadfence();
+    if (atomicAdd(rs.counters + 2, 1) == static_cast<int>(gridDim.x) - 1) {
+      rs.counters[0] = 0;
+      rs.counters[1] = 0;
+      rs.counters[2] = 0;
+    }
   }
 }
 
@@ -374,9 +370,8 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, cudaStream_t s) {
-  const int grid = 8 * num_sms();
-  route_recheck_kernel<<<grid, kRecheckWarps * 32, 0, s>>>(X, WgT, bias, H, score_fn, rs);
-  route_reselect_kernel<<<1, kReselectWarps * 32, 0, s>>>(k, score_fn, alpha, renorm, E_ids, G, rs);
+  route_redecide_kernel<<<2 * num_sms(), kRedecideWarps * 32, 0, s>>>(X, WgT, bias, H, k, score_fn,
+                                                                      alpha, renorm, E_ids, G, rs);
   return cudaGetLastError();
 }
 

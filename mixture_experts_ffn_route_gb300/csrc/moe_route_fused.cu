@@ -395,12 +395,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   if (S > 1) cluster_sync_all(); else __syncthreads();
 
+  // ---------------------------------------------------------------- reduce
+  // This CTA decides rows [rank R, rank R + R).  Their partial sums sit in
+  // that band of every CTA's dump; the band of this CTA's own dump is read by
+  // no other CTA, so the sums (ranks added in order) overwrite it there.  All
+  // S loads of a chunk are issued before any is used (distributed shared
+  // memory is far slower than local).
+  const int R = kBM / S;
+  const int cpr = ncols / 4;
+  if (S > 1 && !*abort_flag) {
+    uint32_t part[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) part[s] = s < S ? map_rank(ring0, s) : 0u;
+    const int n_chunks = R * cpr;
+#pragma unroll 2
+    for (int i = threadIdx.x; i < n_chunks; i += kThreads) {
+      const int r = rank * R + i / cpr;
+      const uint32_t off = dump_off(r, i % cpr, cpr);
+      float4 x[8];
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s < S) x[s] = ld_cluster_f4(part[s] + off);
+      float4 acc = x[0];
+#pragma unroll
+      for (int s = 1; s < 8; ++s)
+        if (s < S) {
+          acc.x += x[s].x; acc.y += x[s].y; acc.z += x[s].z; acc.w += x[s].w;
+        }
+      *reinterpret_cast<float4*>(smem + off) = acc;
+    }
+  }
+  __syncthreads();
+
   // ---------------------------------------------------------------- decide
   if (!*abort_flag) {
-    const int R = kBM / S;  // rows decided by this CTA
-    const int cpr = ncols / 4;
-    uint32_t part[8];
-    for (int s = 0; s < S; ++s) part[s] = S > 1 ? map_rank(ring0, s) : ring0;
     for (int rr = warp; rr < R; rr += kThreads / 32) {
       const int r = rank * R + rr;
       const int t = row0 + r;
@@ -409,19 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
         const int c = lane + 32 * j;
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (c < cpr) {
-          for (int s = 0; s < S; ++s) {  // partial sums added in rank order
-            const uint32_t a = part[s] + dump_off(r, c, cpr);
-            const float4 x = S > 1 ? ld_cluster_f4(a) : *reinterpret_cast<const float4*>(smem + dump_off(r, c, cpr));
-            if (s == 0) {
-              acc = x;
-            } else {
-              acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
-            }
-          }
-        }
-        lg[4 * j] = acc.x; lg[4 * j + 1] = acc.y; lg[4 * j + 2] = acc.z; lg[4 * j + 3] = acc.w;
+        const float4 x = c < cpr ? *reinterpret_cast<const float4*>(smem + dump_off(r, c, cpr))
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        lg[4 * j] = x.x; lg[4 * j + 1] = x.y; lg[4 * j + 2] = x.z; lg[4 * j + 3] = x.w;
       }
       if (p.logits_out != nullptr) {
 #pragma unroll
