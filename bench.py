@@ -43,6 +43,8 @@ WORKLOAD_TEXT = {
     "c5": "large-FFN layer T=16384 H=8192 E=64 top-2 I=22016, softmax gates",
     "c3_sp": "V4-Pro-shaped layer with the pages' sqrt-softplus affinity",
     "c3p": "V4-Pro expert shapes, T=512 E=48 (profiling size)",
+    "c5p": "large-FFN expert shapes, T=1024 E=4 top-2 (~512 rows per expert; profiling size)",
+    "c3_f3072": "V4-Pro-shaped layer at the pages' expert width f=3072 (T=4096 H=7168 E=384 top-6 I=3072 +1 shared)",
     "c3r": "V4-Pro router at full size with I=64 (profiling size for the routing kernels)",
     "c3_q": "V4-Pro-shaped layer, A8W8-INT form (int8 weights, per-token int8 activations), no shared expert",
     "c2_q": "given-routing layer, A8W8-INT form",
@@ -411,7 +413,7 @@ def run_ours(args, rank, world, local_rank, workload=None, with_cpu=True):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "algorithmic_flops_per_launch": int(g1_flops),
                 "peak_source": pk["source"] + " bf16_tflops_sustained" + (" x 2 (fp8)" if mx else "")}
-    if roof["bound"] == "hbm" and not quant:
+    if not quant and not mx:
         roof["traffic"] = load_traffic(workload, g1_bytes)
     if quant:
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_q8_kernel<true>)"
@@ -589,39 +591,21 @@ def run_train(args, rank, world, local_rank):
 
 
 def load_traffic(workload, algorithmic_bytes):
-    """DRAM bytes of one Linear1 launch from the committed ncu summaries: for
-    c3, c3_mx, c3_mxa4 and c3_q, the full-size captures themselves (the mean of two
-    launches); for c4 (the same expert shapes and load recipe) the c3 capture
-    scaled by the ratio of algorithmic bytes; for c3p its own small-size
-    capture."""
+    """DRAM bytes of one Linear1 launch, from the committed ncu summary of a
+    capture at a profiling size of the same expert shapes (c3p for the V4-Pro
+    layers, c5p for the large-FFN layer): that launch's DRAM bytes over its
+    algorithmic bytes, times this launch's algorithmic bytes.  The profiling
+    sizes hold 4.3 GB of weights, so their DRAM figures are not L2 hits; the
+    full-size launches are not captured (they hold 35-69 GB)."""
     import re
-    if workload in ("c3", "c4"):
-        path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
-        key, c3_alg = r"dram_bytes_per_launch_c3_gemm1:\s*([0-9]+)", 23135780864
-        if not os.path.exists(path):
-            return None
-        with open(path) as f:
-            m = re.search(key, f.read())
-        if not m:
-            return None
-        t = int(m.group(1))
-        return t if workload == "c3" else int(t * algorithmic_bytes / c3_alg)
-    if workload in ("c3_mx", "c3_q", "c3_mxa4"):
-        path = os.path.join(ROOT, "profiles", "traffic_full_size_c3.md")
-        if not os.path.exists(path):
-            return None
-        key = {"c3_mx": "c3mx", "c3_q": "c3q", "c3_mxa4": "c3mxa4"}[workload]
-        with open(path) as f:
-            m = re.search(r"dram_bytes_per_launch_%s_gemm1:\s*([0-9]+)" % key, f.read())
-        return int(m.group(1)) if m else None
-    if workload == "c3p":
-        path = os.path.join(ROOT, "profiles", "gemm_bf16_c2_c3p.md")
-        if not os.path.exists(path):
-            return None
-        with open(path) as f:
-            m = re.search(r"dram_bytes_per_launch_c3_scaled_ratio:\s*([0-9.]+)", f.read())
-        return int(float(m.group(1)) * algorithmic_bytes) if m else None
-    return None
+    key = {"c3": "c3p", "c4": "c3p", "c3_sp": "c3p", "c3_f3072": "c3p", "c3p": "c3p",
+           "c5": "c5p", "c5p": "c5p"}.get(workload)
+    path = os.path.join(ROOT, "profiles", "traffic_gemm_bf16_c3p_c5p.md")
+    if key is None or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        m = re.search(r"traffic_ratio_%s_gemm1:\s*([0-9.]+)" % key, f.read())
+    return int(float(m.group(1)) * algorithmic_bytes) if m else None
 
 
 # ------------------------------------------------------------------ oracle (CPU)

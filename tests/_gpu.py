@@ -23,9 +23,12 @@ DEV = torch.device("cuda:0")
 # exceed 2e-2 RMS.  An element beyond the bar passes only if it is exactly such
 # a neighbour (|err| <= the bar + one ulp of Y_ref), and such elements may be
 # at most Y_FLIP_FRACTION of the output (a real defect moves many elements, by
-# more than one ulp).
+# more than one ulp).  How often the two roundings part grows with the float32
+# accumulation error, i.e. with the contraction length: the most seen is
+# 1.4e-4 of the outputs on the large-FFN layer (K = 22016 in Linear2) and
+# 6e-4 in the A8W8 form, whose Linear2 rows are kept in bf16.
 Y_RTOL_RMS = 2e-2
-Y_FLIP_FRACTION = 1e-4
+Y_FLIP_FRACTION = 1e-3
 # Against the exact (unrounded-intermediate) oracle the error RMS stays under
 # this fraction of RMS: the bf16 SwiGLU rows contribute about 2^-9 / sqrt(3)
 # of RMS, the final rounding about 2^-9 / sqrt(3) of each element.
