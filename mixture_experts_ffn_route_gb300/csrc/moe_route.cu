@@ -198,39 +198,36 @@ __device__ __forceinline__ unsigned long long order_key(double v) {
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
-constexpr int kRedecideWarps = 8;
+constexpr int kRedecideWarps = 16;
+constexpr int kRedecideBatch = 14;  // 16-byte loads of Wg^T in flight per lane
 
-// Float64 selection score of one (token, expert) pair, one warp: each bf16 x
-// bf16 product is exact in fp32; the products are summed as unevaluated float
-// pairs (hi, lo) with TwoSum on the fp32 pipes (GB300's fp64 rate is low),
-// eight pairs per lane, folded as float pairs across the lanes in a fixed
-// order, and converted to float64 once.  The logit is within ~1e-12 of the
-// exact value at the workload sizes.  Returned as an order-preserving integer
-// key of score + bias.
-__device__ __forceinline__ unsigned long long pair_key(const uint16_t* __restrict__ X,
-                                                       const uint16_t* __restrict__ WgT,
-                                                       const float* __restrict__ bias, int H, int fn,
-                                                       int t, int e, int lane) {
-  const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
+// Sum over the 16-byte vectors [v_begin, v_end) of the token row xs (shared
+// memory) and Wg^T row e of the bf16 x bf16 products, one warp: each product
+// is exact in fp32; the products are summed as unevaluated float pairs
+// (hi, lo) with TwoSum on the fp32 pipes (GB300's fp64 rate is low), eight
+// pairs per lane, folded as float pairs across the lanes in a fixed order.
+// Returns the pair (H, L) in every lane.
+__device__ __forceinline__ float2 pair_dot(const uint4* __restrict__ xs, const uint16_t* __restrict__ WgT,
+                                           int H, int e, int v_begin, int v_end, int lane) {
   const uint4* wr = reinterpret_cast<const uint4*>(WgT + static_cast<long long>(e) * H);
-  const int vecs = H / 8;  // 16-byte vectors per row
   float hi[8], lo[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.0f;
-  for (int v0 = lane; v0 < vecs; v0 += 8 * 32) {
-    uint4 a[8], b[8];
+  for (int v0 = v_begin + lane; v0 < v_end; v0 += kRedecideBatch * 32) {
+    uint4 b[kRedecideBatch];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {  // all loads of this round first
+    for (int u = 0; u < kRedecideBatch; ++u) {  // all loads of this round first
       const int v = v0 + u * 32;
-      a[u] = v < vecs ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
-      b[u] = v < vecs ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
+      b[u] = v < v_end ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float p[8] = {bf16_lo(a[u].x) * bf16_lo(b[u].x), bf16_hi(a[u].x) * bf16_hi(b[u].x),
-                          bf16_lo(a[u].y) * bf16_lo(b[u].y), bf16_hi(a[u].y) * bf16_hi(b[u].y),
-                          bf16_lo(a[u].z) * bf16_lo(b[u].z), bf16_hi(a[u].z) * bf16_hi(b[u].z),
-                          bf16_lo(a[u].w) * bf16_lo(b[u].w), bf16_hi(a[u].w) * bf16_hi(b[u].w)};
+    for (int u = 0; u < kRedecideBatch; ++u) {
+      const int v = v0 + u * 32;
+      const uint4 a = v < v_end ? xs[v] : make_uint4(0, 0, 0, 0);
+      const float p[8] = {bf16_lo(a.x) * bf16_lo(b[u].x), bf16_hi(a.x) * bf16_hi(b[u].x),
+                          bf16_lo(a.y) * bf16_lo(b[u].y), bf16_hi(a.y) * bf16_hi(b[u].y),
+                          bf16_lo(a.z) * bf16_lo(b[u].z), bf16_hi(a.z) * bf16_hi(b[u].z),
+                          bf16_lo(a.w) * bf16_lo(b[u].w), bf16_hi(a.w) * bf16_hi(b[u].w)};
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float sum, err;
@@ -246,32 +243,60 @@ __device__ __forceinline__ unsigned long long pair_key(const uint16_t* __restric
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
     ff_add(H0, L0, __shfl_xor_sync(0xffffffffu, H0, o), __shfl_xor_sync(0xffffffffu, L0, o));
-  double v = score_f64(static_cast<double>(H0) + static_cast<double>(L0), fn);
-  if (bias != nullptr) v += static_cast<double>(bias[e]);
-  return order_key(v);
+  return make_float2(H0, L0);
 }
 
 // Re-decide the close tokens: one block per listed token (striding over the
-// list).  The block's warps score its candidates in float64 (one pair per warp
-// at a time, keys to rs.key); then warp 0 takes k arg-max rounds over the keys,
-// larger score first, equal scores to the lower id, and writes the ids and the
-// gates, computed from the candidates' listed fp32 logits (and, for softmax,
-// the token's listed normaliser).  The last block to finish zeroes the list
+// list).  The token's row of X goes to shared memory once; the block's warps
+// score its candidates in float64 (each candidate's row split over the warps
+// the group of candidates leaves, the float-pair partial sums added in a
+// fixed order; keys to rs.key); then warp 0 takes k arg-max rounds over the
+// keys, larger score first, equal scores to the lower id, and writes the ids
+// and the gates,
+// computed from the candidates' listed fp32 logits (and, for softmax, the
+// token's listed normaliser).  The last block to finish zeroes the list
 // counters, so the next call starts with empty lists.
 __global__ void __launch_bounds__(kRedecideWarps * 32)
     route_redecide_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
                           const float* __restrict__ bias, int H, int k, int fn, float alpha, int renorm,
                           int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs) {
+  extern __shared__ uint4 xs[];  // [H / 8], then the partial sums
+  float2* part = reinterpret_cast<float2*>(xs + H / 8);  // [kRedecideWarps]
   const int n = *reinterpret_cast<volatile int*>(rs.counters);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int vecs = H / 8;
   for (int j = blockIdx.x; j < n; j += gridDim.x) {
     const int4 f = rs.flagged[j];
     const int t = f.x, base = f.y, count = f.z;
-    for (int i = warp; i < count; i += kRedecideWarps) {
-      const unsigned long long key = pair_key(X, WgT, bias, H, fn, t, rs.pairs[base + i].y, lane);
-      if (lane == 0) rs.key[base + i] = key;
-    }
+    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
+    for (int v = threadIdx.x; v < vecs; v += blockDim.x) xs[v] = __ldg(xr + v);
     __syncthreads();
+    // candidates in groups of g = min(count, warps); the warps of a group's
+    // candidate split the row (ns parts), their float pairs added in order
+    for (int c0 = 0; c0 < count; c0 += kRedecideWarps) {
+      const int g = min(count - c0, kRedecideWarps);
+      const int ns = kRedecideWarps / g;
+      const int c = warp % g, part_i = warp / g;
+      if (part_i < ns) {
+        const int len = (vecs + ns - 1) / ns;
+        const int vb = part_i * len, ve = min(vecs, vb + len);
+        const float2 d = pair_dot(xs, WgT, H, rs.pairs[base + c0 + c].y, vb, ve, lane);
+        if (lane == 0) part[warp] = d;
+      }
+      __syncthreads();
+      if (warp == 0 && lane < g) {
+        float2 acc = part[lane];
+        for (int q = 1; q < ns; ++q) {
+          const float2 d = part[q * g + lane];
+          ff_add(acc.x, acc.y, d.x, d.y);
+        }
+        const int e = rs.pairs[base + c0 + lane].y;
+        double v = score_f64(static_cast<double>(acc.x) + static_cast<double>(acc.y), fn);
+        if (bias != nullptr) v += static_cast<double>(bias[e]);
+        rs.key[base + c0 + lane] = order_key(v);
+      }
+      __syncthreads();
+    }
     if (warp == 0) {
       const float2 nrm = rs.fnorm[j];
       // candidates held in registers, up to 4 per lane (count <= 128); more
@@ -370,8 +395,15 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, cudaStream_t s) {
-  route_redecide_kernel<<<2 * num_sms(), kRedecideWarps * 32, 0, s>>>(X, WgT, bias, H, k, score_fn,
-                                                                      alpha, renorm, E_ids, G, rs);
+  const size_t sh = static_cast<size_t>(H) * 2 + kRedecideWarps * sizeof(float2);
+  if (sh > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_redecide_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sh));
+    if (e != cudaSuccess) return e;
+  }
+  route_redecide_kernel<<<2 * num_sms(), kRedecideWarps * 32, sh, s>>>(X, WgT, bias, H, k, score_fn,
+                                                                       alpha, renorm, E_ids, G, rs);
   return cudaGetLastError();
 }
 

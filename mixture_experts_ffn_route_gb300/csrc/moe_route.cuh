@@ -26,9 +26,14 @@ __device__ __forceinline__ float band_at(float v, int fn) {
   return fn == 2 ? kBandSoftmax * fmaxf(1.0f, fabsf(v)) : kBand;
 }
 
+// fp32 scores with the fast exponential and division (relative errors of a
+// few 1e-6 for |l| <= 20: a sigmoid error of ~1e-6, far inside the band; a
+// logit below -88 gives an infinite denominator and a score of 0); log1p
+// stays the accurate one, since sqrt amplifies the error of a softplus near
+// zero.
 __device__ __forceinline__ float score_f32(float l, int fn) {
-  if (fn == 0) return 1.0f / (1.0f + expf(-l));
-  if (fn == 1) return sqrtf(fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l))));
+  if (fn == 0) return __fdividef(1.0f, 1.0f + __expf(-l));
+  if (fn == 1) return sqrtf(fmaxf(l, 0.0f) + log1pf(__expf(-fabsf(l))));
   return l;  // softmax: select on the logit (monotone in the softmax value)
 }
 
@@ -83,7 +88,7 @@ __device__ __forceinline__ float warp_max(float v) {
 // exp(l - lmax) / zsum over all experts of the token), scaled by alpha and,
 // with renorm, divided by den, the sum of the k affinities.
 __device__ __forceinline__ float affinity_f32(float l, int fn, float lmax, float zsum) {
-  return fn == 2 ? expf(l - lmax) / zsum : score_f32(l, fn);
+  return fn == 2 ? __expf(l - lmax) / zsum : score_f32(l, fn);
 }
 
 }  // namespace moe

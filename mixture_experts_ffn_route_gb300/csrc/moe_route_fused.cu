@@ -40,7 +40,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;  // 16 warps: the decision has one warp per row
 constexpr int kFusedMaxE = 384;                 // 6 boxes of 64 columns
 constexpr int kRingMax = 6 * 128 * 64 * 4;      // 192 KB: the dump of 384 fp32 columns
 constexpr int kBoxBytes = 64 * kBK * 2;         // one 64 x 64 bf16 box of Wg: 8 KB
@@ -135,140 +135,301 @@ __device__ __forceinline__ void transpose_block(const FusedParams& p, int kb, in
   }
 }
 
-// The routing decision of token t from its fp32 logits, one warp: lane l
-// holds the logits of chunks l, l + 32, l + 64 (columns 4c .. 4c + 3).
-__device__ __forceinline__ void decide_row(const FusedParams& p, int t, const float (&lg)[12],
-                                           int lane) {
+// Order-preserving 32-bit key of a float: larger float, larger key (0 is below
+// every float's key: it marks taken or absent entries).
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// The routing decision of NR tokens from their fp32 logits, one warp: lane l
+// holds the logits of chunks l, l + 32, ... (columns 4c .. 4c + 3), NCH
+// chunks per lane (E <= 128 NCH).  The NR rows are decided side by side, so
+// their dependency chains (warp reductions, shuffles) overlap.  Each arg-max
+// round is two single-instruction warp reductions: the largest score key,
+// then the lowest expert id among the lanes holding it (equal scores go to
+// the lower id).  bias_s: the selection bias in shared memory (or null);
+// ids_s[r]: in hash mode row r's k table entries, prefetched into shared
+// memory, then a 1 for a token id outside [0, V) (flagged there).  Rows with
+// valid[r] false are stand-ins (computed, neither listed nor written).
+template <int NCH, int NR>
+__device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)[NR],
+                                            const bool (&valid)[NR], const float (&lg)[NR][4 * NCH],
+                                            const float* bias_s, const int* const (&ids_s)[NR],
+                                            int lane) {
+  constexpr int NS = 4 * NCH;  // slots per lane
   const int E = p.E, k = p.k, fn = p.fn;
-  // column of register slot i
   auto col = [&](int i) { return 4 * (lane + 32 * (i >> 2)) + (i & 3); };
-  float lmax = 0.0f, zsum = 1.0f;
-  if (fn == 2) {
-    float m = -FLT_MAX;
+  float lmax[NR], zsum[NR];
 #pragma unroll
-    for (int i = 0; i < 12; ++i)
-      if (col(i) < E) m = fmaxf(m, lg[i]);
-    lmax = warp_max(m);
-    float z = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 12; ++i)
-      if (col(i) < E) z += expf(lg[i] - lmax);
-    zsum = warp_sum(z);
+  for (int r = 0; r < NR; ++r) {
+    lmax[r] = 0.0f;
+    zsum[r] = 1.0f;
   }
-  int my_sel = -1;    // lane j < k: the j-th id
-  float my_l = 0.0f;  // and its logit
-  bool tok_ok = true;
+  if (fn == 2) {
+    float m[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      m[r] = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (col(i) < E) m[r] = fmaxf(m[r], lg[r][i]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) lmax[r] = warp_max(m[r]);
+    float z[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      z[r] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (col(i) < E) z[r] += __expf(lg[r][i] - lmax[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) zsum[r] = warp_sum(z[r]);
+  }
+  int my_sel[NR];    // lane j < k: the j-th id
+  float my_l[NR];    // and its logit
+  bool tok_ok[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    my_sel[r] = -1;
+    my_l[r] = 0.0f;
+    tok_ok[r] = true;
+  }
   if (p.token_ids != nullptr) {
     // ---------------------------------------------------------------- hash
-    const int tok = __ldg(p.token_ids + t);
-    tok_ok = tok >= 0 && tok < p.V;
-    if (!tok_ok && lane == 0) set_flag(p.status, kFlagBadToken);
+    int mine[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      mine[r] = lane < k ? ids_s[r][lane] : -1;
+      tok_ok[r] = ids_s[r][kMaxK] == 0;
+    }
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
-      const int e = tok_ok ? __ldg(p.tid2eid + static_cast<long long>(tok) * k + j) : -1;
-      float mine = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 12; ++i)
-        if (col(i) == e) mine = lg[i];
-      const float le = __shfl_sync(0xffffffffu, mine, e >= 0 ? (e >> 2) & 31 : 0);
-      if (lane == j) {
-        my_sel = e;
-        my_l = le;
+      for (int r = 0; r < NR; ++r) {
+        const int e = __shfl_sync(0xffffffffu, mine[r], j);
+        float v = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+          if (col(i) == e) v = lg[r][i];
+        v = __shfl_sync(0xffffffffu, v, (e >= 0 ? e >> 2 : 0) & 31);
+        if (lane == j) {
+          my_sel[r] = e;
+          my_l[r] = v;
+        }
       }
     }
   } else {
     // ---------------------------------------------------------------- top-k
-    float sc[12];
+    uint32_t sk[NR][NS];
 #pragma unroll
-    for (int i = 0; i < 12; ++i) {
-      const int e = col(i);
-      sc[i] = -FLT_MAX;
-      if (e < E) {
-        float v = score_f32(lg[i], fn);
-        if (p.bias != nullptr) v += __ldg(p.bias + e);
-        sc[i] = v;
-      }
-    }
-    const int rounds = (k < E) ? k + 1 : k;
-    bool close = false;
-    float prev = 0.0f, kth = 0.0f;
-#pragma unroll 1
-    for (int r = 0; r < rounds; ++r) {
-      float best = -FLT_MAX;
-      int bid = 0x7fffffff;
-      float bl = 0.0f;
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-      for (int i = 0; i < 12; ++i)
-        if (col(i) < E && before(sc[i], col(i), best, bid)) {
-          best = sc[i];
-          bid = col(i);
-          bl = lg[i];
-        }
-      warp_argmax_payload(best, bid, bl);
-#pragma unroll
-      for (int i = 0; i < 12; ++i)
-        if (col(i) == bid) sc[i] = -FLT_MAX;  // taken
-      if (r > 0) close |= (prev - best) < band_at(prev, fn);
-      prev = best;
-      if (r == k - 1) kth = best;
-      if (r < k && lane == r) {
-        my_sel = bid;
-        my_l = bl;
-      }
-    }
-    if (close) {
-      // candidates: every expert within twice the band below the k-th score
-      const float lim = kth - 2.0f * band_at(kth, fn);
-      int count = 0;
-      bool cand[12];
-#pragma unroll
-      for (int i = 0; i < 12; ++i) {
+      for (int i = 0; i < NS; ++i) {
         const int e = col(i);
-        bool c = false;
-        if (e < E) {
-          float v = score_f32(lg[i], fn);
-          if (p.bias != nullptr) v += __ldg(p.bias + e);
-          c = v >= lim;
+        const float v = score_f32(lg[r][i], fn);
+        sk[r][i] = e < E ? fkey(bias_s != nullptr ? v + bias_s[e] : v) : 0u;
+      }
+    const int rounds = (k < E) ? k + 1 : k;
+    bool close[NR];
+    float prev[NR], kth[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      close[r] = false;
+      prev[r] = kth[r] = 0.0f;
+    }
+#pragma unroll 1
+    for (int rd = 0; rd < rounds; ++rd) {
+      uint32_t bk[NR];
+      int bid[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        bk[r] = 0u;
+        bid[r] = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NS; ++i)  // slots ascend in column: the first of equal keys wins
+          if (sk[r][i] > bk[r]) {
+            bk[r] = sk[r][i];
+            bid[r] = col(i);
+          }
+      }
+      uint32_t m[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) m[r] = __reduce_max_sync(0xffffffffu, bk[r]);
+      int win[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        win[r] = static_cast<int>(__reduce_min_sync(
+            0xffffffffu, bk[r] == m[r] ? static_cast<uint32_t>(bid[r]) : 0x7fffffffu));
+      float wl[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        wl[r] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+          if (col(i) == win[r]) {
+            sk[r][i] = 0u;  // taken
+            wl[r] = lg[r][i];
+          }
+      }
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        wl[r] = __shfl_sync(0xffffffffu, wl[r], (win[r] >> 2) & 31);
+        const float best = fkey_value(m[r]);
+        if (rd > 0) close[r] |= (prev[r] - best) < band_at(prev[r], fn);
+        prev[r] = best;
+        if (rd == k - 1) kth[r] = best;
+        if (lane == rd && rd < k) {
+          my_sel[r] = win[r];
+          my_l[r] = wl[r];
         }
-        cand[i] = c;
-        count += __popc(__ballot_sync(0xffffffffu, c));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (!close[r] || !valid[r]) continue;  // warp-uniform
+      // candidates: every expert within twice the band below the k-th score
+      const float lim = kth[r] - 2.0f * band_at(kth[r], fn);
+      int count = 0;
+      bool cand[NS];
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const int e = col(i);
+        const float v = score_f32(lg[r][i], fn);
+        cand[i] = e < E && (bias_s != nullptr ? v + bias_s[e] : v) >= lim;
+        count += __popc(__ballot_sync(0xffffffffu, cand[i]));
       }
       int base = 0;
       if (lane == 0) {
         base = atomicAdd(p.rs.counters + 1, count);
         const int fi = atomicAdd(p.rs.counters + 0, 1);
-        p.rs.flagged[fi] = make_int4(t, base, count, 0);
-        p.rs.fnorm[fi] = make_float2(lmax, zsum);
+        p.rs.flagged[fi] = make_int4(t[r], base, count, 0);
+        p.rs.fnorm[fi] = make_float2(lmax[r], zsum[r]);
       }
       base = __shfl_sync(0xffffffffu, base, 0);
 #pragma unroll
-      for (int i = 0; i < 12; ++i) {
+      for (int i = 0; i < NS; ++i) {
         const unsigned bm = __ballot_sync(0xffffffffu, cand[i]);
         if (cand[i]) {
           const int at = base + __popc(bm & ((1u << lane) - 1u));
-          p.rs.pairs[at] = make_int2(t, col(i));
-          p.rs.plogit[at] = lg[i];
+          p.rs.pairs[at] = make_int2(t[r], col(i));
+          p.rs.plogit[at] = lg[r][i];
         }
         base += __popc(bm);
       }
     }
   }
   // gates (a close token's ids and gates are rewritten by the re-decision)
-  float a = 0.0f;
-  if (lane < k) {
-    if (my_sel >= 0 && my_sel < E) {
-      a = affinity_f32(my_l, fn, lmax, zsum);
-    } else if (tok_ok) {
-      set_flag(p.status, kFlagBadExpert);  // a table entry outside [0, E)
+  float a[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    a[r] = 0.0f;
+    if (lane < k) {
+      if (my_sel[r] >= 0 && my_sel[r] < E) {
+        a[r] = affinity_f32(my_l[r], fn, lmax[r], zsum[r]);
+      } else if (tok_ok[r]) {
+        set_flag(p.status, kFlagBadExpert);  // a table entry outside [0, E)
+      }
     }
   }
-  float den = 0.0f;
-  for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, a, j);
-  if (lane < k) {
-    float g = p.alpha * a;
-    if (p.renorm) g = den > 0.0f ? p.alpha * a / den : 0.0f;
-    p.E_ids[static_cast<long long>(t) * k + lane] = my_sel;
-    p.G[static_cast<long long>(t) * k + lane] = g;
+  float den[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) den[r] = warp_sum(a[r]);  // lanes >= k hold 0
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+    if (lane < k && valid[r]) {
+      float g = p.alpha * a[r];
+      if (p.renorm) g = den[r] > 0.0f ? p.alpha * a[r] / den[r] : 0.0f;
+      p.E_ids[static_cast<long long>(t[r]) * k + lane] = my_sel[r];
+      p.G[static_cast<long long>(t[r]) * k + lane] = g;
+    }
+}
+
+// Rows [rank R, rank R + R) of the tile, NR per warp at a time: their logits
+// from this CTA's (reduced) dump, optionally written out, then decided.
+template <int NCH, int NR>
+__device__ __forceinline__ void decide_band(const FusedParams& p, const uint8_t* smem, int rank,
+                                            int R, int row0, int cpr, const float* bias_s,
+                                            const int* ids_base, int warp, int lane) {
+  constexpr int NW = kThreads / 32;
+  for (int rr0 = warp; rr0 < R; rr0 += NR * NW) {
+    int t[NR];
+    bool valid[NR];
+    float lg[NR][4 * NCH];
+    const int* ids[NR];
+    int nvalid = 0;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      int rr = rr0 + r * NW;
+      valid[r] = rr < R && row0 + rank * R + rr < p.T;
+      nvalid += valid[r] ? 1 : 0;
+      if (!valid[r]) rr = rr0;  // a stand-in row
+      const int row = rank * R + rr;
+      t[r] = row0 + row;
+      ids[r] = ids_base + rr * (kMaxK + 1);
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = lane + 32 * j;
+        const float4 x = c < cpr ? *reinterpret_cast<const float4*>(smem + dump_off(row, c, cpr))
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        lg[r][4 * j] = x.x; lg[r][4 * j + 1] = x.y; lg[r][4 * j + 2] = x.z; lg[r][4 * j + 3] = x.w;
+      }
+    }
+    if (nvalid == 0) break;
+    if (p.logits_out != nullptr) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c = lane + 32 * j;
+          if (valid[r] && 4 * c < p.E)
+            *reinterpret_cast<float4*>(p.logits_out + static_cast<long long>(t[r]) * p.E + 4 * c) =
+                make_float4(lg[r][4 * j], lg[r][4 * j + 1], lg[r][4 * j + 2], lg[r][4 * j + 3]);
+        }
+    }
+    if (p.select) decide_rows<NCH, NR>(p, t, valid, lg, bias_s, ids, lane);
+  }
+}
+
+// Sum of the S partial dumps over this CTA's band of rows [rank R, rank R + R)
+// (R = 128 / S), written over the band in this CTA's own dump, which no other
+// CTA reads.  Ranks are added in order.  Each thread issues the loads of
+// three chunks before using any (distributed shared memory is slow to answer).
+template <int S>
+__device__ __forceinline__ void reduce_band(uint8_t* smem, uint32_t ring0, int rank, int cpr) {
+  constexpr int R = kBM / S;
+  uint32_t part[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) part[s] = map_rank(ring0, s);
+  const int n_chunks = R * cpr;
+  for (int i0 = threadIdx.x; i0 < n_chunks; i0 += 3 * kThreads) {
+    float4 x[3][S];
+    uint32_t off[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int i = i0 + u * kThreads;
+      off[u] = i < n_chunks ? dump_off(rank * R + i / cpr, i % cpr, cpr) : 0u;
+      if (i < n_chunks) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) x[u][s] = ld_cluster_f4(part[s] + off[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      if (i0 + u * kThreads < n_chunks) {
+        float4 acc = x[u][0];
+#pragma unroll
+        for (int s = 1; s < S; ++s) {
+          acc.x += x[u][s].x; acc.y += x[u][s].y; acc.z += x[u][s].z; acc.w += x[u][s].w;
+        }
+        *reinterpret_cast<float4*>(smem + off[u]) = acc;
+      }
+    }
   }
 }
 
@@ -286,6 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tfull = empty0 + 8 * p.stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * p.stages + 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // side tables for the decision: the selection bias [E] and, in hash mode,
+  // each decided row's table entries [R][kMaxK + 1] (the last: 1 for a token
+  // id outside [0, V))
+  float* bias_s = reinterpret_cast<float*>(bar_area + 256);
+  int* ids_s = reinterpret_cast<int*>(bar_area + 256 + kFusedMaxE * 4);
 
   const int S = p.S;
   const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -368,7 +534,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(tfull);  // also after a break: every MMA issued completes before teardown
       drain_wait(tfull, 0, 10000000ull);
     }
-  } else if (warp < 6) {
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ side tables
+    // idle until the decision: fetch what it reads from global memory
+    const int tid = threadIdx.x - 6 * 32, nt = kThreads - 6 * 32;
+    if (p.select && p.bias != nullptr)
+      for (int e = tid; e < p.E; e += nt) bias_s[e] = __ldg(p.bias + e);
+    if (p.select && p.token_ids != nullptr) {
+      const int R = kBM / S;
+      for (int rr = tid; rr < R; rr += nt) {
+        const int t = row0 + rank * R + rr;
+        int* row = ids_s + rr * (kMaxK + 1);
+        if (t >= p.T) continue;
+        const int tok = __ldg(p.token_ids + t);
+        const bool ok = tok >= 0 && tok < p.V;
+        if (!ok) set_flag(p.status, kFlagBadToken);
+        for (int j = 0; j < p.k; ++j)
+          row[j] = ok ? __ldg(p.tid2eid + static_cast<long long>(tok) * p.k + j) : -1;
+        row[kMaxK] = ok ? 0 : 1;
+      }
+    }
+  } else {
     // ------------------------------------------------------------ transpose, dump
     const int tid = threadIdx.x - 64;
     if (p.WgT != nullptr) {
@@ -404,54 +590,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int R = kBM / S;
   const int cpr = ncols / 4;
   if (S > 1 && !*abort_flag) {
-    uint32_t part[8];
-#pragma unroll
-    for (int s = 0; s < 8; ++s) part[s] = s < S ? map_rank(ring0, s) : 0u;
-    const int n_chunks = R * cpr;
-#pragma unroll 2
-    for (int i = threadIdx.x; i < n_chunks; i += kThreads) {
-      const int r = rank * R + i / cpr;
-      const uint32_t off = dump_off(r, i % cpr, cpr);
-      float4 x[8];
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        if (s < S) x[s] = ld_cluster_f4(part[s] + off);
-      float4 acc = x[0];
-#pragma unroll
-      for (int s = 1; s < 8; ++s)
-        if (s < S) {
-          acc.x += x[s].x; acc.y += x[s].y; acc.z += x[s].z; acc.w += x[s].w;
-        }
-      *reinterpret_cast<float4*>(smem + off) = acc;
-    }
+    if (S == 2) reduce_band<2>(smem, ring0, rank, cpr);
+    else if (S == 4) reduce_band<4>(smem, ring0, rank, cpr);
+    else reduce_band<8>(smem, ring0, rank, cpr);
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- decide
   if (!*abort_flag) {
-    for (int rr = warp; rr < R; rr += kThreads / 32) {
-      const int r = rank * R + rr;
-      const int t = row0 + r;
-      if (t >= p.T) break;
-      float lg[12];
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const int c = lane + 32 * j;
-        const float4 x = c < cpr ? *reinterpret_cast<const float4*>(smem + dump_off(r, c, cpr))
-                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        lg[4 * j] = x.x; lg[4 * j + 1] = x.y; lg[4 * j + 2] = x.z; lg[4 * j + 3] = x.w;
-      }
-      if (p.logits_out != nullptr) {
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int c = lane + 32 * j;
-          if (4 * c < p.E)
-            *reinterpret_cast<float4*>(p.logits_out + static_cast<long long>(t) * p.E + 4 * c) =
-                make_float4(lg[4 * j], lg[4 * j + 1], lg[4 * j + 2], lg[4 * j + 3]);
-        }
-      }
-      if (p.select) decide_row(p, t, lg, lane);
-    }
+    const float* bs = p.bias != nullptr ? bias_s : nullptr;
+    if (cpr <= 32)
+      decide_band<1, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
+    else if (cpr <= 64)
+      decide_band<2, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
+    else
+      decide_band<3, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
   }
 
   if (S > 1) cluster_sync_all();  // partial rows stay readable until every CTA is done
@@ -520,11 +673,15 @@ FusedShape fused_shape(int T, int H, int E) {
   const int dump = kBM * nbx * 64 * 4;
   f.ring_bytes = f.stages * f.stage_bytes > dump ? f.stages * f.stage_bytes : dump;
   f.tmem_cols = pow2_at_least(nbx * 64);
-  f.smem_bytes = f.ring_bytes + 1024 + 256;
+  f.smem_bytes = f.ring_bytes + 1024 + 256 + kFusedMaxE * 4 + kBM * (kMaxK + 1) * 4;
   f.S = 1;
   const int sms = num_sms();
+  // the largest S whose clusters are all co-resident in one wave and whose
+  // ranks all get k-blocks; the decision's rows are split S ways as well, so
+  // small layers take clusters too
   for (int cand : {8, 4, 2}) {
-    if (n_rt * cand > sms || nkb < 8 * cand) continue;
+    const int per = (nkb + cand - 1) / cand;
+    if (n_rt * cand > sms || cand > nkb || (cand - 1) * per >= nkb) continue;
     if (max_active_clusters(cand, f.smem_bytes) < n_rt) continue;
     f.S = cand;
     break;
