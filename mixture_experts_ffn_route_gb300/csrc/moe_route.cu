@@ -199,6 +199,7 @@ __device__ __forceinline__ unsigned long long order_key(double v) {
 }
 
 constexpr int kRedecideWarps = 16;
+constexpr int kRedecideList = 512;  // candidates a token's shared lists hold
 constexpr int kRedecideBatch = 14;  // 16-byte loads of Wg^T in flight per lane
 
 // Sum over the 16-byte vectors [v_begin, v_end) of the token row xs (shared
@@ -260,8 +261,15 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
     route_redecide_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
                           const float* __restrict__ bias, int H, int k, int fn, float alpha, int renorm,
                           int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs) {
-  extern __shared__ uint4 xs[];  // [H / 8], then the partial sums
-  float2* part = reinterpret_cast<float2*>(xs + H / 8);  // [kRedecideWarps]
+  extern __shared__ uint4 xs[];  // [H / 8], then the partial sums and the exact list
+  float2* part = reinterpret_cast<float2*>(xs + H / 8);             // [kRedecideWarps]
+  int* exact = reinterpret_cast<int*>(part + kRedecideWarps);       // [kRedecideList]
+  __shared__ float sc[kRedecideList];
+  __shared__ int n_exact;
+  __shared__ unsigned long long key_s[kRedecideList];
+  __shared__ int id_s[kRedecideList];
+  __shared__ int sel_s[kMaxK];
+  __shared__ float aff_s[kMaxK];
   const int n = *reinterpret_cast<volatile int*>(rs.counters);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int vecs = H / 8;
@@ -270,17 +278,50 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
     const int t = f.x, base = f.y, count = f.z;
     const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
     for (int v = threadIdx.x; v < vecs; v += blockDim.x) xs[v] = __ldg(xr + v);
+    // The fp32 selection score of each candidate, as the first decision took
+    // it.  A candidate at least a band away from every other candidate has a
+    // certain place in the order: its float64 key is its fp32 score.  Only
+    // the others are recomputed exactly (all of them when the list is long).
+    const bool small = count <= kRedecideList;
+    for (int i = threadIdx.x; small && i < count; i += blockDim.x) {
+      const int e = rs.pairs[base + i].y;
+      float v = score_f32(rs.plogit[base + i], fn);
+      if (bias != nullptr) v += bias[e];
+      sc[i] = v;
+    }
     __syncthreads();
-    // candidates in groups of g = min(count, warps); the warps of a group's
+    for (int i = threadIdx.x; small && i < count; i += blockDim.x) {
+      bool near = false;
+      for (int q = 0; q < count && !near; ++q)
+        near = q != i && fabsf(sc[i] - sc[q]) < band_at(fmaxf(sc[i], sc[q]), fn);
+      exact[i] = near ? 1 : 0;
+      if (!near) rs.key[base + i] = order_key(static_cast<double>(sc[i]));
+    }
+    __syncthreads();
+    if (warp == 0 && small) {  // the recomputed candidates' list, in candidate order
+      int m = 0;
+      for (int c = 0; c < count; c += 32) {
+        const bool near = c + lane < count && exact[c + lane] != 0;
+        const unsigned b = __ballot_sync(0xffffffffu, near);
+        __syncwarp();
+        if (near) exact[m + __popc(b & ((1u << lane) - 1u))] = c + lane;
+        m += __popc(b);
+      }
+      if (lane == 0) n_exact = m;
+    }
+    __syncthreads();
+    const int ne = small ? n_exact : count;
+    auto exact_at = [&](int c) { return small ? exact[c] : c; };
+    // exact candidates in groups of g = min(ne, warps); the warps of a group's
     // candidate split the row (ns parts), their float pairs added in order
-    for (int c0 = 0; c0 < count; c0 += kRedecideWarps) {
-      const int g = min(count - c0, kRedecideWarps);
+    for (int c0 = 0; c0 < ne; c0 += kRedecideWarps) {
+      const int g = min(ne - c0, kRedecideWarps);
       const int ns = kRedecideWarps / g;
       const int c = warp % g, part_i = warp / g;
       if (part_i < ns) {
         const int len = (vecs + ns - 1) / ns;
         const int vb = part_i * len, ve = min(vecs, vb + len);
-        const float2 d = pair_dot(xs, WgT, H, rs.pairs[base + c0 + c].y, vb, ve, lane);
+        const float2 d = pair_dot(xs, WgT, H, rs.pairs[base + exact_at(c0 + c)].y, vb, ve, lane);
         if (lane == 0) part[warp] = d;
       }
       __syncthreads();
@@ -290,12 +331,47 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
           const float2 d = part[q * g + lane];
           ff_add(acc.x, acc.y, d.x, d.y);
         }
-        const int e = rs.pairs[base + c0 + lane].y;
+        const int i = exact_at(c0 + lane);
+        const int e = rs.pairs[base + i].y;
         double v = score_f64(static_cast<double>(acc.x) + static_cast<double>(acc.y), fn);
         if (bias != nullptr) v += static_cast<double>(bias[e]);
-        rs.key[base + c0 + lane] = order_key(v);
+        rs.key[base + i] = order_key(v);
       }
       __syncthreads();
+    }
+    if (small) {
+      // rank of each candidate among the others (larger key first, equal keys
+      // lower id first): the k ranks below k are the selection, in order
+      for (int i = threadIdx.x; i < count; i += blockDim.x) {
+        key_s[i] = rs.key[base + i];
+        id_s[i] = rs.pairs[base + i].y;
+      }
+      __syncthreads();
+      const float2 nrm = rs.fnorm[j];
+      for (int i = threadIdx.x; i < count; i += blockDim.x) {
+        const unsigned long long v = key_s[i];
+        const int e = id_s[i];
+        int rank = 0;
+        for (int q = 0; q < count; ++q) rank += before(key_s[q], id_s[q], v, e) ? 1 : 0;
+        if (rank < k) {
+          sel_s[rank] = e;
+          aff_s[rank] = affinity_f32(rs.plogit[base + i], fn, nrm.x, nrm.y);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        float den = 0.0f;
+        for (int jj = 0; jj < k; ++jj) den += aff_s[jj];  // in rank order
+        if (lane < k) {
+          const float a = aff_s[lane];
+          float g = alpha * a;
+          if (renorm) g = den > 0.0f ? alpha * a / den : 0.0f;
+          E_ids[static_cast<long long>(t) * k + lane] = sel_s[lane];
+          G[static_cast<long long>(t) * k + lane] = g;
+        }
+      }
+      __syncthreads();
+      continue;
     }
     if (warp == 0) {
       const float2 nrm = rs.fnorm[j];
@@ -395,7 +471,8 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, cudaStream_t s) {
-  const size_t sh = static_cast<size_t>(H) * 2 + kRedecideWarps * sizeof(float2);
+  const size_t sh = static_cast<size_t>(H) * 2 + kRedecideWarps * sizeof(float2) +
+                    kRedecideList * sizeof(int);
   if (sh > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_redecide_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

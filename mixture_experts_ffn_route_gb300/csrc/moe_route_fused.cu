@@ -159,7 +159,8 @@ template <int NCH, int NR>
 __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)[NR],
                                             const bool (&valid)[NR], const float (&lg)[NR][4 * NCH],
                                             const float* bias_s, const int* const (&ids_s)[NR],
-                                            int lane) {
+                                            int* stage_n, int4* stage_f, float2* stage_n2,
+                                            int band_t0, int* out_ids, float* out_g, int lane) {
   constexpr int NS = 4 * NCH;  // slots per lane
   const int E = p.E, k = p.k, fn = p.fn;
   auto col = [&](int i) { return 4 * (lane + 32 * (i >> 2)) + (i & 3); };
@@ -304,14 +305,15 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
         cand[i] = e < E && (bias_s != nullptr ? v + bias_s[e] : v) >= lim;
         count += __popc(__ballot_sync(0xffffffffu, cand[i]));
       }
-      int base = 0;
+      // the token's candidates go to its own slots [t E, t E + count) of the
+      // pair lists; the token is listed in the CTA's staging list, which the
+      // CTA appends to the global list with one atomic after the decisions
+      int base = t[r] * E;
       if (lane == 0) {
-        base = atomicAdd(p.rs.counters + 1, count);
-        const int fi = atomicAdd(p.rs.counters + 0, 1);
-        p.rs.flagged[fi] = make_int4(t[r], base, count, 0);
-        p.rs.fnorm[fi] = make_float2(lmax[r], zsum[r]);
+        const int fi = atomicAdd(stage_n, 1);
+        stage_f[fi] = make_int4(t[r], base, count, 0);
+        stage_n2[fi] = make_float2(lmax[r], zsum[r]);
       }
-      base = __shfl_sync(0xffffffffu, base, 0);
 #pragma unroll
       for (int i = 0; i < NS; ++i) {
         const unsigned bm = __ballot_sync(0xffffffffu, cand[i]);
@@ -345,8 +347,10 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
     if (lane < k && valid[r]) {
       float g = p.alpha * a[r];
       if (p.renorm) g = den[r] > 0.0f ? p.alpha * a[r] / den[r] : 0.0f;
-      p.E_ids[static_cast<long long>(t[r]) * k + lane] = my_sel[r];
-      p.G[static_cast<long long>(t[r]) * k + lane] = g;
+      // into the band's staging rows, written out whole after the decisions
+      const int rb = t[r] - band_t0;
+      out_ids[rb * k + lane] = my_sel[r];
+      out_g[rb * k + lane] = g;
     }
 }
 
@@ -355,7 +359,9 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
 template <int NCH, int NR>
 __device__ __forceinline__ void decide_band(const FusedParams& p, const uint8_t* smem, int rank,
                                             int R, int row0, int cpr, const float* bias_s,
-                                            const int* ids_base, int warp, int lane) {
+                                            const int* ids_base, int* stage_n, int4* stage_f,
+                                            float2* stage_n2, int* out_ids, float* out_g, int warp,
+                                            int lane) {
   constexpr int NW = kThreads / 32;
   for (int rr0 = warp; rr0 < R; rr0 += NR * NW) {
     int t[NR];
@@ -392,7 +398,9 @@ __device__ __forceinline__ void decide_band(const FusedParams& p, const uint8_t*
                 make_float4(lg[r][4 * j], lg[r][4 * j + 1], lg[r][4 * j + 2], lg[r][4 * j + 3]);
         }
     }
-    if (p.select) decide_rows<NCH, NR>(p, t, valid, lg, bias_s, ids, lane);
+    if (p.select)
+      decide_rows<NCH, NR>(p, t, valid, lg, bias_s, ids, stage_n, stage_f, stage_n2, row0 + rank * R,
+                           out_ids, out_g, lane);
   }
 }
 
@@ -452,6 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // id outside [0, V))
   float* bias_s = reinterpret_cast<float*>(bar_area + 256);
   int* ids_s = reinterpret_cast<int*>(bar_area + 256 + kFusedMaxE * 4);
+  // the CTA's close tokens, appended to the global list at the end
+  int4* stage_f = reinterpret_cast<int4*>(bar_area + 256 + kFusedMaxE * 4 + kBM * (kMaxK + 1) * 4);
+  float2* stage_n2 = reinterpret_cast<float2*>(stage_f + kBM);
+  int* stage_n = reinterpret_cast<int*>(tmem_slot + 2);
+  // the band's ids and gates, written out with whole-sector stores at the end
+  int* out_ids = reinterpret_cast<int*>(stage_n2 + kBM);
+  float* out_g = reinterpret_cast<float*>(out_ids + kBM * kMaxK);
 
   const int S = p.S;
   const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -468,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull, 1);
     *abort_flag = 0;
+    *stage_n = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -600,13 +616,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!*abort_flag) {
     const float* bs = p.bias != nullptr ? bias_s : nullptr;
     if (cpr <= 32)
-      decide_band<1, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
+      decide_band<1, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                       warp, lane);
     else if (cpr <= 64)
-      decide_band<2, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
+      decide_band<2, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                       warp, lane);
     else
-      decide_band<3, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, warp, lane);
+      decide_band<3, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                       warp, lane);
   }
 
+  __syncthreads();
+  {
+    __shared__ int list_base;
+    const int nf = *stage_n;
+    if (threadIdx.x == 0 && nf > 0) list_base = atomicAdd(p.rs.counters, nf);
+    if (p.select && !*abort_flag) {
+      const int R = kBM / S;
+      const int t0 = row0 + rank * R;
+      const int n_out = (min(p.T, t0 + R) - t0) * p.k;
+      for (int i = threadIdx.x; i < n_out; i += kThreads) {
+        p.E_ids[static_cast<long long>(t0) * p.k + i] = out_ids[i];
+        p.G[static_cast<long long>(t0) * p.k + i] = out_g[i];
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nf; i += kThreads) {
+      p.rs.flagged[list_base + i] = stage_f[i];
+      p.rs.fnorm[list_base + i] = stage_n2[i];
+    }
+  }
   if (S > 1) cluster_sync_all();  // partial rows stay readable until every CTA is done
   __syncthreads();
   if (warp == 1) {
@@ -673,7 +712,8 @@ FusedShape fused_shape(int T, int H, int E) {
   const int dump = kBM * nbx * 64 * 4;
   f.ring_bytes = f.stages * f.stage_bytes > dump ? f.stages * f.stage_bytes : dump;
   f.tmem_cols = pow2_at_least(nbx * 64);
-  f.smem_bytes = f.ring_bytes + 1024 + 256 + kFusedMaxE * 4 + kBM * (kMaxK + 1) * 4;
+  f.smem_bytes = f.ring_bytes + 1024 + 256 + kFusedMaxE * 4 + kBM * (kMaxK + 1) * 4 +
+                 kBM * (sizeof(int4) + sizeof(float2)) + 2 * kBM * kMaxK * 4;
   f.S = 1;
   const int sms = num_sms();
   // the largest S whose clusters are all co-resident in one wave and whose
