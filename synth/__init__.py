@@ -113,8 +113,9 @@ CONFIGS["c3p_mx"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e4m3")
 CONFIGS["c3p_q"] = dict(CONFIGS["c3p"], shared=0, quant="a8w8")
 CONFIGS["c3p_mxa4"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e2m1")
 # the large-FFN layer's expert shapes and rows per expert (~512) at a size one
-# ncu capture can take (4.3 GB of weights): its traffic ratio scales to c5
-CONFIGS["c5p"] = dict(CONFIGS["c5"], T=1024, E=4)
+# ncu capture can take (4.3 GB of weights), with given routing (ids drawn as
+# for c2): its Linear1 traffic ratio scales to c5
+CONFIGS["c5p"] = dict(CONFIGS["c5"], T=1024, E=4, routing="given")
 # the V4-Pro router at full size with a token-sized FFN (I = 64): a workload
 # whose routing kernels one ncu capture can take (1.1 GB of weights)
 CONFIGS["c3r"] = dict(CONFIGS["c3"], I=64)
