@@ -145,25 +145,65 @@ __device__ __forceinline__ float fkey_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// The routing decision of NR tokens from their fp32 logits, one warp: lane l
-// holds the logits of chunks l, l + 32, ... (columns 4c .. 4c + 3), NCH
-// chunks per lane (E <= 128 NCH).  The NR rows are decided side by side, so
-// their dependency chains (warp reductions, shuffles) overlap.  Each arg-max
-// round is two single-instruction warp reductions: the largest score key,
-// then the lowest expert id among the lanes holding it (equal scores go to
-// the lower id).  bias_s: the selection bias in shared memory (or null);
+// fp32 logit of column e of dump row `row`.
+__device__ __forceinline__ float dump_logit(const uint8_t* smem, int row, int e, int cpr) {
+  return *reinterpret_cast<const float*>(smem + dump_off(row, e >> 2, cpr) + 4 * (e & 3));
+}
+
+// Selection key of column e: the score plus the selection bias b (when the
+// layer has one) as an order-preserving integer, its low 9 bits replaced by
+// 511 - e.  Keys are then unique, a larger key is a larger score or, among
+// scores equal to 2^-14 relative, the lower id, and the id comes back from
+// the key.  0 (below every key) past the last expert.  The truncated score
+// is below the exact one by less than 2^-14 of its magnitude, so a decision
+// whose keys are within that of each other is listed for the float64
+// re-decision with the band (kTrunc below).
+constexpr float kTrunc = 1.0f / 8192.0f;  // 2^-13: twice the truncation
+__device__ __forceinline__ uint32_t sel_key(float l, float b, bool has_bias, int e, int E, int fn) {
+  if (e >= E) return 0u;
+  const float v = score_f32(l, fn);
+  return (fkey(has_bias ? v + b : v) & 0xFFFFFE00u) | static_cast<uint32_t>(511 - e);
+}
+__device__ __forceinline__ int key_id(uint32_t k) { return 511 - static_cast<int>(k & 511u); }
+__device__ __forceinline__ float key_value(uint32_t k) { return fkey_value(k & 0xFFFFFE00u); }
+
+// A lane's best three keys, best first: a sorting network of integer
+// min/max, no branches.
+struct Top3 {
+  uint32_t k0, k1, k2;
+  __device__ __forceinline__ void clear() { k0 = k1 = k2 = 0u; }
+  __device__ __forceinline__ void offer(uint32_t k) {
+    const uint32_t x = min(k0, k);
+    k0 = max(k0, k);
+    const uint32_t y = min(k1, x);
+    k1 = max(k1, x);
+    k2 = max(k2, y);
+  }
+  __device__ __forceinline__ void pop() {
+    k0 = k1;
+    k1 = k2;
+    k2 = 0u;
+  }
+};
+
+// The routing decision of NR tokens from their fp32 logits (rows `row` of
+// the reduced dump), one warp.  Lane l owns the columns of chunks l, l + 32,
+// ... (columns 4c .. 4c + 3); it scores them once and keeps its best three
+// keys.  Each arg-max round is then one single-instruction warp reduction
+// over the lanes' best keys; the winning lane drops its key and, once its
+// three are gone, rescans its columns for the keys below it.  The NR rows are decided side by side, so their dependency
+// chains overlap.  bias_s: the selection bias in shared memory (or null);
 // ids_s[r]: in hash mode row r's k table entries, prefetched into shared
 // memory, then a 1 for a token id outside [0, V) (flagged there).  Rows with
 // valid[r] false are stand-ins (computed, neither listed nor written).
 template <int NCH, int NR>
-__device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)[NR],
-                                            const bool (&valid)[NR], const float (&lg)[NR][4 * NCH],
-                                            const float* bias_s, const int* const (&ids_s)[NR],
-                                            int* stage_n, int4* stage_f, float2* stage_n2,
-                                            int band_t0, int* out_ids, float* out_g, int lane) {
-  constexpr int NS = 4 * NCH;  // slots per lane
+__device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t* smem, int cpr,
+                                            const int (&row)[NR], const int (&t)[NR],
+                                            const bool (&valid)[NR], const float* bias_s,
+                                            const int* const (&ids_s)[NR], int* stage_n, int4* stage_f,
+                                            float2* stage_n2, int band_t0, int* out_ids, float* out_g,
+                                            int lane) {
   const int E = p.E, k = p.k, fn = p.fn;
-  auto col = [&](int i) { return 4 * (lane + 32 * (i >> 2)) + (i & 3); };
   float lmax[NR], zsum[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
@@ -171,23 +211,39 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
     zsum[r] = 1.0f;
   }
   if (fn == 2) {
-    float m[NR];
+    float m[NR], z[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      m[r] = -FLT_MAX;
+    for (int r = 0; r < NR; ++r) m[r] = -FLT_MAX;
+#pragma unroll 1
+    for (int j = 0; j < NCH; ++j) {
+      const int c = lane + 32 * j;
+      if (c >= cpr) break;
 #pragma unroll
-      for (int i = 0; i < NS; ++i)
-        if (col(i) < E) m[r] = fmaxf(m[r], lg[r][i]);
+      for (int r = 0; r < NR; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (4 * c + q < E) m[r] = fmaxf(m[r], xs[q]);
+      }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) lmax[r] = warp_max(m[r]);
-    float z[NR];
-#pragma unroll
     for (int r = 0; r < NR; ++r) {
+      lmax[r] = warp_max(m[r]);
       z[r] = 0.0f;
+    }
+#pragma unroll 1
+    for (int j = 0; j < NCH; ++j) {
+      const int c = lane + 32 * j;
+      if (c >= cpr) break;
 #pragma unroll
-      for (int i = 0; i < NS; ++i)
-        if (col(i) < E) z[r] += __expf(lg[r][i] - lmax[r]);
+      for (int r = 0; r < NR; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (4 * c + q < E) z[r] += __expf(xs[q] - lmax[r]);
+      }
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) zsum[r] = warp_sum(z[r]);
@@ -203,39 +259,40 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
   }
   if (p.token_ids != nullptr) {
     // ---------------------------------------------------------------- hash
-    int mine[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      mine[r] = lane < k ? ids_s[r][lane] : -1;
       tok_ok[r] = ids_s[r][kMaxK] == 0;
-    }
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const int e = __shfl_sync(0xffffffffu, mine[r], j);
-        float v = 0.0f;
-#pragma unroll
-        for (int i = 0; i < NS; ++i)
-          if (col(i) == e) v = lg[r][i];
-        v = __shfl_sync(0xffffffffu, v, (e >= 0 ? e >> 2 : 0) & 31);
-        if (lane == j) {
-          my_sel[r] = e;
-          my_l[r] = v;
-        }
+      if (lane < k) {
+        const int e = ids_s[r][lane];
+        my_sel[r] = e;
+        if (e >= 0 && e < E) my_l[r] = dump_logit(smem, row[r], e, cpr);
       }
     }
   } else {
     // ---------------------------------------------------------------- top-k
-    uint32_t sk[NR][NS];
+    Top3 tl[NR];
+    int left[NR];  // this lane's columns not yet taken
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
+    for (int r = 0; r < NR; ++r) {
+      tl[r].clear();
+      left[r] = 0;
+    }
+    const bool hb = bias_s != nullptr;
+#pragma unroll 1
+    for (int j = 0; j < NCH; ++j) {
+      const int c = lane + 32 * j;
+      if (c >= cpr) break;
+      const float4 b4 = hb ? *reinterpret_cast<const float4*>(bias_s + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float bs[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        const int e = col(i);
-        const float v = score_f32(lg[r][i], fn);
-        sk[r][i] = e < E ? fkey(bias_s != nullptr ? v + bias_s[e] : v) : 0u;
+      for (int r = 0; r < NR; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tl[r].offer(sel_key(xs[q], bs[q], hb, 4 * c + q, E, fn));
+        left[r] += max(0, min(4, E - 4 * c));
       }
+    }
     const int rounds = (k < E) ? k + 1 : k;
     bool close[NR];
     float prev[NR], kth[NR];
@@ -246,83 +303,80 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
     }
 #pragma unroll 1
     for (int rd = 0; rd < rounds; ++rd) {
-      uint32_t bk[NR];
-      int bid[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        bk[r] = 0u;
-        bid[r] = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < NS; ++i)  // slots ascend in column: the first of equal keys wins
-          if (sk[r][i] > bk[r]) {
-            bk[r] = sk[r][i];
-            bid[r] = col(i);
-          }
-      }
       uint32_t m[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) m[r] = __reduce_max_sync(0xffffffffu, bk[r]);
-      int win[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r)
-        win[r] = static_cast<int>(__reduce_min_sync(
-            0xffffffffu, bk[r] == m[r] ? static_cast<uint32_t>(bid[r]) : 0x7fffffffu));
-      float wl[NR];
+      for (int r = 0; r < NR; ++r) m[r] = __reduce_max_sync(0xffffffffu, tl[r].k0);
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        wl[r] = 0.0f;
+        const int win = key_id(m[r]);
+        if (tl[r].k0 == m[r]) {  // the owner of the winning column
+          tl[r].pop();
+          --left[r];
+          if (tl[r].k0 == 0u && left[r] > 0) {
+            // refill: the lane's best three among its keys below m
+#pragma unroll 1
+            for (int j = 0; j < NCH; ++j) {
+              const int c = lane + 32 * j;
+              if (c >= cpr) break;
+              const float4 x = *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
+              const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int i = 0; i < NS; ++i)
-          if (col(i) == win[r]) {
-            sk[r][i] = 0u;  // taken
-            wl[r] = lg[r][i];
+              for (int q = 0; q < 4; ++q) {
+                const int e = 4 * c + q;
+                const uint32_t key = sel_key(xs[q], hb ? bias_s[e] : 0.0f, hb, e, E, fn);
+                if (key < m[r]) tl[r].offer(key);
+              }
+            }
           }
-      }
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        wl[r] = __shfl_sync(0xffffffffu, wl[r], (win[r] >> 2) & 31);
-        const float best = fkey_value(m[r]);
-        if (rd > 0) close[r] |= (prev[r] - best) < band_at(prev[r], fn);
+        }
+        const float best = key_value(m[r]);
+        if (rd > 0)
+          close[r] |= (prev[r] - best) < band_at(prev[r], fn) + kTrunc * fmaxf(fabsf(prev[r]), fabsf(best));
         prev[r] = best;
         if (rd == k - 1) kth[r] = best;
-        if (lane == rd && rd < k) {
-          my_sel[r] = win[r];
-          my_l[r] = wl[r];
+        if (lane == rd && rd < k && win < E) {
+          my_sel[r] = win;
+          my_l[r] = dump_logit(smem, row[r], win, cpr);
         }
       }
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       if (!close[r] || !valid[r]) continue;  // warp-uniform
-      // candidates: every expert within twice the band below the k-th score
+      // candidates: every expert within twice the band below the k-th score;
+      // the token's go to its own slots [t E, t E + count) of the pair
+      // lists, and the token to the CTA's staging list, which the CTA
+      // appends to the global list with one atomic after the decisions
       const float lim = kth[r] - 2.0f * band_at(kth[r], fn);
-      int count = 0;
-      bool cand[NS];
-#pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        const int e = col(i);
-        const float v = score_f32(lg[r][i], fn);
-        cand[i] = e < E && (bias_s != nullptr ? v + bias_s[e] : v) >= lim;
-        count += __popc(__ballot_sync(0xffffffffu, cand[i]));
-      }
-      // the token's candidates go to its own slots [t E, t E + count) of the
-      // pair lists; the token is listed in the CTA's staging list, which the
-      // CTA appends to the global list with one atomic after the decisions
       int base = t[r] * E;
+      const int base0 = base;
+#pragma unroll 1
+      for (int j = 0; j < NCH; ++j) {
+        const int c = lane + 32 * j;
+        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (c < cpr) x = *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = 4 * c + q;
+          bool cand = false;
+          if (c < cpr && e < E) {
+            const float v = score_f32(xs[q], fn);
+            cand = (bias_s != nullptr ? v + bias_s[e] : v) >= lim;
+          }
+          const unsigned bm = __ballot_sync(0xffffffffu, cand);
+          if (cand) {
+            const int at = base + __popc(bm & ((1u << lane) - 1u));
+            p.rs.pairs[at] = make_int2(t[r], e);
+            p.rs.plogit[at] = xs[q];
+          }
+          base += __popc(bm);
+        }
+      }
       if (lane == 0) {
         const int fi = atomicAdd(stage_n, 1);
-        stage_f[fi] = make_int4(t[r], base, count, 0);
+        stage_f[fi] = make_int4(t[r], base0, base - base0, 0);
         stage_n2[fi] = make_float2(lmax[r], zsum[r]);
-      }
-#pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        const unsigned bm = __ballot_sync(0xffffffffu, cand[i]);
-        if (cand[i]) {
-          const int at = base + __popc(bm & ((1u << lane) - 1u));
-          p.rs.pairs[at] = make_int2(t[r], col(i));
-          p.rs.plogit[at] = lg[r][i];
-        }
-        base += __popc(bm);
       }
     }
   }
@@ -334,7 +388,7 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
     if (lane < k) {
       if (my_sel[r] >= 0 && my_sel[r] < E) {
         a[r] = affinity_f32(my_l[r], fn, lmax[r], zsum[r]);
-      } else if (tok_ok[r]) {
+      } else if (tok_ok[r] && valid[r]) {
         set_flag(p.status, kFlagBadExpert);  // a table entry outside [0, E)
       }
     }
@@ -355,71 +409,67 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const int (&t)
 }
 
 // Rows [rank R, rank R + R) of the tile, NR per warp at a time: their logits
-// from this CTA's (reduced) dump, optionally written out, then decided.
+// from this CTA's (reduced) dump, optionally written out, then decided.  A
+// dry pass decides one group of stand-in rows (all invalid: nothing is
+// written or listed) on whatever the shared memory holds, only so that the
+// code is in the instruction caches when the real pass comes.
 template <int NCH, int NR>
 __device__ __forceinline__ void decide_band(const FusedParams& p, const uint8_t* smem, int rank,
                                             int R, int row0, int cpr, const float* bias_s,
                                             const int* ids_base, int* stage_n, int4* stage_f,
                                             float2* stage_n2, int* out_ids, float* out_g, int warp,
-                                            int lane) {
+                                            int lane, bool dry) {
   constexpr int NW = kThreads / 32;
   for (int rr0 = warp; rr0 < R; rr0 += NR * NW) {
-    int t[NR];
+    int row[NR], t[NR];
     bool valid[NR];
-    float lg[NR][4 * NCH];
     const int* ids[NR];
     int nvalid = 0;
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       int rr = rr0 + r * NW;
-      valid[r] = rr < R && row0 + rank * R + rr < p.T;
+      valid[r] = !dry && rr < R && row0 + rank * R + rr < p.T;
       nvalid += valid[r] ? 1 : 0;
       if (!valid[r]) rr = rr0;  // a stand-in row
-      const int row = rank * R + rr;
-      t[r] = row0 + row;
+      row[r] = rank * R + rr;
+      t[r] = row0 + row[r];
       ids[r] = ids_base + rr * (kMaxK + 1);
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const int c = lane + 32 * j;
-        const float4 x = c < cpr ? *reinterpret_cast<const float4*>(smem + dump_off(row, c, cpr))
-                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        lg[r][4 * j] = x.x; lg[r][4 * j + 1] = x.y; lg[r][4 * j + 2] = x.z; lg[r][4 * j + 3] = x.w;
-      }
     }
-    if (nvalid == 0) break;
+    if (nvalid == 0 && !dry) break;
     if (p.logits_out != nullptr) {
 #pragma unroll
       for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const int c = lane + 32 * j;
+#pragma unroll 1
+        for (int c = lane; c < cpr; c += 32)
           if (valid[r] && 4 * c < p.E)
             *reinterpret_cast<float4*>(p.logits_out + static_cast<long long>(t[r]) * p.E + 4 * c) =
-                make_float4(lg[r][4 * j], lg[r][4 * j + 1], lg[r][4 * j + 2], lg[r][4 * j + 3]);
-        }
+                *reinterpret_cast<const float4*>(smem + dump_off(row[r], c, cpr));
     }
     if (p.select)
-      decide_rows<NCH, NR>(p, t, valid, lg, bias_s, ids, stage_n, stage_f, stage_n2, row0 + rank * R,
-                           out_ids, out_g, lane);
+      decide_rows<NCH, NR>(p, smem, cpr, row, t, valid, bias_s, ids, stage_n, stage_f, stage_n2,
+                           row0 + rank * R, out_ids, out_g, lane);
+    if (dry) break;
   }
 }
 
 // Sum of the S partial dumps over this CTA's band of rows [rank R, rank R + R)
 // (R = 128 / S), written over the band in this CTA's own dump, which no other
-// CTA reads.  Ranks are added in order.  Each thread issues the loads of
-// three chunks before using any (distributed shared memory is slow to answer).
+// CTA reads.  Ranks are added in order.  Each thread issues the loads of U
+// chunks (all S partials of each) before using any (distributed shared memory
+// is slow to answer); U S <= 8 keeps them within 32 registers.
 template <int S>
 __device__ __forceinline__ void reduce_band(uint8_t* smem, uint32_t ring0, int rank, int cpr) {
   constexpr int R = kBM / S;
+  constexpr int U = S >= 8 ? 1 : S == 4 ? 2 : 3;
   uint32_t part[S];
 #pragma unroll
   for (int s = 0; s < S; ++s) part[s] = map_rank(ring0, s);
   const int n_chunks = R * cpr;
-  for (int i0 = threadIdx.x; i0 < n_chunks; i0 += 3 * kThreads) {
-    float4 x[3][S];
-    uint32_t off[3];
+  for (int i0 = threadIdx.x; i0 < n_chunks; i0 += U * kThreads) {
+    float4 x[U][S];
+    uint32_t off[U];
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int i = i0 + u * kThreads;
       off[u] = i < n_chunks ? dump_off(rank * R + i / cpr, i % cpr, cpr) : 0u;
       if (i < n_chunks) {
@@ -428,7 +478,7 @@ __device__ __forceinline__ void reduce_band(uint8_t* smem, uint32_t ring0, int r
       }
     }
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
+    for (int u = 0; u < U; ++u) {
       if (i0 + u * kThreads < n_chunks) {
         float4 acc = x[u][0];
 #pragma unroll
@@ -594,36 +644,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  tc_fence_before();
-  if (S > 1) cluster_sync_all(); else __syncthreads();
-
-  // ---------------------------------------------------------------- reduce
-  // This CTA decides rows [rank R, rank R + R).  Their partial sums sit in
-  // that band of every CTA's dump; the band of this CTA's own dump is read by
-  // no other CTA, so the sums (ranks added in order) overwrite it there.  All
-  // S loads of a chunk are issued before any is used (distributed shared
-  // memory is far slower than local).
+  // Warps 6-15 (idle until now) first run the decision once on stand-in
+  // rows (the dry pass: it writes nothing), so that its instructions are
+  // cached when every warp runs it for real, after the reduction.  Only
+  // where the main loop is long enough to hide it (8 k-blocks or more).
   const int R = kBM / S;
   const int cpr = ncols / 4;
-  if (S > 1 && !*abort_flag) {
-    if (S == 2) reduce_band<2>(smem, ring0, rank, cpr);
-    else if (S == 4) reduce_band<4>(smem, ring0, rank, cpr);
-    else reduce_band<8>(smem, ring0, rank, cpr);
-  }
-  __syncthreads();
+  const float* bs = p.bias != nullptr ? bias_s : nullptr;
+#pragma unroll 1
+  for (int pass = (warp >= 6 && p.select && kb1 - kb0 >= 8) ? 0 : 1; pass < 2; ++pass) {
+    if (pass == 1) {
+      tc_fence_before();
+      if (S > 1) cluster_sync_all(); else __syncthreads();
 
-  // ---------------------------------------------------------------- decide
-  if (!*abort_flag) {
-    const float* bs = p.bias != nullptr ? bias_s : nullptr;
-    if (cpr <= 32)
-      decide_band<1, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
-                       warp, lane);
-    else if (cpr <= 64)
-      decide_band<2, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
-                       warp, lane);
-    else
-      decide_band<3, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
-                       warp, lane);
+      // ------------------------------------------------------------ reduce
+      // This CTA decides rows [rank R, rank R + R).  Their partial sums sit
+      // in that band of every CTA's dump; the band of this CTA's own dump is
+      // read by no other CTA, so the sums (ranks added in order) overwrite
+      // it there.  All S loads of a chunk are issued before any is used
+      // (distributed shared memory is far slower than local).
+      if (S > 1 && !*abort_flag) {
+        if (S == 2) reduce_band<2>(smem, ring0, rank, cpr);
+        else if (S == 4) reduce_band<4>(smem, ring0, rank, cpr);
+        else reduce_band<8>(smem, ring0, rank, cpr);
+      }
+      __syncthreads();
+    }
+
+    // -------------------------------------------------------------- decide
+    if (!*abort_flag) {
+      const bool dry = pass == 0;
+      if (cpr <= 32)
+        decide_band<1, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                         warp, lane, dry);
+      else if (cpr <= 64)
+        decide_band<2, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                         warp, lane, dry);
+      else
+        decide_band<3, 2>(p, smem, rank, R, row0, cpr, bs, ids_s, stage_n, stage_f, stage_n2, out_ids, out_g,
+                         warp, lane, dry);
+    }
   }
 
   __syncthreads();

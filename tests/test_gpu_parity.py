@@ -149,6 +149,68 @@ def test_route_equal_scores_go_to_the_lower_id():
     check_gates(G, G_ref)
 
 
+@pytest.mark.parametrize("E,k", [(384, 8), (8, 8), (64, 16)])
+def test_route_one_lane_holds_the_top_entries(E, k):
+    # The fused router's lane l scores the columns 4c .. 4c + 3 of chunks
+    # c = l, l + 32, l + 64 and keeps its best three.  A large bias on lane
+    # 0's columns puts the whole top-(k+1) there, so that lane gives up all
+    # three and rescans its columns (twice at E = 384), with two of its
+    # columns exactly tied (the lower id first).  E = k = 8: every column is
+    # taken, four from each of two lanes.
+    rng = np.random.default_rng(17)
+    T, H = 160, 256
+    X = synth.bf16_bits_from_f32(rng.standard_normal((T, H)))
+    Wg = (rng.standard_normal((H, E)) / 16).astype(np.float32)
+    lane0 = [4 * c + q for c in range(0, (E + 3) // 4, 32) for q in range(4) if 4 * c + q < E]
+    bias = np.zeros(E, np.float32)
+    bias[lane0] = 2.0
+    if len(lane0) > 5:
+        Wg[:, lane0[5]] = Wg[:, lane0[1]]  # an exact tie inside the lane
+    Wg = synth.bf16_bits_from_f32(Wg)
+    p = moe.make_params(T, H, E, k, 64)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    G = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    moe.moe_route(p, bf(X), bf(Wg), torch.from_numpy(bias).to(DEV), None, None, 0, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids = E_ids.cpu().numpy()
+    ids_ref, G_ref, _ = oracle.route(X, Wg, bias, 0, k, 1.0, 1)
+    assert np.array_equal(ids, ids_ref)
+    assert np.isin(ids[:, :min(k, len(lane0))], lane0).all()
+    check_gates(G, G_ref)
+
+
+def test_route_large_scores_a_few_1e4_apart():
+    # The fused router's keys keep 23 bits of the biased score (the low 9
+    # hold the id): at scores near 9 they resolve ~5e-4, coarser than the
+    # decision band of 2e-4.  Experts 3 and 5 carry a bias of 8.5 and differ
+    # by 2.4e-4 in score (one bf16 step of Wg[0] times X[:, 0] = +-1, through
+    # the sigmoid's slope 1/4), in an order that alternates by token: the
+    # pair must still be decided exactly.
+    rng = np.random.default_rng(19)
+    T, H, E, k = 96, 256, 32, 4
+    X = (rng.standard_normal((T, H)) / 8).astype(np.float32)
+    X[:, 0] = np.where(np.arange(T) % 2 == 0, 1.0, -1.0)
+    Wg = (rng.standard_normal((H, E)) / 16).astype(np.float32)
+    Wg[:, 5] = Wg[:, 3]
+    Wg[0, 3] = 2.0 ** -4
+    Wg[0, 5] = 2.0 ** -4 + 2.0 ** -10
+    Xb, Wgb = synth.bf16_bits_from_f32(X), synth.bf16_bits_from_f32(Wg)
+    bias = np.zeros(E, np.float32)
+    bias[[3, 5]] = 8.5
+    p = moe.make_params(T, H, E, k, 64)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    G = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    moe.moe_route(p, bf(Xb), bf(Wgb), torch.from_numpy(bias).to(DEV), None, None, 0, E_ids, G, ws)
+    moe.moe_sync_status(ws)
+    ids = E_ids.cpu().numpy()
+    ids_ref, G_ref, _ = oracle.route(Xb, Wgb, bias, 0, k, 1.0, 1)
+    assert np.array_equal(ids, ids_ref)
+    assert (ids[0::2, :2] == [5, 3]).all() and (ids[1::2, :2] == [3, 5]).all()
+    check_gates(G, G_ref)
+
+
 @pytest.mark.parametrize("score", [0, 1, 2])
 def test_route_near_ties_are_decided_exactly(score):
     # experts 3 and 5 differ only in Wg[0, :], by one bf16 step of 2^-11, and
