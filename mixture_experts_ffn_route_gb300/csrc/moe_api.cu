@@ -30,7 +30,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct WsLayout {
-  size_t status, logits, wgt, flagged, fnorm, pairs, plogit, s64, chunk_cnt, counts, row_off,
+  size_t status, logits, wgt, flagged, fnorm, pairs, plogit, s64, segn, chunk_cnt, counts, row_off,
       tile_off, perm, inv, act, yp, total;
 };
 
@@ -54,6 +54,7 @@ static WsLayout layout(const moe_params& p) {
   L.pairs = take(T * E * 2 * sizeof(int));
   L.plogit = take(T * E * sizeof(float));
   L.s64 = take(T * E * sizeof(double));
+  L.segn = take((T / 16 + 8) * sizeof(int));  // fused router: one count per CTA
   L.chunk_cnt = take((nchunk > 0 ? nchunk : 1) * E * sizeof(int));
   L.counts = take((E + 2) * sizeof(int));
   L.row_off = take((E + 2) * sizeof(int));
@@ -282,6 +283,7 @@ moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_u
 static RouteScratch route_scratch(void* ws, const WsLayout& L) {
   RouteScratch rs;
   rs.counters = at<int>(ws, kRouteCountersAt);
+  rs.seg_n = at<int>(ws, L.segn);
   rs.flagged = at<int4>(ws, L.flagged);
   rs.fnorm = at<float2>(ws, L.fnorm);
   rs.pairs = at<int2>(ws, L.pairs);

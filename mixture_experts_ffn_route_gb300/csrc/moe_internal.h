@@ -198,7 +198,9 @@ int gemm_block_n(GemmKind kind);
 struct RouteScratch {
   int* counters;  // [0] close tokens, [1] candidate pairs, [2] re-decision blocks
                   // done; zero between calls (the re-decision's last block
-                  // zeroes them)
+                  // zeroes them).  General path only.
+  int* seg_n;     // [T / 16]  fused router: close tokens of each CTA's band of
+                  //           rows (its list: flagged[b R .. b R + seg_n[b]))
   int4* flagged;  // [T]      {token, first pair, pair count, 0}
   float2* fnorm;  // [T]      softmax normaliser of a close token {max logit, sum exp}
   int2* pairs;    // [T * E]  {token, expert}
@@ -214,9 +216,15 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                 int score_fn, float alpha, int renorm, int32_t* E_ids, float* G,
                                 const RouteScratch& rs, int* status, cudaStream_t s);
 // The float64 re-decision of the tokens listed in rs (one kernel).
+// Float64 re-decision of the listed close tokens.  The list is n_seg
+// segments of at most seg_len entries: segment b holds seg_n[b] entries at
+// flagged[b seg_len ..).  The general path passes one segment (its counters,
+// which the last block zeroes); the fused router one per CTA, and launches
+// the kernel as its programmatic dependent (pdl).
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
-                                 float* G, const RouteScratch& rs, cudaStream_t s);
+                                 float* G, const RouteScratch& rs, const int* seg_n, int n_seg,
+                                 int seg_len, bool zero_counters, bool pdl, cudaStream_t s);
 // Fused router (moe_route_fused.cu): the gating GEMM on the tensor cores with
 // the scores, the selection bias, the top-k (or the hash lookup), the gates
 // and the listing of close tokens in its epilogue; split over K across a

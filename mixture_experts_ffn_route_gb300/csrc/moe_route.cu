@@ -247,69 +247,127 @@ __device__ __forceinline__ float2 pair_dot(const uint4* __restrict__ xs, const u
   return make_float2(H0, L0);
 }
 
-// Re-decide the close tokens: one block per listed token (striding over the
-// list).  The token's row of X goes to shared memory once; the block's warps
-// score its candidates in float64 (each candidate's row split over the warps
+// Re-decide the close tokens: one block per listed token.  The list is n_seg
+// segments (launch_route_recheck); block b takes entries j = b, b +
+// gridDim.x, ... of the order "entry j / n_seg of segment j mod n_seg".  The
+// token's row of X and its candidates (ids, listed fp32 logits, fp32 scores)
+// go to shared memory.  A candidate at least a band away from every other
+// candidate has a certain place in the order, and its fp32 score is its key;
+// the others are scored in float64 (each candidate's row split over the warps
 // the group of candidates leaves, the float-pair partial sums added in a
-// fixed order; keys to rs.key); then warp 0 takes k arg-max rounds over the
-// keys, larger score first, equal scores to the lower id, and writes the ids
-// and the gates,
-// computed from the candidates' listed fp32 logits (and, for softmax, the
-// token's listed normaliser).  The last block to finish zeroes the list
-// counters, so the next call starts with empty lists.
+// fixed order).  The k candidates of rank below k (larger key first, equal
+// keys lower id first) are the selection, in rank order, with gates from
+// their listed fp32 logits (and, for softmax, the token's listed
+// normaliser).  A list longer than the shared arrays keeps its keys in
+// memory and is taken in k arg-max rounds.  With zero_counters, the last
+// block to finish zeroes the general path's list counters for the next call.
 __global__ void __launch_bounds__(kRedecideWarps * 32)
     route_redecide_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
                           const float* __restrict__ bias, int H, int k, int fn, float alpha, int renorm,
-                          int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs) {
-  extern __shared__ uint4 xs[];  // [H / 8], then the partial sums and the exact list
+                          int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs,
+                          const int* seg_n, int n_seg, int seg_len, int zero_counters) {
+  // launched as the fused router's programmatic dependent: its writes are
+  // visible from here on (a no-op after an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ uint4 xs[];  // [H / 8], then the partial sums, the exact list, the segment counts
   float2* part = reinterpret_cast<float2*>(xs + H / 8);             // [kRedecideWarps]
   int* exact = reinterpret_cast<int*>(part + kRedecideWarps);       // [kRedecideList]
+  int* cnt_s = exact + kRedecideList;                               // [n_seg]
   __shared__ float sc[kRedecideList];
-  __shared__ int n_exact;
+  __shared__ float pl_s[kRedecideList];
+  __shared__ int n_exact, n_total;
+  __shared__ int wsum_s[kRedecideWarps];
   __shared__ unsigned long long key_s[kRedecideList];
   __shared__ int id_s[kRedecideList];
   __shared__ int sel_s[kMaxK];
   __shared__ float aff_s[kMaxK];
-  const int n = *reinterpret_cast<volatile int*>(rs.counters);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int vecs = H / 8;
-  for (int j = blockIdx.x; j < n; j += gridDim.x) {
-    const int4 f = rs.flagged[j];
+  // exclusive prefix of the segment counts (in place): entry j of the
+  // list is entry j - pre[b] of segment b, the last b with pre[b] <= j
+  {
+    const int per = (n_seg + blockDim.x - 1) / blockDim.x;
+    const int lo = min(n_seg, static_cast<int>(threadIdx.x) * per), hi = min(n_seg, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) {
+      cnt_s[i] = reinterpret_cast<const volatile int*>(seg_n)[i];
+      sum += cnt_s[i];
+    }
+    int incl = sum;  // inclusive scan over the threads: warps, then warp totals
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum_s[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < kRedecideWarps ? wsum_s[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      if (lane < kRedecideWarps) wsum_s[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? wsum_s[warp - 1] : 0);
+    for (int i = lo; i < hi; ++i) {
+      const int c = cnt_s[i];
+      cnt_s[i] = run;
+      run += c;
+    }
+    if (threadIdx.x == 0) n_total = wsum_s[kRedecideWarps - 1];
+    __syncthreads();
+  }
+  for (int j = blockIdx.x; j < n_total; j += gridDim.x) {
+    int seg = 0;
+    for (int span = n_seg; span > 1;) {  // the last segment starting at or before j
+      const int half = span >> 1;
+      if (cnt_s[seg + half] <= j) seg += half;
+      span -= half;
+    }
+    const int idx = j - cnt_s[seg];
+    const int4 f = rs.flagged[static_cast<long long>(seg) * seg_len + idx];
     const int t = f.x, base = f.y, count = f.z;
+    const bool small = count <= kRedecideList;
+    // the token row and the candidates, their loads issued together
     const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
     for (int v = threadIdx.x; v < vecs; v += blockDim.x) xs[v] = __ldg(xr + v);
-    // The fp32 selection score of each candidate, as the first decision took
-    // it.  A candidate at least a band away from every other candidate has a
-    // certain place in the order: its float64 key is its fp32 score.  Only
-    // the others are recomputed exactly (all of them when the list is long).
-    const bool small = count <= kRedecideList;
     for (int i = threadIdx.x; small && i < count; i += blockDim.x) {
       const int e = rs.pairs[base + i].y;
-      float v = score_f32(rs.plogit[base + i], fn);
+      const float l = rs.plogit[base + i];
+      float v = score_f32(l, fn);
       if (bias != nullptr) v += bias[e];
+      id_s[i] = e;
+      pl_s[i] = l;
       sc[i] = v;
     }
     __syncthreads();
-    for (int i = threadIdx.x; small && i < count; i += blockDim.x) {
-      bool near = false;
-      for (int q = 0; q < count && !near; ++q)
-        near = q != i && fabsf(sc[i] - sc[q]) < band_at(fmaxf(sc[i], sc[q]), fn);
-      exact[i] = near ? 1 : 0;
-      if (!near) rs.key[base + i] = order_key(static_cast<double>(sc[i]));
-    }
-    __syncthreads();
-    if (warp == 0 && small) {  // the recomputed candidates' list, in candidate order
-      int m = 0;
-      for (int c = 0; c < count; c += 32) {
-        const bool near = c + lane < count && exact[c + lane] != 0;
-        const unsigned b = __ballot_sync(0xffffffffu, near);
-        __syncwarp();
-        if (near) exact[m + __popc(b & ((1u << lane) - 1u))] = c + lane;
-        m += __popc(b);
+    if (small) {
+      // the fp32 selection score of each candidate, as the first decision
+      // took it: only candidates within a band of another are recomputed
+      for (int i = threadIdx.x; i < count; i += blockDim.x) {
+        bool near = false;
+        for (int q = 0; q < count && !near; ++q)
+          near = q != i && fabsf(sc[i] - sc[q]) < band_at(fmaxf(sc[i], sc[q]), fn);
+        exact[i] = near ? 1 : 0;
+        if (!near) key_s[i] = order_key(static_cast<double>(sc[i]));
       }
-      if (lane == 0) n_exact = m;
+      __syncthreads();
+      if (warp == 0) {  // the recomputed candidates' list, in candidate order
+        int m = 0;
+        for (int c = 0; c < count; c += 32) {
+          const bool near = c + lane < count && exact[c + lane] != 0;
+          const unsigned b = __ballot_sync(0xffffffffu, near);
+          __syncwarp();
+          if (near) exact[m + __popc(b & ((1u << lane) - 1u))] = c + lane;
+          m += __popc(b);
+        }
+        if (lane == 0) n_exact = m;
+      }
+      __syncthreads();
     }
-    __syncthreads();
     const int ne = small ? n_exact : count;
     auto exact_at = [&](int c) { return small ? exact[c] : c; };
     // exact candidates in groups of g = min(ne, warps); the warps of a group's
@@ -321,7 +379,8 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
       if (part_i < ns) {
         const int len = (vecs + ns - 1) / ns;
         const int vb = part_i * len, ve = min(vecs, vb + len);
-        const float2 d = pair_dot(xs, WgT, H, rs.pairs[base + exact_at(c0 + c)].y, vb, ve, lane);
+        const int ci = exact_at(c0 + c);
+        const float2 d = pair_dot(xs, WgT, H, small ? id_s[ci] : rs.pairs[base + ci].y, vb, ve, lane);
         if (lane == 0) part[warp] = d;
       }
       __syncthreads();
@@ -332,22 +391,18 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
           ff_add(acc.x, acc.y, d.x, d.y);
         }
         const int i = exact_at(c0 + lane);
-        const int e = rs.pairs[base + i].y;
+        const int e = small ? id_s[i] : rs.pairs[base + i].y;
         double v = score_f64(static_cast<double>(acc.x) + static_cast<double>(acc.y), fn);
         if (bias != nullptr) v += static_cast<double>(bias[e]);
-        rs.key[base + i] = order_key(v);
+        if (small) key_s[i] = order_key(v);
+        else rs.key[base + i] = order_key(v);
       }
       __syncthreads();
     }
     if (small) {
       // rank of each candidate among the others (larger key first, equal keys
       // lower id first): the k ranks below k are the selection, in order
-      for (int i = threadIdx.x; i < count; i += blockDim.x) {
-        key_s[i] = rs.key[base + i];
-        id_s[i] = rs.pairs[base + i].y;
-      }
-      __syncthreads();
-      const float2 nrm = rs.fnorm[j];
+      const float2 nrm = rs.fnorm[static_cast<long long>(seg) * seg_len + idx];
       for (int i = threadIdx.x; i < count; i += blockDim.x) {
         const unsigned long long v = key_s[i];
         const int e = id_s[i];
@@ -355,7 +410,7 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
         for (int q = 0; q < count; ++q) rank += before(key_s[q], id_s[q], v, e) ? 1 : 0;
         if (rank < k) {
           sel_s[rank] = e;
-          aff_s[rank] = affinity_f32(rs.plogit[base + i], fn, nrm.x, nrm.y);
+          aff_s[rank] = affinity_f32(pl_s[i], fn, nrm.x, nrm.y);
         }
       }
       __syncthreads();
@@ -374,7 +429,7 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
       continue;
     }
     if (warp == 0) {
-      const float2 nrm = rs.fnorm[j];
+      const float2 nrm = rs.fnorm[static_cast<long long>(seg) * seg_len + idx];
       // candidates held in registers, up to 4 per lane (count <= 128); more
       // candidates than that are read from memory each round
       constexpr int kHold = 4;
@@ -436,7 +491,7 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
     __syncthreads();
   }
   // the last block to finish zeroes the counters (every block has read them)
-  if (threadIdx.x == 0) {
+  if (zero_counters && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(rs.counters + 2, 1) == static_cast<int>(gridDim.x) - 1) {
       rs.counters[0] = 0;
@@ -470,18 +525,28 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
 
 cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
                                  int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
-                                 float* G, const RouteScratch& rs, cudaStream_t s) {
+                                 float* G, const RouteScratch& rs, const int* seg_n, int n_seg,
+                                 int seg_len, bool zero_counters, bool pdl, cudaStream_t s) {
   const size_t sh = static_cast<size_t>(H) * 2 + kRedecideWarps * sizeof(float2) +
-                    kRedecideList * sizeof(int);
+                    kRedecideList * sizeof(int) + static_cast<size_t>(n_seg) * sizeof(int);
   if (sh > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_redecide_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sh));
     if (e != cudaSuccess) return e;
   }
-  route_redecide_kernel<<<2 * num_sms(), kRedecideWarps * 32, sh, s>>>(X, WgT, bias, H, k, score_fn,
-                                                                       alpha, renorm, E_ids, G, rs);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+  cfg.blockDim = dim3(kRedecideWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = sh;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, route_redecide_kernel, X, WgT, bias, H, k, score_fn, alpha, renorm,
+                            E_ids, G, rs, seg_n, n_seg, seg_len, zero_counters ? 1 : 0);
 }
 
 cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
@@ -502,7 +567,9 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                                       k, score_fn, alpha, renorm, E_ids, G, rs,
                                                       status);
   if (token_ids != nullptr) return cudaGetLastError();
-  return launch_route_recheck(X, WgT, bias, H, score_fn, k, alpha, renorm, E_ids, G, rs, s);
+  // one segment: the compact list and its counter, zeroed after use
+  return launch_route_recheck(X, WgT, bias, H, score_fn, k, alpha, renorm, E_ids, G, rs, rs.counters, 1, T,
+                              true, false, s);
 }
 
 }  // namespace moe

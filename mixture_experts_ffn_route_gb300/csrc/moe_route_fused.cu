@@ -23,13 +23,19 @@
 //               re-decision reads; then copy the accumulator, one row per
 //               thread, into shared memory over the drained operand ring
 //               (16-byte chunks XOR-swizzled by row, conflict-free both ways).
-//   all warps   after the cluster barrier: one warp per row sums the S partial
-//               rows (ranks 0..S-1 in order), scores them, adds the selection
-//               bias, takes k+1 warp arg-max rounds (larger score first, equal
-//               scores to the lower id), writes ids and gates, and lists a
-//               token whose first k+1 scores hold a pair closer than the
-//               decision band, with its candidates, for the float64 re-decision
-//               (moe_route.cu), exactly as the general path does.
+//   warps 6-15  fetch the selection bias (or the hash table rows) into
+//               shared memory, then run the decision once on stand-in rows so
+//               that its code is cached.
+//   all warps   after the cluster barrier: sum the S partial rows of this
+//               CTA's band (ranks 0..S-1 in order); then one warp per row (two
+//               side by side) scores them, adds the selection bias, keeps each
+//               lane's best three keys and takes k+1 warp arg-max rounds
+//               (larger score first, equal scores to the lower id), writes ids
+//               and gates, and lists a token whose first k+1 scores hold a
+//               pair closer than the decision band, with its candidates, in
+//               the CTA's segment of the list for the float64 re-decision
+//               (moe_route.cu), which runs as this kernel's programmatic
+//               dependent.
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -135,14 +141,10 @@ __device__ __forceinline__ void transpose_block(const FusedParams& p, int kb, in
   }
 }
 
-// Order-preserving 32-bit key of a float: larger float, larger key (0 is below
-// every float's key: it marks taken or absent entries).
+// Order-preserving 32-bit key of a float: larger float, larger key.
 __device__ __forceinline__ uint32_t fkey(float v) {
   const uint32_t u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float fkey_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // fp32 logit of column e of dump row `row`.
@@ -154,18 +156,15 @@ __device__ __forceinline__ float dump_logit(const uint8_t* smem, int row, int e,
 // layer has one) as an order-preserving integer, its low 9 bits replaced by
 // 511 - e.  Keys are then unique, a larger key is a larger score or, among
 // scores equal to 2^-14 relative, the lower id, and the id comes back from
-// the key.  0 (below every key) past the last expert.  The truncated score
-// is below the exact one by less than 2^-14 of its magnitude, so a decision
-// whose keys are within that of each other is listed for the float64
-// re-decision with the band (kTrunc below).
-constexpr float kTrunc = 1.0f / 8192.0f;  // 2^-13: twice the truncation
+// the key.  0 (below every key) past the last expert.  Scores that close
+// are far inside the decision band, so their order is settled by the float64
+// re-decision: the closeness test takes the winners' full fp32 scores.
 __device__ __forceinline__ uint32_t sel_key(float l, float b, bool has_bias, int e, int E, int fn) {
   if (e >= E) return 0u;
   const float v = score_f32(l, fn);
   return (fkey(has_bias ? v + b : v) & 0xFFFFFE00u) | static_cast<uint32_t>(511 - e);
 }
 __device__ __forceinline__ int key_id(uint32_t k) { return 511 - static_cast<int>(k & 511u); }
-__device__ __forceinline__ float key_value(uint32_t k) { return fkey_value(k & 0xFFFFFE00u); }
 
 // A lane's best three keys, best first: a sorting network of integer
 // min/max, no branches.
@@ -294,13 +293,9 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t*
       }
     }
     const int rounds = (k < E) ? k + 1 : k;
-    bool close[NR];
-    float prev[NR], kth[NR];
+    int wid[NR];  // lane j < rounds: the j-th winner
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      close[r] = false;
-      prev[r] = kth[r] = 0.0f;
-    }
+    for (int r = 0; r < NR; ++r) wid[r] = E;
 #pragma unroll 1
     for (int rd = 0; rd < rounds; ++rd) {
       uint32_t m[NR];
@@ -308,7 +303,6 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t*
       for (int r = 0; r < NR; ++r) m[r] = __reduce_max_sync(0xffffffffu, tl[r].k0);
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        const int win = key_id(m[r]);
         if (tl[r].k0 == m[r]) {  // the owner of the winning column
           tl[r].pop();
           --left[r];
@@ -329,16 +323,29 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t*
             }
           }
         }
-        const float best = key_value(m[r]);
-        if (rd > 0)
-          close[r] |= (prev[r] - best) < band_at(prev[r], fn) + kTrunc * fmaxf(fabsf(prev[r]), fabsf(best));
-        prev[r] = best;
-        if (rd == k - 1) kth[r] = best;
-        if (lane == rd && rd < k && win < E) {
-          my_sel[r] = win;
-          my_l[r] = dump_logit(smem, row[r], win, cpr);
+        if (lane == rd) wid[r] = key_id(m[r]);
+      }
+    }
+    // the winners' full fp32 scores, one per lane: a pair of consecutive
+    // winners closer than the band (or out of order: keys tie scores within
+    // 2^-14) lists the token for the re-decision
+    bool close[NR];
+    float kth[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      float ev = 0.0f;
+      if (lane < rounds && wid[r] < E) {
+        const float l = dump_logit(smem, row[r], wid[r], cpr);
+        const float v = score_f32(l, fn);
+        ev = hb ? v + bias_s[wid[r]] : v;
+        if (lane < k) {
+          my_sel[r] = wid[r];
+          my_l[r] = l;
         }
       }
+      const float pv = __shfl_up_sync(0xffffffffu, ev, 1);
+      close[r] = __any_sync(0xffffffffu, lane >= 1 && lane < rounds && (pv - ev) < band_at(pv, fn));
+      kth[r] = __shfl_sync(0xffffffffu, ev, k - 1);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -346,7 +353,7 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t*
       // candidates: every expert within twice the band below the k-th score;
       // the token's go to its own slots [t E, t E + count) of the pair
       // lists, and the token to the CTA's staging list, which the CTA
-      // appends to the global list with one atomic after the decisions
+      // writes out as its segment of the re-decision list at the end
       const float lim = kth[r] - 2.0f * band_at(kth[r], fn);
       int base = t[r] * E;
       const int base0 = base;
@@ -687,26 +694,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  {
-    __shared__ int list_base;
-    const int nf = *stage_n;
-    if (threadIdx.x == 0 && nf > 0) list_base = atomicAdd(p.rs.counters, nf);
-    if (p.select && !*abort_flag) {
-      const int R = kBM / S;
-      const int t0 = row0 + rank * R;
-      const int n_out = (min(p.T, t0 + R) - t0) * p.k;
-      for (int i = threadIdx.x; i < n_out; i += kThreads) {
-        p.E_ids[static_cast<long long>(t0) * p.k + i] = out_ids[i];
-        p.G[static_cast<long long>(t0) * p.k + i] = out_g[i];
+  if (p.select && !*abort_flag) {
+    // the band's ids and gates, and (top-k) its close tokens: this CTA's
+    // segment of the re-decision list, flagged[b R ..) with b = blockIdx.x
+    // (the band starts at token b R), and its length
+    const int t0 = row0 + rank * R;
+    const int n_out = (min(p.T, t0 + R) - t0) * p.k;
+    for (int i = threadIdx.x; i < n_out; i += kThreads) {
+      p.E_ids[static_cast<long long>(t0) * p.k + i] = out_ids[i];
+      p.G[static_cast<long long>(t0) * p.k + i] = out_g[i];
+    }
+    if (p.token_ids == nullptr) {
+      const int nf = *stage_n;
+      for (int i = threadIdx.x; i < nf; i += kThreads) {
+        p.rs.flagged[t0 + i] = stage_f[i];
+        p.rs.fnorm[t0 + i] = stage_n2[i];
       }
+      if (threadIdx.x == 0) p.rs.seg_n[blockIdx.x] = nf;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nf; i += kThreads) {
-      p.rs.flagged[list_base + i] = stage_f[i];
-      p.rs.fnorm[list_base + i] = stage_n2[i];
-    }
+  } else if (p.select && p.token_ids == nullptr && threadIdx.x == 0) {
+    p.rs.seg_n[blockIdx.x] = 0;
   }
-  if (S > 1) cluster_sync_all();  // partial rows stay readable until every CTA is done
+  // the re-decision may launch now (it waits for this grid's writes)
+  asm volatile("griddepcontrol.launch_dependents;");
+  // partial rows stay readable until every CTA of the cluster is done with
+  // them: their loads have all returned by the time a CTA arrives here, so
+  // the arrival needs no memory ordering
+  if (S > 1) asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -834,7 +848,7 @@ cudaError_t launch_route_fused(const RouteFusedArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (a.select && a.token_ids == nullptr)
     return launch_route_recheck(a.X, a.WgT, a.bias, a.H, a.score_fn, a.k, a.alpha, a.renorm, a.E_ids,
-                                a.G, a.rs, s);
+                                a.G, a.rs, a.rs.seg_n, p.n_rt * f.S, kBM / f.S, false, true, s);
   return cudaSuccess;
 }
 
