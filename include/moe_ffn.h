@@ -48,7 +48,10 @@ typedef enum moe_status {
   MOE_ERR_BAD_EXPERT_ID = 4, /* device: an expert id outside [0, E)           */
   MOE_ERR_BAD_TOKEN_ID = 5,  /* device: a hash token id outside [0, V)        */
   MOE_ERR_TIMEOUT = 6,       /* device: a pipeline wait ran out of time       */
-  MOE_ERR_CUDA = 7           /* a CUDA runtime call failed                    */
+  MOE_ERR_CUDA = 7,          /* a CUDA runtime call failed                    */
+  MOE_ERR_BOUNDS = 8         /* device, debug build only: an index read from
+                                data was outside the array it indexes (the
+                                access was skipped)                          */
 } moe_status;
 
 /* Affinity a = score(l) of a router logit l. */
@@ -316,6 +319,17 @@ moe_status moe_sync_status(void* ws, size_t ws_bytes, void* stream);
  * status word, which moe_sync_status() then returns.  The GPU context stays
  * usable.  The same bounded wait guards every pipeline wait of the GEMMs. */
 moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
+/* Self-test of the debug build's bounds checks (the library compiled with
+ * MOE_DEBUG_BOUNDS, which checks every index the kernels read from data
+ * against the extent of the array it indexes and skips a bad access instead
+ * of trapping).  Launches one kernel that writes element `index` of a 32-int
+ * array at byte 128 of the workspace's status header through such a check:
+ * an index outside [0, 32) is skipped and recorded, and the next
+ * moe_sync_status() returns MOE_ERR_BOUNDS.  The release library checks
+ * nothing and returns MOE_ERR_UNSUPPORTED without launching.  Not a part of
+ * the layer: it has no counterpart on the pages. */
+moe_status moe_selftest_bounds(void* ws, size_t ws_bytes, int64_t index, void* stream);
 
 /* Static text for a status code. */
 const char* moe_status_string(moe_status s);

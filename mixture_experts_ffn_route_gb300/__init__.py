@@ -17,7 +17,11 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmoe_ffn.so")
+# MOE_FFN_DEBUG_BOUNDS=1 loads the bounds-checked debug build instead (built
+# by build.build(debug=True)): every index the kernels read from data is
+# checked against its array and a bad one reported as MOE_ERR_BOUNDS.
+LIB_PATH = os.path.join(_PKG, "libmoe_ffn_debug.so" if os.environ.get("MOE_FFN_DEBUG_BOUNDS") == "1"
+                        else "libmoe_ffn.so")
 
 SCORE_SIGMOID = 0
 SCORE_SQRT_SOFTPLUS = 1
@@ -36,6 +40,7 @@ MOE_ERR_BAD_EXPERT_ID = 4
 MOE_ERR_BAD_TOKEN_ID = 5
 MOE_ERR_TIMEOUT = 6
 MOE_ERR_CUDA = 7
+MOE_ERR_BOUNDS = 8
 
 # every function the C header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -76,6 +81,7 @@ SIGNATURES = {
                                       ctypes.POINTER(ctypes.c_void_p)]),
     "moe_sync_status": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
+    "moe_selftest_bounds": (ctypes.c_int, [_P, _SZ, ctypes.c_int64, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_abi_version": (ctypes.c_int32, []),
 }
@@ -300,6 +306,12 @@ def moe_forward_mx(p, fmt: int, X, E_ids, G, W1, S1, W2, S2, Y, ws, stage_events
 def moe_selftest_wait_timeout(ws, limit_us: int, stream=None):
     return _check(lib().moe_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)),
                   "moe_selftest_wait_timeout")
+
+
+def moe_selftest_bounds(ws, index: int, stream=None) -> int:
+    """Status of the bounds self-test launch (MOE_ERR_UNSUPPORTED from the
+    release library); the check's outcome comes from moe_sync_status."""
+    return int(lib().moe_selftest_bounds(_ptr(ws), ws.numel(), int(index), _stream(stream)))
 
 
 def moe_sync_status(ws, stream=None, raise_on_error=True) -> int:

@@ -35,7 +35,8 @@ struct WsLayout {
 };
 
 // The status header (256 bytes, zeroed by moe_workspace_init): the status
-// word at byte 0; the router's re-decision list counters at byte 64.
+// word at byte 0; the router's re-decision list counters at byte 64; the
+// debug build's bounds self-test array at byte 128.
 constexpr size_t kRouteCountersAt = 64;
 
 static WsLayout layout(const moe_params& p) {
@@ -222,6 +223,27 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, &abort_flag, limit_ns);
 }
 
+#ifdef MOE_DEBUG_BOUNDS
+// Writes element `index` of a 32-int array through the debug build's bounds
+// check (an index outside [0, 32) is recorded and skipped).
+__global__ void selftest_bounds_kernel(int* arr, long long index) {
+  if (in_bounds(index, 32)) arr[index] = 1;
+}
+#endif
+
+MOE_DEFINE_BOUNDS_TAKE(api)
+
+#ifdef MOE_DEBUG_BOUNDS
+// Any translation unit's bounds word set since the last call (all cleared).
+static bool take_bounds() {
+  int v = 0;
+  for (int w : {bounds_take_api(), bounds_take_dispatch(), bounds_take_gemm(), bounds_take_gemm_mx(),
+                bounds_take_quant(), bounds_take_backward(), bounds_take_route(), bounds_take_route_fused()})
+    v |= w;
+  return v != 0;
+}
+#endif
+
 }  // namespace moe
 
 using namespace moe;
@@ -240,6 +262,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_BAD_TOKEN_ID: return "hash token id outside [0, V)";
     case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
     case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_BOUNDS: return "index outside its array (debug build)";
   }
   return "unknown status";
 }
@@ -264,10 +287,30 @@ moe_status moe_sync_status(void* ws, size_t ws_bytes, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+#ifdef MOE_DEBUG_BOUNDS
+  const bool bounds = take_bounds();
+#else
+  const bool bounds = false;
+#endif
   if (flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
+  if (bounds) return MOE_ERR_BOUNDS;
   if (flags & kFlagBadToken) return MOE_ERR_BAD_TOKEN_ID;
   if (flags & kFlagBadExpert) return MOE_ERR_BAD_EXPERT_ID;
   return MOE_OK;
+}
+
+moe_status moe_selftest_bounds(void* ws, size_t ws_bytes, int64_t index, void* stream) {
+  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+#ifdef MOE_DEBUG_BOUNDS
+  selftest_bounds_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(at<int>(ws, 128),
+                                                                      static_cast<long long>(index));
+  return cuda_status(cudaGetLastError());
+#else
+  (void)index;
+  (void)stream;
+  return MOE_ERR_UNSUPPORTED;
+#endif
 }
 
 moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
@@ -526,6 +569,8 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
     g.status = status;
     if (fuse_k1) {
       g.gather_perm = b.perm;
+      g.gather_k = 1;
+      g.gather_rows = T;  // the extent of G and of Y's rows
       g.gate = G;
     }
     const long long tiles = static_cast<long long>(mt_bound) * g.n_tiles;

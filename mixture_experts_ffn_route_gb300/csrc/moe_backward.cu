@@ -16,13 +16,16 @@ namespace {
 
 constexpr int kRowThreads = 256;
 
-// The token and the gate of permuted row r; false past the last row.
+// The token and the gate of permuted row r; false past the last row.  A
+// permutation entry outside the A assignments (debug build) gives t = -1.
 __device__ __forceinline__ bool row_source(const int* __restrict__ perm, const int* __restrict__ row_off,
-                                           int E, int k, int has_shared, int r, int* t, int* f) {
+                                           int E, int k, int has_shared, long long A, int r, int* t,
+                                           int* f) {
   const int routed = __ldg(row_off + E);
   if (r < routed) {
     *f = __ldg(perm + r);
     *t = *f / k;
+    if (!in_bounds(*f, A)) *t = *f = -1;
     return true;
   }
   if (has_shared && r < __ldg(row_off + E + 1)) {
@@ -40,9 +43,12 @@ __global__ void __launch_bounds__(kRowThreads)
                          const float* __restrict__ Yp, int rows_max, int k, int H, int E,
                          int has_shared, uint16_t* __restrict__ dYp, float* __restrict__ dG) {
   __shared__ float red[kRowThreads / 32];
+  // rows_max = A (+ T shared-expert rows): the assignments A = T k
+  const long long A = has_shared ? static_cast<long long>(rows_max) / (k + 1) * k : rows_max;
   for (int r = blockIdx.x; r < rows_max; r += gridDim.x) {
     int t, f;
-    if (!row_source(perm, row_off, E, k, has_shared, r, &t, &f)) return;
+    if (!row_source(perm, row_off, E, k, has_shared, A, r, &t, &f)) return;
+    if (t < 0) continue;  // block-uniform
     const float g = f >= 0 ? __ldg(G + f) : 1.0f;
     const uint16_t* dy = dY + static_cast<long long>(t) * H;
     const float* yp = Yp + static_cast<long long>(r) * H;
@@ -88,9 +94,11 @@ __global__ void __launch_bounds__(kRowThreads)
     gather_rows_kernel(const uint16_t* __restrict__ X, const int* __restrict__ perm,
                        const int* __restrict__ row_off, int rows_max, int k, int H, int E,
                        int has_shared, uint16_t* __restrict__ Xp) {
+  const long long A = has_shared ? static_cast<long long>(rows_max) / (k + 1) * k : rows_max;
   for (int r = blockIdx.x; r < rows_max; r += gridDim.x) {
     int t, f;
-    if (!row_source(perm, row_off, E, k, has_shared, r, &t, &f)) return;
+    if (!row_source(perm, row_off, E, k, has_shared, A, r, &t, &f)) return;
+    if (t < 0) continue;
     const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<long long>(r) * H);
     for (int c = threadIdx.x; c < H / 8; c += kRowThreads) dst[c] = __ldg(src + c);
@@ -105,11 +113,15 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     int rows[17];
     int n = 0;
+    const long long A = static_cast<long long>(T) * k;
     for (int j = 0; j < k; ++j) {
       const int r = __ldg(inv + static_cast<long long>(t) * k + j);
-      if (r >= 0) rows[n++] = r;
+      if (r >= 0 && in_bounds(r, A)) rows[n++] = r;
     }
-    if (has_shared) rows[n++] = __ldg(row_off + E) + t;
+    if (has_shared) {
+      const int r = __ldg(row_off + E) + t;
+      if (in_bounds(r, A + T)) rows[n++] = r;
+    }
     for (int c = 4 * threadIdx.x; c < H; c += 4 * kRowThreads) {
       float4 s = __ldcs(reinterpret_cast<const float4*>(dXr + static_cast<long long>(t) * H + c));
       float a[4] = {s.x, s.y, s.z, s.w};
@@ -239,5 +251,7 @@ cudaError_t launch_router_bwd(const float* logits, const int32_t* E_ids, const f
   router_bwd_kernel<<<blocks, 256, 0, s>>>(logits, E_ids, dG, T, E, k, score_fn, alpha, renorm, dl);
   return cudaGetLastError();
 }
+
+MOE_DEFINE_BOUNDS_TAKE(backward)
 
 }  // namespace moe

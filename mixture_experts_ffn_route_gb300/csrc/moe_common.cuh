@@ -32,6 +32,36 @@ __device__ __forceinline__ void set_flag(int* status, int flag) {
   if (status) atomicOr(status, flag);
 }
 
+// Bounds checks of the debug build (compiled with MOE_DEBUG_BOUNDS).  Every
+// index the kernels read from data (a permutation or inverse entry, a list
+// entry, an expert id taken from a list) is checked against the extent of the
+// array it indexes before the access; a bad one is recorded in this
+// translation unit's bounds word and the access is skipped (no trap).
+// moe_sync_status() collects the words (MOE_ERR_BOUNDS).  The release build
+// compiles every check to true.
+#ifdef MOE_DEBUG_BOUNDS
+static __device__ int g_bounds_word;  // one per translation unit
+__device__ __forceinline__ bool in_bounds(long long i, long long n) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(&g_bounds_word, 1);
+  return false;
+}
+// Host function `int bounds_take_<tu>()`: this translation unit's bounds
+// word, then cleared.
+#define MOE_DEFINE_BOUNDS_TAKE(tu)                                            \
+  int bounds_take_##tu() {                                                   \
+    int v = 0, z = 0;                                                        \
+    if (cudaMemcpyFromSymbol(&v, g_bounds_word, sizeof(int)) != cudaSuccess) \
+      return -1;                                                             \
+    if (cudaMemcpyToSymbol(g_bounds_word, &z, sizeof(int)) != cudaSuccess)   \
+      return -1;                                                             \
+    return v;                                                                \
+  }
+#else
+__device__ __forceinline__ bool in_bounds(long long, long long) { return true; }
+#define MOE_DEFINE_BOUNDS_TAKE(tu)
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

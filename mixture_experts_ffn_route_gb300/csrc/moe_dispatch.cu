@@ -177,8 +177,10 @@ __global__ void __launch_bounds__(kThreads)
     const unsigned m = __ballot_sync(0xffffffffu, mine);
     if (mine) {
       const int row = pos + __popc(m & ((1u << lane) - 1u));
-      perm[row] = f0 + i;
-      inv[f0 + i] = row;
+      if (in_bounds(row, A)) {
+        perm[row] = f0 + i;
+        inv[f0 + i] = row;
+      }
     }
     pos += __popc(m);
   }
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads)
     const int e = ids[i];
     if (e < 0 || e >= E) continue;
     const int row = __ldg(row_off + e) + __ldg(cb + e) + cnt[(i >> 7) * E + e] + rank[i];
+    if (!in_bounds(row, A)) continue;
     perm[row] = f0 + i;
     inv[f0 + i] = row;
   }
@@ -306,13 +309,14 @@ __global__ void __launch_bounds__(kCombineThreads)
   __syncthreads();
   const int n = k + (has_shared ? 1 : 0);
   const int vecs = H / 8;
+  const long long n_rows = static_cast<long long>(gridDim.x) * (k + (has_shared ? 1 : 0));  // rows of Yp
   for (int c = threadIdx.x; c < vecs; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     for (int j = 0; j < n; ++j) {
       const int p = rows[j];
-      if (p < 0) continue;
+      if (p < 0 || !in_bounds(p, n_rows)) continue;
       float x[8];
       load_row8(Yp + static_cast<long long>(p) * H, c, x);
       const float g = w[j];
@@ -359,5 +363,7 @@ cudaError_t launch_combine_bf16(const uint16_t* Yp, const int* inv, const float*
   combine_kernel<uint16_t><<<T, kCombineThreads, 0, s>>>(Yp, inv, G, row_off, k, H, E, has_shared, Y);
   return cudaGetLastError();
 }
+
+MOE_DEFINE_BOUNDS_TAKE(dispatch)
 
 }  // namespace moe

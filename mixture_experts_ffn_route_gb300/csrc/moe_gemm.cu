@@ -190,7 +190,10 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
             tok[i] = x < p.gather_rows ? x : -1;
           } else {
             const int row = t.row0 + r;
-            tok[i] = row < t.row_end ? __ldg(p.gather_perm + row) / p.gather_k : -1;
+            const int f = row < t.row_end ? __ldg(p.gather_perm + row) : -1;
+            tok[i] = f >= 0 && in_bounds(f, static_cast<long long>(p.gather_rows) * p.gather_k)
+                         ? f / p.gather_k
+                         : -1;
           }
         }
         bool ok = true;
@@ -453,5 +456,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmMaps& maps, const GemmParams& p
     default: return cudaErrorInvalidValue;
   }
 }
+
+MOE_DEFINE_BOUNDS_TAKE(gemm)
 
 }  // namespace moe

@@ -80,13 +80,15 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, uint32_t tb,
     float g = 1.0f;
     if (K1) {
       const int my = wrow0 + lane;
-      g = my < row_end ? __ldg(p.gate + __ldg(p.gather_perm + my)) : 0.0f;
+      const int f = my < row_end ? __ldg(p.gather_perm + my) : -1;
+      g = f >= 0 && in_bounds(f, p.gather_rows) ? __ldg(p.gate + f) : 0.0f;
     }
     int dst[4];  // output row of each of the four rows this lane stores, or -1
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int grow = wrow0 + 8 * i + (lane >> 2);
       dst[i] = grow < row_end ? (K1 ? __ldg(p.gather_perm + grow) : grow) : -1;
+      if (dst[i] >= 0 && !in_bounds(dst[i], p.gather_rows)) dst[i] = -1;
     }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {

@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(256)
       ndst = 0;
       for (int j = 0; j < k; ++j) {
         const int r = __ldg(inv + static_cast<long long>(row) * k + j);
-        if (r >= 0) dst[ndst++] = r;
+        if (r >= 0 && in_bounds(r, static_cast<long long>(rows) * k)) dst[ndst++] = r;
       }
     }
     for (int g = lane; g < groups; g += 32) {
@@ -720,5 +720,7 @@ cudaError_t launch_mx_quant_rows(int fmt, const uint16_t* x, int rows, int cols,
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
+
+MOE_DEFINE_BOUNDS_TAKE(gemm_mx)
 
 }  // namespace moe

@@ -8,6 +8,19 @@
 
 namespace moe {
 
+#ifdef MOE_DEBUG_BOUNDS
+// The bounds words of the debug build, one per translation unit that checks
+// (MOE_DEFINE_BOUNDS_TAKE in moe_common.cuh).
+int bounds_take_api();
+int bounds_take_dispatch();
+int bounds_take_gemm();
+int bounds_take_gemm_mx();
+int bounds_take_quant();
+int bounds_take_backward();
+int bounds_take_route();
+int bounds_take_route_fused();
+#endif
+
 constexpr int kBM = 128;  // GEMM tile rows (tokens)
 constexpr int kBK = 64;   // GEMM k-block (one 128-byte swizzle row of bf16)
 
@@ -221,8 +234,8 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
 // flagged[b seg_len ..).  The general path passes one segment (its counters,
 // which the last block zeroes); the fused router one per CTA, and launches
 // the kernel as its programmatic dependent (pdl).
-cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
-                                 int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
+cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int T, int H,
+                                 int E, int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, const int* seg_n, int n_seg,
                                  int seg_len, bool zero_counters, bool pdl, cudaStream_t s);
 // Fused router (moe_route_fused.cu): the gating GEMM on the tensor cores with

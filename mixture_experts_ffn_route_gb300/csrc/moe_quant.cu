@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       ndst = 0;
       for (int j = 0; j < k; ++j) {
         const int d = __ldg(inv + static_cast<long long>(r) * k + j);
-        if (d >= 0) dst[ndst++] = d;
+        if (d >= 0 && in_bounds(d, static_cast<long long>(rows) * k)) dst[ndst++] = d;
       }
     }
     float amax = 0.0f;
@@ -103,5 +103,7 @@ cudaError_t launch_quant_rows_f32(const float* x, const int* rows_dev, int rows_
       x, rows_dev, rows_max, cols, codes, scales, nullptr, 0);
   return cudaGetLastError();
 }
+
+MOE_DEFINE_BOUNDS_TAKE(quant)
 
 }  // namespace moe

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       warp_argmax(best, bid);
       top[r] = best;
       if (r < k) sel[r] = bid;
-      if (lane == 0) s[bid] = -FLT_MAX;  // taken
+      if (lane == 0 && in_bounds(bid, E)) s[bid] = -FLT_MAX;  // taken
       __syncwarp();
     }
     bool close = false;
@@ -153,8 +153,10 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (lane == 0) {
         base = atomicAdd(rs.counters + 1, count);
         const int fi = atomicAdd(rs.counters + 0, 1);
-        rs.flagged[fi] = make_int4(t, base, count, 0);
-        rs.fnorm[fi] = make_float2(lmax, zsum);
+        if (in_bounds(fi, T)) {
+          rs.flagged[fi] = make_int4(t, base, count, 0);
+          rs.fnorm[fi] = make_float2(lmax, zsum);
+        }
       }
       base = __shfl_sync(0xffffffffu, base, 0);
       for (int e0 = 0; e0 < E; e0 += 32) {
@@ -163,8 +165,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         const unsigned m = __ballot_sync(0xffffffffu, cand);
         if (cand) {
           const int at = base + __popc(m & ((1u << lane) - 1u));
-          rs.pairs[at] = make_int2(t, e);
-          rs.plogit[at] = lrow[e];
+          if (in_bounds(at, static_cast<long long>(T) * E)) {
+            rs.pairs[at] = make_int2(t, e);
+            rs.plogit[at] = lrow[e];
+          }
         }
         base += __popc(m);
       }
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
     route_redecide_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ WgT,
                           const float* __restrict__ bias, int H, int k, int fn, float alpha, int renorm,
                           int32_t* __restrict__ E_ids, float* __restrict__ G, RouteScratch rs,
-                          const int* seg_n, int n_seg, int seg_len, int zero_counters) {
+                          const int* seg_n, int n_seg, int seg_len, int zero_counters, int T, int E) {
   // launched as the fused router's programmatic dependent: its writes are
   // visible from here on (a no-op after an ordinary launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -330,12 +334,16 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
     const int idx = j - cnt_s[seg];
     const int4 f = rs.flagged[static_cast<long long>(seg) * seg_len + idx];
     const int t = f.x, base = f.y, count = f.z;
+    const long long n_pairs = static_cast<long long>(T) * E;
+    if (!in_bounds(t, T) || !in_bounds(base, n_pairs) || !in_bounds(base + count - 1, n_pairs))
+      continue;  // block-uniform
     const bool small = count <= kRedecideList;
     // the token row and the candidates, their loads issued together
     const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * H);
     for (int v = threadIdx.x; v < vecs; v += blockDim.x) xs[v] = __ldg(xr + v);
     for (int i = threadIdx.x; small && i < count; i += blockDim.x) {
-      const int e = rs.pairs[base + i].y;
+      int e = rs.pairs[base + i].y;
+      if (!in_bounds(e, E)) e = 0;
       const float l = rs.plogit[base + i];
       float v = score_f32(l, fn);
       if (bias != nullptr) v += bias[e];
@@ -380,7 +388,9 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
         const int len = (vecs + ns - 1) / ns;
         const int vb = part_i * len, ve = min(vecs, vb + len);
         const int ci = exact_at(c0 + c);
-        const float2 d = pair_dot(xs, WgT, H, small ? id_s[ci] : rs.pairs[base + ci].y, vb, ve, lane);
+        int ce = small ? id_s[ci] : rs.pairs[base + ci].y;
+        if (!in_bounds(ce, E)) ce = 0;
+        const float2 d = pair_dot(xs, WgT, H, ce, vb, ve, lane);
         if (lane == 0) part[warp] = d;
       }
       __syncthreads();
@@ -391,7 +401,8 @@ __global__ void __launch_bounds__(kRedecideWarps * 32)
           ff_add(acc.x, acc.y, d.x, d.y);
         }
         const int i = exact_at(c0 + lane);
-        const int e = small ? id_s[i] : rs.pairs[base + i].y;
+        int e = small ? id_s[i] : rs.pairs[base + i].y;
+        if (!in_bounds(e, E)) e = 0;
         double v = score_f64(static_cast<double>(acc.x) + static_cast<double>(acc.y), fn);
         if (bias != nullptr) v += static_cast<double>(bias[e]);
         if (small) key_s[i] = order_key(v);
@@ -523,8 +534,8 @@ cudaError_t launch_transpose_wg(const uint16_t* Wg, int H, int E, uint16_t* WgT,
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int H,
-                                 int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
+cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const float* bias, int T, int H,
+                                 int E, int score_fn, int k, float alpha, int renorm, int32_t* E_ids,
                                  float* G, const RouteScratch& rs, const int* seg_n, int n_seg,
                                  int seg_len, bool zero_counters, bool pdl, cudaStream_t s) {
   const size_t sh = static_cast<size_t>(H) * 2 + kRedecideWarps * sizeof(float2) +
@@ -546,7 +557,7 @@ cudaError_t launch_route_recheck(const uint16_t* X, const uint16_t* WgT, const f
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, route_redecide_kernel, X, WgT, bias, H, k, score_fn, alpha, renorm,
-                            E_ids, G, rs, seg_n, n_seg, seg_len, zero_counters ? 1 : 0);
+                            E_ids, G, rs, seg_n, n_seg, seg_len, zero_counters ? 1 : 0, T, E);
 }
 
 cudaError_t launch_route_select(const float* logits, const uint16_t* X, const uint16_t* WgT,
@@ -568,8 +579,10 @@ cudaError_t launch_route_select(const float* logits, const uint16_t* X, const ui
                                                       status);
   if (token_ids != nullptr) return cudaGetLastError();
   // one segment: the compact list and its counter, zeroed after use
-  return launch_route_recheck(X, WgT, bias, H, score_fn, k, alpha, renorm, E_ids, G, rs, rs.counters, 1, T,
-                              true, false, s);
+  return launch_route_recheck(X, WgT, bias, T, H, E, score_fn, k, alpha, renorm, E_ids, G, rs, rs.counters,
+                              1, T, true, false, s);
 }
+
+MOE_DEFINE_BOUNDS_TAKE(route)
 
 }  // namespace moe

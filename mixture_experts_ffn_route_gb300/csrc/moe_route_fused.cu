@@ -374,8 +374,10 @@ __device__ __forceinline__ void decide_rows(const FusedParams& p, const uint8_t*
           const unsigned bm = __ballot_sync(0xffffffffu, cand);
           if (cand) {
             const int at = base + __popc(bm & ((1u << lane) - 1u));
-            p.rs.pairs[at] = make_int2(t[r], e);
-            p.rs.plogit[at] = xs[q];
+            if (in_bounds(at, static_cast<long long>(p.T) * E)) {
+              p.rs.pairs[at] = make_int2(t[r], e);
+              p.rs.plogit[at] = xs[q];
+            }
           }
           base += __popc(bm);
         }
@@ -707,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.token_ids == nullptr) {
       const int nf = *stage_n;
       for (int i = threadIdx.x; i < nf; i += kThreads) {
+        if (!in_bounds(t0 + i, p.T)) continue;
         p.rs.flagged[t0 + i] = stage_f[i];
         p.rs.fnorm[t0 + i] = stage_n2[i];
       }
@@ -847,9 +850,11 @@ cudaError_t launch_route_fused(const RouteFusedArgs& a, cudaStream_t s) {
   e = cudaLaunchKernelEx(&cfg, route_fused_kernel, mx, mw, p);
   if (e != cudaSuccess) return e;
   if (a.select && a.token_ids == nullptr)
-    return launch_route_recheck(a.X, a.WgT, a.bias, a.H, a.score_fn, a.k, a.alpha, a.renorm, a.E_ids,
-                                a.G, a.rs, a.rs.seg_n, p.n_rt * f.S, kBM / f.S, false, true, s);
+    return launch_route_recheck(a.X, a.WgT, a.bias, a.T, a.H, a.E, a.score_fn, a.k, a.alpha, a.renorm,
+                                a.E_ids, a.G, a.rs, a.rs.seg_n, p.n_rt * f.S, kBM / f.S, false, true, s);
   return cudaSuccess;
 }
+
+MOE_DEFINE_BOUNDS_TAKE(route_fused)
 
 }  // namespace moe

@@ -17,11 +17,15 @@ def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
 
 
+DEBUG_BOUNDS = os.environ.get("MOE_FFN_DEBUG_BOUNDS") == "1"
+
+
 def _lib_is_stale():
     from mixture_experts_ffn_route_gb300 import build as b
-    if not os.path.exists(b.LIB):
+    lib = b.LIB_DEBUG if DEBUG_BOUNDS else b.LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(b.LIB)
+    t = os.path.getmtime(lib)
     deps = b.sources() + [os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC) if f.endswith((".cuh", ".h"))]
     deps.append(os.path.join(ROOT, "include", "moe_ffn.h"))
     return any(os.path.getmtime(d) > t for d in deps)
@@ -29,11 +33,12 @@ def _lib_is_stale():
 
 @pytest.fixture(scope="session")
 def built_lib():
-    """The in-tree CUDA library, (re)built with nvcc when missing or stale."""
+    """The in-tree CUDA library, (re)built with nvcc when missing or stale
+    (the bounds-checked debug build under MOE_FFN_DEBUG_BOUNDS=1)."""
     from mixture_experts_ffn_route_gb300 import build as b
     if _lib_is_stale():
-        b.build()
-    return b.LIB
+        b.build(debug=DEBUG_BOUNDS)
+    return b.LIB_DEBUG if DEBUG_BOUNDS else b.LIB
 
 
 def pytest_terminal_summary(terminalreporter):
