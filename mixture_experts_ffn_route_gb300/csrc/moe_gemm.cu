@@ -259,7 +259,10 @@ __global__ void __launch_bounds__(KindInfo<KIND>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Each warp owns 32 accumulator rows (its TMEM lane quarter), or 16 after
-    // an M = 64 MMA, which leaves row 16q + l in lane l < 16 of quarter q.  A
+    // an M = 64 MMA, which leaves row 16q + l in lane l < 16 of quarter q (the
+    // tcgen05 data-path layout of an M = 64, one-CTA MMA: the first 16 lanes
+    // of each 32-lane quarter hold all N columns; groups of 63, 64 and 65 rows
+    // are parity cases of their own).  A
     // chunk of 32 columns goes TMEM -> registers (one row per lane) -> a
     // padded shared staging block -> global memory with every store
     // instruction writing whole 128-byte lines (4 rows of fp32 or 8 rows of
