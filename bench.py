@@ -736,6 +736,44 @@ def oracle_leg(r, n_tokens, seed=0):
     return T / (t_route + t_ffn * T / len(rows)), t_route, t_ffn, len(rows)
 
 
+def oracle_expert_leg(r, step, n_cap=256):
+    """One bounded step of the reference arm: the oracle's routing and dispatch
+    of all T tokens, then its expert FFN (swiglu_expert, which decodes the
+    expert's bf16 weights itself) for one active expert, on up to n_cap of the
+    rows routed to it and on one of them alone.  The experts are taken in
+    order of their row counts, largest first, one per step.  The layer's FFN
+    time is modelled from the two calls: each active expert decoded once (the
+    one-row call) plus a cost per routed row (the difference over the other
+    rows), the shared expert counted as one more expert of T rows.  Returns
+    (tokens/s of the layer, route s, decode s, per-row s, rows used)."""
+    import oracle
+    c = r.c
+    T = c["T"]
+    t0 = time.time()
+    ids, _ = r.route()
+    t_route = time.time() - t0
+    counts = np.bincount(ids[(ids >= 0) & (ids < c["E"])].ravel(), minlength=c["E"])
+    order = np.argsort(-counts, kind="stable")
+    active = order[counts[order] > 1]
+    e = int(active[step % len(active)])
+    rows = np.nonzero((ids == e).any(axis=1))[0]
+    rows = np.random.default_rng(step).permutation(rows)[:n_cap]
+    W1 = r.bits(r.dd["W1"][e])
+    W2 = r.bits(r.dd["W2"][e])
+    X64 = oracle.bf16_to_f64(r.X[rows])
+    t0 = time.time()
+    oracle.swiglu_expert(X64[:1], W1, W2)
+    t_one = time.time() - t0
+    t0 = time.time()
+    oracle.swiglu_expert(X64, W1, W2)
+    t_all = time.time() - t0
+    per_row = max(t_all - t_one, 0.0) / max(len(rows) - 1, 1)
+    n_active = int((counts > 0).sum()) + (1 if c["shared"] else 0)
+    n_rows = int(counts.sum()) + (T if c["shared"] else 0)
+    t_layer = t_route + n_active * t_one + n_rows * per_row
+    return T / t_layer, t_route, t_one, per_row, len(rows)
+
+
 def cpu_baseline(dd, n_all=512, n_one=128):
     """The oracle on this host's cores (all, then one) at the bench's workload."""
     r = OracleRunner(dd)
@@ -761,9 +799,10 @@ def cpu_baseline(dd, n_all=512, n_one=128):
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands on this host's cores (rank 0 only), the leg of
-    cpu_baseline with a smaller FFN sample per step so that --steps K
-    --warmup W end within a few minutes."""
+    """The oracle as it stands on this host's cores (rank 0 only), in steps
+    bounded so that --steps K --warmup W end within a few minutes: each step
+    routes all T tokens and runs one expert's FFN (oracle_expert_leg).  The
+    in-line cpu_baseline of the GPU arm runs the full covering sample."""
     if rank != 0:
         return None
     import torch
@@ -771,19 +810,34 @@ def run_reference(args, rank, world):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     dd = synth.make_inputs_torch(args.workload, seed=1234, device=dev)
     r = OracleRunner(dd)
-    n = args.ref_tokens
+    r.route(np.arange(2))  # first-call costs (BLAS start-up) outside the timing
+    quantised = bool(r.c.get("quant") or synth_mx_format(r.c))
+    # the quantised forms keep the covering leg on a small token sample
+    leg = ((lambda i: oracle_leg(r, args.ref_tokens, seed=i)) if quantised
+           else (lambda i: oracle_expert_leg(r, i)))
     for i in range(args.warmup):
-        oracle_leg(r, n, seed=100 + i)
-    vals, secs = [], []
+        leg(1000 + i)
+    vals, secs, parts = [], [], []
     for i in range(args.steps):
         t0 = time.time()
-        v, _, _, n_used = oracle_leg(r, n, seed=i)
+        out = leg(i)
         secs.append(time.time() - t0)
-        vals.append(v)
+        vals.append(out[0])
+        parts.append(out[1:])
     v = len(vals) / sum(1.0 / x for x in vals)  # tokens/s over the K steps (harmonic mean)
-    sample = (f"each step: routing and dispatch of all {dd['cfg']['T']} tokens, then the fp64 "
-              f"expert FFNs and combine of {n} tokens reaching as many experts as they route to "
-              f"(each expert's weights decoded once per step), extrapolated x T/{n}")
+    med = lambda j: float(np.median([p[j] for p in parts]))  # noqa: E731
+    if quantised:
+        sample = (f"each step: routing and dispatch of all {dd['cfg']['T']} tokens, then the fp64 "
+                  f"expert FFNs and combine of {args.ref_tokens} tokens and as many more as reach "
+                  f"every routed expert (each expert's weights decoded once per step), "
+                  f"extrapolated x T/(tokens used)")
+    else:
+        sample = (f"each step: the oracle's routing and dispatch of all {dd['cfg']['T']} tokens "
+                  f"({med(0):.2f} s), then its expert FFN for one expert (the most loaded first, "
+                  f"one per step) on up to 256 of its rows and on one row alone; the layer's FFN "
+                  f"time is modelled as (active experts x the one-row call, {med(1):.2f} s: the "
+                  f"expert's weights decoded) + (routed rows x the per-row cost, "
+                  f"{1e3 * med(2):.2f} ms)")
     return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
@@ -811,7 +865,8 @@ def main(argv=None):
                     help="tokens of the oracle's FFN sample on all cores")
     ap.add_argument("--cpu-tokens-1core", type=int, default=128,
                     help="tokens of the oracle's FFN sample on one core")
-    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=8,
+                    help="tokens of the reference arm's FFN sample per step (quantised forms)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured once in a CUDA graph and replayed")
     ap.add_argument("--train", action="store_true",

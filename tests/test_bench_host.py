@@ -86,3 +86,24 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
         assert key in b
     assert b["extrapolated"] is True and b["cores"] == os.cpu_count()
     assert b["value"] > 0 and b["value_1core"] > 0 and "every routed expert" in b["sample"]
+
+
+def test_reference_step_models_the_layer_from_one_expert():
+    # the bounded step of the reference arm: one expert's FFN on its rows and
+    # on one row, the layer's FFN time modelled from the two (decode per
+    # active expert + cost per routed row); step 0 takes the most loaded
+    # expert, on all its rows up to the cap
+    import oracle
+    import synth
+    dd = synth.make_inputs_torch("c3s", device="cpu")
+    r = bench.OracleRunner(dd)
+    v, t_route, t_dec, per_row, n = bench.oracle_expert_leg(r, 0, n_cap=64)
+    assert v > 0 and t_route >= 0 and t_dec > 0 and per_row >= 0 and 2 <= n <= 64
+    ids, _ = r.route()
+    counts = np.bincount(ids.ravel(), minlength=r.c["E"])
+    assert n == min(64, int(counts.max()))  # the most loaded expert first
+    e = int(np.argmax(counts))
+    rows = np.nonzero((ids == e).any(axis=1))[0][:n]
+    X64 = oracle.bf16_to_f64(r.X[rows])
+    W1, W2 = r.bits(dd["W1"][e]), r.bits(dd["W2"][e])
+    assert oracle.swiglu_expert(X64, W1, W2).shape == (n, r.c["H"])
