@@ -209,6 +209,19 @@ static moe_status run_router_gemm(const moe_params* p, const uint16_t* X, const 
   return cuda_status(launch_gemm(kGemmRouter, maps, g, grid, s));
 }
 
+// L2 capacity of the current device in bytes (cached per device).
+static size_t l2_bytes() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) return 0;
+    cache[dev] = v;
+  }
+  return static_cast<size_t>(cache[dev]);
+}
+
 // Waits on an mbarrier that nothing ever arrives on: the bounded wait must
 // give up after limit_ns and record kFlagTimeout in the status word.
 __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
@@ -508,22 +521,31 @@ static moe_status forward_impl(const moe_params* p, const uint16_t* X, const int
   const int mt_bound = (A + kBM - 1) / kBM + E + (Tsh + kBM - 1) / kBM;
 
   // Linear1 + SwiGLU:  Act = SwiGLU(X[rows of e] W1[e]), the rows gathered from
-  // X by the permutation inside the GEMM; the shared group takes X as it is
+  // X by the permutation inside the GEMM; the shared group takes X as it is.
+  // Where the experts average two row tiles or more and X is larger than L2
+  // (the large-FFN layer), the token rows are first copied into expert order
+  // (over Yp, which Linear2 writes only later) and Linear1 loads them by TMA:
+  // whole boxes of consecutive rows instead of 128 scattered row segments.
+  const bool rows_by_tma = A >= 2 * kBM * E && static_cast<size_t>(T) * H * 2 > l2_bytes();
   {
     GemmMaps maps;
-    bool ok = make_map_rows(&maps.a, X, T, H) && make_map_weights(&maps.b, W1, E, H, 2 * I);
-    maps.a2 = maps.a;
+    uint16_t* Xp = reinterpret_cast<uint16_t*>(Yp);
+    bool ok = make_map_rows(&maps.a, rows_by_tma ? Xp : X, rows_by_tma ? A : T, H) &&
+              make_map_weights(&maps.b, W1, E, H, 2 * I);
+    if (ok) ok = rows_by_tma ? make_map_rows(&maps.a2, X, T, H) : (maps.a2 = maps.a, true);
     if (ok) ok = p->has_shared ? make_map_weights(&maps.b2, Ws1, 1, H, 2 * I) : (maps.b2 = maps.b, true);
     if (!ok) return MOE_ERR_CUDA;
+    if (rows_by_tma && launch_gather_rows(X, b.perm, b.row_off, A, k, H, E, 0, Xp, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     GemmParams g;
     memset(&g, 0, sizeof(g));
     g.row_off = b.row_off;
     g.tile_off = b.tile_off;
     g.num_groups = groups;
     g.shared_group = p->has_shared ? E : -1;
-    g.a2_shared = 0;
+    g.a2_shared = rows_by_tma && p->has_shared ? 1 : 0;
     set_schedule(&g, b);
-    g.gather_src = X;
+    g.gather_src = rows_by_tma ? nullptr : X;
     g.gather_perm = b.perm;
     g.gather_k = k;
     g.gather_rows = T;

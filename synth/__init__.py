@@ -116,6 +116,11 @@ CONFIGS["c3p_mxa4"] = dict(CONFIGS["c3p"], shared=0, quant="mx_e2m1")
 # ncu capture can take (4.3 GB of weights), with given routing (ids drawn as
 # for c2): its Linear1 traffic ratio scales to c5
 CONFIGS["c5p"] = dict(CONFIGS["c5"], T=1024, E=4, routing="given")
+# parity cases of the large-FFN hidden size whose token rows exceed L2 (151 MB)
+# with few, wide experts: the path that copies the rows into expert order and
+# loads them by TMA; with and without a shared expert
+CONFIGS["c5x"] = dict(CONFIGS["c5"], T=9216, E=8, I=256)
+CONFIGS["c5x_sh"] = dict(CONFIGS["c5"], T=9216, E=8, I=256, shared=1)
 # the V4-Pro router at full size with a token-sized FFN (I = 64): a workload
 # whose routing kernels one ncu capture can take (1.1 GB of weights)
 CONFIGS["c3r"] = dict(CONFIGS["c3"], I=64)

@@ -514,7 +514,7 @@ def test_device_wait_limit_reports_timeout():
 # tokens whose Y is compared: (tokens chosen to reach every routed expert, at
 # least this many in all, then this many more random tokens)
 FULL = {"c2": (512, 0), "c3": (512, 256), "c4": (512, 256), "c5": (256, 0), "c3_sp": (512, 256),
-        "c3_f3072": (256, 0)}
+        "c3_f3072": (256, 0), "c5x": (128, 64), "c5x_sh": (128, 64)}
 
 
 def host_expert_weights(w):
