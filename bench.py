@@ -159,15 +159,24 @@ def route_launches(c):
     decision in its epilogue) and, for top-k, the float64 re-decision of close
     tokens; layers of more than 384 experts take the general path (Wg
     transpose, gating GEMM, selection, re-decision; hash: GEMM, selection).
-    The forward adds count, scan, place, Linear1 (row gather fused), Linear2
-    and combine; A8W8 adds the token and the activation quantisation, MX the
-    token one."""
+    The forward adds count, scan, place, Linear1 (row gather fused, or the
+    row copy before it: forward_row_copy), Linear2 and combine; A8W8 adds the
+    token and the activation quantisation, MX the token one."""
     if c["routing"] == "given":
         return 0
     fused = c["E"] <= 384 and c["E"] % 8 == 0
     if c["routing"] == "hash":
         return 1 if fused else 2
     return 2 if fused else 4
+
+
+def forward_row_copy(c):
+    """1 where the bf16 forward copies the token rows into expert order before
+    Linear1 (the experts average two 128-row tiles or more and X exceeds
+    L2: Linear1 then loads them by TMA), else 0; the library's criterion."""
+    import torch
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size if torch.cuda.is_available() else 0
+    return int(c["T"] * c["k"] >= 256 * c["E"] and c["T"] * c["H"] * 2 > l2)
 
 
 def build_step(moe, dd, p, ws, stage_events=None):
@@ -419,7 +428,7 @@ def run_ours(args, rank, world, local_rank, workload=None, with_cpu=True):
         roof["kernel"] = "grouped A8W8 Linear1 + SwiGLU (gemm_q8_kernel<true>)"
     if mx:
         roof["kernel"] = "grouped MX Linear1 + SwiGLU + Q_MX (gemm_mx_kernel<true, %d>)" % moe.MX_FORMATS[mx]
-    launches_per_step = route_launches(c) + (8 if quant else (7 if mx else 6))
+    launches_per_step = route_launches(c) + (8 if quant else (7 if mx else 6 + forward_row_copy(c)))
     out = {
         "metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -584,7 +593,7 @@ def run_train(args, rank, world, local_rank):
                 "h2d_bytes_per_step": int(2 * T * H * 2), "d2h_bytes_per_step": int(2 * T * H * 2)},
         # route + forward 6 + backward: unpermute, gather, 2 dgrad, 2 wgrad,
         # router GEMM, router backward, dWg, dXr, dX sum = 11
-        "gpu_launches": (route_launches(c) + 6 + 11) * K,
+        "gpu_launches": (route_launches(c) + 6 + forward_row_copy(c) + 11) * K,
         "clocks": sampler.summary() if sampler else None,
     }
     return out
