@@ -180,6 +180,35 @@ def test_route_one_lane_holds_the_top_entries(E, k):
     check_gates(G, G_ref)
 
 
+@pytest.mark.parametrize("T", [2048, 5000])
+def test_route_many_close_tokens(T):
+    # Every token ties (three identical, always-selected columns), so every
+    # token is listed for the float64 re-decision: more tokens than its
+    # blocks, each block taking several in turn (and, at T = 5000, the fused
+    # router's list spread over 40 row tiles' segments).
+    rng = np.random.default_rng(29)
+    H, E, k = 128, 16, 4
+    X = synth.bf16_bits_from_f32(rng.standard_normal((T, H)))
+    Wg = rng.standard_normal((H, E)).astype(np.float32) / 11
+    Wg[:, 9] = Wg[:, 2]
+    Wg[:, 13] = Wg[:, 2]
+    bias = np.zeros(E, np.float32)
+    bias[[2, 9, 13]] = 2.0  # above every other score (sigmoid < 1)
+    Wg = synth.bf16_bits_from_f32(Wg)
+    p = moe.make_params(T, H, E, k, 64)
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    G = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    for _ in range(2):  # the lists are rebuilt on every call
+        moe.moe_route(p, bf(X), bf(Wg), torch.from_numpy(bias).to(DEV), None, None, 0, E_ids, G, ws)
+        moe.moe_sync_status(ws)
+        ids = E_ids.cpu().numpy()
+        assert (ids[:, :3] == [2, 9, 13]).all()
+        ids_ref, G_ref, _ = oracle.route(X, Wg, bias, 0, k, 1.0, 1)
+        assert np.array_equal(ids, ids_ref)
+        check_gates(G, G_ref)
+
+
 def test_route_large_scores_a_few_1e4_apart():
     # The fused router's keys keep 23 bits of the biased score (the low 9
     # hold the id): at scores near 9 they resolve ~5e-4, coarser than the
