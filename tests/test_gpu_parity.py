@@ -102,6 +102,9 @@ ROUTER_SHAPES = [
     dict(T=200, H=2048, E=128, k=8, I=64, score="softmax", renorm=0),         # 4
     dict(T=130, H=512, E=320, k=3, I=64, score="sqrt_softplus", bias=True),   # 1, N = 256 + 64
     dict(T=77, H=1024, E=40, k=5, I=64, bias=True),                           # 2, padded columns
+    # more than 384 experts: the general path (fp32 logits, selection kernel)
+    dict(T=300, H=512, E=512, k=8, I=64, bias=True),
+    dict(T=200, H=256, E=448, k=4, I=64, score="softmax", renorm=0),
 ]
 
 
@@ -180,14 +183,29 @@ def test_route_one_lane_holds_the_top_entries(E, k):
     check_gates(G, G_ref)
 
 
-@pytest.mark.parametrize("T", [2048, 5000])
-def test_route_many_close_tokens(T):
+def test_hash_route_general_path():
+    # 512 experts take the general router (fp32 logits, then the selection
+    # kernel's table lookup): ids exactly the table's, gates from the logits
+    h, dd = host_inputs(dict(T=150, H=256, E=512, k=6, I=64, routing="hash", V=1000), seed=37)
+    p = params(h["cfg"])
+    ws = moe.alloc_workspace(p, DEV)
+    E_ids, G = run_route(p, dd, ws)
+    moe.moe_sync_status(ws)
+    ids_ref, G_ref, _ = oracle_route(h)
+    assert np.array_equal(E_ids.cpu().numpy(), ids_ref)
+    check_gates(G, G_ref, "hash, 512 experts")
+
+
+@pytest.mark.parametrize("T,E", [(2048, 16), (5000, 16), (2048, 512)])
+def test_route_many_close_tokens(T, E):
     # Every token ties (three identical, always-selected columns), so every
     # token is listed for the float64 re-decision: more tokens than its
     # blocks, each block taking several in turn (and, at T = 5000, the fused
-    # router's list spread over 40 row tiles' segments).
+    # router's list spread over 40 row tiles' segments; at E = 512 the general
+    # path's single list, whose counters the re-decision zeroes for the next
+    # call).
     rng = np.random.default_rng(29)
-    H, E, k = 128, 16, 4
+    H, k = 128, 4
     X = synth.bf16_bits_from_f32(rng.standard_normal((T, H)))
     Wg = rng.standard_normal((H, E)).astype(np.float32) / 11
     Wg[:, 9] = Wg[:, 2]
