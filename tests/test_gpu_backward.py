@@ -127,11 +127,13 @@ def test_backward_is_deterministic():
                            b[key].view(torch.int16) if key == "dX" else b[key]), key
 
 
-def test_backward_full_size_sampled():
-    """V4-Pro shapes: dX of sampled tokens (each token's input gradient depends
-    on its own path only) and the weight gradients of two lightly loaded
-    experts (all of their rows)."""
-    dd = synth.make_inputs_torch("c3", device=DEV)
+@pytest.mark.parametrize("name", ["c3", "c5x_sh"])
+def test_backward_full_size_sampled(name):
+    """V4-Pro shapes, and the large-FFN hidden size with token rows beyond L2
+    (whose forward loads them by TMA from a copy in expert order): dX of
+    sampled tokens (each token's input gradient depends on its own path only)
+    and the weight gradients of two experts (all of their rows)."""
+    dd = synth.make_inputs_torch(name, device=DEV)
     c = dd["cfg"]
     T, H, E, k = c["T"], c["H"], c["E"], c["k"]
     p = params(c)
@@ -151,13 +153,13 @@ def test_backward_full_size_sampled():
     rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 4, replace=False)]))
     ref = oracle.backward(hX[rows], Wg, ids[rows], dY[rows], W1, W2, Ws1, Ws2, c["score_fn"], c["alpha"],
                           c["renorm"], E=E, round_bf16=True, mass=True, weight_experts=[])
-    _check(out["dX"][torch.from_numpy(rows).to(DEV)].float().cpu().numpy(), ref["dX"], "c3 dX",
+    _check(out["dX"][torch.from_numpy(rows).to(DEV)].float().cpu().numpy(), ref["dX"], f"{name} dX",
            ref["mass_dX"], bf16_out=True)
-    _check(out["dG"].cpu().numpy()[rows], ref["dG"], "c3 dG", ref["mass_dG"])
+    _check(out["dG"].cpu().numpy()[rows], ref["dG"], f"{name} dG", ref["mass_dG"])
     counts = np.bincount(ids.reshape(-1), minlength=E)
     for e in [int(np.argmin(np.where(counts > 0, counts, 1 << 30))), int(np.argsort(counts)[E // 2])]:
         toks = np.where((ids == e).any(axis=1))[0]
         r = oracle.backward(hX[toks], Wg, ids[toks], dY[toks], W1, W2, None, None, c["score_fn"], c["alpha"],
                             c["renorm"], E=E, round_bf16=True, mass=True, weight_experts=[e])
-        _check(out["dW1"][e].cpu().numpy(), r["dW1"][e], f"c3 dW1[{e}] ({len(toks)} rows)", r["mass_dW1"][e])
-        _check(out["dW2"][e].cpu().numpy(), r["dW2"][e], f"c3 dW2[{e}]", r["mass_dW2"][e])
+        _check(out["dW1"][e].cpu().numpy(), r["dW1"][e], f"{name} dW1[{e}] ({len(toks)} rows)", r["mass_dW1"][e])
+        _check(out["dW2"][e].cpu().numpy(), r["dW2"][e], f"{name} dW2[{e}]", r["mass_dW2"][e])
