@@ -44,6 +44,8 @@ WORKLOAD_TEXT = {
     "c3_sp": "V4-Pro-shaped layer with the pages' sqrt-softplus affinity",
     "c3p": "V4-Pro expert shapes, T=512 E=48 (profiling size)",
     "c5p": "large-FFN expert shapes, T=1024 E=4 top-2 (~512 rows per expert; profiling size)",
+    "c5x": "large-FFN hidden size with token rows beyond L2, T=9216 H=8192 E=8 top-2 I=256 (parity case)",
+    "c5x_sh": "c5x with a shared expert (parity case)",
     "c3_f3072": "V4-Pro-shaped layer at the pages' expert width f=3072 (T=4096 H=7168 E=384 top-6 I=3072 +1 shared)",
     "c3r": "V4-Pro router at full size with I=64 (profiling size for the routing kernels)",
     "c3_q": "V4-Pro-shaped layer, A8W8-INT form (int8 weights, per-token int8 activations), no shared expert",
