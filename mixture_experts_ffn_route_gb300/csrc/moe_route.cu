@@ -17,13 +17,17 @@
 //             every expert scoring within twice the band of its k-th score to
 //             a list of (token, expert) pairs, with the pair's fp32 logit (and
 //             the token's softmax normaliser);
-//   redecide  one block per close token: a warp per candidate recomputes the
-//             logit sum_h X[t,h] Wg[h,e] to ~48 bits over a transposed copy of
-//             Wg (contiguous rows; each bf16 product is exact in fp32 and the
-//             sum is carried as float pairs) and its float64 selection score;
-//             then the top-k of those scores, larger score first, equal scores
-//             to the lower id, with gates from the listed fp32 logits.  The
-//             last block zeroes the list counters for the next call.
+//   redecide  one block per close token: the candidates within a band of
+//             another get their logit sum_h X[t,h] Wg[h,e] recomputed to ~48
+//             bits over a transposed copy of Wg (contiguous rows; each bf16
+//             product is exact in fp32 and the sum is carried as float pairs),
+//             each candidate's row split over the block's warps, and a float64
+//             selection score; the others keep their fp32 score; the ranks of
+//             the scores (larger first, equal scores to the lower id) give the
+//             k ids in order, with gates from the listed fp32 logits.  The list
+//             comes in segments (one per CTA of the fused router, one for the
+//             general path, whose counters the last block zeroes for the next
+//             call).
 // The ids then equal those of an exact evaluation except at exact ties.
 #include <float.h>
 
